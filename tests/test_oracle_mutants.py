@@ -1,0 +1,61 @@
+"""Planted mistakes in the oracle must fail its pins (CPU only).
+
+Each mutant is a copy of oracle.c with one plausible mistake (a transposed
+operand, a wrong stride, a dropped or sign-flipped term, a wrong rounding, a
+shifted index). It is compiled to a temporary library and the pin suite
+(test_oracle_pins.py) is run against it in a subprocess; the suite must fail.
+Mutants are chosen so that none reads or writes out of bounds.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "oracle.c")
+
+MUTANTS = {
+    "b_transposed": ("acc = acc + ora_f32_of_bf16(xa_row[c]) * ora_f32_of_bf16(brow[c]);",
+                     "acc = acc + ora_f32_of_bf16(xa_row[c]) * ora_f32_of_bf16(B[(int64_t)c * n_out + j]);"),
+    "a_wrong_stride": ("const uint16_t* arow = A + (int64_t)c * k_in;",
+                       "const uint16_t* arow = A + (int64_t)c;"),
+    "scale_dropped": ("float folded = fmaf(scale, ", "float folded = fmaf(1.0f, "),
+    "scale_sign": ("float folded = fmaf(scale, ", "float folded = fmaf(-scale, "),
+    "scale_before_rounding": ("            d = ora_bf16_of_f32(acc);",
+                              "            d = ora_bf16_of_f32(acc * scale); scale = 1.0f;"),
+    "truncating_bf16": ("        upper += 1u;                               /* carries into the exponent */",
+                        "        upper += 0u;"),
+    "out_stride": ("base_out + (int64_t)i * out_row_stride", "base_out + (int64_t)i * n_out"),
+    "x_stride": ("x + (int64_t)i * x_row_stride", "x + (int64_t)i * k_in"),
+    "slot_zero_skipped": ("if (s < 0 || s >= max_loras) continue;", "if (s < 1 || s >= max_loras) continue;"),
+    "expert_span_shifted": ("if (expert_offsets[k] <= r && r < expert_offsets[k + 1])",
+                            "if (expert_offsets[k] < r && r <= expert_offsets[k + 1])"),
+    "moe_table_expert_major": ("int64_t ti = (int64_t)a * num_experts + e;",
+                               "int64_t ti = (int64_t)e * max_loras + a;"),
+    "last_k_dropped": ("for (int32_t k = 0; k < k_in; ++k)\n                acc = acc + ora_f32_of_bf16(xrow[k])",
+                       "for (int32_t k = 0; k < k_in - 1; ++k)\n                acc = acc + ora_f32_of_bf16(xrow[k])"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_fails_pins(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    mutated = src.replace(old, new, 1)
+    mpath = tmp_path / "oracle.c"
+    mpath.write_text(mutated)
+    # the mutant includes oracle.h from the oracle directory
+    lib = tmp_path / "liboracle_mutant.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                    "-I", os.path.join(ROOT, "oracle"), "-o", str(lib), str(mpath), "-lm"],
+                   check=True)
+    env = dict(os.environ, GATHER_LORA_ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 1, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
+    assert "failed" in r.stdout
