@@ -1,0 +1,269 @@
+// C ABI of the routed multi-LoRA fold (include/gather_lora.h): argument checks,
+// launch geometry, error text, and the pure host helpers. Every check runs
+// before any CUDA call, so a rejected call launches nothing.
+#include "../../include/gather_lora.h"
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "fold_types.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int ok() {
+  g_err[0] = '\0';
+  return LORA_OK;
+}
+
+inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+inline int round_up(int a, int m) { return (a + m - 1) / m * m; }
+inline int round_down(int a, int m) { return a / m * m; }
+inline int pow2_floor(int v) {
+  int p = 1;
+  while (p * 2 <= v) p *= 2;
+  return p;
+}
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shared-memory budgets: two CTAs per SM, or one when the fixed part is large.
+constexpr int kBudgetTwoPerSm = 112 * 1024;
+constexpr int kBudgetOnePerSm = 225 * 1024;
+constexpr int kStageTarget = 24 * 1024;
+
+// Launch geometry. Depends only on the shapes (never on n, the routing or the
+// window), so a row's arithmetic — the k-slices, k-chunks and summation order —
+// is the same in every call with the same (k_in, n_out, max_rank).
+bool make_geometry(bool moe, int rows, int planner_ints, int max_rank, int k_in, int n_out,
+                   glora::FoldGeometry& g) {
+  g = glora::FoldGeometry{};
+  if (moe) {
+    g.cl = pow2_floor(std::min(8, std::max(1, std::max(k_in, n_out) / 256)));
+    g.rt = LORA_MOE_M_TILE;
+  } else {
+    g.cl = pow2_floor(std::min(16, std::max(1, std::max(k_in, n_out) / 512)));
+    g.rt = max_rank <= 64 ? 32 : 16;
+  }
+  g.mr16 = round_up(max_rank, 16);
+  const int mt = g.mr16 / 16;
+  g.gmax = std::min(g.rt, 8 * (glora::kMaxTilesPerWarp * glora::kWarpsPerCta / mt));
+  g.ksl = round_up(static_cast<int>(ceil_div(k_in, g.cl)), 16);
+  g.jsl = round_up(static_cast<int>(ceil_div(n_out, g.cl)), 16);
+  const int srows = g.mr16 + g.rt;
+  int kch = round_down((kStageTarget / srows - 16) / 2, 16);
+  g.kch = std::max(16, std::min(kch, g.ksl));
+  g.pitch_k = g.kch * 2 + 16;
+  g.pitch_b = max_rank * 2 + (max_rank >= 32 ? 16 : 0);
+  const int shrink_stage = srows * g.pitch_k;
+  g.jch = std::max(16, std::min(round_down(shrink_stage / g.pitch_b, 16), g.jsl));
+  g.stage_bytes = round_up(std::max(shrink_stage, g.jch * g.pitch_b), 128);
+  g.pitch_out = g.jsl * 2 + 16;
+  g.pitch_part = max_rank + 4;
+  g.pitch_xa = max_rank * 2 + 16;
+  g.off_ring = glora::kPlanBytes;
+  const int fixed = glora::kPlanBytes + g.rt * g.pitch_out + g.rt * g.pitch_part * 4 + g.rt * g.pitch_xa;
+  int ns = (kBudgetTwoPerSm - fixed) / g.stage_bytes;
+  if (ns < 3) ns = (kBudgetOnePerSm - fixed) / g.stage_bytes;
+  ns = std::min(ns, 8);
+  if (ns < 2) return false;
+  // the ring doubles as planning scratch (bgmv slot histogram / MoE offsets)
+  while (ns * g.stage_bytes < planner_ints * 4 && ns < 8) ++ns;
+  if (ns * g.stage_bytes < planner_ints * 4) g.stage_bytes = round_up(ceil_div(planner_ints * 4, ns), 128);
+  g.ns = ns;
+  g.off_out = g.off_ring + ns * g.stage_bytes;
+  g.off_part = g.off_out + g.rt * g.pitch_out;
+  g.off_xa = g.off_part + g.rt * g.pitch_part * 4;
+  g.smem_bytes = g.off_xa + g.rt * g.pitch_xa;
+  if (g.smem_bytes > kBudgetOnePerSm + 2048) return false;
+  if (moe) {
+    g.clusters = static_cast<int>(std::max(1LL, ceil_div(rows, g.rt)));
+  } else {
+    g.clusters = rows <= 0 ? 0 : rows / g.rt + std::min(rows, planner_ints);
+  }
+  return true;
+}
+
+int check_shape(int32_t max_rank, int32_t k_in, int32_t n_out, int64_t xs, int64_t os) {
+  if (max_rank < 8 || max_rank > LORA_MAX_RANK) return fail(LORA_ERR_SIZE, "max_rank %d outside [8, %d]", max_rank, LORA_MAX_RANK);
+  if (k_in < 8 || k_in > LORA_MAX_K_IN) return fail(LORA_ERR_SIZE, "k_in %d outside [8, %d]", k_in, LORA_MAX_K_IN);
+  if (n_out < 8 || n_out > LORA_MAX_N_OUT) return fail(LORA_ERR_SIZE, "n_out %d outside [8, %d]", n_out, LORA_MAX_N_OUT);
+  if (xs < k_in) return fail(LORA_ERR_STRIDE, "x_row_stride %lld < k_in %d", (long long)xs, k_in);
+  if (os < n_out) return fail(LORA_ERR_STRIDE, "out_row_stride %lld < n_out %d", (long long)os, n_out);
+  if (max_rank % 8 || k_in % 8 || n_out % 8)
+    return fail(LORA_ERR_ALIGN, "max_rank, k_in and n_out must be multiples of 8 (%d, %d, %d)", max_rank, k_in, n_out);
+  if (xs % 8 || os % 8)
+    return fail(LORA_ERR_ALIGN, "row strides must be multiples of 8 elements (%lld, %lld)", (long long)xs, (long long)os);
+  return LORA_OK;
+}
+
+int cuda_fail(int err, const char* what) {
+  return fail(LORA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(static_cast<cudaError_t>(err)));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* lora_last_error(void) { return g_err; }
+
+int lora_bgmv(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_t* base_out, int64_t out_row_stride,
+              const int32_t* seq_slot, int32_t n, const lora_bf16_t* const* a_table,
+              const lora_bf16_t* const* b_table, const float* scale_table, int32_t max_loras,
+              int32_t max_rank, int32_t k_in, int32_t n_out, lora_bf16_t* xa, void* stream) {
+  if (n < 0 || n > LORA_MAX_ROWS) return fail(LORA_ERR_SIZE, "n %d outside [0, %d]", n, LORA_MAX_ROWS);
+  if (max_loras < 1 || max_loras > LORA_MAX_LORAS)
+    return fail(LORA_ERR_SIZE, "max_loras %d outside [1, %d]", max_loras, LORA_MAX_LORAS);
+  int rc = check_shape(max_rank, k_in, n_out, x_row_stride, out_row_stride);
+  if (rc) return rc;
+  if (n == 0) return ok();
+  if (!x || !base_out || !seq_slot || !a_table || !b_table || !scale_table)
+    return fail(LORA_ERR_NULL, "a required pointer is NULL (x, base_out, seq_slot, a_table, b_table, scale_table)");
+  if (!aligned16(x) || !aligned16(base_out) || (xa && !aligned16(xa)))
+    return fail(LORA_ERR_ALIGN, "x, base_out and xa must be 16-byte aligned");
+  glora::BgmvArgs a{};
+  if (!make_geometry(false, n, max_loras, max_rank, k_in, n_out, a.g))
+    return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory for max_rank %d, k_in %d, n_out %d", max_rank, k_in, n_out);
+  a.x = x;
+  a.x_stride = x_row_stride;
+  a.out = base_out;
+  a.out_stride = out_row_stride;
+  a.seq_slot = seq_slot;
+  a.n = n;
+  a.a_table = a_table;
+  a.b_table = b_table;
+  a.scale_table = scale_table;
+  a.max_loras = max_loras;
+  a.max_rank = max_rank;
+  a.k_in = k_in;
+  a.n_out = n_out;
+  a.xa = xa;
+  rc = glora::launch_bgmv(a, stream);
+  return rc ? cuda_fail(rc, "lora_bgmv launch") : ok();
+}
+
+int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_t* base_out,
+                          int64_t out_row_stride, const int32_t* expert_offsets, int32_t num_experts,
+                          const int32_t* sorted_token_ids, int32_t te, const int32_t* row_adapter,
+                          int32_t num_tokens, int32_t row_offset, int32_t row_end,
+                          const lora_bf16_t* const* a_table, const lora_bf16_t* const* b_table,
+                          const float* scale_table, int32_t max_loras, int32_t max_rank, int32_t k_in,
+                          int32_t n_out, lora_bf16_t* xa, void* stream) {
+  if (num_experts < 1 || num_experts > LORA_MAX_EXPERTS)
+    return fail(LORA_ERR_SIZE, "num_experts %d outside [1, %d]", num_experts, LORA_MAX_EXPERTS);
+  if (max_loras < 1 || max_loras > LORA_MAX_LORAS)
+    return fail(LORA_ERR_SIZE, "max_loras %d outside [1, %d]", max_loras, LORA_MAX_LORAS);
+  if (te < 0 || num_tokens < 0) return fail(LORA_ERR_SIZE, "te %d and num_tokens %d must be >= 0", te, num_tokens);
+  if (row_offset < 0 || row_end < row_offset || row_end > te)
+    return fail(LORA_ERR_WINDOW, "window [%d, %d) outside [0, te=%d]", row_offset, row_end, te);
+  int rc = check_shape(max_rank, k_in, n_out, x_row_stride, out_row_stride);
+  if (rc) return rc;
+  if (!x || !base_out || !expert_offsets || !a_table || !b_table || !scale_table)
+    return fail(LORA_ERR_NULL, "a required pointer is NULL (x, base_out, expert_offsets, a_table, b_table, scale_table)");
+  if (row_adapter && !sorted_token_ids)
+    return fail(LORA_ERR_NULL, "sorted_token_ids is required when row_adapter is given");
+  if (!aligned16(x) || !aligned16(base_out) || (xa && !aligned16(xa)))
+    return fail(LORA_ERR_ALIGN, "x, base_out and xa must be 16-byte aligned");
+  glora::MoeArgs a{};
+  if (!make_geometry(true, row_end - row_offset, num_experts + 1, max_rank, k_in, n_out, a.g))
+    return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory for max_rank %d, k_in %d, n_out %d", max_rank, k_in, n_out);
+  a.x = x;
+  a.x_stride = x_row_stride;
+  a.out = base_out;
+  a.out_stride = out_row_stride;
+  a.expert_offsets = expert_offsets;
+  a.num_experts = num_experts;
+  a.sorted_token_ids = sorted_token_ids;
+  a.row_adapter = row_adapter;
+  a.num_tokens = num_tokens;
+  a.row_offset = row_offset;
+  a.row_end = row_end;
+  a.a_table = a_table;
+  a.b_table = b_table;
+  a.scale_table = scale_table;
+  a.max_loras = max_loras;
+  a.max_rank = max_rank;
+  a.k_in = k_in;
+  a.n_out = n_out;
+  a.xa = xa;
+  rc = glora::launch_moe(a, stream);
+  return rc ? cuda_fail(rc, "lora_moe_grouped_fold launch") : ok();
+}
+
+int lora_read_device_status(void* stream, uint32_t* status_out, int clear) {
+  const int rc = glora::read_device_status(stream, status_out, clear);
+  return rc ? cuda_fail(rc, "lora_read_device_status") : ok();
+}
+
+int lora_launch_geometry(int moe, int32_t rows, int32_t max_loras, int32_t max_rank, int32_t k_in,
+                         int32_t n_out, int64_t out[9]) {
+  if (!out) return fail(LORA_ERR_NULL, "out is NULL");
+  int rc = check_shape(max_rank, k_in, n_out, k_in, n_out);
+  if (rc) return rc;
+  glora::FoldGeometry g{};
+  if (!make_geometry(moe != 0, rows, max_loras, max_rank, k_in, n_out, g))
+    return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory");
+  const int64_t v[9] = {g.cl, g.rt, g.ksl, g.jsl, g.kch, g.jch, g.ns, g.clusters, g.smem_bytes};
+  std::memcpy(out, v, sizeof v);
+  return ok();
+}
+
+int32_t lora_grouped_down_wc(int32_t row_offset, int32_t row_end) {
+  if (row_end < row_offset) return -1;
+  const int64_t span = static_cast<int64_t>(row_end) - row_offset;
+  return static_cast<int32_t>(std::max<int64_t>(1, (span + LORA_MOE_M_TILE - 1) / LORA_MOE_M_TILE));
+}
+
+int32_t lora_grouped_down_windows(int32_t total_rows, int32_t cap, int32_t* starts, int32_t* ends,
+                                  int32_t max_windows) {
+  if (cap < 1 || total_rows < 0) return -1;
+  const int64_t count = (static_cast<int64_t>(total_rows) + cap - 1) / cap;
+  if (count > max_windows) return -2;
+  if (count > 0 && (!starts || !ends)) return -1;
+  for (int64_t w = 0; w < count; ++w) {
+    starts[w] = static_cast<int32_t>(w * cap);
+    ends[w] = static_cast<int32_t>(std::min<int64_t>(static_cast<int64_t>(total_rows), (w + 1) * cap));
+  }
+  return static_cast<int32_t>(count);
+}
+
+int lora_pack_expert_tables(const int32_t* expert_ids, const uint64_t* a_addrs, const uint64_t* b_addrs,
+                            const float* scales, int32_t n_entries, uint64_t* a_table, uint64_t* b_table,
+                            float* scale_table, int32_t table_len, int32_t* n_experts_out) {
+  if (!n_experts_out) return -1;
+  *n_experts_out = 0;
+  if (n_entries <= 0) return 1;
+  if (!expert_ids || !a_addrs || !b_addrs || !scales || !a_table || !b_table || !scale_table) return -1;
+  int32_t n_experts = 0;
+  for (int32_t i = 0; i < n_entries; ++i) {
+    if (expert_ids[i] < 0) return -1;
+    n_experts = std::max(n_experts, expert_ids[i] + 1);
+  }
+  if (table_len < n_experts) return -2;
+  for (int32_t e = 0; e < n_experts; ++e) {
+    a_table[e] = 0;
+    b_table[e] = 0;
+    scale_table[e] = 0.0f;
+  }
+  for (int32_t i = 0; i < n_entries; ++i) {  // later entries replace earlier ones
+    a_table[expert_ids[i]] = a_addrs[i];
+    b_table[expert_ids[i]] = b_addrs[i];
+    scale_table[expert_ids[i]] = scales[i];
+  }
+  *n_experts_out = n_experts;
+  return 0;
+}
+
+}  // extern "C"

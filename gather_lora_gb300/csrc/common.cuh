@@ -1,0 +1,141 @@
+// Device helpers shared by the bgmv and MoE fold kernels (sm_103a).
+//
+// Everything here is a thin inline-PTX wrapper: 16-byte asynchronous global->
+// shared copies (cp.async.cg), shared-memory matrix loads (ldmatrix), BF16
+// tensor-core MMA with fp32 accumulation (mma.sync m16n8k16 / m16n8k8), and
+// programmatic-dependent-launch controls (griddepcontrol).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace glora {
+
+constexpr int kThreads = 256;   // every fold kernel runs 8 warps per CTA
+constexpr int kWarps = kThreads / 32;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- asynchronous copies ---------------------------------------------------
+// 16 bytes global -> shared, L2-only (.cg): adapter and activation rows are
+// read once per CTA, so they should not displace L1.
+__device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst_smem), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+// Wait until at most `n` of this thread's most recent copy groups are pending.
+__device__ __forceinline__ void cp_async_wait(int n) {
+  switch (n) {
+    case 0: asm volatile("cp.async.wait_group 0;\n" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;\n" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;\n" ::: "memory"); break;
+    case 3: asm volatile("cp.async.wait_group 3;\n" ::: "memory"); break;
+    case 4: asm volatile("cp.async.wait_group 4;\n" ::: "memory"); break;
+    case 5: asm volatile("cp.async.wait_group 5;\n" ::: "memory"); break;
+    case 6: asm volatile("cp.async.wait_group 6;\n" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 7;\n" ::: "memory"); break;
+  }
+}
+
+// ---- shared-memory matrix fragments ----------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x1(uint32_t addr, uint32_t& r0) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x1.shared.b16 {%0}, [%1];\n" : "=r"(r0) : "r"(addr));
+}
+
+// ---- BF16 tensor-core MMA, fp32 accumulate ----------------------------------
+// D[16x8] += A[16xK] * B[Kx8]; A row-major (K contiguous per row of A), B
+// "col" (K contiguous per column of B). Accumulator layout per lane
+// (g = lane/4, q = lane%4): d0 (g, 2q), d1 (g, 2q+1), d2 (g+8, 2q), d3 (g+8, 2q+1).
+__device__ __forceinline__ void mma_k16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_k8(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(b0));
+}
+
+// One K step (16, or 8 for a ragged tail) of a 16x8 output tile:
+//   a_row_addr: shared address of the A row this lane feeds to ldmatrix,
+//               i.e. A tile row (lane & 15), at the step's first column;
+//   b_row_addr: shared address of the B row (lane & 7), at the step's first column.
+// Column offsets of the second 8-wide half are added here.
+__device__ __forceinline__ void mma_step(float (&acc)[4], uint32_t a_row_addr, uint32_t b_row_addr,
+                                         int kstep, int lane) {
+  if (kstep == 16) {
+    uint32_t a0, a1, a2, a3, b0, b1;
+    ldsm_x4(a_row_addr + ((lane >> 4) << 4), a0, a1, a2, a3);
+    ldsm_x2(b_row_addr + (((lane >> 3) & 1) << 4), b0, b1);
+    mma_k16(acc, a0, a1, a2, a3, b0, b1);
+  } else {
+    uint32_t a0, a1, b0;
+    ldsm_x2(a_row_addr, a0, a1);
+    ldsm_x1(b_row_addr, b0);
+    mma_k8(acc, a0, a1, b0);
+  }
+}
+
+// ---- programmatic dependent launch -----------------------------------------
+// Wait until the preceding grid on the stream has completed and its memory is
+// visible (no-op when the launch carried no programmatic dependency), then let
+// the next grid start launching its CTAs.
+__device__ __forceinline__ void pdl_wait_then_release() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t h) {
+  return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// The fold of one element: bf16( fma(scale, bf16(acc), out) ).
+__device__ __forceinline__ uint16_t fold_one(float acc, float scale, uint16_t out_bits) {
+  const float d = bf16_bits_to_f32(f32_to_bf16_bits(acc));
+  return f32_to_bf16_bits(__fmaf_rn(scale, d, bf16_bits_to_f32(out_bits)));
+}
+
+// Block-wide inclusive sum over the 256 threads (warp shuffles + 8 partials in
+// `warp_sums` shared scratch). Must be called by all threads.
+__device__ __forceinline__ int block_inclusive_sum(int v, int* warp_sums) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  if (lane == 31) warp_sums[warp] = v;
+  __syncthreads();
+  int before = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) before += (w < warp) ? warp_sums[w] : 0;
+  __syncthreads();
+  return v + before;
+}
+
+}  // namespace glora

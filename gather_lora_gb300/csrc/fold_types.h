@@ -1,0 +1,76 @@
+// Plain structs shared by the host launcher (abi.cpp) and the kernels.
+#pragma once
+
+#include <stdint.h>
+
+namespace glora {
+
+constexpr int kMaxRows = 64;        // rows (positions) per cluster work unit
+constexpr int kMaxTilesPerWarp = 8; // 16x8 shrink tiles a warp may own: MT * NT <= 64
+constexpr int kPlanBytes = 4096;    // shared memory reserved for the work-unit plan
+constexpr int kWarpsPerCta = 8;     // fold kernels run 256 threads per CTA
+
+// Launch geometry and shared-memory layout of one fold launch. Every CTA of a
+// cluster of `cl` CTAs owns one k-slice of the shrink (ksl columns of A / x)
+// and one j-slice of the expand (jsl rows of B / columns of out). Inputs
+// stream through a ring of `ns` stages of `stage_bytes`.
+struct FoldGeometry {
+  int cl;           // CTAs per cluster
+  int rt;           // rows per work unit (<= kMaxRows)
+  int ksl, jsl;     // k-slice / j-slice per CTA (multiples of 16)
+  int kch, jch;     // k columns / B rows per ring stage (multiples of 16)
+  int ns;           // ring depth (>= 2)
+  int gmax;         // most rows in one group (MT * ceil(gmax/8) <= 64 shrink tiles)
+  int mr16;         // max_rank rounded up to 16
+  int pitch_k;      // bytes per A or x row in a shrink stage (kch*2 + 16)
+  int pitch_b;      // bytes per B row in an expand stage
+  int pitch_out;    // bytes per staged out row (jsl*2 + 16)
+  int pitch_part;   // floats per partial-sum row (max_rank + 4)
+  int pitch_xa;     // bytes per xa row (max_rank*2 + 16)
+  int stage_bytes;
+  int off_ring, off_out, off_part, off_xa, smem_bytes;
+  int clusters;     // grid = clusters * cl CTAs
+};
+
+struct BgmvArgs {
+  const uint16_t* x;
+  long long x_stride;
+  uint16_t* out;
+  long long out_stride;
+  const int32_t* seq_slot;
+  int n;
+  const uint16_t* const* a_table;
+  const uint16_t* const* b_table;
+  const float* scale_table;
+  int max_loras;
+  int max_rank, k_in, n_out;
+  uint16_t* xa;
+  FoldGeometry g;
+};
+
+struct MoeArgs {
+  const uint16_t* x;
+  long long x_stride;
+  uint16_t* out;
+  long long out_stride;
+  const int32_t* expert_offsets;
+  int num_experts;
+  const int32_t* sorted_token_ids;
+  const int32_t* row_adapter;
+  int num_tokens;
+  int row_offset, row_end;
+  const uint16_t* const* a_table;
+  const uint16_t* const* b_table;
+  const float* scale_table;
+  int max_loras;
+  int max_rank, k_in, n_out;
+  uint16_t* xa;
+  FoldGeometry g;
+};
+
+// Launchers (kernels.cu). Return 0 or a cudaError_t value.
+int launch_bgmv(const BgmvArgs& a, void* stream);
+int launch_moe(const MoeArgs& a, void* stream);
+int read_device_status(void* stream, uint32_t* out, int clear);
+
+}  // namespace glora

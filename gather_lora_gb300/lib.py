@@ -1,0 +1,166 @@
+"""ctypes binding of libgather_lora.so (the C ABI in include/gather_lora.h).
+
+Argument marshalling only: every step of the fold runs in the library's CUDA
+kernels. Device buffers may be passed as torch tensors (their data_ptr() is
+used) or as raw integer addresses; ``stream`` may be a torch.cuda.Stream, a raw
+cudaStream_t integer, or None for torch's current stream. The functions carry
+the C names. A missing library raises at first use: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgather_lora.so")
+
+LORA_OK = 0
+STATUS_NAMES = {-1: "LORA_ERR_NULL", -2: "LORA_ERR_SIZE", -3: "LORA_ERR_STRIDE",
+                -4: "LORA_ERR_ALIGN", -5: "LORA_ERR_WINDOW", -6: "LORA_ERR_CUDA",
+                -7: "LORA_ERR_UNSUPPORTED"}
+LORA_DEV_MISALIGNED = 0x1
+MOE_M_TILE = 64
+
+
+class LoraError(RuntimeError):
+    def __init__(self, code: int, text: str):
+        super().__init__(f"{STATUS_NAMES.get(code, code)}: {text}")
+        self.code = code
+
+
+_lib = None
+
+
+def load():
+    """Load libgather_lora.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with gather_lora_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    lib.lora_bgmv.restype = ctypes.c_int
+    lib.lora_bgmv.argtypes = [P, I64, P, I64, P, I32, P, P, P, I32, I32, I32, I32, P, P]
+    lib.lora_moe_grouped_fold.restype = ctypes.c_int
+    lib.lora_moe_grouped_fold.argtypes = [P, I64, P, I64, P, I32, P, I32, P, I32, I32, I32,
+                                          P, P, P, I32, I32, I32, I32, P, P]
+    lib.lora_last_error.restype = ctypes.c_char_p
+    lib.lora_last_error.argtypes = []
+    lib.lora_read_device_status.restype = ctypes.c_int
+    lib.lora_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
+    lib.lora_launch_geometry.restype = ctypes.c_int
+    lib.lora_launch_geometry.argtypes = [ctypes.c_int, I32, I32, I32, I32, I32, ctypes.POINTER(I64)]
+    lib.lora_grouped_down_wc.restype = I32
+    lib.lora_grouped_down_wc.argtypes = [I32, I32]
+    lib.lora_grouped_down_windows.restype = I32
+    lib.lora_grouped_down_windows.argtypes = [I32, I32, ctypes.POINTER(I32), ctypes.POINTER(I32), I32]
+    lib.lora_pack_expert_tables.restype = ctypes.c_int
+    lib.lora_pack_expert_tables.argtypes = [ctypes.POINTER(I32), ctypes.POINTER(ctypes.c_uint64),
+                                            ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_float),
+                                            I32, ctypes.POINTER(ctypes.c_uint64),
+                                            ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_float),
+                                            I32, ctypes.POINTER(I32)]
+    _lib = lib
+    return lib
+
+
+def _addr(v):
+    if v is None:
+        return None
+    if isinstance(v, int):
+        return v or None
+    return v.data_ptr() or None       # torch tensor
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream or None
+    if isinstance(s, int):
+        return s or None
+    return s.cuda_stream or None      # torch.cuda.Stream
+
+
+def _check(rc: int) -> int:
+    if rc != LORA_OK:
+        raise LoraError(rc, load().lora_last_error().decode())
+    return rc
+
+
+def lora_bgmv(x, x_row_stride, base_out, out_row_stride, seq_slot, n, a_table, b_table,
+              scale_table, max_loras, max_rank, k_in, n_out, xa=None, stream=None):
+    """Routed bgmv fold (see lora_bgmv in include/gather_lora.h)."""
+    return _check(load().lora_bgmv(_addr(x), x_row_stride, _addr(base_out), out_row_stride,
+                                   _addr(seq_slot), n, _addr(a_table), _addr(b_table),
+                                   _addr(scale_table), max_loras, max_rank, k_in, n_out,
+                                   _addr(xa), _stream(stream)))
+
+
+def lora_moe_grouped_fold(x, x_row_stride, base_out, out_row_stride, expert_offsets, num_experts,
+                          sorted_token_ids, te, row_adapter, num_tokens, row_offset, row_end,
+                          a_table, b_table, scale_table, max_loras, max_rank, k_in, n_out,
+                          xa=None, stream=None):
+    """MoE grouped fold of one window (see lora_moe_grouped_fold in include/gather_lora.h)."""
+    return _check(load().lora_moe_grouped_fold(
+        _addr(x), x_row_stride, _addr(base_out), out_row_stride, _addr(expert_offsets),
+        num_experts, _addr(sorted_token_ids), te, _addr(row_adapter), num_tokens, row_offset,
+        row_end, _addr(a_table), _addr(b_table), _addr(scale_table), max_loras, max_rank, k_in,
+        n_out, _addr(xa), _stream(stream)))
+
+
+def lora_last_error() -> str:
+    return load().lora_last_error().decode()
+
+
+def lora_read_device_status(stream=None, clear=True) -> int:
+    v = ctypes.c_uint32(0)
+    _check(load().lora_read_device_status(_stream(stream), ctypes.byref(v), int(clear)))
+    return int(v.value)
+
+
+GEOMETRY_KEYS = ("cluster", "rows_per_tile", "k_slice", "j_slice", "k_chunk", "j_chunk",
+                 "ring_stages", "clusters", "smem_bytes")
+
+
+def lora_launch_geometry(moe, rows, max_loras, max_rank, k_in, n_out) -> dict:
+    out = (ctypes.c_int64 * 9)()
+    _check(load().lora_launch_geometry(int(moe), rows, max_loras, max_rank, k_in, n_out, out))
+    return dict(zip(GEOMETRY_KEYS, list(out)))
+
+
+def lora_grouped_down_wc(row_offset: int, row_end: int) -> int:
+    return int(load().lora_grouped_down_wc(row_offset, row_end))
+
+
+def lora_grouped_down_windows(total_rows: int, cap: int):
+    """Returns the list of (start, end) windows, or raises ValueError."""
+    n_max = max(1, (max(total_rows, 0) + max(cap, 1) - 1) // max(cap, 1))
+    starts = (ctypes.c_int32 * n_max)()
+    ends = (ctypes.c_int32 * n_max)()
+    n = int(load().lora_grouped_down_windows(total_rows, cap, starts, ends, n_max))
+    if n < 0:
+        raise ValueError(f"lora_grouped_down_windows({total_rows}, {cap}) -> {n}")
+    return [(starts[i], ends[i]) for i in range(n)]
+
+
+def lora_pack_expert_tables(entries, table_len=None):
+    """entries: list of (expert_id, a_addr, b_addr, scale). Returns None for an
+    empty list, else (a_table, b_table, scale_table) lists of n_experts entries."""
+    n = len(entries)
+    ids = (ctypes.c_int32 * max(n, 1))(*[e[0] for e in entries])
+    aa = (ctypes.c_uint64 * max(n, 1))(*[e[1] for e in entries])
+    bb = (ctypes.c_uint64 * max(n, 1))(*[e[2] for e in entries])
+    ss = (ctypes.c_float * max(n, 1))(*[e[3] for e in entries])
+    tl = table_len if table_len is not None else max([e[0] for e in entries] + [0]) + 1
+    at = (ctypes.c_uint64 * max(tl, 1))()
+    bt = (ctypes.c_uint64 * max(tl, 1))()
+    st = (ctypes.c_float * max(tl, 1))()
+    ne = ctypes.c_int32(0)
+    rc = load().lora_pack_expert_tables(ids, aa, bb, ss, n, at, bt, st, tl, ctypes.byref(ne))
+    if rc == 1:
+        return None
+    if rc != 0:
+        raise ValueError(f"lora_pack_expert_tables -> {rc}")
+    k = ne.value
+    return list(at[:k]), list(bt[:k]), list(st[:k])

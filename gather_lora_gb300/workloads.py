@@ -306,3 +306,76 @@ def by_name(name: str, seed=None):
           "qkv_kfold_bgmv": qkv_kfold_bgmv, "ffn_down_bgmv": ffn_down_bgmv,
           "moe_down_fold": moe_down_fold}[name]
     return fn() if seed is None else fn(seed)
+
+
+# --- device placement (data movement only) -------------------------------------
+
+@dataclass
+class DeviceBgmv:
+    x: "torch.Tensor"         # int16 [n, x_row_stride] (BF16 bits)
+    out_buf: "torch.Tensor"   # int16 [n, out_row_stride]
+    out_ptr: int              # address of out_buf[0, out_offset]
+    seq_slot: "torch.Tensor"  # int32 [n]
+    a_pool: "torch.Tensor"
+    b_pool: "torch.Tensor"
+    a_table: "torch.Tensor"   # int64 [max_loras] device addresses (0 = NULL)
+    b_table: "torch.Tensor"
+    scale: "torch.Tensor"     # float32 [max_loras]
+    xa: "torch.Tensor"        # int16 [n, max_rank]
+
+
+def _dev(a: np.ndarray, device) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if t.dtype == torch.uint16:
+        t = t.view(torch.int16)
+    return t.to(device)
+
+
+def _table_of(pool: torch.Tensor, present: np.ndarray, device) -> torch.Tensor:
+    stride = pool[0].numel() * pool.element_size() if pool.shape[0] else 0
+    base = pool.data_ptr()
+    addrs = [base + i * stride if present[i] else 0 for i in range(len(present))]
+    return torch.tensor(addrs, dtype=torch.int64, device=device)
+
+
+def bgmv_to_device(wl: BgmvWorkload, device="cuda") -> DeviceBgmv:
+    x = _dev(wl.x.view(np.int16), device)
+    out = _dev(wl.out_buf.view(np.int16), device)
+    a_pool = _dev(wl.a_pool.view(np.int16), device)
+    b_pool = _dev(wl.b_pool.view(np.int16), device)
+    return DeviceBgmv(
+        x=x, out_buf=out, out_ptr=out.data_ptr() + 2 * wl.out_offset,
+        seq_slot=_dev(wl.seq_slot, device), a_pool=a_pool, b_pool=b_pool,
+        a_table=_table_of(a_pool, wl.present, device), b_table=_table_of(b_pool, wl.present, device),
+        scale=_dev(wl.scale, device),
+        xa=torch.zeros((max(wl.n, 1), wl.max_rank), dtype=torch.int16, device=device))
+
+
+@dataclass
+class DeviceMoe:
+    x: "torch.Tensor"
+    out_buf: "torch.Tensor"
+    expert_offsets: "torch.Tensor"
+    sorted_token_ids: "torch.Tensor"
+    row_adapter: "torch.Tensor | None"
+    a_pool: "torch.Tensor"
+    b_pool: "torch.Tensor"
+    a_table: "torch.Tensor"
+    b_table: "torch.Tensor"
+    scale: "torch.Tensor"
+    xa: "torch.Tensor"        # int16 [cap, max_rank] (window-local rows)
+
+
+def moe_to_device(wl: MoeWorkload, device="cuda", xa_rows=None) -> DeviceMoe:
+    a_pool = _dev(wl.a_pool.view(np.int16), device)
+    b_pool = _dev(wl.b_pool.view(np.int16), device)
+    rows = xa_rows if xa_rows is not None else max(wl.cap, 1)
+    return DeviceMoe(
+        x=_dev(wl.x.view(np.int16), device), out_buf=_dev(wl.out_buf.view(np.int16), device),
+        expert_offsets=_dev(wl.expert_offsets, device),
+        sorted_token_ids=_dev(wl.sorted_token_ids, device),
+        row_adapter=None if wl.row_adapter is None else _dev(wl.row_adapter, device),
+        a_pool=a_pool, b_pool=b_pool,
+        a_table=_table_of(a_pool, wl.present, device), b_table=_table_of(b_pool, wl.present, device),
+        scale=_dev(wl.scale, device),
+        xa=torch.zeros((rows, wl.max_rank), dtype=torch.int16, device=device))

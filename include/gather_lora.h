@@ -1,0 +1,214 @@
+/*
+ * gather_lora.h — C ABI of the routed multi-LoRA fold for NVIDIA GB300 (sm_103a).
+ *
+ * Two operations, each one kernel launch on the caller's stream:
+ *
+ *   lora_bgmv             per-request routed LoRA delta over n rows
+ *   lora_moe_grouped_fold the same fold over expert-sorted MoE rows of one window
+ *
+ * and three pure host helpers (no GPU needed) for the MoE windows and tables.
+ *
+ * Conventions for every entry point
+ *   - BF16 values are raw 16-bit patterns (lora_bf16_t); f32 is IEEE float.
+ *   - Every pointer argument of the two folds is DEVICE memory owned by the
+ *     caller; the library allocates, frees and synchronizes nothing, and
+ *     returns as soon as the launch is queued.
+ *   - Strides are in ELEMENTS, not bytes.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *   - Return value: LORA_OK (0), or a negative lora_status. Every argument
+ *     check runs on the host BEFORE any launch: a negative return other than
+ *     LORA_ERR_CUDA means nothing was launched. LORA_ERR_CUDA means the launch
+ *     itself failed; lora_last_error() gives the text (per host thread).
+ *   - Bad DEVICE data is never a fault: a slot outside [0, max_loras), a NULL
+ *     table entry, a token or adapter out of range, a row outside the expert
+ *     spans all mean "this row gets no delta". A table entry that is not
+ *     16-byte aligned is skipped too and sets LORA_DEV_MISALIGNED in the
+ *     device status word (lora_read_device_status).
+ *   - Both folds are capture-safe: the launch shape depends only on the host
+ *     integers passed in, so a CUDA graph captured once replays correctly
+ *     when only device buffer CONTENTS (seq_slot, row_adapter, offsets, x,
+ *     base_out) change.
+ *
+ * Alignment (this library's own restriction; the method states none): x,
+ * base_out and xa must be 16-byte aligned; k_in, n_out, max_rank and both row
+ * strides must be multiples of 8; adapter matrices must be 16-byte aligned.
+ * Otherwise the call returns LORA_ERR_ALIGN (there is no fallback path).
+ *
+ * Numerics (the rounding order of the method): per row, fp32 accumulation of
+ * BF16 products; xa rounded to BF16 (RNE); the expand sum rounded to BF16
+ * (RNE); then out = bf16_rn(fmaf(scale, delta, out)). The fp32 summation
+ * order is fixed by (k_in, max_rank) alone, so a row's result never depends
+ * on which or how many other rows share the call (batch invariance).
+ */
+#ifndef GATHER_LORA_H
+#define GATHER_LORA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t lora_bf16_t;
+
+enum lora_status {
+    LORA_OK = 0,
+    LORA_ERR_NULL = -1,        /* a required pointer is NULL */
+    LORA_ERR_SIZE = -2,        /* a size or count is outside its supported range */
+    LORA_ERR_STRIDE = -3,      /* a row stride is smaller than the row width */
+    LORA_ERR_ALIGN = -4,       /* a pointer, stride or width breaks the alignment rule */
+    LORA_ERR_WINDOW = -5,      /* MoE window outside [0, te] or row_end < row_offset */
+    LORA_ERR_CUDA = -6,        /* the CUDA launch (or a device query) failed */
+    LORA_ERR_UNSUPPORTED = -7  /* the current device cannot run these kernels */
+};
+
+/* Device status bits, set by kernels, read with lora_read_device_status(). */
+#define LORA_DEV_MISALIGNED 0x1u   /* an adapter table entry was not 16-byte aligned */
+
+/* Supported ranges, checked on every call. */
+#define LORA_MAX_RANK 256          /* max_rank in [8, 256], multiple of 8 */
+#define LORA_MAX_K_IN (1 << 20)    /* k_in in [8, 2^20], multiple of 8 */
+#define LORA_MAX_N_OUT (1 << 20)   /* n_out in [8, 2^20], multiple of 8 */
+#define LORA_MAX_ROWS 65536        /* n of lora_bgmv in [0, 65536] */
+#define LORA_MAX_LORAS 4096        /* max_loras of lora_bgmv in [1, 4096] */
+#define LORA_MAX_EXPERTS 1024      /* num_experts of the MoE fold in [1, 1024] */
+#define LORA_MOE_M_TILE 64         /* sorted rows per MoE tile (static grid unit) */
+
+/*
+ * lora_bgmv — per-request routed LoRA delta over n rows.
+ *
+ * Defines: "Function apply_lora_bgmv" (spark_model::layers::ops::lora_delta
+ * rustdoc), the summary, BYTE-IDENTICAL, STRIDES and GRAPH-SAFE paragraphs;
+ * lora_delta.rs (metrale source listing), `LoraRoute` and `LoraPair`.
+ *
+ * For every row i in [0, n) with s = seq_slot[i], 0 <= s < max_loras and both
+ * a_table[s] and b_table[s] non-NULL:
+ *     xa[i, c]  = bf16( sum_k x[i, k] * A_s[c, k] )          c < max_rank
+ *     d[j]      = bf16( sum_c xa[i, c] * B_s[j, c] )         j < n_out
+ *     out[i, j] = bf16( fmaf(scale_table[s], d[j], out[i, j]) )
+ * Every other row, and every element outside out[i, 0:n_out), is left
+ * byte-for-byte unchanged.
+ *
+ *   x            [n rows, x_row_stride] BF16; row i's input is x[i*x_row_stride .. +k_in)
+ *   base_out     [n rows, out_row_stride] BF16, folded IN PLACE; row i's segment is
+ *                base_out[i*out_row_stride .. +n_out). To fold into the K part of an
+ *                interleaved [Q|K|V] row, pass base_out = qkv + q_width and
+ *                out_row_stride = q_width + k_width + v_width.
+ *   seq_slot     [n] int32 adapter slot per row (< 0 = no delta)
+ *   a_table      [max_loras] device pointers to A_s, [max_rank, k_in] row-major BF16
+ *   b_table      [max_loras] device pointers to B_s, [n_out, max_rank] row-major BF16
+ *                (rank-padded: rows of A / columns of B past the adapter's rank are 0)
+ *   scale_table  [max_loras] f32 per-slot scale (alpha/r, or alpha/sqrt(r) for rsLoRA)
+ *   xa           optional [n, max_rank] BF16 output of the shrink (routed rows only
+ *                are written); NULL skips it
+ *   n == 0 is a no-op (returns LORA_OK, nothing launched).
+ */
+int lora_bgmv(const lora_bf16_t* x, int64_t x_row_stride,
+              lora_bf16_t* base_out, int64_t out_row_stride,
+              const int32_t* seq_slot, int32_t n,
+              const lora_bf16_t* const* a_table, const lora_bf16_t* const* b_table,
+              const float* scale_table, int32_t max_loras,
+              int32_t max_rank, int32_t k_in, int32_t n_out,
+              lora_bf16_t* xa, void* stream);
+
+/*
+ * lora_moe_grouped_fold — the fold over expert-sorted MoE rows of one window.
+ *
+ * Defines: "Module moe_lora_grouped" (atlas rustdoc), the module summary and the
+ * `moe_lora_grouped_down`, `MoeExpertRoute` and `MLG_M_TILE` entries (down
+ * projection: x is the sorted [te, k_in] activation, x_gather == 0).
+ *
+ * For every sorted row r in [row_offset, row_end):
+ *   e = the expert with expert_offsets[e] <= r < expert_offsets[e+1]
+ *       (rows outside [expert_offsets[0], expert_offsets[num_experts]) are skipped);
+ *   a = row_adapter ? row_adapter[sorted_token_ids[r]] : 0
+ *       (skipped if the token is outside [0, num_tokens) or a is outside [0, max_loras));
+ *   t = a * num_experts + e (adapter-major tables); skipped if a_table[t] or
+ *       b_table[t] is NULL; otherwise the fold of lora_bgmv is applied to
+ *       x[r*x_row_stride ..] and base_out[r*out_row_stride ..] with A_t, B_t,
+ *       scale_table[t].
+ *
+ *   expert_offsets    [num_experts + 1] int32 prefix sum (non-decreasing)
+ *   sorted_token_ids  [te] int32 sorted row -> token; may be NULL when row_adapter is NULL
+ *   row_adapter       [num_tokens] int32 (< 0 = no delta), or NULL: every row uses adapter 0
+ *   a_table, b_table, scale_table   [max_loras * num_experts], index a*num_experts + e
+ *   xa                optional [row_end - row_offset, max_rank] BF16 shrink output at the
+ *                     LOCAL row r - row_offset (routed rows only); NULL skips it
+ * The window must satisfy 0 <= row_offset <= row_end <= te. The launch grid is
+ * ceil((row_end - row_offset) / LORA_MOE_M_TILE) tiles (at least 1), so calls over
+ * windows [0, cap), [cap, 2cap), ... give the same result as one call over [0, te).
+ */
+int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride,
+                          lora_bf16_t* base_out, int64_t out_row_stride,
+                          const int32_t* expert_offsets, int32_t num_experts,
+                          const int32_t* sorted_token_ids, int32_t te,
+                          const int32_t* row_adapter, int32_t num_tokens,
+                          int32_t row_offset, int32_t row_end,
+                          const lora_bf16_t* const* a_table, const lora_bf16_t* const* b_table,
+                          const float* scale_table, int32_t max_loras,
+                          int32_t max_rank, int32_t k_in, int32_t n_out,
+                          lora_bf16_t* xa, void* stream);
+
+/* Text of the last error returned on this host thread ("" if none). */
+const char* lora_last_error(void);
+
+/*
+ * Device status word: OR of LORA_DEV_* bits set by kernels on the current
+ * device since the last clear. Synchronizes `stream` (a test/diagnostic call,
+ * not for the hot path). clear != 0 resets the word after reading.
+ */
+int lora_read_device_status(void* stream, uint32_t* status_out, int clear);
+
+/*
+ * Launch geometry that lora_bgmv / lora_moe_grouped_fold would use (for
+ * tests and benchmarks). moe == 0: bgmv with `rows` = n; moe != 0: MoE with
+ * `rows` = row_end - row_offset. Writes [cluster, rows_per_tile, k_slice,
+ * j_slice, k_chunk, j_chunk, ring_stages, clusters, smem_bytes] to out[0..8].
+ */
+int lora_launch_geometry(int moe, int32_t rows, int32_t max_loras, int32_t max_rank,
+                         int32_t k_in, int32_t n_out, int64_t out[9]);
+
+/* ---- pure host helpers (no GPU) ------------------------------------------ */
+
+/*
+ * lora_grouped_down_wc — m-tile count of one window: max(1, ceil((row_end -
+ * row_offset) / LORA_MOE_M_TILE)); the MoE fold's tile grid.
+ * Defines: "Module moe_lora_grouped" rustdoc, `grouped_down_wc` entry.
+ * Returns -1 if row_end < row_offset.
+ */
+int32_t lora_grouped_down_wc(int32_t row_offset, int32_t row_end);
+
+/*
+ * lora_grouped_down_windows — contiguous [start, end) windows of `cap` rows
+ * covering 0..total_rows (the last may be shorter). Writes up to max_windows
+ * pairs into starts/ends (host arrays) and returns the number of windows, or
+ * -1 if cap < 1 or total_rows < 0, or -2 if max_windows is too small.
+ * total_rows == 0 gives 0 windows.
+ * Defines: "Module moe_lora_grouped" rustdoc, `grouped_down_windows` entry.
+ */
+int32_t lora_grouped_down_windows(int32_t total_rows, int32_t cap,
+                                  int32_t* starts, int32_t* ends, int32_t max_windows);
+
+/*
+ * lora_pack_expert_tables — dense per-expert tables from (expert_id, a, b,
+ * scale) entries: a_table[e], b_table[e], scale_table[e] for e < n_experts =
+ * max expert_id + 1, with 0 / 0 / 0.0f at experts without an entry; a later
+ * entry for the same expert replaces an earlier one. All arrays are host
+ * memory; table arrays hold table_len entries. Writes n_experts to
+ * *n_experts_out and returns 0; returns 1 (nothing written, *n_experts_out = 0)
+ * when n_entries == 0; -1 on a negative expert id or NULL argument; -2 when
+ * table_len < n_experts.
+ * Defines: "Module moe_lora_grouped" rustdoc, `pack_expert_tables` and
+ * `ExpertTables` entries.
+ */
+int lora_pack_expert_tables(const int32_t* expert_ids, const uint64_t* a_addrs,
+                            const uint64_t* b_addrs, const float* scales, int32_t n_entries,
+                            uint64_t* a_table, uint64_t* b_table, float* scale_table,
+                            int32_t table_len, int32_t* n_experts_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GATHER_LORA_H */

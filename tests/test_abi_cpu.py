@@ -1,0 +1,166 @@
+"""The C-ABI library on the CPU: it loads, exports every declared entry point,
+rejects bad arguments on the host before any CUDA call, and its pure helpers
+follow the MoE window / table rules. No kernel is launched here."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+from gather_lora_gb300 import lib as L
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gather_lora.h")
+FAKE = 0x100000            # a non-NULL, 16-byte aligned address that is never dereferenced
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not os.path.exists(L.LIB_PATH):
+        from gather_lora_gb300 import build
+        build.build()
+    L.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|int32_t|int)\s+(lora_\w+)\s*\(", src, re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("lora_bgmv", "lora_moe_grouped_fold", "lora_last_error", "lora_read_device_status",
+              "lora_launch_geometry", "lora_grouped_down_wc", "lora_grouped_down_windows",
+              "lora_pack_expert_tables"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(L.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    nm = subprocess.run(["nm", "-D", "--defined-only", L.LIB_PATH], capture_output=True, text=True)
+    if nm.returncode == 0:
+        exported = set(re.findall(r" T (lora_\w+)$", nm.stdout, re.M))
+        assert set(declared_functions()) <= exported
+
+
+def _bgmv(**kw):
+    a = dict(x=FAKE, xs=4096, out=FAKE, os=4096, seq=FAKE, n=4, at=FAKE, bt=FAKE, sc=FAKE, L=8,
+             R=16, k=4096, no=4096, xa=FAKE)
+    a.update(kw)
+    return L.load().lora_bgmv(a["x"], a["xs"], a["out"], a["os"], a["seq"], a["n"], a["at"],
+                              a["bt"], a["sc"], a["L"], a["R"], a["k"], a["no"], a["xa"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n=-1), -2), (dict(n=65537), -2), (dict(L=0), -2), (dict(L=5000), -2),
+    (dict(R=0), -2), (dict(R=264), -2), (dict(R=12), -4), (dict(k=4), -2), (dict(k=4100, xs=4104), -4),
+    (dict(no=4097, os=8192), -4), (dict(xs=4088), -3), (dict(os=100, no=128), -3),
+    (dict(xs=4100), -4), (dict(x=None), -1), (dict(out=None), -1), (dict(seq=None), -1),
+    (dict(at=None), -1), (dict(bt=None), -1), (dict(sc=None), -1), (dict(x=FAKE + 2), -4),
+    (dict(out=FAKE + 8), -4), (dict(xa=FAKE + 4), -4),
+])
+def test_bgmv_rejects_bad_arguments_before_launch(kw, code):
+    assert _bgmv(**kw) == code
+    assert L.lora_last_error()
+
+
+def test_bgmv_zero_rows_is_a_no_op():
+    assert _bgmv(n=0, x=None, out=None) == 0
+    assert L.lora_last_error() == ""
+
+
+def _moe(**kw):
+    a = dict(x=FAKE, xs=768, out=FAKE, os=2048, off=FAKE, E=128, sti=FAKE, te=16384, ra=FAKE,
+             nt=2048, lo=0, hi=4096, at=FAKE, bt=FAKE, sc=FAKE, L=16, R=16, k=768, no=2048, xa=FAKE)
+    a.update(kw)
+    return L.load().lora_moe_grouped_fold(a["x"], a["xs"], a["out"], a["os"], a["off"], a["E"],
+                                          a["sti"], a["te"], a["ra"], a["nt"], a["lo"], a["hi"],
+                                          a["at"], a["bt"], a["sc"], a["L"], a["R"], a["k"], a["no"],
+                                          a["xa"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(E=0), -2), (dict(E=1025), -2), (dict(L=0), -2), (dict(te=-1), -2),
+    (dict(lo=-1), -5), (dict(lo=10, hi=5), -5), (dict(hi=16385), -5), (dict(R=4), -2),
+    (dict(k=770, xs=776), -4), (dict(xs=700), -3), (dict(x=None), -1), (dict(off=None), -1),
+    (dict(sti=None), -1), (dict(at=None), -1), (dict(x=FAKE + 2), -4),
+])
+def test_moe_rejects_bad_arguments_before_launch(kw, code):
+    assert _moe(**kw) == code
+
+
+def test_grouped_down_wc():
+    assert L.lora_grouped_down_wc(0, 16384) == 256          # full window: ceil(te / 64)
+    assert L.lora_grouped_down_wc(0, 4096) == 64
+    assert L.lora_grouped_down_wc(4096, 4097) == 1
+    assert L.lora_grouped_down_wc(100, 100) == 1              # at least one tile
+    assert L.lora_grouped_down_wc(0, 65) == 2
+    assert L.lora_grouped_down_wc(5, 4) == -1
+    for lo, hi in [(0, 1), (3, 131), (64, 128), (7, 7000)]:
+        assert L.lora_grouped_down_wc(lo, hi) == max(1, -(-(hi - lo) // 64))
+
+
+def test_grouped_down_windows():
+    assert L.lora_grouped_down_windows(16384, 4096) == [(0, 4096), (4096, 8192), (8192, 12288), (12288, 16384)]
+    assert L.lora_grouped_down_windows(10, 4) == [(0, 4), (4, 8), (8, 10)]
+    assert L.lora_grouped_down_windows(0, 4) == []
+    assert L.lora_grouped_down_windows(3, 4096) == [(0, 3)]
+    with pytest.raises(ValueError):
+        L.lora_grouped_down_windows(10, 0)
+    rng = np.random.default_rng(0)
+    for _ in range(50):
+        total, cap = int(rng.integers(0, 5000)), int(rng.integers(1, 700))
+        w = L.lora_grouped_down_windows(total, cap)
+        covered = [r for lo, hi in w for r in range(lo, hi)]
+        assert covered == list(range(total))
+        assert all(0 < hi - lo <= cap for lo, hi in w)
+
+
+def test_pack_expert_tables():
+    assert L.lora_pack_expert_tables([]) is None
+    a, b, s = L.lora_pack_expert_tables([(2, 0x1000, 0x2000, 0.5), (0, 0x3000, 0x4000, 2.0)])
+    assert a == [0x3000, 0, 0x1000] and b == [0x4000, 0, 0x2000] and s == [2.0, 0.0, 0.5]
+    a, b, s = L.lora_pack_expert_tables([(1, 0x10, 0x20, 1.0), (1, 0x30, 0x40, 3.0)])
+    assert a == [0, 0x30] and b == [0, 0x40] and s == [0.0, 3.0]   # the last entry wins
+    with pytest.raises(ValueError):
+        L.lora_pack_expert_tables([(-1, 1, 2, 1.0)])
+    with pytest.raises(ValueError):
+        L.lora_pack_expert_tables([(5, 1, 2, 1.0)], table_len=3)
+
+
+def test_geometry_depends_on_shapes_only():
+    """The per-row arithmetic (cluster split, k chunks) must not depend on n."""
+    for (L_, R, k, no) in [(32, 16, 4096, 4096), (128, 64, 4096, 1024), (64, 128, 12288, 4096),
+                           (4, 8, 256, 256), (3, 256, 2056, 4096)]:
+        g1 = L.lora_launch_geometry(0, 1, L_, R, k, no)
+        g2 = L.lora_launch_geometry(0, 512, L_, R, k, no)
+        for key in ("cluster", "k_slice", "k_chunk", "j_slice", "j_chunk"):
+            assert g1[key] == g2[key]
+        assert g1["smem_bytes"] <= 227 * 1024
+        assert g1["k_chunk"] % 16 == 0 and g1["j_chunk"] % 16 == 0
+        assert g1["k_slice"] * g1["cluster"] >= k and g1["j_slice"] * g1["cluster"] >= no
+
+
+def test_bgmv_grid_bounds_every_routing():
+    """clusters = n/rt + min(n, max_loras) covers sum_s ceil(count_s / rt) for any routing."""
+    rng = np.random.default_rng(1)
+    for _ in range(200):
+        n, L_ = int(rng.integers(1, 600)), int(rng.integers(1, 300))
+        g = L.lora_launch_geometry(0, n, L_, 16, 1024, 1024)
+        rt = g["rows_per_tile"]
+        slots = rng.integers(-1, L_, size=n) if rng.random() < 0.5 else np.zeros(n, int)
+        counts = np.bincount(slots[slots >= 0], minlength=L_)
+        need = int(np.sum((counts + rt - 1) // rt))
+        assert need <= g["clusters"]
+
+
+def test_moe_geometry_tiles():
+    g = L.lora_launch_geometry(1, 4096, 129, 16, 768, 2048)
+    assert g["rows_per_tile"] == 64 and g["clusters"] == 64
+    assert L.lora_launch_geometry(1, 0, 129, 16, 768, 2048)["clusters"] == 1
