@@ -1,0 +1,562 @@
+#!/usr/bin/env python3
+"""Benchmark of the routed LoRA fold on GB300 (one JSON line on stdout).
+
+Headline workload: the decode q_proj routed bgmv (64 decode rows, k_in = n_out
+= 4096, 32 adapters at max_rank 16, Zipf(1.1) slots with 10% base rows). A step
+is one lora_bgmv call over one batch. The other three fold workloads (strided K
+fold into an interleaved QKV row, dense FFN down_proj, MoE grouped down fold)
+are measured the same way and reported under "workloads".
+
+Timing: inputs are resident in HBM; consecutive steps rotate through enough
+independent copies of every input (adapter pools included) to exceed 2x the L2
+size, so no step finds its data in L2. The K steps are replayed from CUDA graphs
+and timed with CUDA events on the launching stream, bracketed by a barrier and
+a device synchronize; with several ranks the time is the max over ranks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the reference arm of this comparison)
+on the host cores for the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "routed LoRA fold rows/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+HEADLINE = "decode_qproj_bgmv"
+SIDE_WORKLOADS = ("qkv_kfold_bgmv", "ffn_down_bgmv", "moe_down_fold")
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_NAMES = {"bgmv": "lora_bgmv_fold_kernel", "moe": "lora_moe_fold_kernel"}
+
+
+# ----------------------------------------------------------------- helpers
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    for rel in ("gather_lora_gb300/csrc/kernels.cu", "gather_lora_gb300/csrc/common.cuh",
+                "gather_lora_gb300/csrc/fold_types.h", "gather_lora_gb300/csrc/abi.cpp"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernels are unchanged."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_digest") != kernel_source_digest():
+        return None
+    v = d.get("workloads", {}).get(workload, {}).get("dram_bytes_per_launch")
+    return float(v) if v is not None else None
+
+
+def bgmv_algorithmic_bytes(wl) -> dict:
+    """Bytes one launch must move: each routed row's x row, out row read+write and
+    xa row write+read, plus each distinct routed adapter's padded A and B once,
+    plus the routing vector and the three table entries of each distinct slot."""
+    import numpy as np
+    routed = [(i, int(s)) for i, s in enumerate(wl.seq_slot) if 0 <= s < wl.max_loras and wl.present[s]]
+    slots = sorted({s for _, s in routed})
+    per_row = wl.k_in * 2 + wl.n_out * 2 * 2 + wl.max_rank * 2 * 2
+    per_adapter = wl.max_rank * wl.k_in * 2 + wl.n_out * wl.max_rank * 2
+    total = len(routed) * per_row + len(slots) * (per_adapter + 20) + wl.n * 4
+    return dict(bytes=int(total), routed_rows=len(routed), rows=int(wl.n), adapters=len(slots),
+                per_row=per_row, per_adapter=per_adapter,
+                flops=int(2 * len(routed) * wl.max_rank * (wl.k_in + wl.n_out)))
+
+
+def moe_algorithmic_bytes(wl) -> dict:
+    E = wl.num_experts
+    routed, pairs = 0, set()
+    for lo, hi in wl.windows():
+        for r in range(lo, hi):
+            e = int((wl.expert_offsets[1:] <= r).sum())
+            a = 0 if wl.row_adapter is None else int(wl.row_adapter[wl.sorted_token_ids[r]])
+            if a < 0 or a >= wl.max_loras or not wl.present[a * E + e]:
+                continue
+            routed += 1
+            pairs.add((a * E + e, lo))          # an adapter is read once per window it serves
+    per_row = wl.k_in * 2 + wl.n_out * 2 * 2 + wl.max_rank * 2 * 2 + 4 + 4
+    per_adapter = wl.max_rank * wl.k_in * 2 + wl.n_out * wl.max_rank * 2
+    total = routed * per_row + len(pairs) * (per_adapter + 20) + len(wl.windows()) * (E + 1) * 4
+    return dict(bytes=int(total), routed_rows=routed, rows=int(wl.te), adapters=len(pairs),
+                per_row=per_row, per_adapter=per_adapter,
+                flops=int(2 * routed * wl.max_rank * (wl.k_in + wl.n_out)))
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device_selector: str):
+        self.sel = device_selector
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", self.sel], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+            time.sleep(0.3)          # let the first sample land before the timed region
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def smi_selector(torch, dev) -> str:
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:
+        return str(getattr(dev, "index", 0) or 0)
+
+
+# ------------------------------------------------------------- device runs
+class BgmvRunner:
+    def __init__(self, wl, copies, device):
+        import torch
+        from gather_lora_gb300 import workloads as W
+        self.wl = wl
+        base = W.bgmv_to_device(wl, device)
+        self.copies = [base] + [self._clone(base, wl) for _ in range(copies - 1)]
+        self.launches_per_step = 1
+
+    @staticmethod
+    def _clone(d, wl):
+        import torch
+        from gather_lora_gb300 import workloads as W
+        a_pool, b_pool = d.a_pool.clone(), d.b_pool.clone()
+        out = d.out_buf.clone()
+        return W.DeviceBgmv(
+            x=d.x.clone(), out_buf=out, out_ptr=out.data_ptr() + 2 * wl.out_offset,
+            seq_slot=d.seq_slot.clone(), a_pool=a_pool, b_pool=b_pool,
+            a_table=W._table_of(a_pool, wl.present, a_pool.device),
+            b_table=W._table_of(b_pool, wl.present, b_pool.device), scale=d.scale.clone(),
+            xa=d.xa.clone())
+
+    def bytes_per_copy(self):
+        d = self.copies[0]
+        return sum(t.numel() * t.element_size() for t in (d.x, d.out_buf, d.a_pool, d.b_pool))
+
+    def step(self, c, stream):
+        from gather_lora_gb300 import lib as L
+        wl, d = self.wl, self.copies[c]
+        L.lora_bgmv(d.x, wl.x_row_stride, d.out_ptr, wl.out_row_stride, d.seq_slot, wl.n,
+                    d.a_table, d.b_table, d.scale, wl.max_loras, wl.max_rank, wl.k_in, wl.n_out,
+                    xa=d.xa, stream=stream)
+
+
+class MoeRunner:
+    def __init__(self, wl, copies, device):
+        from gather_lora_gb300 import workloads as W
+        self.wl = wl
+        self.windows = wl.windows()
+        self.copies = [W.moe_to_device(wl, device, xa_rows=wl.cap) for _ in range(copies)]
+        self.launches_per_step = len(self.windows)
+
+    def bytes_per_copy(self):
+        d = self.copies[0]
+        return sum(t.numel() * t.element_size() for t in (d.x, d.out_buf, d.a_pool, d.b_pool))
+
+    def step(self, c, stream):
+        from gather_lora_gb300 import lib as L
+        wl, d = self.wl, self.copies[c]
+        for lo, hi in self.windows:
+            L.lora_moe_grouped_fold(d.x, wl.k_in, d.out_buf, wl.n_out, d.expert_offsets,
+                                    wl.num_experts, d.sorted_token_ids, wl.te, d.row_adapter,
+                                    wl.num_tokens, lo, hi, d.a_table, d.b_table, d.scale,
+                                    wl.max_loras, wl.max_rank, wl.k_in, wl.n_out, xa=d.xa,
+                                    stream=stream)
+
+
+def copies_needed(bytes_per_copy, l2_bytes):
+    return max(1, min(64, math.ceil(2 * l2_bytes / max(bytes_per_copy, 1))))
+
+
+def time_steps(runner, steps, warmup, device, dist_ctx, sampler=None):
+    """Warm up, capture CUDA graphs over the rotating copies, time exactly `steps` steps."""
+    import torch
+    C = len(runner.copies)
+    stream = torch.cuda.Stream(device=device)
+    with torch.cuda.stream(stream):
+        for w in range(max(warmup, 1)):
+            runner.step(w % C, stream)
+    torch.cuda.synchronize(device)
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                runner.step(i % C, stream)
+        return g
+
+    per_graph = C * max(1, 64 // C) if C < 64 else C     # >= 64 launches per replay when cheap
+    full, tail = divmod(steps, per_graph)
+    g_full = capture(per_graph) if full else None
+    g_tail = capture(tail) if tail else None
+    for _ in range(2):                                   # graph warm-up (untimed)
+        if g_full:
+            g_full.replay()
+        if g_tail:
+            g_tail.replay()
+    torch.cuda.synchronize(device)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    dist_ctx.barrier()
+    torch.cuda.synchronize(device)
+    ctx = sampler if sampler is not None else _Null()
+    with ctx:
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(full):
+                g_full.replay()
+            if g_tail:
+                g_tail.replay()
+            end.record(stream)
+        torch.cuda.synchronize(device)
+    dist_ctx.barrier()
+    ms = start.elapsed_time(end)
+    return dist_ctx.max(ms), ms
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+class DistCtx:
+    """Barrier and max-over-ranks; a no-op with one process."""
+
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.dist = None
+        if self.world > 1:
+            import torch
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            dist.init_process_group(backend)
+            self.dist = dist
+            self.backend = backend
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, v: float) -> float:
+        return self._reduce(v, "max")
+
+    def sum(self, v: float) -> float:
+        return self._reduce(v, "sum")
+
+    def _reduce(self, v, op):
+        if self.dist is None:
+            return v
+        import torch
+        dev = f"cuda:{self.local_rank}" if self.backend == "nccl" else "cpu"
+        t = torch.tensor([float(v)], dtype=torch.float64, device=dev)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX if op == "max" else self.dist.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+
+
+def aggregate(rows_per_rank: float, ms_max: float, steps: int, n_ranks: int):
+    """Whole-job throughput: all ranks' rows over the slowest rank's time."""
+    total_rows = rows_per_rank * steps * n_ranks
+    return total_rows / (ms_max / 1e3), ms_max / steps
+
+
+# --------------------------------------------------------------- e2e
+def e2e_bgmv(wl, device, steps, warmup, copies):
+    """Same metric through the C ABI with host buffers: every step copies x,
+    seq_slot and base_out from pinned host memory, calls lora_bgmv, and reads
+    base_out back into pinned host memory; all inside the timed region."""
+    import numpy as np
+    import torch
+    from gather_lora_gb300 import lib as L
+    from gather_lora_gb300 import workloads as W
+    devs = [W.bgmv_to_device(wl, device) for _ in range(copies)]
+    hx = torch.from_numpy(wl.x.view(np.int16)).pin_memory()
+    hseq = torch.from_numpy(wl.seq_slot).pin_memory()
+    hout = torch.from_numpy(wl.out_buf.view(np.int16)).pin_memory()
+    hres = torch.empty_like(hout).pin_memory()
+    stream = torch.cuda.Stream(device=device)
+
+    def one(c):
+        d = devs[c % copies]
+        d.x.copy_(hx, non_blocking=True)
+        d.seq_slot.copy_(hseq, non_blocking=True)
+        d.out_buf.copy_(hout, non_blocking=True)
+        L.lora_bgmv(d.x, wl.x_row_stride, d.out_ptr, wl.out_row_stride, d.seq_slot, wl.n,
+                    d.a_table, d.b_table, d.scale, wl.max_loras, wl.max_rank, wl.k_in, wl.n_out,
+                    xa=d.xa, stream=stream)
+        hres.copy_(d.out_buf, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            one(i)
+    torch.cuda.synchronize(device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(steps):
+            one(i)
+        end.record(stream)
+    torch.cuda.synchronize(device)
+    ms = start.elapsed_time(end)
+    h2d = hx.numel() * 2 + hseq.numel() * 4 + hout.numel() * 2
+    d2h = hres.numel() * 2
+    return wl.n * steps / (ms / 1e3), h2d, d2h
+
+
+# ------------------------------------------------------------ CPU oracle
+def oracle_rows_per_s(wl, budget_s: float, rows_per_call=None):
+    """Time the single-threaded oracle on the host over a bounded sample of the
+    batch's rows; returns (rows/s, rows timed, seconds)."""
+    import numpy as np
+    import oracle
+    rows_per_call = rows_per_call or wl.n
+    t0 = time.perf_counter()
+    done = 0
+    i0 = 0
+    while True:
+        idx = np.arange(i0, i0 + rows_per_call) % wl.n
+        out = wl.out_buf[idx].copy()
+        seg = out.reshape(-1)[wl.out_offset:]
+        oracle.lora_bgmv(wl.x[idx].reshape(-1), wl.x_row_stride, seg, wl.out_row_stride,
+                         wl.seq_slot[idx], wl.a_list(), wl.b_list(), wl.scale, wl.max_rank,
+                         wl.k_in, wl.n_out)
+        done += rows_per_call
+        i0 = (i0 + rows_per_call) % wl.n
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return done / el, done, el
+
+
+def run_reference(args):
+    """CPU oracle arm: same workload, metric and unit, on the host cores."""
+    dctx = DistCtx()
+    if dctx.rank != 0:
+        dctx.close()
+        return 0
+    from gather_lora_gb300 import workloads as W
+    import oracle
+    wl = W.by_name(HEADLINE)
+    oracle.load()
+    # calibrate: seconds per row
+    _, n_cal, s_cal = oracle_rows_per_s(wl, 0.5, rows_per_call=4)
+    t_row = s_cal / n_cal
+    budget = 150.0
+    rows_per_step = int(max(1, min(wl.n, budget / max(args.steps + args.warmup, 1) / t_row)))
+    for _ in range(args.warmup):
+        oracle_rows_per_s(wl, 0.0, rows_per_call=rows_per_step)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_rows_per_s(wl, 0.0, rows_per_call=rows_per_step)
+    el = time.perf_counter() - t0
+    value = rows_per_step * args.steps / el
+    sample = f"{rows_per_step} of the {wl.n} decode rows per step (rotating), oracle on 1 host thread"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": HEADLINE, "n": wl.n, "k_in": wl.k_in, "n_out": wl.n_out,
+                   "max_loras": wl.max_loras, "max_rank": wl.max_rank},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    dctx.close()
+    return 0
+
+
+# ------------------------------------------------------------------- main
+def run_ours(args):
+    import torch
+    from gather_lora_gb300 import lib as L
+    from gather_lora_gb300 import workloads as W
+    dctx = DistCtx()
+    device = torch.device("cuda", dctx.local_rank)
+    torch.cuda.set_device(device)
+    L.load()
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20)
+    peak, peak_kind = measured_peaks()
+
+    # headline
+    head = args.only or HEADLINE
+    head_moe = head.startswith("moe")
+    wl = W.by_name(head)
+    alg = moe_algorithmic_bytes(wl) if head_moe else bgmv_algorithmic_bytes(wl)
+    mk = MoeRunner if head_moe else BgmvRunner
+    probe = mk(wl, 1, device)
+    C = copies_needed(probe.bytes_per_copy(), l2)
+    runner = probe if C == 1 else mk(wl, C, device)
+    del probe
+    sampler = ClockSampler(smi_selector(torch, device)) if dctx.rank == 0 else None
+    ms_max, ms_local = time_steps(runner, args.steps, args.warmup, device, dctx, sampler)
+    value, ms_per_step = aggregate(alg["rows"], ms_max, args.steps, dctx.world)
+    kernel_ms = ms_max / args.steps / runner.launches_per_step
+    achieved = alg["bytes"] / (kernel_ms / 1e3) / 1e9
+    clocks = sampler.summary() if sampler else None
+    launches = args.steps * runner.launches_per_step
+    if head_moe:
+        geometry = L.lora_launch_geometry(1, wl.cap, wl.num_experts + 1, wl.max_rank, wl.k_in, wl.n_out)
+    else:
+        geometry = L.lora_launch_geometry(0, wl.n, wl.max_loras, wl.max_rank, wl.k_in, wl.n_out)
+
+    # the other fold workloads (per-GPU numbers, same timing rules)
+    side = {}
+    for name in ([] if args.only else SIDE_WORKLOADS):
+        w2 = W.by_name(name)
+        is_moe = name.startswith("moe")
+        a2 = moe_algorithmic_bytes(w2) if is_moe else bgmv_algorithmic_bytes(w2)
+        mk = MoeRunner if is_moe else BgmvRunner
+        pr = mk(w2, 1, device)
+        c2 = copies_needed(pr.bytes_per_copy(), l2)
+        r2 = pr if c2 == 1 else mk(w2, c2, device)
+        del pr
+        # about 0.3 s of timed work, at least 20 steps
+        est_ms = a2["bytes"] / (0.8 * peak * 1e9) * 1e3 + 0.004 * r2.launches_per_step
+        k2 = int(max(20, min(20000, 300.0 / est_ms)))
+        m2, _ = time_steps(r2, k2, 5, device, dctx)
+        ms2 = m2 / k2
+        gbs2 = a2["bytes"] / (ms2 / 1e3) / 1e9
+        side[name] = {
+            "rows_per_s": a2["rows"] / (ms2 / 1e3), "routed_rows_per_s": a2["routed_rows"] / (ms2 / 1e3),
+            "ms_per_step": ms2, "launches_per_step": r2.launches_per_step, "steps": k2,
+            "algorithmic_bytes": a2["bytes"], "achieved_gbs": gbs2, "frac_of_peak": gbs2 / peak,
+            "frac_of_8tbs": gbs2 / 8000.0, "input_copies": len(r2.copies),
+            "traffic": recorded_traffic(name)}
+        del r2
+        torch.cuda.empty_cache()
+
+    # e2e through the C ABI with host buffers
+    e2e = None
+    if not head_moe:
+        e2e_steps = max(50, min(args.steps, 2000))
+        e2e_val, h2d, d2h = e2e_bgmv(wl, device, e2e_steps, 10, C)
+        e2e = {"value": dctx.sum(e2e_val), "unit": "rows/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+
+    cpu = None
+    if dctx.rank == 0 and not args.no_cpu_baseline and not head_moe:
+        v, n_rows, secs = oracle_rows_per_s(wl, args.cpu_seconds)
+        cpu = {"value": v, "unit": "rows/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n_rows} decode rows of the {HEADLINE} batch ({secs:.1f} s, 1 host thread)"}
+
+    if dctx.rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": dctx.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": head, "rows": alg["rows"], "routed_rows": alg["routed_rows"],
+                       "k_in": wl.k_in, "n_out": wl.n_out, "max_loras": wl.max_loras,
+                       "max_rank": wl.max_rank, "distinct_adapters": alg["adapters"],
+                       "parallelism": f"replicas{dctx.world}",
+                       "l2": f"rotating {C} input copies ({C * runner.bytes_per_copy() / 2**20:.0f} MiB > 2x L2)",
+                       "graph": "CUDA graph replay, programmatic dependent launch"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": recorded_traffic(head),
+                         "peak_kind": peak_kind, "kernel": KERNEL_NAMES["moe" if head_moe else "bgmv"],
+                         "algorithmic_bytes_per_launch": alg["bytes"],
+                         "kernel_ms": kernel_ms, "frac_of_8tbs": achieved / 8000.0},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "geometry": geometry,
+            "workloads": side,
+        }
+        print(json.dumps(line), flush=True)
+    dctx.close()
+    return 0
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100000)
+    p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--only", default=None, help="time one named workload alone (profiling runs)")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be >= 3")
+    return run_reference(args) if args.impl == "reference" else run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

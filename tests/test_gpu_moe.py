@@ -104,14 +104,16 @@ def test_moe_graph_replay_with_new_row_adapter():
                     cap=1024, seed=301)
     windows = wl.windows()
     d = W.moe_to_device(wl, xa_rows=wl.cap)
+    xa_w = torch.zeros((len(windows), wl.cap, wl.max_rank), dtype=torch.int16, device="cuda")
     s = torch.cuda.Stream()
 
     def run():
-        for lo, hi in windows:
+        for w, (lo, hi) in enumerate(windows):
             L.lora_moe_grouped_fold(d.x, wl.k_in, d.out_buf, wl.n_out, d.expert_offsets,
                                     wl.num_experts, d.sorted_token_ids, wl.te, d.row_adapter,
                                     wl.num_tokens, lo, hi, d.a_table, d.b_table, d.scale,
-                                    wl.max_loras, wl.max_rank, wl.k_in, wl.n_out, xa=None, stream=s)
+                                    wl.max_loras, wl.max_rank, wl.k_in, wl.n_out, xa=xa_w[w],
+                                    stream=s)
 
     with torch.cuda.stream(s):
         run()
@@ -132,5 +134,5 @@ def test_moe_graph_replay_with_new_row_adapter():
         torch.cuda.synchronize()
         o_out, o_xas, o_d = oracle_moe(wl, windows)
         routes = _routes_all(wl, windows)
-        # xa is not written in this test (NULL); compare the folds against the oracle's xa
-        compare_moe(wl, windows, to_u16(d.out_buf), o_out, o_xas, o_xas, o_d, routes)
+        g_xas = [to_u16(xa_w[w])[: hi - lo] for w, (lo, hi) in enumerate(windows)]
+        compare_moe(wl, windows, to_u16(d.out_buf), o_out, g_xas, o_xas, o_d, routes)
