@@ -40,58 +40,96 @@ inline int pow2_floor(int v) {
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Shared-memory budgets: two CTAs per SM, or one when the fixed part is large.
-constexpr int kBudgetTwoPerSm = 112 * 1024;
+// The tuning constants can be overridden at build time for measurement sweeps.
+#ifndef GLORA_BUDGET_TWO_PER_SM
+#define GLORA_BUDGET_TWO_PER_SM (112 * 1024)
+#endif
+#ifndef GLORA_STAGE_TARGET
+#define GLORA_STAGE_TARGET (40 * 1024)
+#endif
+#ifndef GLORA_MIN_STAGE
+#define GLORA_MIN_STAGE (24 * 1024)
+#endif
+#ifndef GLORA_MAX_CLUSTER
+#define GLORA_MAX_CLUSTER 8
+#endif
+#ifndef GLORA_MOE_GROUP_ROWS
+#define GLORA_MOE_GROUP_ROWS 16
+#endif
+constexpr int kBudgetTwoPerSm = GLORA_BUDGET_TWO_PER_SM;
 constexpr int kBudgetOnePerSm = 225 * 1024;
-constexpr int kStageTarget = 24 * 1024;
+constexpr int kStageTarget = GLORA_STAGE_TARGET;
+constexpr int kMinStage = GLORA_MIN_STAGE;
+constexpr int kMaxStages = 8;
+
+// Split `total` into equal chunks of at most `cap` (multiples of 16).
+int balanced_chunk(int total, int cap) {
+  cap = std::max(16, round_down(cap, 16));
+  const int n = static_cast<int>(ceil_div(total, cap));
+  return std::min(cap, round_up(static_cast<int>(ceil_div(total, n)), 16));
+}
 
 // Launch geometry. Depends only on the shapes (never on n, the routing or the
 // window), so a row's arithmetic — the k-slices, k-chunks and summation order —
 // is the same in every call with the same (k_in, n_out, max_rank).
-bool make_geometry(bool moe, int rows, int planner_ints, int max_rank, int k_in, int n_out,
-                   glora::FoldGeometry& g) {
+bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_rank, int k_in,
+                   int n_out, glora::FoldGeometry& g) {
   g = glora::FoldGeometry{};
-  if (moe) {
-    g.cl = pow2_floor(std::min(8, std::max(1, std::max(k_in, n_out) / 256)));
-    g.rt = LORA_MOE_M_TILE;
-  } else {
-    g.cl = pow2_floor(std::min(16, std::max(1, std::max(k_in, n_out) / 512)));
-    g.rt = max_rank <= 64 ? 32 : 16;
-  }
+  g.cl = pow2_floor(std::min(GLORA_MAX_CLUSTER, std::max(1, std::max(k_in, n_out) / 512)));
   g.mr16 = round_up(max_rank, 16);
   const int mt = g.mr16 / 16;
-  g.gmax = std::min(g.rt, 8 * (glora::kMaxTilesPerWarp * glora::kWarpsPerCta / mt));
+  const int tile_rows_cap = 8 * (glora::kMaxTilesPerWarp * glora::kConsumerWarps / mt);
+  if (moe) {
+    g.rt = LORA_MOE_M_TILE;
+    g.gmax = std::min(GLORA_MOE_GROUP_ROWS, tile_rows_cap);
+  } else {
+    g.rt = max_rank <= 64 ? 32 : 16;
+    g.gmax = std::min(g.rt, tile_rows_cap);
+  }
+  const int tiles = mt * static_cast<int>(ceil_div(g.gmax, 8));
+  g.maxt = 1;
+  while (g.maxt * glora::kConsumerWarps < tiles) g.maxt *= 2;
   g.ksl = round_up(static_cast<int>(ceil_div(k_in, g.cl)), 16);
   g.jsl = round_up(static_cast<int>(ceil_div(n_out, g.cl)), 16);
-  const int srows = g.mr16 + g.rt;
-  int kch = round_down((kStageTarget / srows - 16) / 2, 16);
-  g.kch = std::max(16, std::min(kch, g.ksl));
+  const int srows = g.mr16 + g.gmax;
+  int kcap = g.ksl;
+  if (srows * (kcap * 2 + 16) > kStageTarget) {
+    kcap = 16;
+    for (int c = 256; c >= 16; c /= 2)
+      if (c <= g.ksl && srows * (c * 2 + 16) <= kStageTarget) { kcap = c; break; }
+  }
+  g.kch = balanced_chunk(g.ksl, kcap);
   g.pitch_k = g.kch * 2 + 16;
   g.pitch_b = max_rank * 2 + (max_rank >= 32 ? 16 : 0);
   const int shrink_stage = srows * g.pitch_k;
-  g.jch = std::max(16, std::min(round_down(shrink_stage / g.pitch_b, 16), g.jsl));
-  g.stage_bytes = round_up(std::max(shrink_stage, g.jch * g.pitch_b), 128);
-  g.pitch_out = g.jsl * 2 + 16;
+  const int S = std::max(shrink_stage, kMinStage);
+  const int jcap = (S - 16 * g.gmax) / (g.pitch_b + 2 * g.gmax);
+  g.jch = balanced_chunk(g.jsl, std::min(jcap, g.jsl));
+  const int expand_stage = g.jch * g.pitch_b + g.gmax * (g.jch * 2 + 16);
+  g.stage_bytes = round_up(std::max(shrink_stage, expand_stage), 128);
   g.pitch_part = max_rank + 4;
   g.pitch_xa = max_rank * 2 + 16;
-  g.off_ring = glora::kPlanBytes;
-  const int fixed = glora::kPlanBytes + g.rt * g.pitch_out + g.rt * g.pitch_part * 4 + g.rt * g.pitch_xa;
+  const int fixed = glora::kPlanBytes + g.rt * g.pitch_part * 4 + g.rt * g.pitch_xa + glora::kWscrBytes;
   int ns = (kBudgetTwoPerSm - fixed) / g.stage_bytes;
-  if (ns < 3) ns = (kBudgetOnePerSm - fixed) / g.stage_bytes;
-  ns = std::min(ns, 8);
+  if (ns < 2) ns = (kBudgetOnePerSm - fixed) / g.stage_bytes;
+  ns = std::min(ns, kMaxStages);
   if (ns < 2) return false;
-  // the ring doubles as planning scratch (bgmv slot histogram / MoE offsets)
-  while (ns * g.stage_bytes < planner_ints * 4 && ns < 8) ++ns;
-  if (ns * g.stage_bytes < planner_ints * 4) g.stage_bytes = round_up(ceil_div(planner_ints * 4, ns), 128);
+  // the ring doubles as planning scratch (bgmv rows + slot counts / MoE offsets)
+  while (ns * g.stage_bytes < planner_ints * 4 && ns < kMaxStages) ++ns;
+  if (ns * g.stage_bytes < planner_ints * 4)
+    g.stage_bytes = round_up(static_cast<int>(ceil_div(planner_ints * 4, ns)), 128);
   g.ns = ns;
-  g.off_out = g.off_ring + ns * g.stage_bytes;
-  g.off_part = g.off_out + g.rt * g.pitch_out;
+  g.off_ring = glora::kPlanBytes;
+  g.off_out = 0;
+  g.off_part = g.off_ring + ns * g.stage_bytes;
   g.off_xa = g.off_part + g.rt * g.pitch_part * 4;
-  g.smem_bytes = g.off_xa + g.rt * g.pitch_xa;
+  g.off_wscr = g.off_xa + g.rt * g.pitch_xa;
+  g.smem_bytes = g.off_wscr + glora::kWscrBytes;
   if (g.smem_bytes > kBudgetOnePerSm + 2048) return false;
   if (moe) {
     g.clusters = static_cast<int>(std::max(1LL, ceil_div(rows, g.rt)));
   } else {
-    g.clusters = rows <= 0 ? 0 : rows / g.rt + std::min(rows, planner_ints);
+    g.clusters = rows <= 0 ? 0 : rows / g.rt + std::min(rows, max_loras);
   }
   return true;
 }
@@ -134,7 +172,7 @@ int lora_bgmv(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_t* base_out,
   if (!aligned16(x) || !aligned16(base_out) || (xa && !aligned16(xa)))
     return fail(LORA_ERR_ALIGN, "x, base_out and xa must be 16-byte aligned");
   glora::BgmvArgs a{};
-  if (!make_geometry(false, n, max_loras, max_rank, k_in, n_out, a.g))
+  if (!make_geometry(false, n, max_loras, ((n + 3) & ~3) + max_loras, max_rank, k_in, n_out, a.g))
     return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory for max_rank %d, k_in %d, n_out %d", max_rank, k_in, n_out);
   a.x = x;
   a.x_stride = x_row_stride;
@@ -177,7 +215,7 @@ int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_
   if (!aligned16(x) || !aligned16(base_out) || (xa && !aligned16(xa)))
     return fail(LORA_ERR_ALIGN, "x, base_out and xa must be 16-byte aligned");
   glora::MoeArgs a{};
-  if (!make_geometry(true, row_end - row_offset, num_experts + 1, max_rank, k_in, n_out, a.g))
+  if (!make_geometry(true, row_end - row_offset, max_loras, num_experts + 1, max_rank, k_in, n_out, a.g))
     return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory for max_rank %d, k_in %d, n_out %d", max_rank, k_in, n_out);
   a.x = x;
   a.x_stride = x_row_stride;
@@ -213,7 +251,9 @@ int lora_launch_geometry(int moe, int32_t rows, int32_t max_loras, int32_t max_r
   int rc = check_shape(max_rank, k_in, n_out, k_in, n_out);
   if (rc) return rc;
   glora::FoldGeometry g{};
-  if (!make_geometry(moe != 0, rows, max_loras, max_rank, k_in, n_out, g))
+  // MoE: max_loras carries num_experts + 1 (the offsets copied to shared memory)
+  const int scratch = moe ? max_loras : ((rows + 3) & ~3) + max_loras;
+  if (!make_geometry(moe != 0, rows, max_loras, scratch, max_rank, k_in, n_out, g))
     return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory");
   const int64_t v[9] = {g.cl, g.rt, g.ksl, g.jsl, g.kch, g.jch, g.ns, g.clusters, g.smem_bytes};
   std::memcpy(out, v, sizeof v);

@@ -1,19 +1,23 @@
 // Device helpers shared by the bgmv and MoE fold kernels (sm_103a).
 //
-// Everything here is a thin inline-PTX wrapper: 16-byte asynchronous global->
-// shared copies (cp.async.cg), shared-memory matrix loads (ldmatrix), BF16
-// tensor-core MMA with fp32 accumulation (mma.sync m16n8k16 / m16n8k8), and
-// programmatic-dependent-launch controls (griddepcontrol).
+// Everything here is a thin inline-PTX wrapper: mbarriers (with bounded
+// waits), 1-D TMA bulk copies global->shared (cp.async.bulk), 16-byte
+// asynchronous copies (cp.async.cg), shared-memory matrix loads (ldmatrix),
+// BF16 tensor-core MMA with fp32 accumulation (mma.sync m16n8k16 / m16n8k8),
+// and programmatic-dependent-launch controls (griddepcontrol).
 #pragma once
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "fold_types.h"
+
 namespace glora {
 
-constexpr int kThreads = 256;   // every fold kernel runs 8 warps per CTA
+constexpr int kThreads = (kConsumerWarps + kProducerWarps) * 32;
 constexpr int kWarps = kThreads / 32;
+constexpr long long kWaitLimitCycles = 4000000000LL;  // give up on an mbarrier after ~2 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -42,6 +46,61 @@ __device__ __forceinline__ void cp_async_wait(int n) {
   }
 }
 
+// ---- mbarriers and TMA bulk copies -----------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+// Test phase `parity` of an mbarrier. If it is not complete the thread is
+// suspended in hardware until it completes or `hint_ns` elapse, so waiting
+// warps do not spin on issue slots.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+// Wait for phase `parity` of an mbarrier; false after kWaitLimitCycles SM
+// clocks without it. The limit is measured with the SM-local cycle counter:
+// reading the global nanosecond timer costs about half a microsecond.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  constexpr uint32_t kHintNs = 1000000;
+  if (mbar_try_wait(bar, parity, kHintNs)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity, kHintNs)) {
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  }
+  return true;
+}
+
+// 1-D TMA copy of `bytes` (multiple of 16, both addresses 16-byte aligned)
+// from global to this CTA's shared memory, completing on mbarrier `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+               ::"r"(dst_smem), "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// Order this thread's generic-proxy shared-memory accesses before later
+// async-proxy (TMA) accesses of the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+// Barrier among the consumer warps only (named barrier 1).
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;\n" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
 // ---- shared-memory matrix fragments ----------------------------------------
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
@@ -56,6 +115,19 @@ __device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r
 }
 __device__ __forceinline__ void ldsm_x1(uint32_t addr, uint32_t& r0) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x1.shared.b16 {%0}, [%1];\n" : "=r"(r0) : "r"(addr));
+}
+
+// Transposing forms: with .trans, lane (g = lane/4, q = lane%4) exchanges the
+// pair [row 2q][col g], [row 2q+1][col g] of each 8x8 matrix (low half first),
+// which is the accumulator layout of an m16n8 tile whose N index is the row.
+__device__ __forceinline__ void ldsm_x2_trans(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];\n"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+__device__ __forceinline__ void stsm_x2_trans(uint32_t addr, uint32_t r0, uint32_t r1) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x2.trans.shared.b16 [%0], {%1,%2};\n" ::"r"(addr), "r"(r0), "r"(r1)
+               : "memory");
 }
 
 // ---- BF16 tensor-core MMA, fp32 accumulate ----------------------------------
@@ -119,9 +191,20 @@ __device__ __forceinline__ uint16_t fold_one(float acc, float scale, uint16_t ou
   const float d = bf16_bits_to_f32(f32_to_bf16_bits(acc));
   return f32_to_bf16_bits(__fmaf_rn(scale, d, bf16_bits_to_f32(out_bits)));
 }
+__device__ __forceinline__ uint32_t fold_one_bits(float acc, float scale, uint16_t out_bits) {
+  return fold_one(acc, scale, out_bits);
+}
 
-// Block-wide inclusive sum over the 256 threads (warp shuffles + 8 partials in
-// `warp_sums` shared scratch). Must be called by all threads.
+// The fold of two elements packed as BF16 pairs (low half first).
+__device__ __forceinline__ uint32_t fold_pair(float acc_lo, float acc_hi, float scale, uint32_t out2) {
+  const uint32_t lo = fold_one_bits(acc_lo, scale, static_cast<uint16_t>(out2 & 0xffffu));
+  const uint32_t hi = fold_one_bits(acc_hi, scale, static_cast<uint16_t>(out2 >> 16));
+  return lo | (hi << 16);
+}
+
+
+// Block-wide inclusive sum over all kThreads threads (warp shuffles + one
+// partial per warp in `warp_sums` shared scratch). Must be called by all threads.
 __device__ __forceinline__ int block_inclusive_sum(int v, int* warp_sums) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll

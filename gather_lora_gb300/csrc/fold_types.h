@@ -7,8 +7,10 @@ namespace glora {
 
 constexpr int kMaxRows = 64;        // rows (positions) per cluster work unit
 constexpr int kMaxTilesPerWarp = 8; // 16x8 shrink tiles a warp may own: MT * NT <= 64
-constexpr int kPlanBytes = 4096;    // shared memory reserved for the work-unit plan
-constexpr int kWarpsPerCta = 8;     // fold kernels run 256 threads per CTA
+constexpr int kPlanBytes = 5120;    // shared memory reserved for the work-unit plan
+constexpr int kConsumerWarps = 8;   // tensor-core / fold warps per CTA
+constexpr int kProducerWarps = 4;   // TMA-issuing warps per CTA (one warpgroup)
+constexpr int kWscrBytes = kConsumerWarps * 8 * 48;  // per-CTA transpose scratch of the consumer warps
 
 // Launch geometry and shared-memory layout of one fold launch. Every CTA of a
 // cluster of `cl` CTAs owns one k-slice of the shrink (ksl columns of A / x)
@@ -20,7 +22,8 @@ struct FoldGeometry {
   int ksl, jsl;     // k-slice / j-slice per CTA (multiples of 16)
   int kch, jch;     // k columns / B rows per ring stage (multiples of 16)
   int ns;           // ring depth (>= 2)
-  int gmax;         // most rows in one group (MT * ceil(gmax/8) <= 64 shrink tiles)
+  int gmax;         // most rows in one group (MT * ceil(gmax/8) <= 8 * maxt shrink tiles)
+  int maxt;         // shrink tiles per consumer warp the kernel instance holds (1, 2, 4, 8)
   int mr16;         // max_rank rounded up to 16
   int pitch_k;      // bytes per A or x row in a shrink stage (kch*2 + 16)
   int pitch_b;      // bytes per B row in an expand stage
@@ -28,7 +31,7 @@ struct FoldGeometry {
   int pitch_part;   // floats per partial-sum row (max_rank + 4)
   int pitch_xa;     // bytes per xa row (max_rank*2 + 16)
   int stage_bytes;
-  int off_ring, off_out, off_part, off_xa, smem_bytes;
+  int off_ring, off_out, off_part, off_xa, off_wscr, smem_bytes;
   int clusters;     // grid = clusters * cl CTAs
 };
 

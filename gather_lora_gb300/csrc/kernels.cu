@@ -11,20 +11,23 @@
 //     groups that share one adapter (bgmv: rows of one slot; MoE: the
 //     (adapter, expert) groups of a 64-row tile of sorted rows). Every CTA of
 //     the cluster builds the same plan from the routing data.
-//   * Shrink: CTA `rank` contracts its k-slice [rank*ksl, +ksl) of every
-//     group's A with the group's x rows on the tensor cores (mma.sync BF16,
-//     fp32 accumulate), adapter and activation chunks streaming through a
-//     cp.async ring so each adapter byte is read once per unit.
-//   * The fp32 partials of the cl k-slices are reduced in distributed shared
-//     memory in rank order (reduce-scatter), rounded to BF16 once, and the
-//     BF16 xa is pushed to every CTA of the cluster.
-//   * Expand + fold: CTA `rank` takes its j-slice of every group's B (streamed
-//     through the same ring, prefetched while the shrink finishes), computes
-//     d = bf16(xa @ B^T) on the tensor cores and folds
-//     out = bf16(fma(scale, d, out)) into a staged copy of the out rows, which
-//     is written back with 16-byte stores.
-// A row's fp32 summation order is fixed by (k_in, max_rank, cl): it never
-// depends on which other rows share its launch, group or tile.
+//   * A producer warpgroup per CTA streams the unit's data with 1-D TMA bulk
+//     copies into a ring of shared-memory stages (full / empty mbarriers);
+//     each item's copies are spread over its four warps, because the request
+//     rate of one issuing warp, not HBM, limits small copies:
+//     first [group, k-chunk] items (A rows of this CTA's k-slice and the
+//     group's x rows), then [group, j-chunk] items (B rows of this CTA's
+//     j-slice and the matching out-row segments).
+//   * Eight consumer warps contract each shrink item on the tensor cores
+//     (mma.sync BF16, fp32 accumulate). The fp32 partials of the cl k-slices
+//     are reduced in distributed shared memory in rank order (reduce-scatter),
+//     rounded to BF16 once, and the BF16 xa is pushed to every CTA.
+//   * For each expand item the consumers compute d = bf16(xa @ B^T), fold
+//     out = bf16(fma(scale, d, out)) against the staged out segment in
+//     registers, and store the result straight to global memory (the stage is
+//     only read, so it can be refilled by TMA without a proxy fence).
+// A row's fp32 summation order is fixed by (k_in, max_rank, cl, k chunking):
+// it never depends on which other rows share its launch, group or tile.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <limits.h>
@@ -40,11 +43,18 @@ __device__ unsigned int g_lora_status = 0;
 namespace glora {
 
 constexpr unsigned kDevMisaligned = 0x1u;
+constexpr unsigned kDevTimeout = 0x2u;
+constexpr int kMaxStages = 8;
+constexpr int kScratchPitch = 48;                    // bytes per row of a warp's transpose scratch
+constexpr int kScratchPerWarp = 8 * kScratchPitch;   // one 8-row x 16-column BF16 tile
 
 // Work-unit plan, identical in every CTA of a cluster.
 struct Plan {
+  unsigned long long full[kMaxStages];   // mbarriers: stage filled (TMA bytes landed)
+  unsigned long long empty[kMaxStages];  // mbarriers: stage released by the consumer warps
   int G;                           // groups (0: nothing to do)
   int NV;                          // valid positions (sum of group sizes)
+  int failed;                      // an mbarrier wait gave up: no further stores
   int warp_sums[kWarps];
   int found_slot, found_tile, found_rows;  // bgmv planning scratch
   int members[kMaxRows];           // positions, grouped, ascending within a group
@@ -52,6 +62,8 @@ struct Plan {
   int grow[kMaxRows];              // position -> row of x / base_out
   int xarow[kMaxRows];             // position -> row of xa
   int key[kMaxRows];               // MoE: table index of the position (INT_MAX: skipped)
+  int flag[kMaxRows];              // MoE: sorted index starts a group
+  unsigned ballots[2];
   float gscale[kMaxRows];
   float pscale[kMaxRows];
   const uint16_t* gA[kMaxRows];
@@ -71,119 +83,164 @@ struct EngineArgs {
   int max_rank, k_in, n_out;
 };
 
-// Shrink, cluster exchange, expand + fold for one planned work unit.
-__device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeometry& g, const Plan& pl,
+__device__ __forceinline__ void record_timeout(Plan& pl) {
+  atomicOr(&g_lora_status, kDevTimeout);
+  pl.failed = 1;
+}
+
+// Shrink, cluster exchange, expand + fold for one planned work unit. Called by
+// all kThreads threads of every CTA of the cluster. MAXT bounds the 16x8
+// shrink tiles one consumer warp owns (MT * ceil(group rows / 8) <= 8 * MAXT).
+template <int MAXT>
+__device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeometry& g, Plan& pl,
                                             unsigned char* smem, const cg::cluster_group& cluster,
                                             int crank) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   unsigned char* ring = smem + g.off_ring;
-  unsigned char* out_s = smem + g.off_out;
+  const uint32_t ring_u32 = smem_u32(ring);
   float* part_s = reinterpret_cast<float*>(smem + g.off_part);
   uint16_t* xa_s = reinterpret_cast<uint16_t*>(smem + g.off_xa);
   const int G = pl.G, NV = pl.NV;
-  const int xa_pitch_el = g.pitch_xa >> 1;
+  const int ns = g.ns;
 
   const int k_lo = crank * g.ksl, k_hi = min(k_lo + g.ksl, p.k_in);
   const int j_lo = crank * g.jsl, j_hi = min(j_lo + g.jsl, p.n_out);
   const int nk = k_hi > k_lo ? (k_hi - k_lo + g.kch - 1) / g.kch : 0;
   const int nj = j_hi > j_lo ? (j_hi - j_lo + g.jch - 1) / g.jch : 0;
   const int n_shrink = G * nk, n_items = G * (nk + nj);
-  const int jw = max(j_hi - j_lo, 0);
+  const int out_region = g.jch * g.pitch_b;   // byte offset of the out rows inside an expand stage
+  const int pitch_o = g.jch * 2 + 16;
 
-  // Prologue: this CTA's out segment of every valid row (needed at the end).
-  {
-    const int cpr = jw >> 3;
-    for (int q = tid; q < NV * cpr; q += kThreads) {
-      const int mi = q / cpr, c = q - mi * cpr, pos = pl.members[mi];
-      cp_async16(smem_u32(out_s + pos * g.pitch_out + c * 16),
-                 p.out + (long long)pl.grow[pos] * p.out_stride + j_lo + c * 8);
+  if (tid == 0) {
+    for (int s = 0; s < ns; ++s) {
+      mbar_init(smem_u32(&pl.full[s]), kProducerWarps);
+      mbar_init(smem_u32(&pl.empty[s]), kConsumerWarps);
     }
-    cp_async_commit();
+    pl.failed = 0;
+    mbar_fence_init();
   }
+  __syncthreads();
 
-  // Ring items: [group g, k-chunk] for the shrink, then [group g, j-chunk] for
-  // the expand. Item `it` lives in stage it % ns. Always commits a group so
-  // that the wait counts stay uniform.
-  auto issue = [&](int it) {
-    if (it < n_items) {
-      unsigned char* st = ring + (it % g.ns) * g.stage_bytes;
+  if (warp >= kConsumerWarps) {
+    // ===================== producer warpgroup =====================
+    const int pid = tid - kConsumerWarps * 32;  // 0 .. 32 * kProducerWarps - 1
+    constexpr int kP = kProducerWarps * 32;
+    auto produce = [&](int it) {
+      const int s = it % ns;
+      const uint32_t full = smem_u32(&pl.full[s]);
+      if (it >= ns && !mbar_wait(smem_u32(&pl.empty[s]), ((it / ns) - 1) & 1)) {
+        if (lane == 0) record_timeout(pl);
+      }
+      const uint32_t st = ring_u32 + s * g.stage_bytes;
       if (it < n_shrink) {
+        // copies: A rows 0..max_rank-1, then the group's x rows
         const int gi = it / nk, kc = it - gi * nk;
-        const int k0 = k_lo + kc * g.kch, klen = min(g.kch, k_hi - k0), cpr = klen >> 3;
+        const int k0 = k_lo + kc * g.kch, bytes = min(g.kch, k_hi - k0) * 2;
         const int m0 = pl.gstart[gi], R = pl.gstart[gi + 1] - m0;
-        const uint16_t* A = pl.gA[gi];
-        const int na = p.max_rank * cpr, tot = na + R * cpr;
-        for (int q = tid; q < tot; q += kThreads) {
-          if (q < na) {
-            const int c = q / cpr, ch = q - c * cpr;
-            cp_async16(smem_u32(st + c * g.pitch_k + ch * 16), A + (long long)c * p.k_in + k0 + ch * 8);
+        const int ncopy = p.max_rank + R;
+        int mine = 0;
+        for (int q = pid; q < ncopy; q += kP) mine += bytes;
+        mine = __reduce_add_sync(0xffffffffu, mine);
+        if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(mine));
+        __syncwarp();
+        const uint16_t* A = pl.gA[gi] + k0;
+        for (int q = pid; q < ncopy; q += kP) {
+          if (q < p.max_rank) {
+            bulk_g2s(st + q * g.pitch_k, A + (long long)q * p.k_in, bytes, full);
           } else {
-            const int qq = q - na, r = qq / cpr, ch = qq - r * cpr;
-            cp_async16(smem_u32(st + (g.mr16 + r) * g.pitch_k + ch * 16),
-                       p.x + (long long)pl.grow[pl.members[m0 + r]] * p.x_stride + k0 + ch * 8);
+            const int r = q - p.max_rank;
+            bulk_g2s(st + (g.mr16 + r) * g.pitch_k,
+                     p.x + (long long)pl.grow[pl.members[m0 + r]] * p.x_stride + k0, bytes, full);
           }
         }
       } else {
+        // copies: B (one contiguous chunk, or one per row when rows are padded), then out rows
         const int e = it - n_shrink, gi = e / nj, jc = e - gi * nj;
-        const int j0 = j_lo + jc * g.jch, jlen = min(g.jch, j_hi - j0), cpr = p.max_rank >> 3;
-        const uint16_t* B = pl.gB[gi];
-        for (int q = tid; q < jlen * cpr; q += kThreads) {
-          const int j = q / cpr, ch = q - j * cpr;
-          cp_async16(smem_u32(st + j * g.pitch_b + ch * 16), B + (long long)(j0 + j) * p.max_rank + ch * 8);
-        }
-      }
-    }
-    cp_async_commit();
-  };
-  for (int it = 0; it < g.ns - 1; ++it) issue(it);
-
-  // ---- shrink: fp32 partial xa of this k-slice ------------------------------
-  const int MT = g.mr16 >> 4;
-  float acc[kMaxTilesPerWarp][4];
-#pragma unroll
-  for (int i = 0; i < kMaxTilesPerWarp; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-  if (nk == 0) {  // empty k-slice: the partials are zero
-    for (int e = tid; e < NV * p.max_rank; e += kThreads) {
-      const int mi = e / p.max_rank, c = e - mi * p.max_rank;
-      part_s[pl.members[mi] * g.pitch_part + c] = 0.f;
-    }
-  }
-  for (int it = 0; it < n_shrink; ++it) {
-    cp_async_wait(g.ns - 2);
-    __syncthreads();
-    issue(it + g.ns - 1);
-    const int gi = it / nk, kc = it - gi * nk;
-    const int m0 = pl.gstart[gi], R = pl.gstart[gi + 1] - m0, NT = (R + 7) >> 3, ntiles = MT * NT;
-    const int k0 = k_lo + kc * g.kch, klen = min(g.kch, k_hi - k0);
-    const uint32_t st_a = smem_u32(ring + (it % g.ns) * g.stage_bytes);
-    const uint32_t st_x = st_a + g.mr16 * g.pitch_k;
-    for (int kk = 0; kk < klen; kk += 16) {
-      const int kstep = min(16, klen - kk);
-#pragma unroll
-      for (int i = 0; i < kMaxTilesPerWarp; ++i) {
-        const int t = warp + i * kWarps;
-        if (t < ntiles) {
-          const int mt = t % MT, nt = t / MT;
-          mma_step(acc[i], st_a + (mt * 16 + (lane & 15)) * g.pitch_k + kk * 2,
-                   st_x + (nt * 8 + (lane & 7)) * g.pitch_k + kk * 2, kstep, lane);
-        }
-      }
-    }
-    if (kc == nk - 1) {  // group complete: partials -> shared memory
-#pragma unroll
-      for (int i = 0; i < kMaxTilesPerWarp; ++i) {
-        const int t = warp + i * kWarps;
-        if (t < ntiles) {
-          const int mt = t % MT, nt = t / MT;
-          const int c0 = mt * 16 + (lane >> 2), r0 = nt * 8 + 2 * (lane & 3);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const int c = c0 + (v >> 1) * 8, r = r0 + (v & 1);
-            if (c < p.max_rank && r < R) part_s[pl.members[m0 + r] * g.pitch_part + c] = acc[i][v];
+        const int j0 = j_lo + jc * g.jch, jlen = min(g.jch, j_hi - j0);
+        const int m0 = pl.gstart[gi], R = pl.gstart[gi + 1] - m0;
+        const int brow = p.max_rank * 2;
+        const bool contiguous = g.pitch_b == brow;
+        const int nb = contiguous ? 1 : jlen;
+        const int ncopy = nb + R;
+        int mine = 0;
+        for (int q = pid; q < ncopy; q += kP) mine += q < nb ? (contiguous ? jlen * brow : brow) : jlen * 2;
+        mine = __reduce_add_sync(0xffffffffu, mine);
+        if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(mine));
+        __syncwarp();
+        const uint16_t* B = pl.gB[gi] + (long long)j0 * p.max_rank;
+        for (int q = pid; q < ncopy; q += kP) {
+          if (q < nb) {
+            if (contiguous) bulk_g2s(st, B, jlen * brow, full);
+            else bulk_g2s(st + q * g.pitch_b, B + (long long)q * p.max_rank, brow, full);
+          } else {
+            const int r = q - nb;
+            bulk_g2s(st + out_region + r * pitch_o,
+                     p.out + (long long)pl.grow[pl.members[m0 + r]] * p.out_stride + j0, jlen * 2, full);
           }
         }
-        acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
       }
+    };
+    // Items whose stage is freed by shrink work can be issued before the
+    // cluster exchange; the rest only after it (their stages are released by
+    // expand work, which needs the exchanged xa).
+    const int pre = min(n_items, n_shrink + ns);
+    for (int it = 0; it < pre; ++it) produce(it);
+    cluster.sync();
+    cluster.sync();
+    for (int it = pre; it < n_items; ++it) produce(it);
+    return;
+  }
+
+  // ========================= consumer warps =========================
+  const int MT = g.mr16 >> 4;
+  int it = 0;
+  for (int gi = 0; gi < G && nk > 0; ++gi) {
+    const int m0 = pl.gstart[gi], R = pl.gstart[gi + 1] - m0, NT = (R + 7) >> 3, ntiles = MT * NT;
+    uint32_t a_off[MAXT], x_off[MAXT];
+    float acc[MAXT][4];
+#pragma unroll
+    for (int i = 0; i < MAXT; ++i) {
+      const int t = warp + i * kConsumerWarps;
+      const int mt = t % MT, nt = t / MT;
+      a_off[i] = (mt * 16 + (lane & 15)) * g.pitch_k;
+      x_off[i] = (g.mr16 + nt * 8 + (lane & 7)) * g.pitch_k;
+      acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    }
+    for (int kc = 0; kc < nk; ++kc, ++it) {
+      const int s = it % ns;
+      if (!mbar_wait(smem_u32(&pl.full[s]), (it / ns) & 1) && lane == 0) record_timeout(pl);
+      const uint32_t st = ring_u32 + s * g.stage_bytes;
+      const int klen = min(g.kch, k_hi - (k_lo + kc * g.kch));
+      for (int kk = 0; kk < klen; kk += 16) {
+        const int kstep = min(16, klen - kk);
+#pragma unroll
+        for (int i = 0; i < MAXT; ++i) {
+          if (warp + i * kConsumerWarps < ntiles)
+            mma_step(acc[i], st + a_off[i] + kk * 2, st + x_off[i] + kk * 2, kstep, lane);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&pl.empty[s]));
+    }
+    // group complete: this k-slice's partial sums -> shared memory
+#pragma unroll
+    for (int i = 0; i < MAXT; ++i) {
+      const int t = warp + i * kConsumerWarps;
+      if (t < ntiles) {
+        const int mt = t % MT, nt = t / MT;
+        const int c0 = mt * 16 + (lane >> 2), r0 = nt * 8 + 2 * (lane & 3);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int c = c0 + (v >> 1) * 8, r = r0 + (v & 1);
+          if (c < p.max_rank && r < R) part_s[pl.members[m0 + r] * g.pitch_part + c] = acc[i][v];
+        }
+      }
+    }
+  }
+  if (nk == 0) {  // empty k-slice: the partials are zero
+    for (int e = tid; e < NV * p.max_rank; e += kConsumerWarps * 32) {
+      const int mi = e / p.max_rank, c = e - mi * p.max_rank;
+      part_s[pl.members[mi] * g.pitch_part + c] = 0.f;
     }
   }
 
@@ -192,69 +249,83 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
   {
     const int E = NV * p.max_rank, per = (E + g.cl - 1) / g.cl;
     const int e_lo = crank * per, e_hi = min(e_lo + per, E);
-    for (int e = e_lo + tid; e < e_hi; e += kThreads) {
+    const int xa_pitch_el = g.pitch_xa >> 1;
+    const bool store = pl.failed == 0;
+    for (int e = e_lo + tid; e < e_hi; e += kConsumerWarps * 32) {
       const int mi = e / p.max_rank, c = e - mi * p.max_rank, pos = pl.members[mi];
       const int off = pos * g.pitch_part + c;
-      float s = cluster.map_shared_rank(part_s, 0)[off];
-      for (int q = 1; q < g.cl; ++q) s += cluster.map_shared_rank(part_s, q)[off];
-      const uint16_t xb = f32_to_bf16_bits(s);
+      float sum = cluster.map_shared_rank(part_s, 0)[off];
+      for (int q = 1; q < g.cl; ++q) sum += cluster.map_shared_rank(part_s, q)[off];
+      const uint16_t xb = f32_to_bf16_bits(sum);
       const int xoff = pos * xa_pitch_el + c;
       for (int q = 0; q < g.cl; ++q) cluster.map_shared_rank(xa_s, q)[xoff] = xb;
-      if (p.xa) p.xa[(long long)pl.xarow[pos] * p.max_rank + c] = xb;
+      if (p.xa && store) p.xa[(long long)pl.xarow[pos] * p.max_rank + c] = xb;
     }
   }
   cluster.sync();
 
   // ---- expand + fold over this CTA's j-slice ---------------------------------
+  // Per 16x8 tile (16 output columns x 8 rows): d = bf16(B_tile @ xa^T) on the
+  // tensor cores, the staged old out values enter in accumulator layout through
+  // ldmatrix.trans, the fold runs in registers, stmatrix.trans turns the BF16
+  // result row-major in a warp-private scratch, and each row leaves with one
+  // 16-byte store. The TMA-filled stage is only read.
   const uint32_t xa_base = smem_u32(xa_s);
-  for (int it = n_shrink; it < n_items; ++it) {
-    cp_async_wait(g.ns - 2);
-    __syncthreads();
-    issue(it + g.ns - 1);
-    const int e = it - n_shrink, gi = e / nj, jc = e - gi * nj;
+  const uint32_t wscr = smem_u32(smem + g.off_wscr) + warp * kScratchPerWarp;
+  it = n_shrink;
+  for (int gi = 0; gi < G; ++gi) {
     const int m0 = pl.gstart[gi], R = pl.gstart[gi + 1] - m0, NT = (R + 7) >> 3;
-    const int j0 = j_lo + jc * g.jch, jlen = min(g.jch, j_hi - j0), MTj = (jlen + 15) >> 4;
-    const int tiles = MTj * NT;
     const float scale = pl.gscale[gi];
-    const uint32_t st_b = smem_u32(ring + (it % g.ns) * g.stage_bytes);
-    for (int t = warp; t < tiles; t += kWarps) {
-      const int mt = t % MTj, nt = t / MTj;
-      const int bpos = pl.members[m0 + min(nt * 8 + (lane & 7), R - 1)];
-      float d4[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int kk = 0; kk < p.max_rank; kk += 16) {
-        mma_step(d4, st_b + (mt * 16 + (lane & 15)) * g.pitch_b + kk * 2,
-                 xa_base + bpos * g.pitch_xa + kk * 2, min(16, p.max_rank - kk), lane);
-      }
-      const int jj0 = mt * 16 + (lane >> 2), rr0 = nt * 8 + 2 * (lane & 3);
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        const int jj = jj0 + (v >> 1) * 8, rr = rr0 + (v & 1);
-        if (jj < jlen && rr < R) {
-          uint16_t* o = reinterpret_cast<uint16_t*>(out_s + pl.members[m0 + rr] * g.pitch_out) + (j0 - j_lo) + jj;
-          *o = fold_one(d4[v], scale, *o);
+    for (int jc = 0; jc < nj; ++jc, ++it) {
+      const int s = it % ns;
+      if (!mbar_wait(smem_u32(&pl.full[s]), (it / ns) & 1) && lane == 0) record_timeout(pl);
+      const uint32_t st = ring_u32 + s * g.stage_bytes;
+      const int j0 = j_lo + jc * g.jch, jlen = min(g.jch, j_hi - j0), MTj = (jlen + 15) >> 4;
+      const bool store = pl.failed == 0;
+      for (int nt = 0; nt < NT; ++nt) {
+        // mma B operand: xa row of this lane's column (rows past R repeat the last one)
+        const uint32_t xrow = xa_base + pl.members[m0 + min(nt * 8 + (lane & 7), R - 1)] * g.pitch_xa;
+        // ldmatrix.trans source: staged out row (lane & 7), second 8 columns for lanes 8..15
+        const uint32_t orow = st + out_region + (nt * 8 + (lane & 7)) * pitch_o + ((lane >> 3) & 1) * 16;
+        // this lane's output row for the final 16-byte stores (lanes 0..15)
+        const int srow = nt * 8 + (lane >> 1);
+        uint16_t* gout = nullptr;
+        if (lane < 16 && srow < R)
+          gout = p.out + (long long)pl.grow[pl.members[m0 + srow]] * p.out_stride + j0 + (lane & 1) * 8;
+        for (int mt = warp; mt < MTj; mt += kConsumerWarps) {
+          float d4[4] = {0.f, 0.f, 0.f, 0.f};
+          const uint32_t brow = st + (mt * 16 + (lane & 15)) * g.pitch_b;
+          for (int kk = 0; kk < p.max_rank; kk += 16)
+            mma_step(d4, brow + kk * 2, xrow + kk * 2, min(16, p.max_rank - kk), lane);
+          uint32_t o0, o1;
+          ldsm_x2_trans(orow + mt * 32, o0, o1);
+          const uint32_t f0 = fold_pair(d4[0], d4[1], scale, o0);
+          const uint32_t f1 = fold_pair(d4[2], d4[3], scale, o1);
+          stsm_x2_trans(wscr + (lane & 7) * kScratchPitch + ((lane >> 3) & 1) * 16, f0, f1);
+          __syncwarp();
+          if (gout && store && mt * 16 + (lane & 1) * 8 < jlen) {
+            uint4 v;
+            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                         : "r"(wscr + (lane >> 1) * kScratchPitch + (lane & 1) * 16));
+            *reinterpret_cast<uint4*>(gout + mt * 16) = v;
+          }
+          __syncwarp();
         }
       }
-    }
-  }
-  cp_async_wait(0);
-  __syncthreads();
-
-  // ---- write the folded out segments back -----------------------------------
-  {
-    const int cpr = jw >> 3;
-    for (int q = tid; q < NV * cpr; q += kThreads) {
-      const int mi = q / cpr, c = q - mi * cpr, pos = pl.members[mi];
-      const uint4 v = *reinterpret_cast<const uint4*>(out_s + pos * g.pitch_out + c * 16);
-      *reinterpret_cast<uint4*>(p.out + (long long)pl.grow[pos] * p.out_stride + j_lo + c * 8) = v;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&pl.empty[s]));
     }
   }
 }
 
 // ============================================================================
 // Routed bgmv: work unit = up to rt rows of one slot, in ascending row order.
-// Units are numbered slot by slot (ascending slot, then ascending tile), so the
-// static grid bound is n/rt + min(n, max_loras) units.
+// Units are numbered slot by slot (ascending slot, then ascending tile) over
+// every slot that has rows, so the static grid bound is n/rt + min(n, max_loras)
+// units; a unit whose slot has a NULL table entry finds nothing to do.
 // ============================================================================
+template <int MAXT>
 __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __grid_constant__ BgmvArgs p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const FoldGeometry& g = p.g;
@@ -266,27 +337,16 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
 
   pdl_wait_then_release();
 
-  // Routed rows per slot (histogram in the not-yet-used ring).
-  int* cnt = reinterpret_cast<int*>(smem + g.off_ring);
+  // seq_slot and the per-slot row counts live in the not-yet-used ring.
+  int* ss = reinterpret_cast<int*>(smem + g.off_ring);
+  int* cnt = ss + ((p.n + 3) & ~3);
+  for (int i = tid; i < p.n; i += kThreads) ss[i] = p.seq_slot[i];
   for (int s = tid; s < p.max_loras; s += kThreads) cnt[s] = 0;
   if (tid == 0) pl.found_slot = -1;
   __syncthreads();
   for (int i = tid; i < p.n; i += kThreads) {
-    const int s = p.seq_slot[i];
+    const int s = ss[i];
     if (s >= 0 && s < p.max_loras) atomicAdd(&cnt[s], 1);
-  }
-  __syncthreads();
-  for (int s = tid; s < p.max_loras; s += kThreads) {
-    if (cnt[s] > 0) {
-      const uintptr_t a = reinterpret_cast<uintptr_t>(p.a_table[s]);
-      const uintptr_t b = reinterpret_cast<uintptr_t>(p.b_table[s]);
-      if (a == 0 || b == 0) {
-        cnt[s] = 0;
-      } else if ((a | b) & 15u) {
-        cnt[s] = 0;
-        if (unit == 0 && crank == 0) atomicOr(&g_lora_status, kDevMisaligned);
-      }
-    }
   }
   __syncthreads();
   // Units per slot, prefix over slots, locate this cluster's (slot, tile).
@@ -310,13 +370,20 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
   const int slot = pl.found_slot;
   if (slot < 0) return;  // every CTA of the cluster takes this branch together
   const int R = pl.found_rows, want_lo = pl.found_tile * g.rt;
-
+  const uint16_t* tab_a = nullptr;  // table entries: the loads overlap the row compaction below
+  const uint16_t* tab_b = nullptr;
+  float tab_s = 0.f;
+  if (tid == 0) {
+    tab_a = p.a_table[slot];
+    tab_b = p.b_table[slot];
+    tab_s = p.scale_table[slot];
+  }
   // Rows of this slot in ascending order; keep ranks [want_lo, want_lo + R).
   {
     int base = 0;
     for (int i0 = 0; i0 < p.n; i0 += kThreads) {
       const int i = i0 + tid;
-      const bool f = (i < p.n) && (p.seq_slot[i] == slot);
+      const bool f = (i < p.n) && (ss[i] == slot);
       const unsigned bal = __ballot_sync(0xffffffffu, f);
       if (lane == 0) pl.warp_sums[warp] = __popc(bal);
       __syncthreads();
@@ -339,24 +406,35 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
     }
   }
   if (tid == 0) {
-    pl.G = 1;
+    pl.gA[0] = tab_a;
+    pl.gB[0] = tab_b;
+    pl.gscale[0] = tab_s;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(tab_a), b = reinterpret_cast<uintptr_t>(tab_b);
+    int G = 1;
+    if (a == 0 || b == 0) {
+      G = 0;
+    } else if ((a | b) & 15u) {
+      G = 0;
+      if (crank == 0) atomicOr(&g_lora_status, kDevMisaligned);
+    }
+    pl.G = G;
     pl.NV = R;
     pl.gstart[0] = 0;
     pl.gstart[1] = R;
-    pl.gA[0] = p.a_table[slot];
-    pl.gB[0] = p.b_table[slot];
-    pl.gscale[0] = p.scale_table[slot];
   }
   __syncthreads();
+  if (pl.G == 0) return;  // NULL or misaligned adapter: rows stay unchanged
 
   const EngineArgs ea{p.x, p.x_stride, p.out, p.out_stride, p.xa, p.max_rank, p.k_in, p.n_out};
-  fold_engine(ea, g, pl, smem, cluster, crank);
+  fold_engine<MAXT>(ea, g, pl, smem, cluster, crank);
 }
 
 // ============================================================================
 // MoE grouped fold: work unit = one 64-row tile of the window's sorted rows,
-// split into (adapter, expert) groups; grid = ceil(window / 64) tiles (>= 1).
+// split into (adapter, expert) groups of at most gmax rows; grid =
+// ceil(window / 64) tiles (>= 1).
 // ============================================================================
+template <int MAXT>
 __global__ void __launch_bounds__(kThreads, 2) lora_moe_fold_kernel(const __grid_constant__ MoeArgs p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const FoldGeometry& g = p.g;
@@ -373,6 +451,8 @@ __global__ void __launch_bounds__(kThreads, 2) lora_moe_fold_kernel(const __grid
   const int T = min(g.rt, p.row_end - r0);
   int* offs = reinterpret_cast<int*>(smem + g.off_ring);  // expert_offsets copy (ring not yet used)
   for (int i = tid; i <= E; i += kThreads) offs[i] = p.expert_offsets[i];
+  int token = -1;
+  if (p.row_adapter && tid < T) token = p.sorted_token_ids[r0 + tid];   // overlaps the offsets load
   __syncthreads();
 
   // Per position: expert by binary search, adapter gate, table entry.
@@ -390,8 +470,7 @@ __global__ void __launch_bounds__(kThreads, 2) lora_moe_fold_kernel(const __grid
         int a = 0;
         bool ok = true;
         if (p.row_adapter) {
-          const int t = p.sorted_token_ids[r];
-          if (t < 0 || t >= p.num_tokens) ok = false; else a = p.row_adapter[t];
+          if (token < 0 || token >= p.num_tokens) ok = false; else a = p.row_adapter[token];
         }
         if (ok && a >= 0 && a < p.max_loras) {
           const int idx = a * E + e;
@@ -416,43 +495,55 @@ __global__ void __launch_bounds__(kThreads, 2) lora_moe_fold_kernel(const __grid
     pl.xarow[tid] = r - p.row_offset;
   }
   __syncthreads();
-  // Stable sort of the valid positions by table index.
+  // Stable sort of the valid positions by table index; a group starts at the
+  // first position of each index and again after every gmax rows of it.
   int nv = 0;
   {
     int k = INT_MAX;
     if (tid < g.rt) {
       k = pl.key[tid];
-      int rank = 0;
+      int rank = 0, same_before = 0;
       for (int u = 0; u < g.rt; ++u) {
         const int ku = pl.key[u];
         rank += (ku < k) || (ku == k && u < tid);
+        same_before += (ku == k && u < tid);
       }
-      if (k != INT_MAX) pl.members[rank] = tid;
+      if (k != INT_MAX) {
+        pl.members[rank] = tid;
+        pl.flag[rank] = (same_before % g.gmax) == 0;
+      }
     }
     nv = __syncthreads_count(tid < g.rt && k != INT_MAX);
   }
   if (nv == 0) return;  // every CTA of the cluster takes this branch together
-  if (tid == 0) {
-    int G = 0, prev = INT_MAX;
-    for (int i = 0; i < nv; ++i) {
-      const int pos = pl.members[i], k = pl.key[pos];
-      if (i == 0 || k != prev || i - pl.gstart[G - 1] >= g.gmax) {
-        pl.gstart[G] = i;
-        pl.gA[G] = pl.pA[pos];
-        pl.gB[G] = pl.pB[pos];
-        pl.gscale[G] = pl.pscale[pos];
-        ++G;
-        prev = k;
-      }
+  if (tid < kMaxRows) {
+    const bool f = tid < nv && pl.flag[tid];
+    const unsigned bal = __ballot_sync(0xffffffffu, f);
+    if ((tid & 31) == 0) pl.ballots[tid >> 5] = bal;
+  }
+  __syncthreads();
+  if (tid < nv) {
+    const unsigned b0 = pl.ballots[0], b1 = pl.ballots[1];
+    const unsigned below = tid < 32 ? (b0 & ((1u << tid) - 1u)) : b0;
+    const int gid = __popc(below) + (tid < 32 ? 0 : __popc(b1 & ((1u << (tid - 32)) - 1u)));
+    if (pl.flag[tid]) {
+      const int pos = pl.members[tid];
+      pl.gstart[gid] = tid;
+      pl.gA[gid] = pl.pA[pos];
+      pl.gB[gid] = pl.pB[pos];
+      pl.gscale[gid] = pl.pscale[pos];
     }
-    pl.gstart[G] = nv;
-    pl.G = G;
-    pl.NV = nv;
+    if (tid == 0) {
+      const int G = __popc(b0) + __popc(b1);
+      pl.G = G;
+      pl.NV = nv;
+      pl.gstart[G] = nv;
+    }
   }
   __syncthreads();
 
   const EngineArgs ea{p.x, p.x_stride, p.out, p.out_stride, p.xa, p.max_rank, p.k_in, p.n_out};
-  fold_engine(ea, g, pl, smem, cluster, crank);
+  fold_engine<MAXT>(ea, g, pl, smem, cluster, crank);
 }
 
 // ============================================================================
@@ -462,6 +553,7 @@ template <typename Args>
 static int launch_fold(void (*kernel)(Args), const Args& a, void* stream) {
   const FoldGeometry& g = a.g;
   if (g.clusters <= 0) return 0;
+  if (g.ns > kMaxStages) return static_cast<int>(cudaErrorInvalidValue);
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_bytes);
   if (err != cudaSuccess) return static_cast<int>(err);
   if (g.cl > 8) {
@@ -486,8 +578,24 @@ static int launch_fold(void (*kernel)(Args), const Args& a, void* stream) {
   return static_cast<int>(err);
 }
 
-int launch_bgmv(const BgmvArgs& a, void* stream) { return launch_fold(lora_bgmv_fold_kernel, a, stream); }
-int launch_moe(const MoeArgs& a, void* stream) { return launch_fold(lora_moe_fold_kernel, a, stream); }
+int launch_bgmv(const BgmvArgs& a, void* stream) {
+  switch (a.g.maxt) {
+    case 1: return launch_fold(lora_bgmv_fold_kernel<1>, a, stream);
+    case 2: return launch_fold(lora_bgmv_fold_kernel<2>, a, stream);
+    case 4: return launch_fold(lora_bgmv_fold_kernel<4>, a, stream);
+    case 8: return launch_fold(lora_bgmv_fold_kernel<8>, a, stream);
+    default: return static_cast<int>(cudaErrorInvalidValue);
+  }
+}
+int launch_moe(const MoeArgs& a, void* stream) {
+  switch (a.g.maxt) {
+    case 1: return launch_fold(lora_moe_fold_kernel<1>, a, stream);
+    case 2: return launch_fold(lora_moe_fold_kernel<2>, a, stream);
+    case 4: return launch_fold(lora_moe_fold_kernel<4>, a, stream);
+    case 8: return launch_fold(lora_moe_fold_kernel<8>, a, stream);
+    default: return static_cast<int>(cudaErrorInvalidValue);
+  }
+}
 
 int read_device_status(void* stream, uint32_t* out, int clear) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);

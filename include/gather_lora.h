@@ -70,7 +70,7 @@ enum lora_status {
 #define LORA_MAX_RANK 256          /* max_rank in [8, 256], multiple of 8 */
 #define LORA_MAX_K_IN (1 << 20)    /* k_in in [8, 2^20], multiple of 8 */
 #define LORA_MAX_N_OUT (1 << 20)   /* n_out in [8, 2^20], multiple of 8 */
-#define LORA_MAX_ROWS 65536        /* n of lora_bgmv in [0, 65536] */
+#define LORA_MAX_ROWS 8192         /* n of lora_bgmv in [0, 8192] */
 #define LORA_MAX_LORAS 4096        /* max_loras of lora_bgmv in [1, 4096] */
 #define LORA_MAX_EXPERTS 1024      /* num_experts of the MoE fold in [1, 1024] */
 #define LORA_MOE_M_TILE 64         /* sorted rows per MoE tile (static grid unit) */

@@ -58,7 +58,7 @@ def _bgmv(**kw):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(n=-1), -2), (dict(n=65537), -2), (dict(L=0), -2), (dict(L=5000), -2),
+    (dict(n=-1), -2), (dict(n=8193), -2), (dict(L=0), -2), (dict(L=5000), -2),
     (dict(R=0), -2), (dict(R=264), -2), (dict(R=12), -4), (dict(k=4), -2), (dict(k=4100, xs=4104), -4),
     (dict(no=4097, os=8192), -4), (dict(xs=4088), -3), (dict(os=100, no=128), -3),
     (dict(xs=4100), -4), (dict(x=None), -1), (dict(out=None), -1), (dict(seq=None), -1),
