@@ -86,9 +86,6 @@ bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_
     g.rt = max_rank <= 64 ? 32 : 16;
     g.gmax = std::min(g.rt, tile_rows_cap);
   }
-  const int tiles = mt * static_cast<int>(ceil_div(g.gmax, 8));
-  g.maxt = 1;
-  while (g.maxt * glora::kConsumerWarps < tiles) g.maxt *= 2;
   g.ksl = round_up(static_cast<int>(ceil_div(k_in, g.cl)), 16);
   g.jsl = round_up(static_cast<int>(ceil_div(n_out, g.cl)), 16);
   const int srows = g.mr16 + g.gmax;
@@ -99,6 +96,18 @@ bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_
       if (c <= g.ksl && srows * (c * 2 + 16) <= kStageTarget) { kcap = c; break; }
   }
   g.kch = balanced_chunk(g.ksl, kcap);
+  // A unit's items either each go to the one consumer warp that owns their
+  // ring slot (many small MoE groups whose shrink is a single k-chunk: the
+  // latency chains of several items overlap) or are split tile by tile over
+  // all consumer warps in order (one bgmv group, or larger groups).
+  const int tiles = mt * static_cast<int>(ceil_div(g.gmax, 8));
+  g.group_parallel = (moe && tiles <= 4 && g.kch >= g.ksl) ? 1 : 0;
+  g.maxt = 1;
+  if (g.group_parallel) {
+    while (g.maxt < tiles) g.maxt *= 2;
+  } else {
+    while (g.maxt * glora::kConsumerWarps < tiles) g.maxt *= 2;
+  }
   g.pitch_k = g.kch * 2 + 16;
   g.pitch_b = max_rank * 2 + (max_rank >= 32 ? 16 : 0);
   const int shrink_stage = srows * g.pitch_k;

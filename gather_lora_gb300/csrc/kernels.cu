@@ -114,7 +114,7 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
   if (tid == 0) {
     for (int s = 0; s < ns; ++s) {
       mbar_init(smem_u32(&pl.full[s]), kProducerWarps);
-      mbar_init(smem_u32(&pl.empty[s]), kConsumerWarps);
+      mbar_init(smem_u32(&pl.empty[s]), g.group_parallel ? 1 : kConsumerWarps);
     }
     pl.failed = 0;
     mbar_fence_init();
@@ -123,8 +123,14 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
 
   if (warp >= kConsumerWarps) {
     // ===================== producer warpgroup =====================
-    const int pid = tid - kConsumerWarps * 32;  // 0 .. 32 * kProducerWarps - 1
+    // All four producer warps serve every item, in item order (an mbarrier
+    // parity wait only tells the current phase from the one before it). One
+    // warp serializes its TMA requests, so an item's copies are dealt out
+    // round-robin: copy q goes to warp q % 4; each warp arrives once on the
+    // item's full barrier with the bytes it issued.
+    const int pw = warp - kConsumerWarps;
     constexpr int kP = kProducerWarps * 32;
+    const int q0 = pw + kProducerWarps * lane;
     auto produce = [&](int it) {
       const int s = it % ns;
       const uint32_t full = smem_u32(&pl.full[s]);
@@ -138,13 +144,11 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
         const int k0 = k_lo + kc * g.kch, bytes = min(g.kch, k_hi - k0) * 2;
         const int m0 = pl.gstart[gi], R = pl.gstart[gi + 1] - m0;
         const int ncopy = p.max_rank + R;
-        int mine = 0;
-        for (int q = pid; q < ncopy; q += kP) mine += bytes;
-        mine = __reduce_add_sync(0xffffffffu, mine);
-        if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(mine));
+        const int mine = ncopy > pw ? (ncopy - pw + kProducerWarps - 1) / kProducerWarps : 0;
+        if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(mine * bytes));
         __syncwarp();
         const uint16_t* A = pl.gA[gi] + k0;
-        for (int q = pid; q < ncopy; q += kP) {
+        for (int q = q0; q < ncopy; q += kP) {
           if (q < p.max_rank) {
             bulk_g2s(st + q * g.pitch_k, A + (long long)q * p.k_in, bytes, full);
           } else {
@@ -163,12 +167,12 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
         const int nb = contiguous ? 1 : jlen;
         const int ncopy = nb + R;
         int mine = 0;
-        for (int q = pid; q < ncopy; q += kP) mine += q < nb ? (contiguous ? jlen * brow : brow) : jlen * 2;
+        for (int q = q0; q < ncopy; q += kP) mine += q < nb ? (contiguous ? jlen * brow : brow) : jlen * 2;
         mine = __reduce_add_sync(0xffffffffu, mine);
         if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(mine));
         __syncwarp();
         const uint16_t* B = pl.gB[gi] + (long long)j0 * p.max_rank;
-        for (int q = pid; q < ncopy; q += kP) {
+        for (int q = q0; q < ncopy; q += kP) {
           if (q < nb) {
             if (contiguous) bulk_g2s(st, B, jlen * brow, full);
             else bulk_g2s(st + q * g.pitch_b, B + (long long)q * p.max_rank, brow, full);
@@ -192,22 +196,30 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
   }
 
   // ========================= consumer warps =========================
+  // Tile-parallel (one group per unit, bgmv): every consumer warp takes part
+  // in every item, in order, splitting its tiles. Slot-parallel (many small
+  // groups, MoE, one k-chunk per group): consumer warp w alone serves ring
+  // slot w and computes all tiles of each item in it, so the latency chains of
+  // up to eight items overlap while every slot keeps one in-order consumer.
+  const bool gpar = g.group_parallel != 0;
+  const bool idle = gpar && warp >= ns;          // slot-parallel with fewer slots than warps
+  const int g_first = gpar ? warp : 0, g_step = gpar ? ns : 1;
+  const int t_first = gpar ? 0 : warp, t_step = gpar ? 1 : kConsumerWarps;
   const int MT = g.mr16 >> 4;
-  int it = 0;
-  for (int gi = 0; gi < G && nk > 0; ++gi) {
+  for (int gi = g_first; gi < G && nk > 0 && !idle; gi += g_step) {
     const int m0 = pl.gstart[gi], R = pl.gstart[gi + 1] - m0, NT = (R + 7) >> 3, ntiles = MT * NT;
     uint32_t a_off[MAXT], x_off[MAXT];
     float acc[MAXT][4];
 #pragma unroll
     for (int i = 0; i < MAXT; ++i) {
-      const int t = warp + i * kConsumerWarps;
+      const int t = t_first + i * t_step;
       const int mt = t % MT, nt = t / MT;
       a_off[i] = (mt * 16 + (lane & 15)) * g.pitch_k;
       x_off[i] = (g.mr16 + nt * 8 + (lane & 7)) * g.pitch_k;
       acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     }
-    for (int kc = 0; kc < nk; ++kc, ++it) {
-      const int s = it % ns;
+    for (int kc = 0; kc < nk; ++kc) {
+      const int it = gi * nk + kc, s = it % ns;
       if (!mbar_wait(smem_u32(&pl.full[s]), (it / ns) & 1) && lane == 0) record_timeout(pl);
       const uint32_t st = ring_u32 + s * g.stage_bytes;
       const int klen = min(g.kch, k_hi - (k_lo + kc * g.kch));
@@ -215,7 +227,7 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
         const int kstep = min(16, klen - kk);
 #pragma unroll
         for (int i = 0; i < MAXT; ++i) {
-          if (warp + i * kConsumerWarps < ntiles)
+          if (t_first + i * t_step < ntiles)
             mma_step(acc[i], st + a_off[i] + kk * 2, st + x_off[i] + kk * 2, kstep, lane);
         }
       }
@@ -225,7 +237,7 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
     // group complete: this k-slice's partial sums -> shared memory
 #pragma unroll
     for (int i = 0; i < MAXT; ++i) {
-      const int t = warp + i * kConsumerWarps;
+      const int t = t_first + i * t_step;
       if (t < ntiles) {
         const int mt = t % MT, nt = t / MT;
         const int c0 = mt * 16 + (lane >> 2), r0 = nt * 8 + 2 * (lane & 3);
@@ -272,12 +284,14 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
   // 16-byte store. The TMA-filled stage is only read.
   const uint32_t xa_base = smem_u32(xa_s);
   const uint32_t wscr = smem_u32(smem + g.off_wscr) + warp * kScratchPerWarp;
-  it = n_shrink;
-  for (int gi = 0; gi < G; ++gi) {
+  // expand items e = gi * nj + jc, ring item n_shrink + e
+  const int e_first = gpar ? ((warp - n_shrink) % ns + ns) % ns : 0, e_step = gpar ? ns : 1;
+  for (int e = e_first; e < G * nj && !idle; e += e_step) {
+    const int gi = e / nj, jc = e - gi * nj;
     const int m0 = pl.gstart[gi], R = pl.gstart[gi + 1] - m0, NT = (R + 7) >> 3;
     const float scale = pl.gscale[gi];
-    for (int jc = 0; jc < nj; ++jc, ++it) {
-      const int s = it % ns;
+    {
+      const int it = n_shrink + e, s = it % ns;
       if (!mbar_wait(smem_u32(&pl.full[s]), (it / ns) & 1) && lane == 0) record_timeout(pl);
       const uint32_t st = ring_u32 + s * g.stage_bytes;
       const int j0 = j_lo + jc * g.jch, jlen = min(g.jch, j_hi - j0), MTj = (jlen + 15) >> 4;
@@ -292,7 +306,7 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
         uint16_t* gout = nullptr;
         if (lane < 16 && srow < R)
           gout = p.out + (long long)pl.grow[pl.members[m0 + srow]] * p.out_stride + j0 + (lane & 1) * 8;
-        for (int mt = warp; mt < MTj; mt += kConsumerWarps) {
+        for (int mt = t_first; mt < MTj; mt += t_step) {
           float d4[4] = {0.f, 0.f, 0.f, 0.f};
           const uint32_t brow = st + (mt * 16 + (lane & 15)) * g.pitch_b;
           for (int kk = 0; kk < p.max_rank; kk += 16)

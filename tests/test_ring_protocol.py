@@ -1,0 +1,132 @@
+"""CPU model of the fold kernels' shared-memory ring protocol.
+
+The kernels stream items (shrink k-chunks, then expand j-chunks) through `ns`
+ring slots guarded by a full and an empty mbarrier per slot, and wait with
+mbarrier parity tests. A parity test only tells the current phase of a barrier
+from the one before it: if a waiter can be two phases ahead, the wait passes
+falsely and a later arrival lands in the wrong phase. This model replays the
+kernels' exact schedule (every producer warp serves every item in order and
+arrives once per item; consumers either all take every item in order, or each
+owns one slot) under random interleavings and checks that no parity wait
+passes early, no arrival lands in a wrong phase, and the schedule never
+deadlocks, including across the two cluster barriers between shrink and expand.
+It also shows that a schedule in which producer warps split items by index
+(the broken variant) fails.
+"""
+from __future__ import annotations
+
+import random
+
+import pytest
+
+PRODUCER_WARPS, CONSUMER_WARPS = 4, 8
+
+
+class Barrier:
+    def __init__(self, count):
+        self.count, self.pending, self.phase, self.tx = count, count, 0, 0
+
+    def _check(self):
+        if self.pending == 0 and self.tx == 0:
+            self.phase += 1
+            self.pending = self.count
+
+    def arrive(self, phase, tx=0):
+        assert phase == self.phase, f"arrival for phase {phase} lands in phase {self.phase}"
+        self.tx += tx
+        self.pending -= 1
+        self._check()
+
+    def complete_tx(self, b):
+        self.tx -= b
+        self._check()
+
+    def try_wait(self, phase):
+        ok = (self.phase & 1) != (phase & 1)        # the hardware parity rule
+        if ok:
+            assert self.phase > phase, f"parity wait for phase {phase} passed in phase {self.phase}"
+        return ok
+
+
+def run(ns, n_shrink, n_items, slot_parallel, seed, producer_split="all"):
+    rng = random.Random(seed)
+    full = [Barrier(PRODUCER_WARPS) for _ in range(ns)]
+    empty = [Barrier(1 if slot_parallel else CONSUMER_WARPS) for _ in range(ns)]
+    pre = min(n_items, n_shrink + ns)
+
+    def producer(pw):
+        if producer_split == "all":
+            a, b = list(range(pre)), list(range(pre, n_items))
+        else:   # items dealt to warps by index (broken)
+            a = [i for i in range(pre) if i % PRODUCER_WARPS == pw]
+            b = [i for i in range(pre, n_items) if i % PRODUCER_WARPS == pw]
+        return a + ["SYNC", "SYNC"] + b
+
+    def consumer(w):
+        if slot_parallel:
+            if w >= ns:
+                return ["SYNC", "SYNC"]
+            return ([i for i in range(n_shrink) if i % ns == w] + ["SYNC", "SYNC"]
+                    + [i for i in range(n_shrink, n_items) if i % ns == w])
+        return list(range(n_shrink)) + ["SYNC", "SYNC"] + list(range(n_shrink, n_items))
+
+    agents = [("P", producer(p)) for p in range(PRODUCER_WARPS)] + \
+             [("C", consumer(w)) for w in range(CONSUMER_WARPS)]
+    pc = [0] * len(agents)
+    waited = [False] * len(agents)
+    at_sync = [None] * len(agents)
+    inflight = []
+    per_copy = 1
+    for _ in range(500000):
+        live = [i for i in range(len(agents)) if pc[i] < len(agents[i][1])]
+        if not live and not inflight:
+            return
+        choice = rng.choice(live + (["land"] if inflight else []))
+        if choice == "land":
+            s = inflight.pop(rng.randrange(len(inflight)))
+            full[s].complete_tx(per_copy)
+            continue
+        kind, prog = agents[choice]
+        op = prog[pc[choice]]
+        if op == "SYNC":
+            sid = sum(1 for x in prog[:pc[choice] + 1] if x == "SYNC")
+            at_sync[choice] = sid
+            if all(at_sync[i] == sid for i in range(len(agents))):
+                for i in range(len(agents)):
+                    pc[i] += 1
+                    at_sync[i] = None
+            continue
+        s, u = op % ns, op // ns
+        if kind == "P":
+            if not waited[choice]:
+                waited[choice] = u == 0 or empty[s].try_wait(u - 1)
+                continue
+            full[s].arrive(u, tx=per_copy)
+            inflight.append(s)
+        else:
+            if not waited[choice]:
+                waited[choice] = full[s].try_wait(u)
+                continue
+            empty[s].arrive(u)
+        waited[choice] = False
+        pc[choice] += 1
+    raise AssertionError("no progress: the schedule deadlocks")
+
+
+@pytest.mark.parametrize("slot_parallel", [False, True])
+@pytest.mark.parametrize("ns", [2, 3, 4, 6, 8])
+def test_ring_schedule_is_sound(slot_parallel, ns):
+    for n_shrink in (0, 1, 5, 16):
+        for n_exp in (0, 1, 3, 32):
+            for seed in range(3):
+                run(ns, n_shrink, n_shrink + n_exp, slot_parallel, seed)
+
+
+def test_items_split_by_index_across_producers_is_unsound():
+    failures = 0
+    for seed in range(20):
+        try:
+            run(2, 12, 16, False, seed, producer_split="by_index")
+        except AssertionError:
+            failures += 1
+    assert failures == 20
