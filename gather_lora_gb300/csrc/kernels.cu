@@ -45,6 +45,7 @@ namespace glora {
 constexpr unsigned kDevMisaligned = 0x1u;
 constexpr unsigned kDevTimeout = 0x2u;
 constexpr int kMaxStages = 8;
+constexpr int kTmaRowBytes = 128;                    // shorter rows are copied with 16-byte cp.async
 constexpr int kScratchPitch = 48;                    // bytes per row of a warp's transpose scratch
 constexpr int kScratchPerWarp = 8 * kScratchPitch;   // one 8-row x 16-column BF16 tile
 
@@ -113,8 +114,8 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
 
   if (tid == 0) {
     for (int s = 0; s < ns; ++s) {
-      mbar_init(smem_u32(&pl.full[s]), kProducerWarps);
-      mbar_init(smem_u32(&pl.empty[s]), g.group_parallel ? 1 : kConsumerWarps);
+      mbar_init(smem_u32(&pl.full[s]), kProducerWarps * 32);
+      mbar_init(smem_u32(&pl.empty[s]), kConsumerWarps);
     }
     pl.failed = 0;
     mbar_fence_init();
@@ -124,13 +125,32 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
   if (warp >= kConsumerWarps) {
     // ===================== producer warpgroup =====================
     // All four producer warps serve every item, in item order (an mbarrier
-    // parity wait only tells the current phase from the one before it). One
-    // warp serializes its TMA requests, so an item's copies are dealt out
-    // round-robin: copy q goes to warp q % 4; each warp arrives once on the
-    // item's full barrier with the bytes it issued.
+    // parity wait only tells the current phase from the one before it). Rows
+    // of at least kTmaRowBytes go by 1-D TMA (copy q to warp q % 4, since one
+    // warp serializes its TMA requests); shorter rows go as 16-byte cp.async
+    // chunks spread over all 128 producer threads. Every producer thread first
+    // registers the TMA bytes it issues, then arrives on the item's full
+    // barrier once its own cp.async chunks have landed.
     const int pw = warp - kConsumerWarps;
+    const int pt = tid - kConsumerWarps * 32;          // 0 .. 127
     constexpr int kP = kProducerWarps * 32;
-    const int q0 = pw + kProducerWarps * lane;
+    const int q0 = pw + kProducerWarps * lane;         // this thread's first TMA copy
+    // rows [0, nrows) of `row_bytes` each: TMA copies or cp.async chunks
+    auto copy_rows = [&](int nrows, int row_bytes, auto src_of, auto dst_of, uint32_t full, int& tma_bytes,
+                         bool issue) {
+      if (row_bytes >= kTmaRowBytes) {
+        for (int q = q0; q < nrows; q += kP) {
+          if (issue) bulk_g2s(dst_of(q), src_of(q), row_bytes, full);
+          else tma_bytes += row_bytes;
+        }
+      } else if (issue) {
+        const int cpr = row_bytes >> 4;
+        for (int c = pt; c < nrows * cpr; c += kP) {
+          const int r = c / cpr, ch = c - r * cpr;
+          cp_async16(dst_of(r) + ch * 16, reinterpret_cast<const char*>(src_of(r)) + ch * 16);
+        }
+      }
+    };
     auto produce = [&](int it) {
       const int s = it % ns;
       const uint32_t full = smem_u32(&pl.full[s]);
@@ -138,51 +158,46 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
         if (lane == 0) record_timeout(pl);
       }
       const uint32_t st = ring_u32 + s * g.stage_bytes;
+      int tma_bytes = 0;
       if (it < n_shrink) {
-        // copies: A rows 0..max_rank-1, then the group's x rows
+        // A rows 0..max_rank-1 of this k-chunk, then the group's x rows
         const int gi = it / nk, kc = it - gi * nk;
         const int k0 = k_lo + kc * g.kch, bytes = min(g.kch, k_hi - k0) * 2;
         const int m0 = pl.gstart[gi], R = pl.gstart[gi + 1] - m0;
-        const int ncopy = p.max_rank + R;
-        const int mine = ncopy > pw ? (ncopy - pw + kProducerWarps - 1) / kProducerWarps : 0;
-        if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(mine * bytes));
-        __syncwarp();
         const uint16_t* A = pl.gA[gi] + k0;
-        for (int q = q0; q < ncopy; q += kP) {
-          if (q < p.max_rank) {
-            bulk_g2s(st + q * g.pitch_k, A + (long long)q * p.k_in, bytes, full);
-          } else {
-            const int r = q - p.max_rank;
-            bulk_g2s(st + (g.mr16 + r) * g.pitch_k,
-                     p.x + (long long)pl.grow[pl.members[m0 + r]] * p.x_stride + k0, bytes, full);
-          }
-        }
+        auto a_src = [&](int r) { return A + (long long)r * p.k_in; };
+        auto a_dst = [&](int r) { return st + r * g.pitch_k; };
+        auto x_src = [&](int r) { return p.x + (long long)pl.grow[pl.members[m0 + r]] * p.x_stride + k0; };
+        auto x_dst = [&](int r) { return st + (g.mr16 + r) * g.pitch_k; };
+        copy_rows(p.max_rank, bytes, a_src, a_dst, full, tma_bytes, false);
+        copy_rows(R, bytes, x_src, x_dst, full, tma_bytes, false);
+        if (tma_bytes) mbar_expect_tx(full, static_cast<uint32_t>(tma_bytes));
+        copy_rows(p.max_rank, bytes, a_src, a_dst, full, tma_bytes, true);
+        copy_rows(R, bytes, x_src, x_dst, full, tma_bytes, true);
       } else {
-        // copies: B (one contiguous chunk, or one per row when rows are padded), then out rows
+        // B (one contiguous chunk when rows are unpadded, else row by row), then out rows
         const int e = it - n_shrink, gi = e / nj, jc = e - gi * nj;
         const int j0 = j_lo + jc * g.jch, jlen = min(g.jch, j_hi - j0);
         const int m0 = pl.gstart[gi], R = pl.gstart[gi + 1] - m0;
         const int brow = p.max_rank * 2;
-        const bool contiguous = g.pitch_b == brow;
-        const int nb = contiguous ? 1 : jlen;
-        const int ncopy = nb + R;
-        int mine = 0;
-        for (int q = q0; q < ncopy; q += kP) mine += q < nb ? (contiguous ? jlen * brow : brow) : jlen * 2;
-        mine = __reduce_add_sync(0xffffffffu, mine);
-        if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(mine));
-        __syncwarp();
         const uint16_t* B = pl.gB[gi] + (long long)j0 * p.max_rank;
-        for (int q = q0; q < ncopy; q += kP) {
-          if (q < nb) {
-            if (contiguous) bulk_g2s(st, B, jlen * brow, full);
-            else bulk_g2s(st + q * g.pitch_b, B + (long long)q * p.max_rank, brow, full);
-          } else {
-            const int r = q - nb;
-            bulk_g2s(st + out_region + r * pitch_o,
-                     p.out + (long long)pl.grow[pl.members[m0 + r]] * p.out_stride + j0, jlen * 2, full);
-          }
+        auto b_src = [&](int r) { return B + (long long)r * p.max_rank; };
+        auto b_dst = [&](int r) { return st + r * g.pitch_b; };
+        auto o_src = [&](int r) { return p.out + (long long)pl.grow[pl.members[m0 + r]] * p.out_stride + j0; };
+        auto o_dst = [&](int r) { return st + out_region + r * pitch_o; };
+        const bool contiguous = g.pitch_b == brow;
+        if (contiguous && pt == 0) tma_bytes += jlen * brow;
+        if (!contiguous) copy_rows(jlen, brow, b_src, b_dst, full, tma_bytes, false);
+        copy_rows(R, jlen * 2, o_src, o_dst, full, tma_bytes, false);
+        if (tma_bytes) mbar_expect_tx(full, static_cast<uint32_t>(tma_bytes));
+        if (contiguous) {
+          if (pt == 0) bulk_g2s(st, B, jlen * brow, full);
+        } else {
+          copy_rows(jlen, brow, b_src, b_dst, full, tma_bytes, true);
         }
+        copy_rows(R, jlen * 2, o_src, o_dst, full, tma_bytes, true);
       }
+      cp_async_arrive_noinc(full);
     };
     // Items whose stage is freed by shrink work can be issued before the
     // cluster exchange; the rest only after it (their stages are released by
@@ -196,11 +211,13 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
   }
 
   // ========================= consumer warps =========================
-  // Tile-parallel (one group per unit, bgmv): every consumer warp takes part
-  // in every item, in order, splitting its tiles. Slot-parallel (many small
-  // groups, MoE, one k-chunk per group): consumer warp w alone serves ring
-  // slot w and computes all tiles of each item in it, so the latency chains of
-  // up to eight items overlap while every slot keeps one in-order consumer.
+  // Shrink items are either tile-parallel (one group per unit, bgmv): every
+  // consumer warp takes part in every item, in order, splitting its tiles; or
+  // slot-parallel (many small MoE groups whose shrink is one k-chunk): consumer
+  // warp w alone serves ring slot w, computes all tiles of each shrink item in
+  // it and releases the slot with all eight arrivals, so the latency chains of
+  // several groups overlap while every slot keeps one in-order consumer.
+  // Expand items are always tile-parallel.
   const bool gpar = g.group_parallel != 0;
   const bool idle = gpar && warp >= ns;          // slot-parallel with fewer slots than warps
   const int g_first = gpar ? warp : 0, g_step = gpar ? ns : 1;
@@ -232,7 +249,7 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&pl.empty[s]));
+      if (lane == 0) mbar_arrive_count(smem_u32(&pl.empty[s]), gpar ? kConsumerWarps : 1);
     }
     // group complete: this k-slice's partial sums -> shared memory
 #pragma unroll
@@ -285,8 +302,7 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
   const uint32_t xa_base = smem_u32(xa_s);
   const uint32_t wscr = smem_u32(smem + g.off_wscr) + warp * kScratchPerWarp;
   // expand items e = gi * nj + jc, ring item n_shrink + e
-  const int e_first = gpar ? ((warp - n_shrink) % ns + ns) % ns : 0, e_step = gpar ? ns : 1;
-  for (int e = e_first; e < G * nj && !idle; e += e_step) {
+  for (int e = 0; e < G * nj; ++e) {
     const int gi = e / nj, jc = e - gi * nj;
     const int m0 = pl.gstart[gi], R = pl.gstart[gi + 1] - m0, NT = (R + 7) >> 3;
     const float scale = pl.gscale[gi];
@@ -306,7 +322,7 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
         uint16_t* gout = nullptr;
         if (lane < 16 && srow < R)
           gout = p.out + (long long)pl.grow[pl.members[m0 + srow]] * p.out_stride + j0 + (lane & 1) * 8;
-        for (int mt = t_first; mt < MTj; mt += t_step) {
+        for (int mt = warp; mt < MTj; mt += kConsumerWarps) {
           float d4[4] = {0.f, 0.f, 0.f, 0.f};
           const uint32_t brow = st + (mt * 16 + (lane & 15)) * g.pitch_b;
           for (int kk = 0; kk < p.max_rank; kk += 16)

@@ -65,6 +65,8 @@ enum lora_status {
 
 /* Device status bits, set by kernels, read with lora_read_device_status(). */
 #define LORA_DEV_MISALIGNED 0x1u   /* an adapter table entry was not 16-byte aligned */
+#define LORA_DEV_TIMEOUT 0x2u      /* a kernel gave up waiting for its own copies (~2 s); its
+                                      results were not stored */
 
 /* Supported ranges, checked on every call. */
 #define LORA_MAX_RANK 256          /* max_rank in [8, 256], multiple of 8 */

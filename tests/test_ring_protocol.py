@@ -6,8 +6,9 @@ mbarrier parity tests. A parity test only tells the current phase of a barrier
 from the one before it: if a waiter can be two phases ahead, the wait passes
 falsely and a later arrival lands in the wrong phase. This model replays the
 kernels' exact schedule (every producer warp serves every item in order and
-arrives once per item; consumers either all take every item in order, or each
-owns one slot) under random interleavings and checks that no parity wait
+arrives once per item; consumers either all take every item in order, or, for
+shrink items, each owns one slot and releases it with all eight arrivals)
+under random interleavings and checks that no parity wait
 passes early, no arrival lands in a wrong phase, and the schedule never
 deadlocks, including across the two cluster barriers between shrink and expand.
 It also shows that a schedule in which producer warps split items by index
@@ -51,7 +52,7 @@ class Barrier:
 def run(ns, n_shrink, n_items, slot_parallel, seed, producer_split="all"):
     rng = random.Random(seed)
     full = [Barrier(PRODUCER_WARPS) for _ in range(ns)]
-    empty = [Barrier(1 if slot_parallel else CONSUMER_WARPS) for _ in range(ns)]
+    empty = [Barrier(CONSUMER_WARPS) for _ in range(ns)]
     pre = min(n_items, n_shrink + ns)
 
     def producer(pw):
@@ -63,11 +64,9 @@ def run(ns, n_shrink, n_items, slot_parallel, seed, producer_split="all"):
         return a + ["SYNC", "SYNC"] + b
 
     def consumer(w):
-        if slot_parallel:
-            if w >= ns:
-                return ["SYNC", "SYNC"]
-            return ([i for i in range(n_shrink) if i % ns == w] + ["SYNC", "SYNC"]
-                    + [i for i in range(n_shrink, n_items) if i % ns == w])
+        if slot_parallel:   # shrink items: slot owner only; expand items: every warp in order
+            sh = [i for i in range(n_shrink) if i % ns == w] if w < ns else []
+            return sh + ["SYNC", "SYNC"] + list(range(n_shrink, n_items))
         return list(range(n_shrink)) + ["SYNC", "SYNC"] + list(range(n_shrink, n_items))
 
     agents = [("P", producer(p)) for p in range(PRODUCER_WARPS)] + \
@@ -107,7 +106,8 @@ def run(ns, n_shrink, n_items, slot_parallel, seed, producer_split="all"):
             if not waited[choice]:
                 waited[choice] = full[s].try_wait(u)
                 continue
-            empty[s].arrive(u)
+            for _ in range(CONSUMER_WARPS if (slot_parallel and op < n_shrink) else 1):
+                empty[s].arrive(u)
         waited[choice] = False
         pc[choice] += 1
     raise AssertionError("no progress: the schedule deadlocks")
