@@ -75,7 +75,9 @@ int balanced_chunk(int total, int cap) {
 bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_rank, int k_in,
                    int n_out, glora::FoldGeometry& g) {
   g = glora::FoldGeometry{};
-  g.cl = pow2_floor(std::min(GLORA_MAX_CLUSTER, std::max(1, std::max(k_in, n_out) / 512)));
+  // bgmv: a cluster splits each unit's k (shrink) and n_out (expand); MoE units
+  // are many and small, so one CTA folds whole groups.
+  g.cl = moe ? 1 : pow2_floor(std::min(GLORA_MAX_CLUSTER, std::max(1, std::max(k_in, n_out) / 512)));
   g.mr16 = round_up(max_rank, 16);
   const int mt = g.mr16 / 16;
   const int tile_rows_cap = 8 * (glora::kMaxTilesPerWarp * glora::kConsumerWarps / mt);
@@ -92,7 +94,8 @@ bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_
   int kcap = g.ksl;
   if (srows * (kcap * 2 + 16) > kStageTarget) {
     kcap = 16;
-    for (int c = 256; c >= 16; c /= 2)
+    static const int kCands[] = {512, 384, 256, 128, 64, 32, 16};
+    for (int c : kCands)
       if (c <= g.ksl && srows * (c * 2 + 16) <= kStageTarget) { kcap = c; break; }
   }
   g.kch = balanced_chunk(g.ksl, kcap);
@@ -135,7 +138,7 @@ bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_
   g.off_wscr = g.off_xa + g.rt * g.pitch_xa;
   g.smem_bytes = g.off_wscr + glora::kWscrBytes;
   if (g.smem_bytes > kBudgetOnePerSm + 2048) return false;
-  if (moe) {
+  if (moe) {  // tiles; the caller multiplies by the adapter count
     g.clusters = static_cast<int>(std::max(1LL, ceil_div(rows, g.rt)));
   } else {
     g.clusters = rows <= 0 ? 0 : rows / g.rt + std::min(rows, max_loras);
@@ -226,6 +229,11 @@ int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_
   glora::MoeArgs a{};
   if (!make_geometry(true, row_end - row_offset, max_loras, num_experts + 1, max_rank, k_in, n_out, a.g))
     return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory for max_rank %d, k_in %d, n_out %d", max_rank, k_in, n_out);
+  {
+    const long long units = static_cast<long long>(a.g.clusters) * (row_adapter ? max_loras : 1);
+    if (units > (1LL << 30)) return fail(LORA_ERR_SIZE, "window x adapters too large (%lld units)", units);
+    a.g.clusters = static_cast<int>(units);
+  }
   a.x = x;
   a.x_stride = x_row_stride;
   a.out = base_out;
@@ -260,10 +268,10 @@ int lora_launch_geometry(int moe, int32_t rows, int32_t max_loras, int32_t max_r
   int rc = check_shape(max_rank, k_in, n_out, k_in, n_out);
   if (rc) return rc;
   glora::FoldGeometry g{};
-  // MoE: max_loras carries num_experts + 1 (the offsets copied to shared memory)
-  const int scratch = moe ? max_loras : ((rows + 3) & ~3) + max_loras;
+  const int scratch = moe ? LORA_MAX_EXPERTS + 1 : ((rows + 3) & ~3) + max_loras;
   if (!make_geometry(moe != 0, rows, max_loras, scratch, max_rank, k_in, n_out, g))
     return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory");
+  if (moe) g.clusters *= max_loras;
   const int64_t v[9] = {g.cl, g.rt, g.ksl, g.jsl, g.kch, g.jch, g.ns, g.clusters, g.smem_bytes};
   std::memcpy(out, v, sizeof v);
   return ok();

@@ -225,32 +225,54 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
   const int MT = g.mr16 >> 4;
   for (int gi = g_first; gi < G && nk > 0 && !idle; gi += g_step) {
     const int m0 = pl.gstart[gi], R = pl.gstart[gi + 1] - m0, NT = (R + 7) >> 3, ntiles = MT * NT;
+    // Two accumulator chains per tile (even / odd k-steps of each chunk) when a
+    // warp holds few tiles, so consecutive MMAs do not wait on each other; the
+    // chains are added once per group, in a fixed order.
+    constexpr int kChains = MAXT <= 2 ? 2 : 1;
     uint32_t a_off[MAXT], x_off[MAXT];
-    float acc[MAXT][4];
+    float acc[kChains][MAXT][4];
 #pragma unroll
     for (int i = 0; i < MAXT; ++i) {
       const int t = t_first + i * t_step;
       const int mt = t % MT, nt = t / MT;
       a_off[i] = (mt * 16 + (lane & 15)) * g.pitch_k;
       x_off[i] = (g.mr16 + nt * 8 + (lane & 7)) * g.pitch_k;
-      acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < kChains; ++ch) acc[ch][i][0] = acc[ch][i][1] = acc[ch][i][2] = acc[ch][i][3] = 0.f;
     }
     for (int kc = 0; kc < nk; ++kc) {
       const int it = gi * nk + kc, s = it % ns;
       if (!mbar_wait(smem_u32(&pl.full[s]), (it / ns) & 1) && lane == 0) record_timeout(pl);
       const uint32_t st = ring_u32 + s * g.stage_bytes;
       const int klen = min(g.kch, k_hi - (k_lo + kc * g.kch));
-      for (int kk = 0; kk < klen; kk += 16) {
+      int kk = 0;
+      for (; kk + 16 * kChains <= klen; kk += 16 * kChains) {
+#pragma unroll
+        for (int ch = 0; ch < kChains; ++ch) {
+#pragma unroll
+          for (int i = 0; i < MAXT; ++i) {
+            if (t_first + i * t_step < ntiles)
+              mma_step(acc[ch][i], st + a_off[i] + (kk + 16 * ch) * 2, st + x_off[i] + (kk + 16 * ch) * 2, 16, lane);
+          }
+        }
+      }
+      for (; kk < klen; kk += 16) {   // remaining steps (and a k8 tail) on the first chain
         const int kstep = min(16, klen - kk);
 #pragma unroll
         for (int i = 0; i < MAXT; ++i) {
           if (t_first + i * t_step < ntiles)
-            mma_step(acc[i], st + a_off[i] + kk * 2, st + x_off[i] + kk * 2, kstep, lane);
+            mma_step(acc[0][i], st + a_off[i] + kk * 2, st + x_off[i] + kk * 2, kstep, lane);
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive_count(smem_u32(&pl.empty[s]), gpar ? kConsumerWarps : 1);
     }
+#pragma unroll
+    for (int ch = 1; ch < kChains; ++ch)
+#pragma unroll
+      for (int i = 0; i < MAXT; ++i)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) acc[0][i][v] += acc[ch][i][v];
     // group complete: this k-slice's partial sums -> shared memory
 #pragma unroll
     for (int i = 0; i < MAXT; ++i) {
@@ -261,7 +283,7 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           const int c = c0 + (v >> 1) * 8, r = r0 + (v & 1);
-          if (c < p.max_rank && r < R) part_s[pl.members[m0 + r] * g.pitch_part + c] = acc[i][v];
+          if (c < p.max_rank && r < R) part_s[pl.members[m0 + r] * g.pitch_part + c] = acc[0][i][v];
         }
       }
     }
@@ -460,9 +482,11 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
 }
 
 // ============================================================================
-// MoE grouped fold: work unit = one 64-row tile of the window's sorted rows,
-// split into (adapter, expert) groups of at most gmax rows; grid =
-// ceil(window / 64) tiles (>= 1).
+// MoE grouped fold: work unit = the rows of one adapter within one 64-row tile
+// of the window's sorted rows, split into runs of one expert of at most gmax
+// rows (the rows are sorted by expert, so each run is one (adapter, expert)
+// group). grid = ceil(window / 64) tiles (>= 1) x (max_loras, or 1 without a
+// row_adapter); every unit folds whole groups over the full k_in and n_out.
 // ============================================================================
 template <int MAXT>
 __global__ void __launch_bounds__(kThreads, 2) lora_moe_fold_kernel(const __grid_constant__ MoeArgs p) {
@@ -470,24 +494,26 @@ __global__ void __launch_bounds__(kThreads, 2) lora_moe_fold_kernel(const __grid
   const FoldGeometry& g = p.g;
   const cg::cluster_group cluster = cg::this_cluster();
   const int crank = static_cast<int>(cluster.block_rank());
-  const int tile = static_cast<int>(blockIdx.x) / g.cl;
-  const int tid = threadIdx.x;
+  const int adapters = p.row_adapter ? p.max_loras : 1;
+  const int unit = static_cast<int>(blockIdx.x) / g.cl;
+  const int tile = unit / adapters, adapter = unit - tile * adapters;
+  const int tid = threadIdx.x, lane = tid & 31;
   Plan& pl = *reinterpret_cast<Plan*>(smem);
   const int E = p.num_experts;
 
   pdl_wait_then_release();
 
-  const int r0 = p.row_offset + tile * g.rt;
-  const int T = min(g.rt, p.row_end - r0);
+  const int r0 = p.row_offset + tile * kMaxRows;
+  const int T = min(kMaxRows, p.row_end - r0);
   int* offs = reinterpret_cast<int*>(smem + g.off_ring);  // expert_offsets copy (ring not yet used)
   for (int i = tid; i <= E; i += kThreads) offs[i] = p.expert_offsets[i];
   int token = -1;
   if (p.row_adapter && tid < T) token = p.sorted_token_ids[r0 + tid];   // overlaps the offsets load
   __syncthreads();
 
-  // Per position: expert by binary search, adapter gate, table entry.
-  if (tid < g.rt) {
-    int key = INT_MAX;
+  // Per position: expert by binary search, then the adapter gate.
+  int expert = -1;
+  if (tid < kMaxRows) {
     const int r = r0 + tid;
     if (tid < T && r >= offs[0] && r < offs[E]) {
       int lo = 0, hi = E;  // largest e in [0, E) with offs[e] <= r
@@ -495,82 +521,98 @@ __global__ void __launch_bounds__(kThreads, 2) lora_moe_fold_kernel(const __grid
         const int mid = (lo + hi) >> 1;
         if (offs[mid] <= r) lo = mid; else hi = mid;
       }
-      const int e = lo;
-      if (offs[e] <= r && r < offs[e + 1]) {
+      if (offs[lo] <= r && r < offs[lo + 1]) {
         int a = 0;
         bool ok = true;
         if (p.row_adapter) {
           if (token < 0 || token >= p.num_tokens) ok = false; else a = p.row_adapter[token];
         }
-        if (ok && a >= 0 && a < p.max_loras) {
-          const int idx = a * E + e;
-          const uint16_t* A = p.a_table[idx];
-          const uint16_t* B = p.b_table[idx];
-          const uintptr_t ua = reinterpret_cast<uintptr_t>(A), ub = reinterpret_cast<uintptr_t>(B);
-          if (ua != 0 && ub != 0) {
-            if ((ua | ub) & 15u) {
-              atomicOr(&g_lora_status, kDevMisaligned);
-            } else {
-              key = idx;
-              pl.pA[tid] = A;
-              pl.pB[tid] = B;
-              pl.pscale[tid] = p.scale_table[idx];
-            }
-          }
-        }
+        if (ok && a == adapter) expert = lo;   // a outside [0, max_loras) matches no unit
       }
     }
-    pl.key[tid] = key;
+    pl.key[tid] = expert;
     pl.grow[tid] = r;
     pl.xarow[tid] = r - p.row_offset;
   }
-  __syncthreads();
-  // Stable sort of the valid positions by table index; a group starts at the
-  // first position of each index and again after every gmax rows of it.
-  int nv = 0;
-  {
-    int k = INT_MAX;
-    if (tid < g.rt) {
-      k = pl.key[tid];
-      int rank = 0, same_before = 0;
-      for (int u = 0; u < g.rt; ++u) {
-        const int ku = pl.key[u];
-        rank += (ku < k) || (ku == k && u < tid);
-        same_before += (ku == k && u < tid);
-      }
-      if (k != INT_MAX) {
-        pl.members[rank] = tid;
-        pl.flag[rank] = (same_before % g.gmax) == 0;
-      }
-    }
-    nv = __syncthreads_count(tid < g.rt && k != INT_MAX);
-  }
-  if (nv == 0) return;  // every CTA of the cluster takes this branch together
+  // Ordered compaction of this adapter's positions (ballots over the 64 positions).
   if (tid < kMaxRows) {
-    const bool f = tid < nv && pl.flag[tid];
-    const unsigned bal = __ballot_sync(0xffffffffu, f);
-    if ((tid & 31) == 0) pl.ballots[tid >> 5] = bal;
+    const unsigned bal = __ballot_sync(0xffffffffu, expert >= 0);
+    if (lane == 0) pl.ballots[tid >> 5] = bal;
+  }
+  __syncthreads();
+  const unsigned b0 = pl.ballots[0], b1 = pl.ballots[1];
+  const int nv = __popc(b0) + __popc(b1);
+  if (nv == 0) return;  // nothing for this adapter in this tile
+  if (tid < kMaxRows && expert >= 0) {
+    const int rank = tid < 32 ? __popc(b0 & ((1u << tid) - 1u)) : __popc(b0) + __popc(b1 & ((1u << (tid - 32)) - 1u));
+    pl.members[rank] = tid;
+  }
+  __syncthreads();
+  // Groups: a new group where the expert changes, and every gmax rows of a run.
+  if (tid < kMaxRows) {
+    bool start = false;
+    int e = -1;
+    if (tid < nv) {
+      e = pl.key[pl.members[tid]];
+      int run = 0;  // rows of the same expert before this one (members are in expert order)
+      for (int u = tid - 1; u >= 0 && pl.key[pl.members[u]] == e; --u) ++run;
+      start = (run % g.gmax) == 0;
+    }
+    const unsigned sb = __ballot_sync(0xffffffffu, start);
+    if (lane == 0) pl.ballots[tid >> 5] = sb;
+    __syncwarp();
+    pl.flag[tid] = start ? e : -1;
   }
   __syncthreads();
   if (tid < nv) {
-    const unsigned b0 = pl.ballots[0], b1 = pl.ballots[1];
-    const unsigned below = tid < 32 ? (b0 & ((1u << tid) - 1u)) : b0;
-    const int gid = __popc(below) + (tid < 32 ? 0 : __popc(b1 & ((1u << (tid - 32)) - 1u)));
-    if (pl.flag[tid]) {
-      const int pos = pl.members[tid];
+    const unsigned s0 = pl.ballots[0], s1 = pl.ballots[1];
+    const unsigned below = tid < 32 ? (s0 & ((1u << tid) - 1u)) : s0;
+    const int gid = __popc(below) + (tid < 32 ? 0 : __popc(s1 & ((1u << (tid - 32)) - 1u)));
+    const int e = pl.flag[tid];
+    if (e >= 0) {
+      const int idx = adapter * E + e;
+      const uint16_t* A = p.a_table[idx];
+      const uint16_t* B = p.b_table[idx];
+      const uintptr_t ua = reinterpret_cast<uintptr_t>(A), ub = reinterpret_cast<uintptr_t>(B);
+      const bool usable = ua != 0 && ub != 0 && ((ua | ub) & 15u) == 0;
+      if (ua != 0 && ub != 0 && !usable) atomicOr(&g_lora_status, kDevMisaligned);
       pl.gstart[gid] = tid;
-      pl.gA[gid] = pl.pA[pos];
-      pl.gB[gid] = pl.pB[pos];
-      pl.gscale[gid] = pl.pscale[pos];
+      pl.gA[gid] = usable ? A : nullptr;
+      pl.gB[gid] = B;
+      pl.gscale[gid] = usable ? p.scale_table[idx] : 0.f;
     }
     if (tid == 0) {
-      const int G = __popc(b0) + __popc(b1);
+      const int G = __popc(s0) + __popc(s1);
       pl.G = G;
       pl.NV = nv;
       pl.gstart[G] = nv;
     }
   }
   __syncthreads();
+  // Drop groups whose adapter matrices are NULL or misaligned (their rows stay unchanged).
+  if (tid == 0) {
+    int G = 0, nvk = 0;
+    const int G0 = pl.G;
+    for (int gi = 0; gi < G0; ++gi) {
+      const int a0 = pl.gstart[gi], a1 = pl.gstart[gi + 1];
+      if (pl.gA[gi] == nullptr) continue;
+      const uint16_t* A = pl.gA[gi];
+      const uint16_t* B = pl.gB[gi];
+      const float sc = pl.gscale[gi];
+      for (int i = a0; i < a1; ++i) pl.members[nvk + (i - a0)] = pl.members[i];
+      pl.gstart[G] = nvk;
+      pl.gA[G] = A;
+      pl.gB[G] = B;
+      pl.gscale[G] = sc;
+      nvk += a1 - a0;
+      ++G;
+    }
+    pl.gstart[G] = nvk;
+    pl.G = G;
+    pl.NV = nvk;
+  }
+  __syncthreads();
+  if (pl.G == 0) return;
 
   const EngineArgs ea{p.x, p.x_stride, p.out, p.out_stride, p.xa, p.max_rank, p.k_in, p.n_out};
   fold_engine<MAXT>(ea, g, pl, smem, cluster, crank);

@@ -138,8 +138,10 @@ int lora_bgmv(const lora_bf16_t* x, int64_t x_row_stride,
  *   xa                optional [row_end - row_offset, max_rank] BF16 shrink output at the
  *                     LOCAL row r - row_offset (routed rows only); NULL skips it
  * The window must satisfy 0 <= row_offset <= row_end <= te. The launch grid is
- * ceil((row_end - row_offset) / LORA_MOE_M_TILE) tiles (at least 1), so calls over
- * windows [0, cap), [cap, 2cap), ... give the same result as one call over [0, te).
+ * ceil((row_end - row_offset) / LORA_MOE_M_TILE) tiles (at least 1) times the
+ * adapters (max_loras with a row_adapter, else 1); each CTA folds the rows of
+ * one adapter in one tile. Calls over windows [0, cap), [cap, 2cap), ... give
+ * the same result as one call over [0, te).
  */
 int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride,
                           lora_bf16_t* base_out, int64_t out_row_stride,
@@ -165,8 +167,10 @@ int lora_read_device_status(void* stream, uint32_t* status_out, int clear);
 /*
  * Launch geometry that lora_bgmv / lora_moe_grouped_fold would use (for
  * tests and benchmarks). moe == 0: bgmv with `rows` = n; moe != 0: MoE with
- * `rows` = row_end - row_offset. Writes [cluster, rows_per_tile, k_slice,
- * j_slice, k_chunk, j_chunk, ring_stages, clusters, smem_bytes] to out[0..8].
+ * `rows` = row_end - row_offset and max_loras = the number of adapters the
+ * grid covers (max_loras with a row_adapter, 1 without). Writes [cluster,
+ * rows_per_tile, k_slice, j_slice, k_chunk, j_chunk, ring_stages, clusters,
+ * smem_bytes] to out[0..8].
  */
 int lora_launch_geometry(int moe, int32_t rows, int32_t max_loras, int32_t max_rank,
                          int32_t k_in, int32_t n_out, int64_t out[9]);

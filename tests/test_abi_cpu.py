@@ -161,6 +161,8 @@ def test_bgmv_grid_bounds_every_routing():
 
 
 def test_moe_geometry_tiles():
-    g = L.lora_launch_geometry(1, 4096, 129, 16, 768, 2048)
-    assert g["rows_per_tile"] == 64 and g["clusters"] == 64
-    assert L.lora_launch_geometry(1, 0, 129, 16, 768, 2048)["clusters"] == 1
+    g = L.lora_launch_geometry(1, 4096, 16, 16, 768, 2048)
+    assert g["rows_per_tile"] == 64 and g["cluster"] == 1
+    assert g["clusters"] == 64 * 16                     # tiles x adapters
+    assert L.lora_launch_geometry(1, 4096, 1, 16, 768, 2048)["clusters"] == 64
+    assert L.lora_launch_geometry(1, 0, 1, 16, 768, 2048)["clusters"] == 1
