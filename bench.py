@@ -466,11 +466,13 @@ def run_ours(args):
     ms_max, ms_local = time_steps(runner, args.steps, args.warmup, device, dctx, sampler)
     value, ms_per_step = aggregate(alg["rows"], ms_max, args.steps, dctx.world)
     kernel_ms = ms_max / args.steps / runner.launches_per_step
-    achieved = alg["bytes"] / (kernel_ms / 1e3) / 1e9
+    bytes_per_launch = alg["bytes"] / runner.launches_per_step
+    achieved = bytes_per_launch / (kernel_ms / 1e3) / 1e9
     clocks = sampler.summary() if sampler else None
     launches = args.steps * runner.launches_per_step
     if head_moe:
-        geometry = L.lora_launch_geometry(1, wl.cap, wl.num_experts + 1, wl.max_rank, wl.k_in, wl.n_out)
+        geometry = L.lora_launch_geometry(1, wl.cap, wl.max_loras if wl.row_adapter is not None else 1,
+                                          wl.max_rank, wl.k_in, wl.n_out)
     else:
         geometry = L.lora_launch_geometry(0, wl.n, wl.max_loras, wl.max_rank, wl.k_in, wl.n_out)
 
@@ -529,7 +531,7 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": recorded_traffic(head),
                          "peak_kind": peak_kind, "kernel": KERNEL_NAMES["moe" if head_moe else "bgmv"],
-                         "algorithmic_bytes_per_launch": alg["bytes"],
+                         "algorithmic_bytes_per_launch": bytes_per_launch,
                          "kernel_ms": kernel_ms, "frac_of_8tbs": achieved / 8000.0},
             "cpu_baseline": cpu,
             "e2e": e2e,

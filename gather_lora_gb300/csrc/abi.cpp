@@ -56,11 +56,15 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 #ifndef GLORA_MOE_GROUP_ROWS
 #define GLORA_MOE_GROUP_ROWS 16
 #endif
+#ifndef GLORA_MOE_MIN_UNITS
+#define GLORA_MOE_MIN_UNITS 128
+#endif
 constexpr int kBudgetTwoPerSm = GLORA_BUDGET_TWO_PER_SM;
 constexpr int kBudgetOnePerSm = 225 * 1024;
 constexpr int kStageTarget = GLORA_STAGE_TARGET;
 constexpr int kMinStage = GLORA_MIN_STAGE;
 constexpr int kMaxStages = 8;
+constexpr long long kMoeMinUnits = GLORA_MOE_MIN_UNITS;  // MoE work units that keep the GPU busy
 
 // Split `total` into equal chunks of at most `cap` (multiples of 16).
 int balanced_chunk(int total, int cap) {
@@ -138,9 +142,15 @@ bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_
   g.off_wscr = g.off_xa + g.rt * g.pitch_xa;
   g.smem_bytes = g.off_wscr + glora::kWscrBytes;
   if (g.smem_bytes > kBudgetOnePerSm + 2048) return false;
-  if (moe) {  // tiles; the caller multiplies by the adapter count
-    g.clusters = static_cast<int>(std::max(1LL, ceil_div(rows, g.rt)));
+  if (moe) {
+    // MoE (max_loras = adapters the grid covers): the largest scan tile that
+    // still gives kMoeMinUnits work units; at least one tile.
+    g.tile_rows = LORA_MOE_M_TILE;
+    for (int tr = glora::kMaxTileRows; tr > LORA_MOE_M_TILE; tr /= 2)
+      if (ceil_div(rows, tr) * max_loras >= kMoeMinUnits) { g.tile_rows = tr; break; }
+    g.clusters = static_cast<int>(std::max(1LL, ceil_div(rows, g.tile_rows)) * max_loras);
   } else {
+    g.tile_rows = g.rt;
     g.clusters = rows <= 0 ? 0 : rows / g.rt + std::min(rows, max_loras);
   }
   return true;
@@ -227,13 +237,9 @@ int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_
   if (!aligned16(x) || !aligned16(base_out) || (xa && !aligned16(xa)))
     return fail(LORA_ERR_ALIGN, "x, base_out and xa must be 16-byte aligned");
   glora::MoeArgs a{};
-  if (!make_geometry(true, row_end - row_offset, max_loras, num_experts + 1, max_rank, k_in, n_out, a.g))
+  if (!make_geometry(true, row_end - row_offset, row_adapter ? max_loras : 1, num_experts + 1, max_rank, k_in,
+                     n_out, a.g))
     return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory for max_rank %d, k_in %d, n_out %d", max_rank, k_in, n_out);
-  {
-    const long long units = static_cast<long long>(a.g.clusters) * (row_adapter ? max_loras : 1);
-    if (units > (1LL << 30)) return fail(LORA_ERR_SIZE, "window x adapters too large (%lld units)", units);
-    a.g.clusters = static_cast<int>(units);
-  }
   a.x = x;
   a.x_stride = x_row_stride;
   a.out = base_out;
@@ -271,7 +277,6 @@ int lora_launch_geometry(int moe, int32_t rows, int32_t max_loras, int32_t max_r
   const int scratch = moe ? LORA_MAX_EXPERTS + 1 : ((rows + 3) & ~3) + max_loras;
   if (!make_geometry(moe != 0, rows, max_loras, scratch, max_rank, k_in, n_out, g))
     return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory");
-  if (moe) g.clusters *= max_loras;
   const int64_t v[9] = {g.cl, g.rt, g.ksl, g.jsl, g.kch, g.jch, g.ns, g.clusters, g.smem_bytes};
   std::memcpy(out, v, sizeof v);
   return ok();

@@ -197,20 +197,21 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
-// The fold of one element: bf16( fma(scale, bf16(acc), out) ).
-__device__ __forceinline__ uint16_t fold_one(float acc, float scale, uint16_t out_bits) {
-  const float d = bf16_bits_to_f32(f32_to_bf16_bits(acc));
-  return f32_to_bf16_bits(__fmaf_rn(scale, d, bf16_bits_to_f32(out_bits)));
-}
-__device__ __forceinline__ uint32_t fold_one_bits(float acc, float scale, uint16_t out_bits) {
-  return fold_one(acc, scale, out_bits);
+// Two fp32 values -> one BF16 pair (round to nearest even), `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
-// The fold of two elements packed as BF16 pairs (low half first).
+// The fold of two elements packed as BF16 pairs (low half first): per
+// element bf16( fma(scale, bf16(acc), out) ), with both roundings done as
+// pair conversions.
 __device__ __forceinline__ uint32_t fold_pair(float acc_lo, float acc_hi, float scale, uint32_t out2) {
-  const uint32_t lo = fold_one_bits(acc_lo, scale, static_cast<uint16_t>(out2 & 0xffffu));
-  const uint32_t hi = fold_one_bits(acc_hi, scale, static_cast<uint16_t>(out2 >> 16));
-  return lo | (hi << 16);
+  const uint32_t d2 = pack_bf16x2(acc_lo, acc_hi);
+  const float d_lo = __uint_as_float(d2 << 16), d_hi = __uint_as_float(d2 & 0xffff0000u);
+  const float o_lo = __uint_as_float(out2 << 16), o_hi = __uint_as_float(out2 & 0xffff0000u);
+  return pack_bf16x2(__fmaf_rn(scale, d_lo, o_lo), __fmaf_rn(scale, d_hi, o_hi));
 }
 
 

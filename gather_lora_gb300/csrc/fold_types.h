@@ -5,9 +5,10 @@
 
 namespace glora {
 
-constexpr int kMaxRows = 64;        // rows (positions) per cluster work unit
-constexpr int kMaxTilesPerWarp = 8; // 16x8 shrink tiles a warp may own: MT * NT <= 64
-constexpr int kPlanBytes = 5120;    // shared memory reserved for the work-unit plan
+constexpr int kMaxRows = 64;        // rows (positions) per pass of a work unit
+constexpr int kMaxTileRows = 256;   // sorted rows one MoE work unit scans
+constexpr int kMaxTilesPerWarp = 4; // 16x8 shrink tiles a warp may own: MT * NT <= 32
+constexpr int kPlanBytes = 6144;    // shared memory reserved for the work-unit plan
 constexpr int kConsumerWarps = 8;   // tensor-core / fold warps per CTA
 constexpr int kProducerWarps = 4;   // TMA-issuing warps per CTA (one warpgroup)
 constexpr int kWscrBytes = kConsumerWarps * 8 * 48;  // per-CTA transpose scratch of the consumer warps
@@ -18,12 +19,13 @@ constexpr int kWscrBytes = kConsumerWarps * 8 * 48;  // per-CTA transpose scratc
 // stream through a ring of `ns` stages of `stage_bytes`.
 struct FoldGeometry {
   int cl;           // CTAs per cluster
-  int rt;           // rows per work unit (<= kMaxRows)
+  int rt;           // rows per pass of a work unit (<= kMaxRows)
+  int tile_rows;    // MoE: sorted rows scanned per work unit (64, 128 or 256)
   int ksl, jsl;     // k-slice / j-slice per CTA (multiples of 16)
   int kch, jch;     // k columns / B rows per ring stage (multiples of 16)
   int ns;           // ring depth (>= 2)
   int gmax;         // most rows in one group (MT * ceil(gmax/8) <= 8 * maxt shrink tiles)
-  int maxt;         // shrink tiles per consumer warp the kernel instance holds (1, 2, 4, 8)
+  int maxt;         // shrink tiles per consumer warp the kernel instance holds (1, 2, 4)
   int group_parallel;  // 1: each consumer warp owns whole groups; 0: warps split every item's tiles
   int mr16;         // max_rank rounded up to 16
   int pitch_k;      // bytes per A or x row in a shrink stage (kch*2 + 16)

@@ -62,15 +62,13 @@ struct Plan {
   int gstart[kMaxRows + 1];        // group g = members[gstart[g] .. gstart[g+1])
   int grow[kMaxRows];              // position -> row of x / base_out
   int xarow[kMaxRows];             // position -> row of xa
-  int key[kMaxRows];               // MoE: table index of the position (INT_MAX: skipped)
-  int flag[kMaxRows];              // MoE: sorted index starts a group
+  int flag[kMaxRows];              // MoE: the expert where a position starts a group, else -1
   unsigned ballots[2];
   float gscale[kMaxRows];
-  float pscale[kMaxRows];
   const uint16_t* gA[kMaxRows];
   const uint16_t* gB[kMaxRows];
-  const uint16_t* pA[kMaxRows];
-  const uint16_t* pB[kMaxRows];
+  int tpos[kMaxTileRows];          // MoE: tile rows routed to this unit's adapter, ascending
+  int tkey[kMaxTileRows];          // MoE: their experts
 };
 
 static_assert(sizeof(Plan) <= kPlanBytes, "plan does not fit its shared-memory reservation");
@@ -89,13 +87,30 @@ __device__ __forceinline__ void record_timeout(Plan& pl) {
   pl.failed = 1;
 }
 
-// Shrink, cluster exchange, expand + fold for one planned work unit. Called by
-// all kThreads threads of every CTA of the cluster. MAXT bounds the 16x8
-// shrink tiles one consumer warp owns (MT * ceil(group rows / 8) <= 8 * MAXT).
+// The ring's mbarriers, initialized once per CTA; passes of a work unit keep
+// counting ring items from where the previous pass stopped. Called by all threads.
+__device__ __forceinline__ void ring_init(Plan& pl, int ns) {
+  fence_proxy_async_smem();   // planning scratch in the ring: generic accesses before TMA writes
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ns; ++s) {
+      mbar_init(smem_u32(&pl.full[s]), kProducerWarps * 32);
+      mbar_init(smem_u32(&pl.empty[s]), kConsumerWarps);
+    }
+    pl.failed = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+}
+
+// Shrink, cluster exchange, expand + fold for one planned pass of a work unit.
+// Called by all kThreads threads of every CTA of the cluster, after
+// ring_init(); `it0` ring items were used by earlier passes. Returns the ring
+// items this pass used. MAXT bounds the 16x8 shrink tiles one consumer warp
+// owns (MT * ceil(group rows / 8) <= 8 * MAXT).
 template <int MAXT>
-__device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeometry& g, Plan& pl,
-                                            unsigned char* smem, const cg::cluster_group& cluster,
-                                            int crank) {
+__device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeometry& g, Plan& pl,
+                                           unsigned char* smem, const cg::cluster_group& cluster,
+                                           int crank, int it0) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   unsigned char* ring = smem + g.off_ring;
   const uint32_t ring_u32 = smem_u32(ring);
@@ -111,16 +126,10 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
   const int n_shrink = G * nk, n_items = G * (nk + nj);
   const int out_region = g.jch * g.pitch_b;   // byte offset of the out rows inside an expand stage
   const int pitch_o = g.jch * 2 + 16;
-
-  if (tid == 0) {
-    for (int s = 0; s < ns; ++s) {
-      mbar_init(smem_u32(&pl.full[s]), kProducerWarps * 32);
-      mbar_init(smem_u32(&pl.empty[s]), kConsumerWarps);
-    }
-    pl.failed = 0;
-    mbar_fence_init();
-  }
-  __syncthreads();
+  // CTA-wide barrier of the exchange (a cluster barrier when the cluster has peers)
+  auto unit_sync = [&]() {
+    if (g.cl > 1) cluster.sync(); else __syncthreads();
+  };
 
   if (warp >= kConsumerWarps) {
     // ===================== producer warpgroup =====================
@@ -152,9 +161,9 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
       }
     };
     auto produce = [&](int it) {
-      const int s = it % ns;
+      const int ri = it0 + it, s = ri % ns;   // ring item
       const uint32_t full = smem_u32(&pl.full[s]);
-      if (it >= ns && !mbar_wait(smem_u32(&pl.empty[s]), ((it / ns) - 1) & 1)) {
+      if (ri >= ns && !mbar_wait(smem_u32(&pl.empty[s]), ((ri / ns) - 1) & 1)) {
         if (lane == 0) record_timeout(pl);
       }
       const uint32_t st = ring_u32 + s * g.stage_bytes;
@@ -204,10 +213,10 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
     // expand work, which needs the exchanged xa).
     const int pre = min(n_items, n_shrink + ns);
     for (int it = 0; it < pre; ++it) produce(it);
-    cluster.sync();
-    cluster.sync();
+    unit_sync();
+    unit_sync();
     for (int it = pre; it < n_items; ++it) produce(it);
-    return;
+    return n_items;
   }
 
   // ========================= consumer warps =========================
@@ -220,7 +229,8 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
   // Expand items are always tile-parallel.
   const bool gpar = g.group_parallel != 0;
   const bool idle = gpar && warp >= ns;          // slot-parallel with fewer slots than warps
-  const int g_first = gpar ? warp : 0, g_step = gpar ? ns : 1;
+  // slot-parallel: group gi's one shrink item is ring item it0 + gi, in slot (it0 + gi) % ns
+  const int g_first = gpar ? ((warp - it0 % ns) + ns) % ns : 0, g_step = gpar ? ns : 1;
   const int t_first = gpar ? 0 : warp, t_step = gpar ? 1 : kConsumerWarps;
   const int MT = g.mr16 >> 4;
   for (int gi = g_first; gi < G && nk > 0 && !idle; gi += g_step) {
@@ -241,8 +251,8 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
       for (int ch = 0; ch < kChains; ++ch) acc[ch][i][0] = acc[ch][i][1] = acc[ch][i][2] = acc[ch][i][3] = 0.f;
     }
     for (int kc = 0; kc < nk; ++kc) {
-      const int it = gi * nk + kc, s = it % ns;
-      if (!mbar_wait(smem_u32(&pl.full[s]), (it / ns) & 1) && lane == 0) record_timeout(pl);
+      const int ri = it0 + gi * nk + kc, s = ri % ns;
+      if (!mbar_wait(smem_u32(&pl.full[s]), (ri / ns) & 1) && lane == 0) record_timeout(pl);
       const uint32_t st = ring_u32 + s * g.stage_bytes;
       const int klen = min(g.kch, k_hi - (k_lo + kc * g.kch));
       int kk = 0;
@@ -296,7 +306,7 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
   }
 
   // ---- cluster exchange: xa = bf16(sum of the cl partials, in rank order) ----
-  cluster.sync();
+  unit_sync();
   {
     const int E = NV * p.max_rank, per = (E + g.cl - 1) / g.cl;
     const int e_lo = crank * per, e_hi = min(e_lo + per, E);
@@ -313,7 +323,7 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
       if (p.xa && store) p.xa[(long long)pl.xarow[pos] * p.max_rank + c] = xb;
     }
   }
-  cluster.sync();
+  unit_sync();
 
   // ---- expand + fold over this CTA's j-slice ---------------------------------
   // Per 16x8 tile (16 output columns x 8 rows): d = bf16(B_tile @ xa^T) on the
@@ -329,8 +339,8 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
     const int m0 = pl.gstart[gi], R = pl.gstart[gi + 1] - m0, NT = (R + 7) >> 3;
     const float scale = pl.gscale[gi];
     {
-      const int it = n_shrink + e, s = it % ns;
-      if (!mbar_wait(smem_u32(&pl.full[s]), (it / ns) & 1) && lane == 0) record_timeout(pl);
+      const int ri = it0 + n_shrink + e, s = ri % ns;
+      if (!mbar_wait(smem_u32(&pl.full[s]), (ri / ns) & 1) && lane == 0) record_timeout(pl);
       const uint32_t st = ring_u32 + s * g.stage_bytes;
       const int j0 = j_lo + jc * g.jch, jlen = min(g.jch, j_hi - j0), MTj = (jlen + 15) >> 4;
       const bool store = pl.failed == 0;
@@ -369,6 +379,7 @@ __device__ __forceinline__ void fold_engine(const EngineArgs& p, const FoldGeome
       if (lane == 0) mbar_arrive(smem_u32(&pl.empty[s]));
     }
   }
+  return n_items;
 }
 
 // ============================================================================
@@ -477,16 +488,19 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
   __syncthreads();
   if (pl.G == 0) return;  // NULL or misaligned adapter: rows stay unchanged
 
+  ring_init(pl, g.ns);
   const EngineArgs ea{p.x, p.x_stride, p.out, p.out_stride, p.xa, p.max_rank, p.k_in, p.n_out};
-  fold_engine<MAXT>(ea, g, pl, smem, cluster, crank);
+  fold_engine<MAXT>(ea, g, pl, smem, cluster, crank, 0);
 }
 
 // ============================================================================
-// MoE grouped fold: work unit = the rows of one adapter within one 64-row tile
-// of the window's sorted rows, split into runs of one expert of at most gmax
-// rows (the rows are sorted by expert, so each run is one (adapter, expert)
-// group). grid = ceil(window / 64) tiles (>= 1) x (max_loras, or 1 without a
-// row_adapter); every unit folds whole groups over the full k_in and n_out.
+// MoE grouped fold: work unit = the rows of one adapter within one tile of
+// tile_rows sorted rows of the window. grid = ceil(window / tile_rows) tiles
+// (>= 1) x (max_loras, or 1 without a row_adapter). The unit's rows, in sorted
+// order, are folded in passes of up to kMaxRows rows; a pass is split into
+// runs of one expert of at most gmax rows (the rows are sorted by expert, so
+// each run belongs to one (adapter, expert) group), and every group is folded
+// over the full k_in and n_out.
 // ============================================================================
 template <int MAXT>
 __global__ void __launch_bounds__(kThreads, 2) lora_moe_fold_kernel(const __grid_constant__ MoeArgs p) {
@@ -497,25 +511,25 @@ __global__ void __launch_bounds__(kThreads, 2) lora_moe_fold_kernel(const __grid
   const int adapters = p.row_adapter ? p.max_loras : 1;
   const int unit = static_cast<int>(blockIdx.x) / g.cl;
   const int tile = unit / adapters, adapter = unit - tile * adapters;
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   Plan& pl = *reinterpret_cast<Plan*>(smem);
   const int E = p.num_experts;
 
   pdl_wait_then_release();
 
-  const int r0 = p.row_offset + tile * kMaxRows;
-  const int T = min(kMaxRows, p.row_end - r0);
+  const int r0 = p.row_offset + tile * g.tile_rows;
+  const int T = min(g.tile_rows, p.row_end - r0);
   int* offs = reinterpret_cast<int*>(smem + g.off_ring);  // expert_offsets copy (ring not yet used)
   for (int i = tid; i <= E; i += kThreads) offs[i] = p.expert_offsets[i];
   int token = -1;
   if (p.row_adapter && tid < T) token = p.sorted_token_ids[r0 + tid];   // overlaps the offsets load
   __syncthreads();
 
-  // Per position: expert by binary search, then the adapter gate.
+  // Per tile row: expert by binary search, then the adapter gate.
   int expert = -1;
-  if (tid < kMaxRows) {
+  if (tid < T) {
     const int r = r0 + tid;
-    if (tid < T && r >= offs[0] && r < offs[E]) {
+    if (r >= offs[0] && r < offs[E]) {
       int lo = 0, hi = E;  // largest e in [0, E) with offs[e] <= r
       while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -530,92 +544,99 @@ __global__ void __launch_bounds__(kThreads, 2) lora_moe_fold_kernel(const __grid
         if (ok && a == adapter) expert = lo;   // a outside [0, max_loras) matches no unit
       }
     }
-    pl.key[tid] = expert;
-    pl.grow[tid] = r;
-    pl.xarow[tid] = r - p.row_offset;
   }
-  // Ordered compaction of this adapter's positions (ballots over the 64 positions).
-  if (tid < kMaxRows) {
-    const unsigned bal = __ballot_sync(0xffffffffu, expert >= 0);
-    if (lane == 0) pl.ballots[tid >> 5] = bal;
-  }
+  // Ordered compaction of this adapter's rows (one ballot per warp).
+  const unsigned bal = __ballot_sync(0xffffffffu, expert >= 0);
+  if (lane == 0) pl.warp_sums[warp] = __popc(bal);
   __syncthreads();
-  const unsigned b0 = pl.ballots[0], b1 = pl.ballots[1];
-  const int nv = __popc(b0) + __popc(b1);
-  if (nv == 0) return;  // nothing for this adapter in this tile
-  if (tid < kMaxRows && expert >= 0) {
-    const int rank = tid < 32 ? __popc(b0 & ((1u << tid) - 1u)) : __popc(b0) + __popc(b1 & ((1u << (tid - 32)) - 1u));
-    pl.members[rank] = tid;
+  int before = 0, npos = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const int c = pl.warp_sums[w];
+    before += (w < warp) ? c : 0;
+    npos += c;
   }
-  __syncthreads();
-  // Groups: a new group where the expert changes, and every gmax rows of a run.
-  if (tid < kMaxRows) {
-    bool start = false;
-    int e = -1;
-    if (tid < nv) {
-      e = pl.key[pl.members[tid]];
-      int run = 0;  // rows of the same expert before this one (members are in expert order)
-      for (int u = tid - 1; u >= 0 && pl.key[pl.members[u]] == e; --u) ++run;
-      start = (run % g.gmax) == 0;
-    }
-    const unsigned sb = __ballot_sync(0xffffffffu, start);
-    if (lane == 0) pl.ballots[tid >> 5] = sb;
-    __syncwarp();
-    pl.flag[tid] = start ? e : -1;
+  if (npos == 0) return;  // nothing for this adapter in this tile
+  if (expert >= 0) {
+    const int rank = before + __popc(bal & ((1u << lane) - 1u));
+    pl.tpos[rank] = tid;
+    pl.tkey[rank] = expert;
   }
-  __syncthreads();
-  if (tid < nv) {
-    const unsigned s0 = pl.ballots[0], s1 = pl.ballots[1];
-    const unsigned below = tid < 32 ? (s0 & ((1u << tid) - 1u)) : s0;
-    const int gid = __popc(below) + (tid < 32 ? 0 : __popc(s1 & ((1u << (tid - 32)) - 1u)));
-    const int e = pl.flag[tid];
-    if (e >= 0) {
-      const int idx = adapter * E + e;
-      const uint16_t* A = p.a_table[idx];
-      const uint16_t* B = p.b_table[idx];
-      const uintptr_t ua = reinterpret_cast<uintptr_t>(A), ub = reinterpret_cast<uintptr_t>(B);
-      const bool usable = ua != 0 && ub != 0 && ((ua | ub) & 15u) == 0;
-      if (ua != 0 && ub != 0 && !usable) atomicOr(&g_lora_status, kDevMisaligned);
-      pl.gstart[gid] = tid;
-      pl.gA[gid] = usable ? A : nullptr;
-      pl.gB[gid] = B;
-      pl.gscale[gid] = usable ? p.scale_table[idx] : 0.f;
-    }
-    if (tid == 0) {
-      const int G = __popc(s0) + __popc(s1);
-      pl.G = G;
-      pl.NV = nv;
-      pl.gstart[G] = nv;
-    }
-  }
-  __syncthreads();
-  // Drop groups whose adapter matrices are NULL or misaligned (their rows stay unchanged).
-  if (tid == 0) {
-    int G = 0, nvk = 0;
-    const int G0 = pl.G;
-    for (int gi = 0; gi < G0; ++gi) {
-      const int a0 = pl.gstart[gi], a1 = pl.gstart[gi + 1];
-      if (pl.gA[gi] == nullptr) continue;
-      const uint16_t* A = pl.gA[gi];
-      const uint16_t* B = pl.gB[gi];
-      const float sc = pl.gscale[gi];
-      for (int i = a0; i < a1; ++i) pl.members[nvk + (i - a0)] = pl.members[i];
-      pl.gstart[G] = nvk;
-      pl.gA[G] = A;
-      pl.gB[G] = B;
-      pl.gscale[G] = sc;
-      nvk += a1 - a0;
-      ++G;
-    }
-    pl.gstart[G] = nvk;
-    pl.G = G;
-    pl.NV = nvk;
-  }
-  __syncthreads();
-  if (pl.G == 0) return;
+  ring_init(pl, g.ns);   // (its barrier also publishes tpos / tkey)
 
   const EngineArgs ea{p.x, p.x_stride, p.out, p.out_stride, p.xa, p.max_rank, p.k_in, p.n_out};
-  fold_engine<MAXT>(ea, g, pl, smem, cluster, crank);
+  int it0 = 0;
+  for (int base = 0; base < npos; base += kMaxRows) {
+    const int P = min(kMaxRows, npos - base);
+    // Groups: a new group where the expert changes, and every gmax rows of a run.
+    if (tid < kMaxRows) {
+      bool start = false;
+      int e = -1;
+      if (tid < P) {
+        e = pl.tkey[base + tid];
+        int run = 0;  // rows of the same expert before this one in the pass
+        for (int u = tid - 1; u >= 0 && pl.tkey[base + u] == e; --u) ++run;
+        start = (run % g.gmax) == 0;
+        const int r = r0 + pl.tpos[base + tid];
+        pl.members[tid] = tid;
+        pl.grow[tid] = r;
+        pl.xarow[tid] = r - p.row_offset;
+      }
+      const unsigned sb = __ballot_sync(0xffffffffu, start);
+      if (lane == 0) pl.ballots[tid >> 5] = sb;
+      pl.flag[tid] = start ? e : -1;
+    }
+    __syncthreads();
+    if (tid < P) {
+      const unsigned s0 = pl.ballots[0], s1 = pl.ballots[1];
+      const unsigned below = tid < 32 ? (s0 & ((1u << tid) - 1u)) : s0;
+      const int gid = __popc(below) + (tid < 32 ? 0 : __popc(s1 & ((1u << (tid - 32)) - 1u)));
+      const int e = pl.flag[tid];
+      if (e >= 0) {
+        const int idx = adapter * E + e;
+        const uint16_t* A = p.a_table[idx];
+        const uint16_t* B = p.b_table[idx];
+        const uintptr_t ua = reinterpret_cast<uintptr_t>(A), ub = reinterpret_cast<uintptr_t>(B);
+        const bool usable = ua != 0 && ub != 0 && ((ua | ub) & 15u) == 0;
+        if (ua != 0 && ub != 0 && !usable) atomicOr(&g_lora_status, kDevMisaligned);
+        pl.gstart[gid] = tid;
+        pl.gA[gid] = usable ? A : nullptr;
+        pl.gB[gid] = B;
+        pl.gscale[gid] = usable ? p.scale_table[idx] : 0.f;
+      }
+      if (tid == 0) {
+        const int G = __popc(s0) + __popc(s1);
+        pl.G = G;
+        pl.gstart[G] = P;
+      }
+    }
+    __syncthreads();
+    // Drop groups whose adapter matrices are NULL or misaligned (their rows stay unchanged).
+    if (tid == 0) {
+      int G = 0, nvk = 0;
+      const int G0 = pl.G;
+      for (int gi = 0; gi < G0; ++gi) {
+        const int a0 = pl.gstart[gi], a1 = pl.gstart[gi + 1];
+        if (pl.gA[gi] == nullptr) continue;
+        const uint16_t* A = pl.gA[gi];
+        const uint16_t* B = pl.gB[gi];
+        const float sc = pl.gscale[gi];
+        for (int i = a0; i < a1; ++i) pl.members[nvk + (i - a0)] = pl.members[i];
+        pl.gstart[G] = nvk;
+        pl.gA[G] = A;
+        pl.gB[G] = B;
+        pl.gscale[G] = sc;
+        nvk += a1 - a0;
+        ++G;
+      }
+      pl.gstart[G] = nvk;
+      pl.G = G;
+      pl.NV = nvk;
+    }
+    __syncthreads();
+    if (pl.G > 0) it0 += fold_engine<MAXT>(ea, g, pl, smem, cluster, crank, it0);
+    __syncthreads();   // the next pass rewrites the plan
+  }
 }
 
 // ============================================================================
@@ -655,7 +676,6 @@ int launch_bgmv(const BgmvArgs& a, void* stream) {
     case 1: return launch_fold(lora_bgmv_fold_kernel<1>, a, stream);
     case 2: return launch_fold(lora_bgmv_fold_kernel<2>, a, stream);
     case 4: return launch_fold(lora_bgmv_fold_kernel<4>, a, stream);
-    case 8: return launch_fold(lora_bgmv_fold_kernel<8>, a, stream);
     default: return static_cast<int>(cudaErrorInvalidValue);
   }
 }
@@ -664,7 +684,6 @@ int launch_moe(const MoeArgs& a, void* stream) {
     case 1: return launch_fold(lora_moe_fold_kernel<1>, a, stream);
     case 2: return launch_fold(lora_moe_fold_kernel<2>, a, stream);
     case 4: return launch_fold(lora_moe_fold_kernel<4>, a, stream);
-    case 8: return launch_fold(lora_moe_fold_kernel<8>, a, stream);
     default: return static_cast<int>(cudaErrorInvalidValue);
   }
 }

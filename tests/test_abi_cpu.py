@@ -161,8 +161,12 @@ def test_bgmv_grid_bounds_every_routing():
 
 
 def test_moe_geometry_tiles():
+    # the largest scan tile (256, 128, 64 rows) that still gives >= 128 units
     g = L.lora_launch_geometry(1, 4096, 16, 16, 768, 2048)
     assert g["rows_per_tile"] == 64 and g["cluster"] == 1
-    assert g["clusters"] == 64 * 16                     # tiles x adapters
+    assert g["clusters"] == 16 * 16                     # 256-row tiles x adapters
+    assert L.lora_launch_geometry(1, 4096, 4, 16, 768, 2048)["clusters"] == 32 * 4
     assert L.lora_launch_geometry(1, 4096, 1, 16, 768, 2048)["clusters"] == 64
+    assert L.lora_launch_geometry(1, 100, 1, 16, 768, 2048)["clusters"] == 2
     assert L.lora_launch_geometry(1, 0, 1, 16, 768, 2048)["clusters"] == 1
+    assert L.lora_launch_geometry(1, 0, 16, 16, 768, 2048)["clusters"] == 16

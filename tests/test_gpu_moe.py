@@ -77,6 +77,34 @@ def test_moe_random(case):
     compare_moe(wl, windows, g_out, o_out, g_xas, o_xas, o_d, routes, min_exact=0.97)
 
 
+def _skewed(seed):
+    """One adapter takes 90% of the tokens: a 256-row tile then holds far more
+    than 64 rows of it, which the kernel folds in several passes."""
+    wl = W.make_moe("moe_skew", num_tokens=1024, top_k=4, num_experts=8, k_in=256, n_out=512,
+                    max_loras=16, max_rank=16, rank=16, alpha=16.0, adapter_base_frac=0.0,
+                    cap=4096, seed=seed)
+    rng = np.random.default_rng(seed)
+    wl.row_adapter = np.where(rng.random(wl.num_tokens) < 0.9, 0,
+                              rng.integers(1, 16, wl.num_tokens)).astype(np.int32)
+    return wl
+
+
+def test_moe_multi_pass_units():
+    wl = _skewed(321)
+    assert wl.te == 4096
+    assert L.lora_launch_geometry(1, 4096, 16, 16, 256, 512)["clusters"] == 16 * 16  # 256-row tiles
+    windows = [(0, 4096)]
+    g_out, g_xas = gpu_moe(wl, windows)
+    o_out, o_xas, o_d = oracle_moe(wl, windows)
+    compare_moe(wl, windows, g_out, o_out, g_xas, o_xas, o_d, _routes_all(wl, windows))
+    # scan tiles of 256, 128 and 64 rows (windows of 4096, 1000 and 300) give the same bits
+    for cap in (1000, 300):
+        ws = [(lo, min(lo + cap, wl.te)) for lo in range(0, wl.te, cap)]
+        w_out, w_xas = gpu_moe(wl, ws)
+        assert np.array_equal(w_out, g_out)
+        assert np.array_equal(np.concatenate(w_xas), g_xas[0])
+
+
 def test_moe_rows_outside_spans_bad_tokens_and_empty_window():
     wl = W.make_moe("moe_bad", num_tokens=40, top_k=4, num_experts=8, k_in=64, n_out=64,
                     max_loras=2, max_rank=16, rank=16, alpha=16.0, adapter_base_frac=0.0,

@@ -49,25 +49,42 @@ class Barrier:
         return ok
 
 
-def run(ns, n_shrink, n_items, slot_parallel, seed, producer_split="all"):
+def run(ns, n_shrink, n_items, slot_parallel, seed, producer_split="all", passes=None):
+    """`passes`: [(n_shrink, n_items), ...] folded one after the other by one
+    CTA; ring item numbers continue across passes and a CTA barrier separates them."""
     rng = random.Random(seed)
     full = [Barrier(PRODUCER_WARPS) for _ in range(ns)]
     empty = [Barrier(CONSUMER_WARPS) for _ in range(ns)]
-    pre = min(n_items, n_shrink + ns)
+    passes = passes or [(n_shrink, n_items)]
+    shrink_items = set()
+    it0 = 0
+    bounds = []
+    for ps, pn in passes:
+        bounds.append((it0, ps, pn))
+        shrink_items.update(range(it0, it0 + ps))
+        it0 += pn
 
     def producer(pw):
-        if producer_split == "all":
-            a, b = list(range(pre)), list(range(pre, n_items))
-        else:   # items dealt to warps by index (broken)
-            a = [i for i in range(pre) if i % PRODUCER_WARPS == pw]
-            b = [i for i in range(pre, n_items) if i % PRODUCER_WARPS == pw]
-        return a + ["SYNC", "SYNC"] + b
+        prog = []
+        for base, ps, pn in bounds:
+            pre = min(pn, ps + ns)
+            if producer_split == "all":
+                a, b = list(range(pre)), list(range(pre, pn))
+            else:   # items dealt to warps by index (broken)
+                a = [i for i in range(pre) if i % PRODUCER_WARPS == pw]
+                b = [i for i in range(pre, pn) if i % PRODUCER_WARPS == pw]
+            prog += [base + i for i in a] + ["SYNC", "SYNC"] + [base + i for i in b] + ["SYNC"]
+        return prog
 
     def consumer(w):
-        if slot_parallel:   # shrink items: slot owner only; expand items: every warp in order
-            sh = [i for i in range(n_shrink) if i % ns == w] if w < ns else []
-            return sh + ["SYNC", "SYNC"] + list(range(n_shrink, n_items))
-        return list(range(n_shrink)) + ["SYNC", "SYNC"] + list(range(n_shrink, n_items))
+        prog = []
+        for base, ps, pn in bounds:
+            if slot_parallel:   # shrink items: slot owner only; expand items: every warp in order
+                sh = [base + i for i in range(ps) if (base + i) % ns == w] if w < ns else []
+            else:
+                sh = [base + i for i in range(ps)]
+            prog += sh + ["SYNC", "SYNC"] + [base + i for i in range(ps, pn)] + ["SYNC"]
+        return prog
 
     agents = [("P", producer(p)) for p in range(PRODUCER_WARPS)] + \
              [("C", consumer(w)) for w in range(CONSUMER_WARPS)]
@@ -106,7 +123,7 @@ def run(ns, n_shrink, n_items, slot_parallel, seed, producer_split="all"):
             if not waited[choice]:
                 waited[choice] = full[s].try_wait(u)
                 continue
-            for _ in range(CONSUMER_WARPS if (slot_parallel and op < n_shrink) else 1):
+            for _ in range(CONSUMER_WARPS if (slot_parallel and op in shrink_items) else 1):
                 empty[s].arrive(u)
         waited[choice] = False
         pc[choice] += 1
@@ -120,6 +137,15 @@ def test_ring_schedule_is_sound(slot_parallel, ns):
         for n_exp in (0, 1, 3, 32):
             for seed in range(3):
                 run(ns, n_shrink, n_shrink + n_exp, slot_parallel, seed)
+
+
+@pytest.mark.parametrize("slot_parallel", [False, True])
+@pytest.mark.parametrize("ns", [2, 3, 5])
+def test_ring_schedule_across_passes_is_sound(slot_parallel, ns):
+    # item counts of successive passes leave the ring at every offset
+    for passes in ([(1, 4), (2, 9), (1, 1)], [(3, 8), (0, 5), (4, 4), (2, 7)], [(5, 6)] * 4):
+        for seed in range(3):
+            run(ns, 0, 0, slot_parallel, seed, passes=passes)
 
 
 def test_items_split_by_index_across_producers_is_unsound():
