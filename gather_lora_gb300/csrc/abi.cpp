@@ -87,7 +87,7 @@ bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_
   const int tile_rows_cap = 8 * (glora::kMaxTilesPerWarp * glora::kConsumerWarps / mt);
   if (moe) {
     g.rt = LORA_MOE_M_TILE;
-    g.gmax = std::min(GLORA_MOE_GROUP_ROWS, tile_rows_cap);
+    g.gmax = std::min(std::min(GLORA_MOE_GROUP_ROWS, 32), tile_rows_cap);
   } else {
     g.rt = max_rank <= 64 ? 32 : 16;
     g.gmax = std::min(g.rt, tile_rows_cap);
@@ -125,7 +125,7 @@ bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_
   g.stage_bytes = round_up(std::max(shrink_stage, expand_stage), 128);
   g.pitch_part = max_rank + 4;
   g.pitch_xa = max_rank * 2 + 16;
-  const int fixed = glora::kPlanBytes + g.rt * g.pitch_part * 4 + g.rt * g.pitch_xa + glora::kWscrBytes;
+  const int fixed = glora::kPlanBytes + g.rt * g.pitch_part * 4 + g.rt * g.pitch_xa;
   int ns = (kBudgetTwoPerSm - fixed) / g.stage_bytes;
   if (ns < 2) ns = (kBudgetOnePerSm - fixed) / g.stage_bytes;
   ns = std::min(ns, kMaxStages);
@@ -139,8 +139,7 @@ bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_
   g.off_out = 0;
   g.off_part = g.off_ring + ns * g.stage_bytes;
   g.off_xa = g.off_part + g.rt * g.pitch_part * 4;
-  g.off_wscr = g.off_xa + g.rt * g.pitch_xa;
-  g.smem_bytes = g.off_wscr + glora::kWscrBytes;
+  g.smem_bytes = g.off_xa + g.rt * g.pitch_xa;
   if (g.smem_bytes > kBudgetOnePerSm + 2048) return false;
   if (moe) {
     // MoE (max_loras = adapters the grid covers): the largest scan tile that

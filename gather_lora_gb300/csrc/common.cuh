@@ -131,16 +131,6 @@ __device__ __forceinline__ void ldsm_x1(uint32_t addr, uint32_t& r0) {
 // Transposing forms: with .trans, lane (g = lane/4, q = lane%4) exchanges the
 // pair [row 2q][col g], [row 2q+1][col g] of each 8x8 matrix (low half first),
 // which is the accumulator layout of an m16n8 tile whose N index is the row.
-__device__ __forceinline__ void ldsm_x2_trans(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];\n"
-               : "=r"(r0), "=r"(r1)
-               : "r"(addr));
-}
-__device__ __forceinline__ void stsm_x2_trans(uint32_t addr, uint32_t r0, uint32_t r1) {
-  asm volatile("stmatrix.sync.aligned.m8n8.x2.trans.shared.b16 [%0], {%1,%2};\n" ::"r"(addr), "r"(r0), "r"(r1)
-               : "memory");
-}
-
 // ---- BF16 tensor-core MMA, fp32 accumulate ----------------------------------
 // D[16x8] += A[16xK] * B[Kx8]; A row-major (K contiguous per row of A), B
 // "col" (K contiguous per column of B). Accumulator layout per lane

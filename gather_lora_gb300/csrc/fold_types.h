@@ -11,7 +11,6 @@ constexpr int kMaxTilesPerWarp = 4; // 16x8 shrink tiles a warp may own: MT * NT
 constexpr int kPlanBytes = 6144;    // shared memory reserved for the work-unit plan
 constexpr int kConsumerWarps = 8;   // tensor-core / fold warps per CTA
 constexpr int kProducerWarps = 4;   // TMA-issuing warps per CTA (one warpgroup)
-constexpr int kWscrBytes = kConsumerWarps * 8 * 48;  // per-CTA transpose scratch of the consumer warps
 
 // Launch geometry and shared-memory layout of one fold launch. Every CTA of a
 // cluster of `cl` CTAs owns one k-slice of the shrink (ksl columns of A / x)
@@ -24,7 +23,7 @@ struct FoldGeometry {
   int ksl, jsl;     // k-slice / j-slice per CTA (multiples of 16)
   int kch, jch;     // k columns / B rows per ring stage (multiples of 16)
   int ns;           // ring depth (>= 2)
-  int gmax;         // most rows in one group (MT * ceil(gmax/8) <= 8 * maxt shrink tiles)
+  int gmax;         // most rows in one group (<= 32; MT * ceil(gmax/8) <= 8 * maxt shrink tiles)
   int maxt;         // shrink tiles per consumer warp the kernel instance holds (1, 2, 4)
   int group_parallel;  // 1: each consumer warp owns whole groups; 0: warps split every item's tiles
   int mr16;         // max_rank rounded up to 16
@@ -34,7 +33,7 @@ struct FoldGeometry {
   int pitch_part;   // floats per partial-sum row (max_rank + 4)
   int pitch_xa;     // bytes per xa row (max_rank*2 + 16)
   int stage_bytes;
-  int off_ring, off_out, off_part, off_xa, off_wscr, smem_bytes;
+  int off_ring, off_out, off_part, off_xa, smem_bytes;
   int clusters;     // grid = clusters * cl CTAs
 };
 

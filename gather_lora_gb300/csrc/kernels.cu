@@ -33,6 +33,8 @@
 #include <limits.h>
 
 #include "common.cuh"
+
+#include <type_traits>
 #include "fold_types.h"
 
 namespace cg = cooperative_groups;
@@ -46,8 +48,6 @@ constexpr unsigned kDevMisaligned = 0x1u;
 constexpr unsigned kDevTimeout = 0x2u;
 constexpr int kMaxStages = 8;
 constexpr int kTmaRowBytes = 128;                    // shorter rows are copied with 16-byte cp.async
-constexpr int kScratchPitch = 48;                    // bytes per row of a warp's transpose scratch
-constexpr int kScratchPerWarp = 8 * kScratchPitch;   // one 8-row x 16-column BF16 tile
 
 // Work-unit plan, identical in every CTA of a cluster.
 struct Plan {
@@ -144,22 +144,6 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
     const int pt = tid - kConsumerWarps * 32;          // 0 .. 127
     constexpr int kP = kProducerWarps * 32;
     const int q0 = pw + kProducerWarps * lane;         // this thread's first TMA copy
-    // rows [0, nrows) of `row_bytes` each: TMA copies or cp.async chunks
-    auto copy_rows = [&](int nrows, int row_bytes, auto src_of, auto dst_of, uint32_t full, int& tma_bytes,
-                         bool issue) {
-      if (row_bytes >= kTmaRowBytes) {
-        for (int q = q0; q < nrows; q += kP) {
-          if (issue) bulk_g2s(dst_of(q), src_of(q), row_bytes, full);
-          else tma_bytes += row_bytes;
-        }
-      } else if (issue) {
-        const int cpr = row_bytes >> 4;
-        for (int c = pt; c < nrows * cpr; c += kP) {
-          const int r = c / cpr, ch = c - r * cpr;
-          cp_async16(dst_of(r) + ch * 16, reinterpret_cast<const char*>(src_of(r)) + ch * 16);
-        }
-      }
-    };
     auto produce = [&](int it) {
       const int ri = it0 + it, s = ri % ns;   // ring item
       const uint32_t full = smem_u32(&pl.full[s]);
@@ -167,44 +151,59 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
         if (lane == 0) record_timeout(pl);
       }
       const uint32_t st = ring_u32 + s * g.stage_bytes;
-      int tma_bytes = 0;
+      // An item is two row sets. Set 0: the adapter rows (A rows of this
+      // k-chunk, or B rows of this j-chunk: one copy when B is unpadded), at a
+      // fixed stride. Set 1: the group's activation rows (x, shrink) or output
+      // rows (out, expand), gathered through the plan. Row r of a set goes from
+      // src + row(r) * stride (elements) to dst + r * pitch (bytes).
+      const uint16_t* src0;
+      const uint16_t* src1;
+      long long stride0, stride1;
+      uint32_t dst0, dst1;
+      int n0, bytes0, pitch0, n1, bytes1, pitch1, m0;
       if (it < n_shrink) {
-        // A rows 0..max_rank-1 of this k-chunk, then the group's x rows
         const int gi = it / nk, kc = it - gi * nk;
         const int k0 = k_lo + kc * g.kch, bytes = min(g.kch, k_hi - k0) * 2;
-        const int m0 = pl.gstart[gi], R = pl.gstart[gi + 1] - m0;
-        const uint16_t* A = pl.gA[gi] + k0;
-        auto a_src = [&](int r) { return A + (long long)r * p.k_in; };
-        auto a_dst = [&](int r) { return st + r * g.pitch_k; };
-        auto x_src = [&](int r) { return p.x + (long long)pl.grow[pl.members[m0 + r]] * p.x_stride + k0; };
-        auto x_dst = [&](int r) { return st + (g.mr16 + r) * g.pitch_k; };
-        copy_rows(p.max_rank, bytes, a_src, a_dst, full, tma_bytes, false);
-        copy_rows(R, bytes, x_src, x_dst, full, tma_bytes, false);
-        if (tma_bytes) mbar_expect_tx(full, static_cast<uint32_t>(tma_bytes));
-        copy_rows(p.max_rank, bytes, a_src, a_dst, full, tma_bytes, true);
-        copy_rows(R, bytes, x_src, x_dst, full, tma_bytes, true);
+        m0 = pl.gstart[gi];
+        src0 = pl.gA[gi] + k0; stride0 = p.k_in; dst0 = st; n0 = p.max_rank; bytes0 = bytes; pitch0 = g.pitch_k;
+        src1 = p.x + k0; stride1 = p.x_stride; dst1 = st + g.mr16 * g.pitch_k; n1 = pl.gstart[gi + 1] - m0;
+        bytes1 = bytes; pitch1 = g.pitch_k;
       } else {
-        // B (one contiguous chunk when rows are unpadded, else row by row), then out rows
         const int e = it - n_shrink, gi = e / nj, jc = e - gi * nj;
         const int j0 = j_lo + jc * g.jch, jlen = min(g.jch, j_hi - j0);
-        const int m0 = pl.gstart[gi], R = pl.gstart[gi + 1] - m0;
         const int brow = p.max_rank * 2;
-        const uint16_t* B = pl.gB[gi] + (long long)j0 * p.max_rank;
-        auto b_src = [&](int r) { return B + (long long)r * p.max_rank; };
-        auto b_dst = [&](int r) { return st + r * g.pitch_b; };
-        auto o_src = [&](int r) { return p.out + (long long)pl.grow[pl.members[m0 + r]] * p.out_stride + j0; };
-        auto o_dst = [&](int r) { return st + out_region + r * pitch_o; };
-        const bool contiguous = g.pitch_b == brow;
-        if (contiguous && pt == 0) tma_bytes += jlen * brow;
-        if (!contiguous) copy_rows(jlen, brow, b_src, b_dst, full, tma_bytes, false);
-        copy_rows(R, jlen * 2, o_src, o_dst, full, tma_bytes, false);
-        if (tma_bytes) mbar_expect_tx(full, static_cast<uint32_t>(tma_bytes));
-        if (contiguous) {
-          if (pt == 0) bulk_g2s(st, B, jlen * brow, full);
-        } else {
-          copy_rows(jlen, brow, b_src, b_dst, full, tma_bytes, true);
+        m0 = pl.gstart[gi];
+        src0 = pl.gB[gi] + (long long)j0 * p.max_rank; stride0 = p.max_rank; dst0 = st; pitch0 = g.pitch_b;
+        if (g.pitch_b == brow) { n0 = 1; bytes0 = jlen * brow; } else { n0 = jlen; bytes0 = brow; }
+        src1 = p.out + j0; stride1 = p.out_stride; dst1 = st + out_region; n1 = pl.gstart[gi + 1] - m0;
+        bytes1 = jlen * 2; pitch1 = pitch_o;
+      }
+      // TMA bytes this thread issues (rows q0, q0 + kP, ... of each TMA set)
+      const int mine0 = bytes0 >= kTmaRowBytes && q0 < n0 ? (n0 - 1 - q0) / kP + 1 : 0;
+      const int mine1 = bytes1 >= kTmaRowBytes && q0 < n1 ? (n1 - 1 - q0) / kP + 1 : 0;
+      const int tx = mine0 * bytes0 + mine1 * bytes1;
+      if (tx) mbar_expect_tx(full, static_cast<uint32_t>(tx));
+#pragma unroll 1
+      for (int set = 0; set < 2; ++set) {
+        const uint16_t* src = set ? src1 : src0;
+        const long long stride = set ? stride1 : stride0;
+        const uint32_t dst = set ? dst1 : dst0;
+        const int n = set ? n1 : n0, bytes = set ? bytes1 : bytes0, pitch = set ? pitch1 : pitch0;
+        if (bytes >= kTmaRowBytes) {
+#pragma unroll 1
+          for (int q = q0; q < n; q += kP) {
+            const int row = set ? pl.grow[pl.members[m0 + q]] : q;
+            bulk_g2s(dst + q * pitch, src + row * stride, bytes, full);
+          }
+        } else {   // short rows: 16-byte cp.async chunks over all producer threads
+          const int cpr = bytes >> 4;
+#pragma unroll 1
+          for (int c = pt; c < n * cpr; c += kP) {
+            const int q = c / cpr, ch = c - q * cpr;
+            const int row = set ? pl.grow[pl.members[m0 + q]] : q;
+            cp_async16(dst + q * pitch + ch * 16, reinterpret_cast<const char*>(src + row * stride) + ch * 16);
+          }
         }
-        copy_rows(R, jlen * 2, o_src, o_dst, full, tma_bytes, true);
       }
       cp_async_arrive_noinc(full);
     };
@@ -235,10 +234,13 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
   const int MT = g.mr16 >> 4;
   for (int gi = g_first; gi < G && nk > 0 && !idle; gi += g_step) {
     const int m0 = pl.gstart[gi], R = pl.gstart[gi + 1] - m0, NT = (R + 7) >> 3, ntiles = MT * NT;
-    // Two accumulator chains per tile (even / odd k-steps of each chunk) when a
-    // warp holds few tiles, so consecutive MMAs do not wait on each other; the
-    // chains are added once per group, in a fixed order.
-    constexpr int kChains = MAXT <= 2 ? 2 : 1;
+    // Independent accumulator chains per tile (k-steps dealt round-robin over
+    // the chains within each chunk) when a warp holds few tiles, so consecutive
+    // MMAs do not wait on each other; the chains are added once per group, in
+    // a fixed order. When all of a warp's tiles share one A row block (the
+    // warp stride is a multiple of MT), its A fragment is loaded once per k-step.
+    constexpr int kChains = MAXT == 1 ? 4 : (MAXT == 2 ? 2 : 1);
+    const bool share_a = !gpar && (kConsumerWarps % MT) == 0;
     uint32_t a_off[MAXT], x_off[MAXT];
     float acc[kChains][MAXT][4];
 #pragma unroll
@@ -250,6 +252,40 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
 #pragma unroll
       for (int ch = 0; ch < kChains; ++ch) acc[ch][i][0] = acc[ch][i][1] = acc[ch][i][2] = acc[ch][i][3] = 0.f;
     }
+    // one k-step (16, or an 8-wide tail) of every tile of this warp into chain `ch`
+    auto step = [&](uint32_t st, int kk, int kstep, float (&ac)[MAXT][4]) {
+      if (share_a) {
+        if (kstep == 16) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(st + a_off[0] + kk * 2 + ((lane >> 4) << 4), a0, a1, a2, a3);
+#pragma unroll
+          for (int i = 0; i < MAXT; ++i) {
+            if (t_first + i * t_step < ntiles) {
+              uint32_t b0, b1;
+              ldsm_x2(st + x_off[i] + kk * 2 + (((lane >> 3) & 1) << 4), b0, b1);
+              mma_k16(ac[i], a0, a1, a2, a3, b0, b1);
+            }
+          }
+        } else {
+          uint32_t a0, a1;
+          ldsm_x2(st + a_off[0] + kk * 2, a0, a1);
+#pragma unroll
+          for (int i = 0; i < MAXT; ++i) {
+            if (t_first + i * t_step < ntiles) {
+              uint32_t b0;
+              ldsm_x1(st + x_off[i] + kk * 2, b0);
+              mma_k8(ac[i], a0, a1, b0);
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < MAXT; ++i) {
+          if (t_first + i * t_step < ntiles)
+            mma_step(ac[i], st + a_off[i] + kk * 2, st + x_off[i] + kk * 2, kstep, lane);
+        }
+      }
+    };
     for (int kc = 0; kc < nk; ++kc) {
       const int ri = it0 + gi * nk + kc, s = ri % ns;
       if (!mbar_wait(smem_u32(&pl.full[s]), (ri / ns) & 1) && lane == 0) record_timeout(pl);
@@ -258,22 +294,9 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
       int kk = 0;
       for (; kk + 16 * kChains <= klen; kk += 16 * kChains) {
 #pragma unroll
-        for (int ch = 0; ch < kChains; ++ch) {
-#pragma unroll
-          for (int i = 0; i < MAXT; ++i) {
-            if (t_first + i * t_step < ntiles)
-              mma_step(acc[ch][i], st + a_off[i] + (kk + 16 * ch) * 2, st + x_off[i] + (kk + 16 * ch) * 2, 16, lane);
-          }
-        }
+        for (int ch = 0; ch < kChains; ++ch) step(st, kk + 16 * ch, 16, acc[ch]);
       }
-      for (; kk < klen; kk += 16) {   // remaining steps (and a k8 tail) on the first chain
-        const int kstep = min(16, klen - kk);
-#pragma unroll
-        for (int i = 0; i < MAXT; ++i) {
-          if (t_first + i * t_step < ntiles)
-            mma_step(acc[0][i], st + a_off[i] + kk * 2, st + x_off[i] + kk * 2, kstep, lane);
-        }
-      }
+      for (; kk < klen; kk += 16) step(st, kk, min(16, klen - kk), acc[0]);   // remaining steps on chain 0
       __syncwarp();
       if (lane == 0) mbar_arrive_count(smem_u32(&pl.empty[s]), gpar ? kConsumerWarps : 1);
     }
@@ -326,58 +349,128 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
   unit_sync();
 
   // ---- expand + fold over this CTA's j-slice ---------------------------------
-  // Per 16x8 tile (16 output columns x 8 rows): d = bf16(B_tile @ xa^T) on the
-  // tensor cores, the staged old out values enter in accumulator layout through
-  // ldmatrix.trans, the fold runs in registers, stmatrix.trans turns the BF16
-  // result row-major in a warp-private scratch, and each row leaves with one
-  // 16-byte store. The TMA-filled stage is only read.
+  // Work comes in 16-column blocks of two 16x8 tensor-core tiles (16 group rows
+  // x 8 consecutive output columns each), with the xa rows as the A operand:
+  // their fragments are loaded once per item (max_rank <= 32). Lane (g, q)
+  // holds columns 2q, 2q+1 of each tile for rows g and g + 8; it folds them
+  // with the staged old values in registers, and one exchange with lane q ^ 1
+  // leaves it four adjacent columns, so each row leaves as one full 32-byte
+  // sector of 8-byte stores. The TMA-filled stage is only read. Consumer warp
+  // w takes blocks w, w + 8, ...
   const uint32_t xa_base = smem_u32(xa_s);
-  const uint32_t wscr = smem_u32(smem + g.off_wscr) + warp * kScratchPerWarp;
-  // expand items e = gi * nj + jc, ring item n_shrink + e
+  const int gq = lane >> 2, q = lane & 3;
+  const bool odd = (q & 1) != 0;
+  const int scol = odd ? 2 * q + 6 : 2 * q;                            // first stored column
+  const int brow4 = (lane >> 4) * 8 + (lane & 7), bk4 = ((lane >> 3) & 1) << 4;   // ldmatrix.x4 of B
+  const int brow2 = ((lane >> 3) & 1) * 8 + (lane & 7);                // ldmatrix.x2 of B (k8 tail)
   for (int e = 0; e < G * nj; ++e) {
     const int gi = e / nj, jc = e - gi * nj;
-    const int m0 = pl.gstart[gi], R = pl.gstart[gi + 1] - m0, NT = (R + 7) >> 3;
+    const int m0 = pl.gstart[gi], R = pl.gstart[gi + 1] - m0;
     const float scale = pl.gscale[gi];
-    {
-      const int ri = it0 + n_shrink + e, s = ri % ns;
-      if (!mbar_wait(smem_u32(&pl.full[s]), (ri / ns) & 1) && lane == 0) record_timeout(pl);
-      const uint32_t st = ring_u32 + s * g.stage_bytes;
-      const int j0 = j_lo + jc * g.jch, jlen = min(g.jch, j_hi - j0), MTj = (jlen + 15) >> 4;
-      const bool store = pl.failed == 0;
-      for (int nt = 0; nt < NT; ++nt) {
-        // mma B operand: xa row of this lane's column (rows past R repeat the last one)
-        const uint32_t xrow = xa_base + pl.members[m0 + min(nt * 8 + (lane & 7), R - 1)] * g.pitch_xa;
-        // ldmatrix.trans source: staged out row (lane & 7), second 8 columns for lanes 8..15
-        const uint32_t orow = st + out_region + (nt * 8 + (lane & 7)) * pitch_o + ((lane >> 3) & 1) * 16;
-        // this lane's output row for the final 16-byte stores (lanes 0..15)
-        const int srow = nt * 8 + (lane >> 1);
-        uint16_t* gout = nullptr;
-        if (lane < 16 && srow < R)
-          gout = p.out + (long long)pl.grow[pl.members[m0 + srow]] * p.out_stride + j0 + (lane & 1) * 8;
-        for (int mt = warp; mt < MTj; mt += kConsumerWarps) {
-          float d4[4] = {0.f, 0.f, 0.f, 0.f};
-          const uint32_t brow = st + (mt * 16 + (lane & 15)) * g.pitch_b;
-          for (int kk = 0; kk < p.max_rank; kk += 16)
-            mma_step(d4, brow + kk * 2, xrow + kk * 2, min(16, p.max_rank - kk), lane);
-          uint32_t o0, o1;
-          ldsm_x2_trans(orow + mt * 32, o0, o1);
-          const uint32_t f0 = fold_pair(d4[0], d4[1], scale, o0);
-          const uint32_t f1 = fold_pair(d4[2], d4[3], scale, o1);
-          stsm_x2_trans(wscr + (lane & 7) * kScratchPitch + ((lane >> 3) & 1) * 16, f0, f1);
-          __syncwarp();
-          if (gout && store && mt * 16 + (lane & 1) * 8 < jlen) {
-            uint4 v;
-            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                         : "r"(wscr + (lane >> 1) * kScratchPitch + (lane & 1) * 16));
-            *reinterpret_cast<uint4*>(gout + mt * 16) = v;
+    const int ri = it0 + n_shrink + e, s = ri % ns;
+    if (!mbar_wait(smem_u32(&pl.full[s]), (ri / ns) & 1) && lane == 0) record_timeout(pl);
+    const uint32_t st = ring_u32 + s * g.stage_bytes;
+    const int j0 = j_lo + jc * g.jch, jlen = min(g.jch, j_hi - j0), NCB = (jlen + 15) >> 4;
+    const bool store = pl.failed == 0;
+    // xa row (lane & 15) of each 16-row tile (rows past R repeat the last one)
+    uint32_t a_row[2];
+#pragma unroll
+    for (int mr = 0; mr < 2; ++mr) a_row[mr] = xa_base + pl.members[m0 + min(mr * 16 + (lane & 15), R - 1)] * g.pitch_xa;
+    // rows gq + 8 * hh: staged old values (rows past R read the last row, in
+    // bounds) and output pointers (NULL past R)
+    uint32_t old_row[4];
+    uint16_t* orow[4];
+#pragma unroll
+    for (int hh = 0; hh < 4; ++hh) {
+      const int r = hh * 8 + gq;
+      old_row[hh] = st + out_region + min(r, R - 1) * pitch_o + 4 * q;
+      orow[hh] = (r < R && store) ? p.out + (long long)pl.grow[pl.members[m0 + r]] * p.out_stride + j0 + scol : nullptr;
+    }
+    // The block loop, compiled per row-tile count MR (1, 2) and per KS, the
+    // k16 steps whose xa fragments stay in registers (1: max_rank 16, 2:
+    // max_rank 32; 0: any max_rank, fragments loaded per step, k8 tail).
+    auto blocks = [&](auto mr_c, auto ks_c) {
+      constexpr int MR = decltype(mr_c)::value, KS = decltype(ks_c)::value;
+      uint32_t af[MR][KS > 0 ? KS : 1][4];
+      if (KS > 0) {
+#pragma unroll
+        for (int mr = 0; mr < MR; ++mr)
+#pragma unroll
+          for (int ks = 0; ks < (KS > 0 ? KS : 1); ++ks)
+            ldsm_x4(a_row[mr] + ks * 32 + ((lane >> 4) << 4), af[mr][ks][0], af[mr][ks][1], af[mr][ks][2], af[mr][ks][3]);
+      }
+      for (int cb = warp; cb < NCB; cb += kConsumerWarps) {
+        float d[MR][2][4];
+#pragma unroll
+        for (int mr = 0; mr < MR; ++mr)
+#pragma unroll
+          for (int t = 0; t < 2; ++t) d[mr][t][0] = d[mr][t][1] = d[mr][t][2] = d[mr][t][3] = 0.f;
+        const uint32_t bblk = st + cb * 16 * g.pitch_b;
+        if (KS > 0) {
+#pragma unroll
+          for (int ks = 0; ks < (KS > 0 ? KS : 1); ++ks) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(bblk + brow4 * g.pitch_b + ks * 32 + bk4, b0, b1, b2, b3);
+#pragma unroll
+            for (int mr = 0; mr < MR; ++mr) {
+              mma_k16(d[mr][0], af[mr][ks][0], af[mr][ks][1], af[mr][ks][2], af[mr][ks][3], b0, b1);
+              mma_k16(d[mr][1], af[mr][ks][0], af[mr][ks][1], af[mr][ks][2], af[mr][ks][3], b2, b3);
+            }
           }
-          __syncwarp();
+        } else {
+          int kk = 0;
+          for (; kk + 16 <= p.max_rank; kk += 16) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(bblk + brow4 * g.pitch_b + kk * 2 + bk4, b0, b1, b2, b3);
+#pragma unroll
+            for (int mr = 0; mr < MR; ++mr) {
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4(a_row[mr] + kk * 2 + ((lane >> 4) << 4), a0, a1, a2, a3);
+              mma_k16(d[mr][0], a0, a1, a2, a3, b0, b1);
+              mma_k16(d[mr][1], a0, a1, a2, a3, b2, b3);
+            }
+          }
+          if (kk < p.max_rank) {                     // k8 tail (max_rank % 16 == 8)
+            uint32_t b0, b1;
+            ldsm_x2(bblk + brow2 * g.pitch_b + kk * 2, b0, b1);
+#pragma unroll
+            for (int mr = 0; mr < MR; ++mr) {
+              uint32_t a0, a1;
+              ldsm_x2(a_row[mr] + kk * 2, a0, a1);
+              mma_k8(d[mr][0], a0, a1, b0);
+              mma_k8(d[mr][1], a0, a1, b1);
+            }
+          }
+        }
+        const int c0 = cb * 16;
+        const bool col_ok = c0 + scol < jlen;         // the last block may hold only 8 columns
+#pragma unroll
+        for (int hh = 0; hh < 2 * MR; ++hh) {
+          const int mr = hh >> 1, h = hh & 1;
+          if (hh == 0 || hh * 8 < R) {                // warp-uniform: this row half has rows
+            uint32_t o0, o1;
+            asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(o0) : "r"(old_row[hh] + c0 * 2));
+            asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(o1) : "r"(old_row[hh] + c0 * 2 + 16));
+            const uint32_t f0 = fold_pair(d[mr][0][2 * h], d[mr][0][2 * h + 1], scale, o0);
+            const uint32_t f1 = fold_pair(d[mr][1][2 * h], d[mr][1][2 * h + 1], scale, o1);
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, odd ? f0 : f1, 1);
+            uint16_t* o = orow[hh];
+            if (o && col_ok) {
+              const uint32_t lo = odd ? recv : f0, hi = odd ? f1 : recv;
+              asm volatile("st.global.v2.b32 [%0], {%1, %2};\n" ::"l"(o + c0), "r"(lo), "r"(hi) : "memory");
+            }
+          }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&pl.empty[s]));
-    }
+    };
+    using I1 = std::integral_constant<int, 1>;
+    using I2 = std::integral_constant<int, 2>;
+    using I0 = std::integral_constant<int, 0>;
+    if (p.max_rank == 16) { if (R <= 16) blocks(I1{}, I1{}); else blocks(I2{}, I1{}); }
+    else if (p.max_rank == 32) { if (R <= 16) blocks(I1{}, I2{}); else blocks(I2{}, I2{}); }
+    else { if (R <= 16) blocks(I1{}, I0{}); else blocks(I2{}, I0{}); }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&pl.empty[s]));
   }
   return n_items;
 }
