@@ -109,11 +109,18 @@ bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_
   // all consumer warps in order (one bgmv group, or larger groups).
   const int tiles = mt * static_cast<int>(ceil_div(g.gmax, 8));
   g.group_parallel = (moe && tiles <= 4 && g.kch >= g.ksl) ? 1 : 0;
+  // Tile-parallel groups of few tiles also split k over the consumer warps:
+  // ksplit k-phases of kConsumerWarps / ksplit warps each.
+  // (Only without cluster peers: with peers the cluster already splits k, and
+  // the extra planes would lengthen the exchange.)
+  g.ksplit = 1;
+  if (!g.group_parallel && g.cl == 1)
+    while (g.ksplit < glora::kConsumerWarps && (glora::kConsumerWarps / (2 * g.ksplit)) >= tiles) g.ksplit *= 2;
   g.maxt = 1;
   if (g.group_parallel) {
     while (g.maxt < tiles) g.maxt *= 2;
   } else {
-    while (g.maxt * glora::kConsumerWarps < tiles) g.maxt *= 2;
+    while (g.maxt * (glora::kConsumerWarps / g.ksplit) < tiles) g.maxt *= 2;
   }
   g.pitch_k = g.kch * 2 + 16;
   g.pitch_b = max_rank * 2 + (max_rank >= 32 ? 16 : 0);
@@ -125,7 +132,7 @@ bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_
   g.stage_bytes = round_up(std::max(shrink_stage, expand_stage), 128);
   g.pitch_part = max_rank + 4;
   g.pitch_xa = max_rank * 2 + 16;
-  const int fixed = glora::kPlanBytes + g.rt * g.pitch_part * 4 + g.rt * g.pitch_xa;
+  const int fixed = glora::kPlanBytes + g.ksplit * g.rt * g.pitch_part * 4 + g.rt * g.pitch_xa;
   int ns = (kBudgetTwoPerSm - fixed) / g.stage_bytes;
   if (ns < 2) ns = (kBudgetOnePerSm - fixed) / g.stage_bytes;
   ns = std::min(ns, kMaxStages);
@@ -138,7 +145,7 @@ bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_
   g.off_ring = glora::kPlanBytes;
   g.off_out = 0;
   g.off_part = g.off_ring + ns * g.stage_bytes;
-  g.off_xa = g.off_part + g.rt * g.pitch_part * 4;
+  g.off_xa = g.off_part + g.ksplit * g.rt * g.pitch_part * 4;
   g.smem_bytes = g.off_xa + g.rt * g.pitch_xa;
   if (g.smem_bytes > kBudgetOnePerSm + 2048) return false;
   if (moe) {

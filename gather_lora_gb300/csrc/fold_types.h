@@ -26,6 +26,7 @@ struct FoldGeometry {
   int gmax;         // most rows in one group (<= 32; MT * ceil(gmax/8) <= 8 * maxt shrink tiles)
   int maxt;         // shrink tiles per consumer warp the kernel instance holds (1, 2, 4)
   int group_parallel;  // 1: each consumer warp owns whole groups; 0: warps split every item's tiles
+  int ksplit;       // tile-parallel: k-phases the consumer warps form (1, 2, 4, 8; partial planes of part_s)
   int mr16;         // max_rank rounded up to 16
   int pitch_k;      // bytes per A or x row in a shrink stage (kch*2 + 16)
   int pitch_b;      // bytes per B row in an expand stage

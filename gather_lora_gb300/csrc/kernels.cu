@@ -226,12 +226,19 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
   // it and releases the slot with all eight arrivals, so the latency chains of
   // several groups overlap while every slot keeps one in-order consumer.
   // Expand items are always tile-parallel.
+  // Tile-parallel items with few tiles are also split over k: the consumer
+  // warps form KS k-phases of TW warps; phase kp takes k-steps kp, kp + KS, ...
+  // of every chunk and keeps its partial sums in its own plane of part_s, and
+  // the exchange adds the planes in phase order.
   const bool gpar = g.group_parallel != 0;
   const bool idle = gpar && warp >= ns;          // slot-parallel with fewer slots than warps
   // slot-parallel: group gi's one shrink item is ring item it0 + gi, in slot (it0 + gi) % ns
   const int g_first = gpar ? ((warp - it0 % ns) + ns) % ns : 0, g_step = gpar ? ns : 1;
-  const int t_first = gpar ? 0 : warp, t_step = gpar ? 1 : kConsumerWarps;
+  const int KS = gpar ? 1 : g.ksplit, TW = kConsumerWarps / KS;
+  const int kp = gpar ? 0 : warp / TW;
+  const int t_first = gpar ? 0 : warp % TW, t_step = gpar ? 1 : TW;
   const int MT = g.mr16 >> 4;
+  const int plane = g.rt * g.pitch_part;         // floats per k-phase plane of part_s
   for (int gi = g_first; gi < G && nk > 0 && !idle; gi += g_step) {
     const int m0 = pl.gstart[gi], R = pl.gstart[gi + 1] - m0, NT = (R + 7) >> 3, ntiles = MT * NT;
     // Independent accumulator chains per tile (k-steps dealt round-robin over
@@ -240,7 +247,7 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
     // a fixed order. When all of a warp's tiles share one A row block (the
     // warp stride is a multiple of MT), its A fragment is loaded once per k-step.
     constexpr int kChains = MAXT == 1 ? 4 : (MAXT == 2 ? 2 : 1);
-    const bool share_a = !gpar && (kConsumerWarps % MT) == 0;
+    const bool share_a = !gpar && (TW % MT) == 0;
     uint32_t a_off[MAXT], x_off[MAXT];
     float acc[kChains][MAXT][4];
 #pragma unroll
@@ -291,12 +298,13 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
       if (!mbar_wait(smem_u32(&pl.full[s]), (ri / ns) & 1) && lane == 0) record_timeout(pl);
       const uint32_t st = ring_u32 + s * g.stage_bytes;
       const int klen = min(g.kch, k_hi - (k_lo + kc * g.kch));
-      int kk = 0;
-      for (; kk + 16 * kChains <= klen; kk += 16 * kChains) {
+      const int nst = (klen + 15) >> 4, nfull = klen >> 4;   // k-steps of this chunk (the last may be 8 wide)
+      int si = kp;
+      for (; si + KS * (kChains - 1) < nfull; si += KS * kChains) {
 #pragma unroll
-        for (int ch = 0; ch < kChains; ++ch) step(st, kk + 16 * ch, 16, acc[ch]);
+        for (int ch = 0; ch < kChains; ++ch) step(st, (si + ch * KS) * 16, 16, acc[ch]);
       }
-      for (; kk < klen; kk += 16) step(st, kk, min(16, klen - kk), acc[0]);   // remaining steps on chain 0
+      for (; si < nst; si += KS) step(st, si * 16, min(16, klen - si * 16), acc[0]);   // the rest on chain 0
       __syncwarp();
       if (lane == 0) mbar_arrive_count(smem_u32(&pl.empty[s]), gpar ? kConsumerWarps : 1);
     }
@@ -316,18 +324,31 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           const int c = c0 + (v >> 1) * 8, r = r0 + (v & 1);
-          if (c < p.max_rank && r < R) part_s[pl.members[m0 + r] * g.pitch_part + c] = acc[0][i][v];
+          if (c < p.max_rank && r < R) part_s[kp * plane + pl.members[m0 + r] * g.pitch_part + c] = acc[0][i][v];
         }
       }
     }
   }
   if (nk == 0) {  // empty k-slice: the partials are zero
-    for (int e = tid; e < NV * p.max_rank; e += kConsumerWarps * 32) {
-      const int mi = e / p.max_rank, c = e - mi * p.max_rank;
-      part_s[pl.members[mi] * g.pitch_part + c] = 0.f;
+    for (int e = tid; e < KS * NV * p.max_rank; e += kConsumerWarps * 32) {
+      const int ph = e / (NV * p.max_rank), r = e - ph * NV * p.max_rank;
+      const int mi = r / p.max_rank, c = r - mi * p.max_rank;
+      part_s[ph * plane + pl.members[mi] * g.pitch_part + c] = 0.f;
     }
   }
 
+  // With cluster peers, each CTA first adds its own k-phase planes into plane
+  // 0 (in phase order), so the exchange reads one plane per rank.
+  if (KS > 1 && g.cl > 1) {
+    consumer_sync();
+    for (int e = tid; e < NV * p.max_rank; e += kConsumerWarps * 32) {
+      const int mi = e / p.max_rank, c = e - mi * p.max_rank;
+      const int off = pl.members[mi] * g.pitch_part + c;
+      float v = part_s[off];
+      for (int ph = 1; ph < KS; ++ph) v += part_s[ph * plane + off];
+      part_s[off] = v;
+    }
+  }
   // ---- cluster exchange: xa = bf16(sum of the cl partials, in rank order) ----
   unit_sync();
   {
@@ -338,8 +359,15 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
     for (int e = e_lo + tid; e < e_hi; e += kConsumerWarps * 32) {
       const int mi = e / p.max_rank, c = e - mi * p.max_rank, pos = pl.members[mi];
       const int off = pos * g.pitch_part + c;
-      float sum = cluster.map_shared_rank(part_s, 0)[off];
-      for (int q = 1; q < g.cl; ++q) sum += cluster.map_shared_rank(part_s, q)[off];
+      // rank order; k-phase order within a rank (already folded into plane 0 with peers)
+      float sum;
+      if (g.cl > 1) {
+        sum = cluster.map_shared_rank(part_s, 0)[off];
+        for (int q = 1; q < g.cl; ++q) sum += cluster.map_shared_rank(part_s, q)[off];
+      } else {
+        sum = part_s[off];
+        for (int ph = 1; ph < KS; ++ph) sum += part_s[ph * plane + off];
+      }
       const uint16_t xb = f32_to_bf16_bits(sum);
       const int xoff = pos * xa_pitch_el + c;
       for (int q = 0; q < g.cl; ++q) cluster.map_shared_rank(xa_s, q)[xoff] = xb;
