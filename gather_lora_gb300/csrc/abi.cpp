@@ -157,6 +157,7 @@ bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_
     g.clusters = static_cast<int>(std::max(1LL, ceil_div(rows, g.tile_rows)) * max_loras);
   } else {
     g.tile_rows = g.rt;
+    g.direct = max_loras <= rows ? 1 : 0;   // same unit count as the slot-by-slot numbering
     g.clusters = rows <= 0 ? 0 : rows / g.rt + std::min(rows, max_loras);
   }
   return true;

@@ -57,7 +57,7 @@ struct Plan {
   int NV;                          // valid positions (sum of group sizes)
   int failed;                      // an mbarrier wait gave up: no further stores
   int warp_sums[kWarps];
-  int found_slot, found_tile, found_rows;  // bgmv planning scratch
+  int found_slot, found_tile;      // bgmv planning scratch
   int members[kMaxRows];           // positions, grouped, ascending within a group
   int gstart[kMaxRows + 1];        // group g = members[gstart[g] .. gstart[g+1])
   int grow[kMaxRows];              // position -> row of x / base_out
@@ -505,9 +505,12 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
 
 // ============================================================================
 // Routed bgmv: work unit = up to rt rows of one slot, in ascending row order.
-// Units are numbered slot by slot (ascending slot, then ascending tile) over
-// every slot that has rows, so the static grid bound is n/rt + min(n, max_loras)
-// units; a unit whose slot has a NULL table entry finds nothing to do.
+// Direct numbering (max_loras <= n): unit s < max_loras is tile 0 of slot s, so
+// its table entries are loaded at once, beside seq_slot; units from max_loras
+// on are the further tiles (1, 2, ...) of slots with more than rt rows, in slot
+// order. Otherwise units are numbered slot by slot over every slot that has
+// rows. Either way the static grid bound is n/rt + min(n, max_loras) units; a
+// unit that finds no rows, or whose slot has a NULL table entry, does nothing.
 // ============================================================================
 template <int MAXT>
 __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __grid_constant__ BgmvArgs p) {
@@ -521,48 +524,60 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
 
   pdl_wait_then_release();
 
-  // seq_slot and the per-slot row counts live in the not-yet-used ring.
-  int* ss = reinterpret_cast<int*>(smem + g.off_ring);
-  int* cnt = ss + ((p.n + 3) & ~3);
-  for (int i = tid; i < p.n; i += kThreads) ss[i] = p.seq_slot[i];
-  for (int s = tid; s < p.max_loras; s += kThreads) cnt[s] = 0;
-  if (tid == 0) pl.found_slot = -1;
-  __syncthreads();
-  for (int i = tid; i < p.n; i += kThreads) {
-    const int s = ss[i];
-    if (s >= 0 && s < p.max_loras) atomicAdd(&cnt[s], 1);
-  }
-  __syncthreads();
-  // Units per slot, prefix over slots, locate this cluster's (slot, tile).
-  {
-    const int per = (p.max_loras + kThreads - 1) / kThreads;
-    const int lo = min(tid * per, p.max_loras), hi = min(lo + per, p.max_loras);
-    int local = 0;
-    for (int s = lo; s < hi; ++s) local += (cnt[s] + g.rt - 1) / g.rt;
-    int run = block_inclusive_sum(local, pl.warp_sums) - local;
-    for (int s = lo; s < hi; ++s) {
-      const int t = (cnt[s] + g.rt - 1) / g.rt;
-      if (unit >= run && unit < run + t) {
-        pl.found_slot = s;
-        pl.found_tile = unit - run;
-        pl.found_rows = min(g.rt, cnt[s] - (unit - run) * g.rt);
-      }
-      run += t;
-    }
-  }
-  __syncthreads();
-  const int slot = pl.found_slot;
-  if (slot < 0) return;  // every CTA of the cluster takes this branch together
-  const int R = pl.found_rows, want_lo = pl.found_tile * g.rt;
-  const uint16_t* tab_a = nullptr;  // table entries: the loads overlap the row compaction below
+  const bool first_tile = g.direct && unit < p.max_loras;
+  int slot = first_tile ? unit : -1, tile = 0;
+  const uint16_t* tab_a = nullptr;  // table entries: the loads overlap the scans below
   const uint16_t* tab_b = nullptr;
   float tab_s = 0.f;
-  if (tid == 0) {
+  if (first_tile && tid == 0) {
     tab_a = p.a_table[slot];
     tab_b = p.b_table[slot];
     tab_s = p.scale_table[slot];
   }
-  // Rows of this slot in ascending order; keep ranks [want_lo, want_lo + R).
+  // seq_slot (and the per-slot row counts) live in the not-yet-used ring.
+  int* ss = reinterpret_cast<int*>(smem + g.off_ring);
+  int* cnt = ss + ((p.n + 3) & ~3);
+  for (int i = tid; i < p.n; i += kThreads) ss[i] = p.seq_slot[i];
+  if (!first_tile) {
+    for (int s = tid; s < p.max_loras; s += kThreads) cnt[s] = 0;
+    if (tid == 0) pl.found_slot = -1;
+    __syncthreads();
+    for (int i = tid; i < p.n; i += kThreads) {
+      const int s = ss[i];
+      if (s >= 0 && s < p.max_loras) atomicAdd(&cnt[s], 1);
+    }
+    __syncthreads();
+    // Tiles per slot (direct numbering: only the tiles after the first), prefix
+    // over slots, locate this cluster's (slot, tile).
+    const int v = g.direct ? unit - p.max_loras : unit, t0 = g.direct ? 1 : 0;
+    const int per = (p.max_loras + kThreads - 1) / kThreads;
+    const int lo = min(tid * per, p.max_loras), hi = min(lo + per, p.max_loras);
+    int local = 0;
+    for (int s = lo; s < hi; ++s) local += max(0, (cnt[s] + g.rt - 1) / g.rt - t0);
+    int run = block_inclusive_sum(local, pl.warp_sums) - local;
+    for (int s = lo; s < hi; ++s) {
+      const int t = max(0, (cnt[s] + g.rt - 1) / g.rt - t0);
+      if (v >= run && v < run + t) {
+        pl.found_slot = s;
+        pl.found_tile = t0 + v - run;
+      }
+      run += t;
+    }
+    __syncthreads();
+    slot = pl.found_slot;
+    if (slot < 0) return;  // every CTA of the cluster takes this branch together
+    tile = pl.found_tile;
+    if (tid == 0) {
+      tab_a = p.a_table[slot];
+      tab_b = p.b_table[slot];
+      tab_s = p.scale_table[slot];
+    }
+  } else {
+    __syncthreads();
+  }
+  // Rows of this slot in ascending order; keep ranks [want_lo, want_lo + rt).
+  const int want_lo = tile * g.rt;
+  int R;
   {
     int base = 0;
     for (int i0 = 0; i0 < p.n; i0 += kThreads) {
@@ -579,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
         total += c;
       }
       const int rank = base + before + __popc(bal & ((1u << lane) - 1u));
-      if (f && rank >= want_lo && rank < want_lo + R) {
+      if (f && rank >= want_lo && rank < want_lo + g.rt) {
         const int pos = rank - want_lo;
         pl.members[pos] = pos;
         pl.grow[pos] = i;
@@ -588,7 +603,9 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
       base += total;
       __syncthreads();
     }
+    R = min(g.rt, base - want_lo);
   }
+  if (R <= 0) return;  // no rows for this unit (every thread computed the same count)
   if (tid == 0) {
     pl.gA[0] = tab_a;
     pl.gB[0] = tab_b;

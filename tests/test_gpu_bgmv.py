@@ -94,6 +94,19 @@ def test_bgmv_one_hot_slot_heavy():
     compare_bgmv(wl, g_out, o_out, g_xa, o_xa, o_d)
 
 
+def test_bgmv_units_numbered_slot_by_slot():
+    """max_loras > n: units are numbered over the slots that have rows (not one
+    per slot), including a slot with more than one tile of rows and slots at
+    both ends of the table."""
+    seq = np.random.default_rng(3).permutation([150] * 40 + [3] * 30 + [199] * 5 + [0] * 5)
+    wl = W.make_bgmv("many_slots", n=80, k_in=1032, n_out=520, max_loras=200, max_rank=16,
+                     rank_choices=(16, 8), alpha=32.0, rslora=False,
+                     slot_law="list:" + ",".join(str(int(v)) for v in seq), slot_base_frac=0.0, seed=11)
+    g_out, g_xa = gpu_bgmv(wl)
+    o_out, o_xa, o_d = oracle_bgmv(wl)
+    compare_bgmv(wl, g_out, o_out, g_xa, o_xa, o_d)
+
+
 @pytest.mark.parametrize("name", ["decode_qproj_bgmv", "qkv_kfold_bgmv", "ffn_down_bgmv"])
 def test_bgmv_batch_invariance(name):
     """Each row folded alone (n = 1 per call) is bit-identical to the batched call."""
