@@ -65,6 +65,7 @@ constexpr int kStageTarget = GLORA_STAGE_TARGET;
 constexpr int kMinStage = GLORA_MIN_STAGE;
 constexpr int kMaxStages = 8;
 constexpr long long kMoeMinUnits = GLORA_MOE_MIN_UNITS;  // MoE work units that keep the GPU busy
+constexpr int kGatherBytes = 24 * 1024;                  // largest all-gather buffer of the exchange
 
 // Split `total` into equal chunks of at most `cap` (multiples of 16).
 int balanced_chunk(int total, int cap) {
@@ -113,8 +114,12 @@ bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_
   // ksplit k-phases of kConsumerWarps / ksplit warps each.
   // (Only without cluster peers: with peers the cluster already splits k, and
   // the extra planes would lengthen the exchange.)
+  // With cluster peers and small partials, the exchange is an all-gather of
+  // the fp32 partials (one cluster barrier; planes folded locally), which also
+  // lets the k-phase split run under a cluster.
+  g.gather = (g.cl > 1 && g.cl * g.rt * (max_rank + 4) * 4 <= kGatherBytes) ? 1 : 0;
   g.ksplit = 1;
-  if (!g.group_parallel && g.cl == 1)
+  if (!g.group_parallel && (g.cl == 1 || g.gather))
     while (g.ksplit < glora::kConsumerWarps && (glora::kConsumerWarps / (2 * g.ksplit)) >= tiles) g.ksplit *= 2;
   g.maxt = 1;
   if (g.group_parallel) {
@@ -132,7 +137,8 @@ bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_
   g.stage_bytes = round_up(std::max(shrink_stage, expand_stage), 128);
   g.pitch_part = max_rank + 4;
   g.pitch_xa = max_rank * 2 + 16;
-  const int fixed = glora::kPlanBytes + g.ksplit * g.rt * g.pitch_part * 4 + g.rt * g.pitch_xa;
+  const int planes = g.ksplit + (g.gather ? g.cl : 0);   // partial planes (+ the all-gather slots)
+  const int fixed = glora::kPlanBytes + planes * g.rt * g.pitch_part * 4 + g.rt * g.pitch_xa;
   int ns = (kBudgetTwoPerSm - fixed) / g.stage_bytes;
   if (ns < 2) ns = (kBudgetOnePerSm - fixed) / g.stage_bytes;
   ns = std::min(ns, kMaxStages);
@@ -145,7 +151,7 @@ bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_
   g.off_ring = glora::kPlanBytes;
   g.off_out = 0;
   g.off_part = g.off_ring + ns * g.stage_bytes;
-  g.off_xa = g.off_part + g.ksplit * g.rt * g.pitch_part * 4;
+  g.off_xa = g.off_part + planes * g.rt * g.pitch_part * 4;
   g.smem_bytes = g.off_xa + g.rt * g.pitch_xa;
   if (g.smem_bytes > kBudgetOnePerSm + 2048) return false;
   if (moe) {

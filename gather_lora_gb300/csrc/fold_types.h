@@ -28,6 +28,7 @@ struct FoldGeometry {
   int group_parallel;  // 1: each consumer warp owns whole groups; 0: warps split every item's tiles
   int ksplit;       // tile-parallel: k-phases the consumer warps form (1, 2, 4, 8; partial planes of part_s)
   int direct;       // bgmv: unit s < max_loras is tile 0 of slot s (max_loras <= rows)
+  int gather;       // exchange by all-gather of fp32 partials into cl planes after the k-phase planes
   int mr16;         // max_rank rounded up to 16
   int pitch_k;      // bytes per A or x row in a shrink stage (kch*2 + 16)
   int pitch_b;      // bytes per B row in an expand stage

@@ -213,7 +213,7 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
     const int pre = min(n_items, n_shrink + ns);
     for (int it = 0; it < pre; ++it) produce(it);
     unit_sync();
-    unit_sync();
+    if (!g.gather) unit_sync();
     for (int it = pre; it < n_items; ++it) produce(it);
     return n_items;
   }
@@ -337,29 +337,54 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
     }
   }
 
-  // With cluster peers, each CTA first adds its own k-phase planes into plane
-  // 0 (in phase order), so the exchange reads one plane per rank.
-  if (KS > 1 && g.cl > 1) {
+  // ---- exchange: xa = bf16(sum of the partials: cluster ranks in order, and
+  //      k-phase planes in order within a rank) ----
+  const int xa_pitch_el = g.pitch_xa >> 1;
+  const bool store_xa = p.xa != nullptr && pl.failed == 0;
+  if (g.gather) {
+    // All-gather: each CTA adds its k-phase planes and stores the result into
+    // slot crank of every peer's gather buffer (one cluster barrier); then every
+    // CTA adds the cl slots in rank order itself.
+    float* gath = part_s + KS * plane;
     consumer_sync();
     for (int e = tid; e < NV * p.max_rank; e += kConsumerWarps * 32) {
       const int mi = e / p.max_rank, c = e - mi * p.max_rank;
       const int off = pl.members[mi] * g.pitch_part + c;
       float v = part_s[off];
       for (int ph = 1; ph < KS; ++ph) v += part_s[ph * plane + off];
-      part_s[off] = v;
+      for (int q = 0; q < g.cl; ++q) cluster.map_shared_rank(gath, q)[crank * plane + off] = v;
     }
-  }
-  // ---- cluster exchange: xa = bf16(sum of the cl partials, in rank order) ----
-  unit_sync();
-  {
+    unit_sync();
+    for (int e = tid; e < NV * p.max_rank; e += kConsumerWarps * 32) {
+      const int mi = e / p.max_rank, c = e - mi * p.max_rank, pos = pl.members[mi];
+      const int off = pos * g.pitch_part + c;
+      float sum = gath[off];
+      for (int q = 1; q < g.cl; ++q) sum += gath[q * plane + off];
+      const uint16_t xb = f32_to_bf16_bits(sum);
+      xa_s[pos * xa_pitch_el + c] = xb;
+      if (store_xa && e % g.cl == crank) p.xa[(long long)pl.xarow[pos] * p.max_rank + c] = xb;
+    }
+    consumer_sync();
+  } else {
+    // Reduce-scatter: CTA crank adds its share of the elements over the ranks'
+    // partials (each rank first folds its own k-phase planes) and pushes the
+    // BF16 result to every CTA of the cluster.
+    if (KS > 1 && g.cl > 1) {
+      consumer_sync();
+      for (int e = tid; e < NV * p.max_rank; e += kConsumerWarps * 32) {
+        const int mi = e / p.max_rank, c = e - mi * p.max_rank;
+        const int off = pl.members[mi] * g.pitch_part + c;
+        float v = part_s[off];
+        for (int ph = 1; ph < KS; ++ph) v += part_s[ph * plane + off];
+        part_s[off] = v;
+      }
+    }
+    unit_sync();
     const int E = NV * p.max_rank, per = (E + g.cl - 1) / g.cl;
     const int e_lo = crank * per, e_hi = min(e_lo + per, E);
-    const int xa_pitch_el = g.pitch_xa >> 1;
-    const bool store = pl.failed == 0;
     for (int e = e_lo + tid; e < e_hi; e += kConsumerWarps * 32) {
       const int mi = e / p.max_rank, c = e - mi * p.max_rank, pos = pl.members[mi];
       const int off = pos * g.pitch_part + c;
-      // rank order; k-phase order within a rank (already folded into plane 0 with peers)
       float sum;
       if (g.cl > 1) {
         sum = cluster.map_shared_rank(part_s, 0)[off];
@@ -371,10 +396,10 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
       const uint16_t xb = f32_to_bf16_bits(sum);
       const int xoff = pos * xa_pitch_el + c;
       for (int q = 0; q < g.cl; ++q) cluster.map_shared_rank(xa_s, q)[xoff] = xb;
-      if (p.xa && store) p.xa[(long long)pl.xarow[pos] * p.max_rank + c] = xb;
+      if (store_xa) p.xa[(long long)pl.xarow[pos] * p.max_rank + c] = xb;
     }
+    unit_sync();
   }
-  unit_sync();
 
   // ---- expand + fold over this CTA's j-slice ---------------------------------
   // Work comes in 16-column blocks of two 16x8 tensor-core tiles (16 group rows
