@@ -416,33 +416,27 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
   const int scol = odd ? 2 * q + 6 : 2 * q;                            // first stored column
   const int brow4 = (lane >> 4) * 8 + (lane & 7), bk4 = ((lane >> 3) & 1) << 4;   // ldmatrix.x4 of B
   const int brow2 = ((lane >> 3) & 1) * 8 + (lane & 7);                // ldmatrix.x2 of B (k8 tail)
-  for (int e = 0; e < G * nj; ++e) {
-    const int gi = e / nj, jc = e - gi * nj;
+  for (int gi = 0; gi < G; ++gi) {
     const int m0 = pl.gstart[gi], R = pl.gstart[gi + 1] - m0;
     const float scale = pl.gscale[gi];
-    const int ri = it0 + n_shrink + e, s = ri % ns;
-    if (!mbar_wait(smem_u32(&pl.full[s]), (ri / ns) & 1) && lane == 0) record_timeout(pl);
-    const uint32_t st = ring_u32 + s * g.stage_bytes;
-    const int j0 = j_lo + jc * g.jch, jlen = min(g.jch, j_hi - j0), NCB = (jlen + 15) >> 4;
-    const bool store = pl.failed == 0;
-    // xa row (lane & 15) of each 16-row tile (rows past R repeat the last one)
-    uint32_t a_row[2];
+    // Per group: xa row (lane & 15) of each 16-row tile (rows past R repeat the
+    // last one), and for rows gq + 8 * hh the offset of the staged old values
+    // inside a stage (rows past R read the last row, in bounds) and the output
+    // row (NULL past R).
+    uint32_t a_row[2], rowoff[4];
+    uint16_t* obase[4];
 #pragma unroll
     for (int mr = 0; mr < 2; ++mr) a_row[mr] = xa_base + pl.members[m0 + min(mr * 16 + (lane & 15), R - 1)] * g.pitch_xa;
-    // rows gq + 8 * hh: staged old values (rows past R read the last row, in
-    // bounds) and output pointers (NULL past R)
-    uint32_t old_row[4];
-    uint16_t* orow[4];
 #pragma unroll
     for (int hh = 0; hh < 4; ++hh) {
       const int r = hh * 8 + gq;
-      old_row[hh] = st + out_region + min(r, R - 1) * pitch_o + 4 * q;
-      orow[hh] = (r < R && store) ? p.out + (long long)pl.grow[pl.members[m0 + r]] * p.out_stride + j0 + scol : nullptr;
+      rowoff[hh] = out_region + min(r, R - 1) * pitch_o + 4 * q;
+      obase[hh] = r < R ? p.out + (long long)pl.grow[pl.members[m0 + r]] * p.out_stride + scol : nullptr;
     }
-    // The block loop, compiled per row-tile count MR (1, 2) and per KS, the
-    // k16 steps whose xa fragments stay in registers (1: max_rank 16, 2:
-    // max_rank 32; 0: any max_rank, fragments loaded per step, k8 tail).
-    auto blocks = [&](auto mr_c, auto ks_c) {
+    // The group's expand items, compiled per row-tile count MR (1, 2) and per
+    // KS, the k16 steps whose xa fragments stay in registers (1: max_rank 16,
+    // 2: max_rank 32; 0: any max_rank, fragments loaded per step, k8 tail).
+    auto items = [&](auto mr_c, auto ks_c) {
       constexpr int MR = decltype(mr_c)::value, KS = decltype(ks_c)::value;
       uint32_t af[MR][KS > 0 ? KS : 1][4];
       if (KS > 0) {
@@ -452,78 +446,85 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
           for (int ks = 0; ks < (KS > 0 ? KS : 1); ++ks)
             ldsm_x4(a_row[mr] + ks * 32 + ((lane >> 4) << 4), af[mr][ks][0], af[mr][ks][1], af[mr][ks][2], af[mr][ks][3]);
       }
-      for (int cb = warp; cb < NCB; cb += kConsumerWarps) {
-        float d[MR][2][4];
+      for (int jc = 0; jc < nj; ++jc) {
+        const int ri = it0 + n_shrink + gi * nj + jc, s = ri % ns;
+        if (!mbar_wait(smem_u32(&pl.full[s]), (ri / ns) & 1) && lane == 0) record_timeout(pl);
+        const uint32_t st = ring_u32 + s * g.stage_bytes;
+        const int j0 = j_lo + jc * g.jch, jlen = min(g.jch, j_hi - j0), NCB = (jlen + 15) >> 4;
+        const bool store = pl.failed == 0;
+        for (int cb = warp; cb < NCB; cb += kConsumerWarps) {
+          float d[MR][2][4];
 #pragma unroll
-        for (int mr = 0; mr < MR; ++mr)
+          for (int mr = 0; mr < MR; ++mr)
 #pragma unroll
-          for (int t = 0; t < 2; ++t) d[mr][t][0] = d[mr][t][1] = d[mr][t][2] = d[mr][t][3] = 0.f;
-        const uint32_t bblk = st + cb * 16 * g.pitch_b;
-        if (KS > 0) {
+            for (int t = 0; t < 2; ++t) d[mr][t][0] = d[mr][t][1] = d[mr][t][2] = d[mr][t][3] = 0.f;
+          const uint32_t bblk = st + cb * 16 * g.pitch_b;
+          if (KS > 0) {
 #pragma unroll
-          for (int ks = 0; ks < (KS > 0 ? KS : 1); ++ks) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(bblk + brow4 * g.pitch_b + ks * 32 + bk4, b0, b1, b2, b3);
+            for (int ks = 0; ks < (KS > 0 ? KS : 1); ++ks) {
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4(bblk + brow4 * g.pitch_b + ks * 32 + bk4, b0, b1, b2, b3);
 #pragma unroll
-            for (int mr = 0; mr < MR; ++mr) {
-              mma_k16(d[mr][0], af[mr][ks][0], af[mr][ks][1], af[mr][ks][2], af[mr][ks][3], b0, b1);
-              mma_k16(d[mr][1], af[mr][ks][0], af[mr][ks][1], af[mr][ks][2], af[mr][ks][3], b2, b3);
+              for (int mr = 0; mr < MR; ++mr) {
+                mma_k16(d[mr][0], af[mr][ks][0], af[mr][ks][1], af[mr][ks][2], af[mr][ks][3], b0, b1);
+                mma_k16(d[mr][1], af[mr][ks][0], af[mr][ks][1], af[mr][ks][2], af[mr][ks][3], b2, b3);
+              }
+            }
+          } else {
+            int kk = 0;
+            for (; kk + 16 <= p.max_rank; kk += 16) {
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4(bblk + brow4 * g.pitch_b + kk * 2 + bk4, b0, b1, b2, b3);
+#pragma unroll
+              for (int mr = 0; mr < MR; ++mr) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(a_row[mr] + kk * 2 + ((lane >> 4) << 4), a0, a1, a2, a3);
+                mma_k16(d[mr][0], a0, a1, a2, a3, b0, b1);
+                mma_k16(d[mr][1], a0, a1, a2, a3, b2, b3);
+              }
+            }
+            if (kk < p.max_rank) {                     // k8 tail (max_rank % 16 == 8)
+              uint32_t b0, b1;
+              ldsm_x2(bblk + brow2 * g.pitch_b + kk * 2, b0, b1);
+#pragma unroll
+              for (int mr = 0; mr < MR; ++mr) {
+                uint32_t a0, a1;
+                ldsm_x2(a_row[mr] + kk * 2, a0, a1);
+                mma_k8(d[mr][0], a0, a1, b0);
+                mma_k8(d[mr][1], a0, a1, b1);
+              }
             }
           }
-        } else {
-          int kk = 0;
-          for (; kk + 16 <= p.max_rank; kk += 16) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(bblk + brow4 * g.pitch_b + kk * 2 + bk4, b0, b1, b2, b3);
+          const int c0 = cb * 16;
+          const bool col_ok = c0 + scol < jlen;         // the last block may hold only 8 columns
 #pragma unroll
-            for (int mr = 0; mr < MR; ++mr) {
-              uint32_t a0, a1, a2, a3;
-              ldsm_x4(a_row[mr] + kk * 2 + ((lane >> 4) << 4), a0, a1, a2, a3);
-              mma_k16(d[mr][0], a0, a1, a2, a3, b0, b1);
-              mma_k16(d[mr][1], a0, a1, a2, a3, b2, b3);
-            }
-          }
-          if (kk < p.max_rank) {                     // k8 tail (max_rank % 16 == 8)
-            uint32_t b0, b1;
-            ldsm_x2(bblk + brow2 * g.pitch_b + kk * 2, b0, b1);
-#pragma unroll
-            for (int mr = 0; mr < MR; ++mr) {
-              uint32_t a0, a1;
-              ldsm_x2(a_row[mr] + kk * 2, a0, a1);
-              mma_k8(d[mr][0], a0, a1, b0);
-              mma_k8(d[mr][1], a0, a1, b1);
+          for (int hh = 0; hh < 2 * MR; ++hh) {
+            const int mr = hh >> 1, h = hh & 1;
+            if (hh == 0 || hh * 8 < R) {                // warp-uniform: this row half has rows
+              uint32_t o0, o1;
+              asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(o0) : "r"(st + rowoff[hh] + c0 * 2));
+              asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(o1) : "r"(st + rowoff[hh] + c0 * 2 + 16));
+              const uint32_t f0 = fold_pair(d[mr][0][2 * h], d[mr][0][2 * h + 1], scale, o0);
+              const uint32_t f1 = fold_pair(d[mr][1][2 * h], d[mr][1][2 * h + 1], scale, o1);
+              const uint32_t recv = __shfl_xor_sync(0xffffffffu, odd ? f0 : f1, 1);
+              uint16_t* o = obase[hh];
+              if (o && store && col_ok) {
+                const uint32_t lo = odd ? recv : f0, hi = odd ? f1 : recv;
+                asm volatile("st.global.v2.b32 [%0], {%1, %2};\n" ::"l"(o + j0 + c0), "r"(lo), "r"(hi) : "memory");
+              }
             }
           }
         }
-        const int c0 = cb * 16;
-        const bool col_ok = c0 + scol < jlen;         // the last block may hold only 8 columns
-#pragma unroll
-        for (int hh = 0; hh < 2 * MR; ++hh) {
-          const int mr = hh >> 1, h = hh & 1;
-          if (hh == 0 || hh * 8 < R) {                // warp-uniform: this row half has rows
-            uint32_t o0, o1;
-            asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(o0) : "r"(old_row[hh] + c0 * 2));
-            asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(o1) : "r"(old_row[hh] + c0 * 2 + 16));
-            const uint32_t f0 = fold_pair(d[mr][0][2 * h], d[mr][0][2 * h + 1], scale, o0);
-            const uint32_t f1 = fold_pair(d[mr][1][2 * h], d[mr][1][2 * h + 1], scale, o1);
-            const uint32_t recv = __shfl_xor_sync(0xffffffffu, odd ? f0 : f1, 1);
-            uint16_t* o = orow[hh];
-            if (o && col_ok) {
-              const uint32_t lo = odd ? recv : f0, hi = odd ? f1 : recv;
-              asm volatile("st.global.v2.b32 [%0], {%1, %2};\n" ::"l"(o + c0), "r"(lo), "r"(hi) : "memory");
-            }
-          }
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&pl.empty[s]));
       }
     };
     using I1 = std::integral_constant<int, 1>;
     using I2 = std::integral_constant<int, 2>;
     using I0 = std::integral_constant<int, 0>;
-    if (p.max_rank == 16) { if (R <= 16) blocks(I1{}, I1{}); else blocks(I2{}, I1{}); }
-    else if (p.max_rank == 32) { if (R <= 16) blocks(I1{}, I2{}); else blocks(I2{}, I2{}); }
-    else { if (R <= 16) blocks(I1{}, I0{}); else blocks(I2{}, I0{}); }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&pl.empty[s]));
+    if (p.max_rank == 16) { if (R <= 16) items(I1{}, I1{}); else items(I2{}, I1{}); }
+    else if (p.max_rank == 32) { if (R <= 16) items(I1{}, I2{}); else items(I2{}, I2{}); }
+    else { if (R <= 16) items(I1{}, I0{}); else items(I2{}, I0{}); }
   }
   return n_items;
 }
