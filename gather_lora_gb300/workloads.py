@@ -105,7 +105,7 @@ class MoeWorkload:
     max_loras: int
     max_rank: int
     cap: int
-    x: np.ndarray                # uint16 [te, k_in]
+    x: np.ndarray                # uint16 [te, k_in] (down), or [num_tokens, k_in] token-major (x_gather)
     out_buf: np.ndarray          # uint16 [te, n_out]
     expert_offsets: np.ndarray   # int32 [E+1]
     sorted_token_ids: np.ndarray  # int32 [te]
@@ -115,6 +115,7 @@ class MoeWorkload:
     b_pool: np.ndarray           # uint16 [max_loras * E, n_out, max_rank]
     scale: np.ndarray            # float32 [max_loras * E]
     meta: dict = field(default_factory=dict)
+    x_gather: bool = False       # gate/up: sorted row r reads token row sorted_token_ids[r] of x
 
     def windows(self):
         return [(s, min(s + self.cap, self.te)) for s in range(0, self.te, self.cap)] or [(0, 0)]
@@ -207,7 +208,7 @@ def make_bgmv(name, *, n, k_in, n_out, max_loras, max_rank, rank_choices, alpha,
 
 def make_moe(name, *, num_tokens, top_k, num_experts, k_in, n_out, max_loras, max_rank,
              rank, alpha, adapter_base_frac, cap, seed, use_row_adapter=True,
-             present_frac=1.0, b_std=0.02) -> MoeWorkload:
+             present_frac=1.0, b_std=0.02, x_gather=False) -> MoeWorkload:
     """Draw one MoE grouped-fold workload.
 
     Routing: each token takes the top_k experts of N(0,1) logits (softmax is
@@ -229,9 +230,12 @@ def make_moe(name, *, num_tokens, top_k, num_experts, k_in, n_out, max_loras, ma
     expert_offsets = np.zeros(num_experts + 1, dtype=np.int32)
     expert_offsets[1:] = np.cumsum(counts)
     te = int(expert_offsets[-1])
-    g = rng.standard_normal((te, k_in), dtype=np.float32)
-    u = rng.standard_normal((te, k_in), dtype=np.float32)
-    x = to_bf16_bits((g / (1.0 + np.exp(-g))) * u)
+    if x_gather:   # gate/up input: token-major hidden states ~ N(0, 1)
+        x = to_bf16_bits(rng.standard_normal((num_tokens, k_in), dtype=np.float32))
+    else:          # down input: post-SiLU sorted activations
+        g = rng.standard_normal((te, k_in), dtype=np.float32)
+        u = rng.standard_normal((te, k_in), dtype=np.float32)
+        x = to_bf16_bits((g / (1.0 + np.exp(-g))) * u)
     out_buf = to_bf16_bits(rng.standard_normal((te, n_out), dtype=np.float32))
     if use_row_adapter:
         ra = rng.integers(0, max_loras, size=num_tokens).astype(np.int32)
@@ -248,7 +252,73 @@ def make_moe(name, *, num_tokens, top_k, num_experts, k_in, n_out, max_loras, ma
     scale = np.where(present, lora_scale(alpha, rank, False), 0.0).astype(np.float32)
     return MoeWorkload(name, num_tokens, top_k, num_experts, te, k_in, n_out, max_loras,
                        max_rank, cap, x, out_buf, expert_offsets, sorted_token_ids, ra,
-                       present, a_pool, b_pool, scale, meta=dict(seed=seed))
+                       present, a_pool, b_pool, scale, meta=dict(seed=seed), x_gather=x_gather)
+
+
+@dataclass
+class MoeGatherWorkload:
+    """One decode-path MoE fold over flat, unsorted (token, slot) rows on the host:
+    row r = token * top_k + j takes expert indices[r] and adapter
+    row_adapter[r // top_k]; tables are adapter-major (a * E + e)."""
+    name: str
+    num_tokens: int
+    top_k: int
+    num_experts: int
+    k_in: int
+    n_out: int
+    max_loras: int
+    max_rank: int
+    x: np.ndarray                # uint16 [n_rows, k_in]
+    out_buf: np.ndarray          # uint16 [n_rows, n_out]
+    indices: np.ndarray          # int32 [n_rows]
+    row_adapter: np.ndarray | None  # int32 [num_tokens] or None
+    present: np.ndarray          # bool [max_loras * E]
+    a_pool: np.ndarray
+    b_pool: np.ndarray
+    scale: np.ndarray            # float32 [max_loras * E]
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def n_rows(self):
+        return self.num_tokens * self.top_k
+
+    def a_list(self):
+        return [self.a_pool[i] if self.present[i] else None for i in range(len(self.present))]
+
+    def b_list(self):
+        return [self.b_pool[i] if self.present[i] else None for i in range(len(self.present))]
+
+
+def make_moe_gather(name, *, num_tokens, top_k, num_experts, k_in, n_out, max_loras, max_rank,
+                    rank, alpha, adapter_base_frac, seed, use_row_adapter=True,
+                    present_frac=1.0, b_std=0.02) -> MoeGatherWorkload:
+    """Draw one decode-path MoE workload: routing as in make_moe (top_k experts of
+    N(0,1) logits per token), rows left in (token, slot) order; x = SiLU(N)*N per
+    row (post-SiLU down_proj input), base_out ~ N(0,1)."""
+    rng = np.random.default_rng(seed)
+    logits = rng.standard_normal((num_tokens, num_experts), dtype=np.float32)
+    indices = np.argsort(-logits, axis=1, kind="stable")[:, :top_k].reshape(-1).astype(np.int32)
+    n_rows = num_tokens * top_k
+    g = rng.standard_normal((n_rows, k_in), dtype=np.float32)
+    u = rng.standard_normal((n_rows, k_in), dtype=np.float32)
+    x = to_bf16_bits((g / (1.0 + np.exp(-g))) * u)
+    out_buf = to_bf16_bits(rng.standard_normal((n_rows, n_out), dtype=np.float32))
+    if use_row_adapter:
+        ra = rng.integers(0, max_loras, size=num_tokens).astype(np.int32)
+        ra[rng.random(num_tokens) < adapter_base_frac] = -1
+    else:
+        ra = None
+    count = max_loras * num_experts
+    present = np.ones(count, dtype=bool)
+    if present_frac < 1.0:
+        present = rng.random(count) < present_frac
+    ranks = np.where(present, rank, 0).astype(np.int32)
+    a_pool, b_pool = _pack_pool(rng, count, present, ranks, max_rank, k_in, n_out,
+                                1.0 / math.sqrt(k_in), b_std)
+    scale = np.where(present, lora_scale(alpha, rank, False), 0.0).astype(np.float32)
+    return MoeGatherWorkload(name, num_tokens, top_k, num_experts, k_in, n_out, max_loras,
+                             max_rank, x, out_buf, indices, ra, present, a_pool, b_pool, scale,
+                             meta=dict(seed=seed))
 
 
 # --- the five named workloads --------------------------------------------------

@@ -57,9 +57,16 @@ def _bind(lib):
         u16p, u16p, ctypes.c_int32]
     lib.ora_lora_moe_grouped_fold.restype = ctypes.c_int
     lib.ora_lora_moe_grouped_fold.argtypes = [
-        u16p, ctypes.c_int64, u16p, ctypes.c_int64,
+        u16p, ctypes.c_int64, ctypes.c_int32, u16p, ctypes.c_int64,
         u16p, ctypes.c_int32, u16p, ctypes.c_int32, u16p, ctypes.c_int32,
         ctypes.c_int32, ctypes.c_int32,
+        u16p, u16p, u16p, ctypes.c_int32,
+        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+        u16p, u16p, ctypes.c_int32]
+    lib.ora_lora_moe_gather_bgmv.restype = ctypes.c_int
+    lib.ora_lora_moe_gather_bgmv.argtypes = [
+        u16p, ctypes.c_int64, u16p, ctypes.c_int64,
+        u16p, ctypes.c_int32, ctypes.c_int32, u16p, ctypes.c_int32, ctypes.c_int32,
         u16p, u16p, u16p, ctypes.c_int32,
         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
         u16p, u16p, ctypes.c_int32]
@@ -139,11 +146,13 @@ def lora_bgmv(x, x_row_stride, base_out, out_row_stride, seq_slot, a_list, b_lis
 def lora_moe_grouped_fold(x, x_row_stride, base_out, out_row_stride, expert_offsets,
                           sorted_token_ids, row_adapter, num_tokens, row_offset, row_end,
                           a_list, b_list, scale_table, max_rank, k_in, n_out, mode=0,
-                          lib=None):
+                          lib=None, x_gather=False):
     """Apply the MoE grouped fold to one window [row_offset, row_end) in place.
 
     Tables are lists of length max_loras * num_experts, adapter-major
     (index a * num_experts + e). row_adapter may be None (every row adapter 0).
+    x_gather: x is token-major and sorted row r reads row sorted_token_ids[r]
+    (gate/up); otherwise x is the sorted [te, k_in] activation (down).
     Returns (xa [row_end-row_offset, max_rank], d [te, n_out]).
     """
     lib = lib or load()
@@ -162,10 +171,40 @@ def lora_moe_grouped_fold(x, x_row_stride, base_out, out_row_stride, expert_offs
     xa = np.zeros((max(row_end - row_offset, 1), max_rank), dtype=np.uint16)
     d = np.zeros((max(te, 1), n_out), dtype=np.uint16)
     rc = lib.ora_lora_moe_grouped_fold(
-        _ptr(x), x_row_stride, _ptr(base_out), out_row_stride,
+        _ptr(x), x_row_stride, 1 if x_gather else 0, _ptr(base_out), out_row_stride,
         _ptr(offs), num_experts, _ptr(sti), te, _ptr(ra), num_tokens,
         row_offset, row_end, _ptr(a_tab), _ptr(b_tab), _ptr(scale), max_loras,
         max_rank, k_in, n_out, _ptr(xa), _ptr(d), mode)
     if rc != 0:
         raise ValueError(f"oracle lora_moe_grouped_fold rejected its arguments (rc={rc})")
     return xa[: row_end - row_offset], d[:te]
+
+
+def lora_moe_gather_bgmv(x, x_row_stride, base_out, out_row_stride, indices, top_k,
+                         row_adapter, num_tokens, num_experts, a_list, b_list, scale_table,
+                         max_rank, k_in, n_out, mode=0, lib=None):
+    """Apply the decode-path MoE fold over flat (token, slot) rows in place.
+
+    Row r: expert indices[r], adapter row_adapter[r // top_k] (None: adapter 0),
+    table index a * num_experts + e. Returns (xa [n_rows, max_rank], d [n_rows, n_out]).
+    """
+    lib = lib or load()
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    assert base_out.dtype == np.uint16 and base_out.flags.c_contiguous
+    idx = np.ascontiguousarray(indices, dtype=np.int32)
+    n_rows = int(idx.shape[0])
+    ra = None if row_adapter is None else np.ascontiguousarray(row_adapter, dtype=np.int32)
+    a_tab, a_keep = _table(a_list)
+    b_tab, b_keep = _table(b_list)
+    assert len(a_list) % num_experts == 0
+    max_loras = len(a_list) // num_experts
+    scale = np.ascontiguousarray(scale_table, dtype=np.float32)
+    xa = np.zeros((max(n_rows, 1), max_rank), dtype=np.uint16)
+    d = np.zeros((max(n_rows, 1), n_out), dtype=np.uint16)
+    rc = lib.ora_lora_moe_gather_bgmv(
+        _ptr(x), x_row_stride, _ptr(base_out), out_row_stride, _ptr(idx), n_rows, top_k,
+        _ptr(ra), num_tokens, num_experts, _ptr(a_tab), _ptr(b_tab), _ptr(scale), max_loras,
+        max_rank, k_in, n_out, _ptr(xa), _ptr(d), mode)
+    if rc != 0:
+        raise ValueError(f"oracle lora_moe_gather_bgmv rejected its arguments (rc={rc})")
+    return xa[:n_rows], d[:n_rows]

@@ -5,8 +5,8 @@
  * load this library. The product path (gather_lora_gb300, libgather_lora.so)
  * never calls it and shares no code, header or helper with it.
  *
- * What it computes is the plain per-row definition of the two operations, with
- * the rounding points that the pages fix and nothing else:
+ * What it computes is the plain per-row definition of the operations, with the
+ * rounding points that the pages fix and nothing else:
  *
  *   Function apply_lora_bgmv page (spark_model::layers::ops::lora_delta rustdoc),
  *   summary and "BYTE-IDENTICAL" paragraph:
@@ -21,8 +21,14 @@
  *     device expert_offsets prefix sum, token from sorted_token_ids, adapter gate
  *     from moe_row_adapter[token] (< 0 = base, NULL table = every row adapter 0),
  *     xa indexed at the LOCAL row r - row_offset; same fold math as the bgmv.
+ *     Down (x_gather == 0): x is the sorted [te, k_in] activation at row r;
+ *     gate/up (x_gather == 1): x is token-major and sorted row r reads row
+ *     sorted_token_ids[r] of it.
+ *   Same page, moe_lora_gather_bgmv entry: the decode-path twin over flat,
+ *     unsorted (token, slot) rows; expert from indices[row], adapter gate from
+ *     row_adapter[row / top_k].
  *
- * Readings where the pages are silent (each also listed in the design doc):
+ * Readings where the pages are silent:
  *   - fp32 -> BF16 is round-to-nearest-even.
  *   - fp32 accumulation is a plain sequential sum in index order (k, then c).
  *     Products of two BF16 values are exact in fp32, so fused or unfused
@@ -171,7 +177,7 @@ int ora_lora_bgmv(const uint16_t* x, int64_t x_row_stride,
 
 /* ---- MoE grouped fold over one window of expert-sorted rows --------------- */
 
-int ora_lora_moe_grouped_fold(const uint16_t* x, int64_t x_row_stride,
+int ora_lora_moe_grouped_fold(const uint16_t* x, int64_t x_row_stride, int32_t x_gather,
                               uint16_t* base_out, int64_t out_row_stride,
                               const int32_t* expert_offsets, int32_t num_experts,
                               const int32_t* sorted_token_ids, int32_t te,
@@ -195,12 +201,14 @@ int ora_lora_moe_grouped_fold(const uint16_t* x, int64_t x_row_stride,
             if (expert_offsets[k] <= r && r < expert_offsets[k + 1]) { e = k; break; }
         }
         if (e < 0) continue;
-        int32_t a = 0;
-        if (row_adapter) {
-            int32_t t = sorted_token_ids[r];
+        /* the row's token: needed for the adapter gate and for the gate/up
+           input (x_gather: x is token-major, row t of it feeds sorted row r) */
+        int32_t t = -1;
+        if (row_adapter || x_gather) {
+            t = sorted_token_ids[r];
             if (t < 0 || t >= num_tokens) continue;
-            a = row_adapter[t];
         }
+        int32_t a = row_adapter ? row_adapter[t] : 0;
         if (a < 0 || a >= max_loras) continue;
         int64_t ti = (int64_t)a * num_experts + e;
         const uint16_t* A = a_table[ti];
@@ -209,8 +217,51 @@ int ora_lora_moe_grouped_fold(const uint16_t* x, int64_t x_row_stride,
         int64_t local = r - row_offset;
         uint16_t* xa_row = xa ? xa + local * max_rank : xa_tmp;
         uint16_t* d_row = d_out ? d_out + (int64_t)r * n_out : NULL;
-        fold_one_row(x + (int64_t)r * x_row_stride, base_out + (int64_t)r * out_row_stride,
+        const int64_t xr = x_gather ? t : r;
+        fold_one_row(x + xr * x_row_stride, base_out + (int64_t)r * out_row_stride,
                      A, B, scale_table[ti], max_rank, k_in, n_out, xa_row, d_row, mode);
+    }
+    return 0;
+}
+
+/*
+ * Decode-path MoE fold over flat, unsorted (token, slot) rows ("Module
+ * moe_lora_grouped", moe_lora_gather_bgmv): row r takes its expert from
+ * indices[r] and its adapter from row_adapter[r / top_k] (< 0: no delta;
+ * row_adapter == NULL: adapter 0). The table entry is a * num_experts + e as
+ * for the grouped fold; rows with an expert outside [0, num_experts), a token
+ * outside [0, num_tokens), an adapter outside [0, max_loras) or a NULL entry
+ * are skipped. x and base_out are [n_rows, .] at row r; xa [n_rows, max_rank]
+ * and d_out [n_rows, n_out] at row r.
+ */
+int ora_lora_moe_gather_bgmv(const uint16_t* x, int64_t x_row_stride,
+                             uint16_t* base_out, int64_t out_row_stride,
+                             const int32_t* indices, int32_t n_rows, int32_t top_k,
+                             const int32_t* row_adapter, int32_t num_tokens, int32_t num_experts,
+                             const uint16_t* const* a_table, const uint16_t* const* b_table,
+                             const float* scale_table, int32_t max_loras,
+                             int32_t max_rank, int32_t k_in, int32_t n_out,
+                             uint16_t* xa, uint16_t* d_out, int32_t mode)
+{
+    if (num_experts <= 0 || top_k <= 0 || max_rank <= 0 || k_in <= 0 || n_out <= 0 || max_loras < 0) return -1;
+    if (n_rows < 0 || x_row_stride < k_in || out_row_stride < n_out) return -1;
+    uint16_t xa_tmp[4096];
+    if (max_rank > 4096) return -1;
+    for (int32_t r = 0; r < n_rows; ++r) {
+        const int32_t e = indices[r];
+        if (e < 0 || e >= num_experts) continue;
+        const int32_t t = r / top_k;
+        if (t >= num_tokens) continue;
+        const int32_t a = row_adapter ? row_adapter[t] : 0;
+        if (a < 0 || a >= max_loras) continue;
+        const int64_t entry = (int64_t)a * num_experts + e;
+        const uint16_t* A = a_table[entry];
+        const uint16_t* B = b_table[entry];
+        if (A == NULL || B == NULL) continue;
+        uint16_t* xa_row = xa ? xa + (int64_t)r * max_rank : xa_tmp;
+        uint16_t* d_row = d_out ? d_out + (int64_t)r * n_out : NULL;
+        fold_one_row(x + (int64_t)r * x_row_stride, base_out + (int64_t)r * out_row_stride,
+                     A, B, scale_table[entry], max_rank, k_in, n_out, xa_row, d_row, mode);
     }
     return 0;
 }

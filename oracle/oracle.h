@@ -27,7 +27,9 @@ int ora_lora_bgmv(const uint16_t* x, int64_t x_row_stride,
                   int32_t max_rank, int32_t k_in, int32_t n_out,
                   uint16_t* xa, uint16_t* d_out, int32_t mode);
 
-int ora_lora_moe_grouped_fold(const uint16_t* x, int64_t x_row_stride,
+/* x_gather != 0: x is token-major [num_tokens, .] and sorted row r reads row
+   sorted_token_ids[r] of it (gate/up); 0: x is [te, .] at row r (down). */
+int ora_lora_moe_grouped_fold(const uint16_t* x, int64_t x_row_stride, int32_t x_gather,
                               uint16_t* base_out, int64_t out_row_stride,
                               const int32_t* expert_offsets, int32_t num_experts,
                               const int32_t* sorted_token_ids, int32_t te,
@@ -37,5 +39,14 @@ int ora_lora_moe_grouped_fold(const uint16_t* x, int64_t x_row_stride,
                               const float* scale_table, int32_t max_loras,
                               int32_t max_rank, int32_t k_in, int32_t n_out,
                               uint16_t* xa, uint16_t* d_out, int32_t mode);
+
+int ora_lora_moe_gather_bgmv(const uint16_t* x, int64_t x_row_stride,
+                             uint16_t* base_out, int64_t out_row_stride,
+                             const int32_t* indices, int32_t n_rows, int32_t top_k,
+                             const int32_t* row_adapter, int32_t num_tokens, int32_t num_experts,
+                             const uint16_t* const* a_table, const uint16_t* const* b_table,
+                             const float* scale_table, int32_t max_loras,
+                             int32_t max_rank, int32_t k_in, int32_t n_out,
+                             uint16_t* xa, uint16_t* d_out, int32_t mode);
 
 #endif

@@ -35,6 +35,10 @@ MUTANTS = {
                             "if (expert_offsets[k] < r && r <= expert_offsets[k + 1])"),
     "moe_table_expert_major": ("int64_t ti = (int64_t)a * num_experts + e;",
                                "int64_t ti = (int64_t)e * max_loras + a;"),
+    "gate_up_reads_sorted_row": ("const int64_t xr = x_gather ? t : r;", "const int64_t xr = r;"),
+    "gather_token_of_row": ("const int32_t t = r / top_k;", "const int32_t t = r % top_k;"),
+    "gather_table_expert_major": ("const int64_t entry = (int64_t)a * num_experts + e;",
+                                  "const int64_t entry = (int64_t)e * max_loras + a;"),
     "last_k_dropped": ("for (int32_t k = 0; k < k_in; ++k)\n                acc = acc + ora_f32_of_bf16(xrow[k])",
                        "for (int32_t k = 0; k < k_in - 1; ++k)\n                acc = acc + ora_f32_of_bf16(xrow[k])"),
 }

@@ -384,3 +384,97 @@ def test_moe_exact_rational_rows():
         assert agree >= 0.9
         checked += 1
     assert checked > 5
+
+
+# ------------------------------------------------ MoE gate/up (x_gather) and decode gather
+def test_moe_gate_up_reads_token_rows():
+    """x_gather: sorted row r reads row sorted_token_ids[r] of the token-major
+    input, so the fold equals the down fold of the pre-gathered rows; without
+    a row_adapter, rows whose token is out of range are skipped."""
+    wl = _small_moe(seed=13)
+    rng = np.random.default_rng(13)
+    x_tok = W.to_bf16_bits(rng.standard_normal((wl.num_tokens, wl.k_in), dtype=np.float32))
+    for ra in (wl.row_adapter, None):
+        o1, o2 = wl.out_buf.copy(), wl.out_buf.copy()
+        xa1, d1 = oracle.lora_moe_grouped_fold(
+            x_tok, wl.k_in, o1, wl.n_out, wl.expert_offsets, wl.sorted_token_ids, ra,
+            wl.num_tokens, 0, wl.te, wl.a_list(), wl.b_list(), wl.scale, wl.max_rank,
+            wl.k_in, wl.n_out, x_gather=True)
+        xa2, d2 = oracle.lora_moe_grouped_fold(
+            x_tok[wl.sorted_token_ids], wl.k_in, o2, wl.n_out, wl.expert_offsets,
+            wl.sorted_token_ids, ra, wl.num_tokens, 0, wl.te, wl.a_list(), wl.b_list(),
+            wl.scale, wl.max_rank, wl.k_in, wl.n_out)
+        assert np.array_equal(o1, o2) and np.array_equal(xa1, xa2) and np.array_equal(d1, d2)
+        assert not np.array_equal(o1, wl.out_buf)
+    sti = wl.sorted_token_ids.copy()
+    sti[3] = -1
+    o3 = wl.out_buf.copy()
+    oracle.lora_moe_grouped_fold(x_tok, wl.k_in, o3, wl.n_out, wl.expert_offsets, sti, None,
+                                 wl.num_tokens, 0, wl.te, wl.a_list(), wl.b_list(), wl.scale,
+                                 wl.max_rank, wl.k_in, wl.n_out, x_gather=True)
+    assert np.array_equal(o3[3], wl.out_buf[3])
+
+
+def _small_gather(seed=21, use_row_adapter=True, present_frac=0.8):
+    return W.make_moe_gather("gather_small", num_tokens=9, top_k=3, num_experts=5, k_in=40,
+                             n_out=24, max_loras=3, max_rank=8, rank=8, alpha=16.0,
+                             adapter_base_frac=0.25, seed=seed, use_row_adapter=use_row_adapter,
+                             present_frac=present_frac)
+
+
+def _run_gather(wl, indices=None, row_adapter="wl"):
+    out = wl.out_buf.copy()
+    ra = wl.row_adapter if isinstance(row_adapter, str) else row_adapter
+    xa, d = oracle.lora_moe_gather_bgmv(wl.x, wl.k_in, out, wl.n_out,
+                                        wl.indices if indices is None else indices, wl.top_k,
+                                        ra, wl.num_tokens, wl.num_experts, wl.a_list(),
+                                        wl.b_list(), wl.scale, wl.max_rank, wl.k_in, wl.n_out)
+    return out, xa, d
+
+
+def test_gather_bgmv_equals_bgmv_with_derived_slots():
+    """Row r of the decode gather fold is the bgmv row with slot
+    row_adapter[r // top_k] * E + indices[r] over the adapter-major tables."""
+    wl = _small_gather()
+    idx = wl.indices.copy()
+    idx[2] = wl.num_experts          # expert out of range
+    idx[5] = -1
+    out, xa, d = _run_gather(wl, indices=idx)
+    E = wl.num_experts
+    ra = wl.row_adapter[np.arange(wl.n_rows) // wl.top_k]
+    slot = np.where((ra >= 0) & (idx >= 0) & (idx < E), ra * E + idx, -1).astype(np.int32)
+    ob = wl.out_buf.copy()
+    xb, db = oracle.lora_bgmv(wl.x, wl.k_in, ob, wl.n_out, slot, wl.a_list(), wl.b_list(),
+                              wl.scale, wl.max_rank, wl.k_in, wl.n_out)
+    assert np.array_equal(out, ob) and np.array_equal(d, db)
+    routed = [r for r in range(wl.n_rows) if slot[r] >= 0 and wl.present[slot[r]]]
+    assert len(routed) > 5
+    assert np.array_equal(xa[routed], xb[routed])
+    for r in range(wl.n_rows):
+        if r not in routed:
+            assert np.array_equal(out[r], wl.out_buf[r])
+
+
+def test_gather_bgmv_equals_grouped_fold_after_sorting():
+    """Sorting the flat rows by (expert, token) and folding them with the grouped
+    fold gives the same rows."""
+    wl = _small_gather(seed=22, present_frac=1.0)
+    out, xa, d = _run_gather(wl)
+    tok = np.arange(wl.n_rows) // wl.top_k
+    order = np.lexsort((tok, wl.indices))
+    counts = np.bincount(wl.indices, minlength=wl.num_experts)
+    offs = np.zeros(wl.num_experts + 1, np.int32)
+    offs[1:] = np.cumsum(counts)
+    os_ = wl.out_buf[order].copy()
+    xs, _ = oracle.lora_moe_grouped_fold(wl.x[order], wl.k_in, os_, wl.n_out, offs,
+                                         tok[order].astype(np.int32), wl.row_adapter,
+                                         wl.num_tokens, 0, wl.n_rows, wl.a_list(), wl.b_list(),
+                                         wl.scale, wl.max_rank, wl.k_in, wl.n_out)
+    assert np.array_equal(out[order], os_)
+
+
+def test_gather_bgmv_null_row_adapter_is_adapter_zero():
+    wl = _small_gather(seed=23)
+    o1, _, _ = _run_gather(wl, row_adapter=None)
+    o2, _, _ = _run_gather(wl, row_adapter=np.zeros(wl.num_tokens, np.int32))
+    assert np.array_equal(o1, o2)
