@@ -36,9 +36,11 @@ if ROOT not in sys.path:
 
 METRIC = "routed LoRA fold rows/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 HEADLINE = "decode_qproj_bgmv"
-SIDE_WORKLOADS = ("qkv_kfold_bgmv", "ffn_down_bgmv", "moe_down_fold")
+SIDE_WORKLOADS = ("qkv_kfold_bgmv", "ffn_down_bgmv", "moe_down_fold", "moe_gateup_fold",
+                  "moe_decode_gather")
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_NAMES = {"bgmv": "lora_bgmv_fold_kernel", "moe": "lora_moe_fold_kernel"}
+KERNEL_NAMES = {"bgmv": "lora_bgmv_fold_kernel", "moe": "lora_moe_fold_kernel",
+                "gather": "lora_bgmv_fold_kernel"}
 
 
 # ----------------------------------------------------------------- helpers
@@ -107,6 +109,39 @@ def moe_algorithmic_bytes(wl) -> dict:
     return dict(bytes=int(total), routed_rows=routed, rows=int(wl.te), adapters=len(pairs),
                 per_row=per_row, per_adapter=per_adapter,
                 flops=int(2 * routed * wl.max_rank * (wl.k_in + wl.n_out)))
+
+
+def gather_algorithmic_bytes(wl) -> dict:
+    """Decode-path MoE fold: like the bgmv, with the (adapter, expert) table entry of
+    each row as its slot, plus the expert index per row and the adapter per token."""
+    E = wl.num_experts
+    routed, tables = 0, set()
+    for r in range(wl.n_rows):
+        e, t = int(wl.indices[r]), r // wl.top_k
+        a = 0 if wl.row_adapter is None else int(wl.row_adapter[t])
+        if not 0 <= e < E or a < 0 or a >= wl.max_loras or not wl.present[a * E + e]:
+            continue
+        routed += 1
+        tables.add(a * E + e)
+    per_row = wl.k_in * 2 + wl.n_out * 2 * 2 + wl.max_rank * 2 * 2 + 4
+    per_adapter = wl.max_rank * wl.k_in * 2 + wl.n_out * wl.max_rank * 2
+    total = routed * per_row + len(tables) * (per_adapter + 20) + wl.num_tokens * 4
+    return dict(bytes=int(total), routed_rows=routed, rows=int(wl.n_rows), adapters=len(tables),
+                per_row=per_row, per_adapter=per_adapter,
+                flops=int(2 * routed * wl.max_rank * (wl.k_in + wl.n_out)))
+
+
+def workload_kind(wl) -> str:
+    from gather_lora_gb300 import workloads as W
+    if isinstance(wl, W.MoeGatherWorkload):
+        return "gather"
+    return "moe" if isinstance(wl, W.MoeWorkload) else "bgmv"
+
+
+def algorithmic_bytes(wl) -> dict:
+    k = workload_kind(wl)
+    return {"bgmv": bgmv_algorithmic_bytes, "moe": moe_algorithmic_bytes,
+            "gather": gather_algorithmic_bytes}[k](wl)
 
 
 class ClockSampler:
@@ -226,7 +261,30 @@ class MoeRunner:
                                     wl.num_experts, d.sorted_token_ids, wl.te, d.row_adapter,
                                     wl.num_tokens, lo, hi, d.a_table, d.b_table, d.scale,
                                     wl.max_loras, wl.max_rank, wl.k_in, wl.n_out, xa=d.xa,
-                                    stream=stream)
+                                    stream=stream, x_gather=wl.x_gather)
+
+
+class GatherRunner:
+    def __init__(self, wl, copies, device):
+        from gather_lora_gb300 import workloads as W
+        self.wl = wl
+        self.copies = [W.gather_to_device(wl, device) for _ in range(copies)]
+        self.launches_per_step = 1
+
+    def bytes_per_copy(self):
+        d = self.copies[0]
+        return sum(t.numel() * t.element_size() for t in (d.x, d.out_buf, d.a_pool, d.b_pool))
+
+    def step(self, c, stream):
+        from gather_lora_gb300 import lib as L
+        wl, d = self.wl, self.copies[c]
+        L.lora_moe_gather_bgmv(d.x, wl.k_in, d.out_buf, wl.n_out, d.indices, wl.n_rows, wl.top_k,
+                               d.row_adapter, wl.num_tokens, wl.num_experts, d.a_table, d.b_table,
+                               d.scale, wl.max_loras, wl.max_rank, wl.k_in, wl.n_out, xa=d.xa,
+                               stream=stream)
+
+
+RUNNERS = {"bgmv": BgmvRunner, "moe": MoeRunner, "gather": GatherRunner}
 
 
 def copies_needed(bytes_per_copy, l2_bytes):
@@ -454,10 +512,11 @@ def run_ours(args):
 
     # headline
     head = args.only or HEADLINE
-    head_moe = head.startswith("moe")
     wl = W.by_name(head)
-    alg = moe_algorithmic_bytes(wl) if head_moe else bgmv_algorithmic_bytes(wl)
-    mk = MoeRunner if head_moe else BgmvRunner
+    head_kind = workload_kind(wl)
+    head_moe = head_kind == "moe"
+    alg = algorithmic_bytes(wl)
+    mk = RUNNERS[head_kind]
     probe = mk(wl, 1, device)
     C = copies_needed(probe.bytes_per_copy(), l2)
     runner = probe if C == 1 else mk(wl, C, device)
@@ -473,6 +532,9 @@ def run_ours(args):
     if head_moe:
         geometry = L.lora_launch_geometry(1, wl.cap, wl.max_loras if wl.row_adapter is not None else 1,
                                           wl.max_rank, wl.k_in, wl.n_out)
+    elif head_kind == "gather":
+        geometry = L.lora_launch_geometry(2, wl.n_rows, wl.max_loras * wl.num_experts, wl.max_rank,
+                                          wl.k_in, wl.n_out)
     else:
         geometry = L.lora_launch_geometry(0, wl.n, wl.max_loras, wl.max_rank, wl.k_in, wl.n_out)
 
@@ -480,9 +542,8 @@ def run_ours(args):
     side = {}
     for name in ([] if args.only else SIDE_WORKLOADS):
         w2 = W.by_name(name)
-        is_moe = name.startswith("moe")
-        a2 = moe_algorithmic_bytes(w2) if is_moe else bgmv_algorithmic_bytes(w2)
-        mk = MoeRunner if is_moe else BgmvRunner
+        a2 = algorithmic_bytes(w2)
+        mk = RUNNERS[workload_kind(w2)]
         pr = mk(w2, 1, device)
         c2 = copies_needed(pr.bytes_per_copy(), l2)
         r2 = pr if c2 == 1 else mk(w2, c2, device)
@@ -504,14 +565,14 @@ def run_ours(args):
 
     # e2e through the C ABI with host buffers
     e2e = None
-    if not head_moe:
+    if head_kind == "bgmv":
         e2e_steps = max(50, min(args.steps, 2000))
         e2e_val, h2d, d2h = e2e_bgmv(wl, device, e2e_steps, 10, C)
         e2e = {"value": dctx.sum(e2e_val), "unit": "rows/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": e2e_steps}
 
     cpu = None
-    if dctx.rank == 0 and not args.no_cpu_baseline and not head_moe:
+    if dctx.rank == 0 and not args.no_cpu_baseline and head_kind == "bgmv":
         v, n_rows, secs = oracle_rows_per_s(wl, args.cpu_seconds)
         cpu = {"value": v, "unit": "rows/s", "cores": 1, "kind": "oracle",
                "sample": f"{n_rows} decode rows of the {HEADLINE} batch ({secs:.1f} s, 1 host thread)"}
@@ -530,7 +591,7 @@ def run_ours(args):
                        "graph": "CUDA graph replay, programmatic dependent launch"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": recorded_traffic(head),
-                         "peak_kind": peak_kind, "kernel": KERNEL_NAMES["moe" if head_moe else "bgmv"],
+                         "peak_kind": peak_kind, "kernel": KERNEL_NAMES[head_kind],
                          "algorithmic_bytes_per_launch": bytes_per_launch,
                          "kernel_ms": kernel_ms, "frac_of_8tbs": achieved / 8000.0},
             "cpu_baseline": cpu,

@@ -78,11 +78,11 @@ int balanced_chunk(int total, int cap) {
 // window), so a row's arithmetic — the k-slices, k-chunks and summation order —
 // is the same in every call with the same (k_in, n_out, max_rank).
 bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_rank, int k_in,
-                   int n_out, glora::FoldGeometry& g) {
+                   int n_out, glora::FoldGeometry& g, int max_cl = GLORA_MAX_CLUSTER) {
   g = glora::FoldGeometry{};
   // bgmv: a cluster splits each unit's k (shrink) and n_out (expand); MoE units
   // are many and small, so one CTA folds whole groups.
-  g.cl = moe ? 1 : pow2_floor(std::min(GLORA_MAX_CLUSTER, std::max(1, std::max(k_in, n_out) / 512)));
+  g.cl = moe ? 1 : pow2_floor(std::min(max_cl, std::max(1, std::max(k_in, n_out) / 512)));
   g.mr16 = round_up(max_rank, 16);
   const int mt = g.mr16 / 16;
   const int tile_rows_cap = 8 * (glora::kMaxTilesPerWarp * glora::kConsumerWarps / mt);
@@ -110,13 +110,11 @@ bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_
   // all consumer warps in order (one bgmv group, or larger groups).
   const int tiles = mt * static_cast<int>(ceil_div(g.gmax, 8));
   g.group_parallel = (moe && tiles <= 4 && g.kch >= g.ksl) ? 1 : 0;
-  // Tile-parallel groups of few tiles also split k over the consumer warps:
-  // ksplit k-phases of kConsumerWarps / ksplit warps each.
-  // (Only without cluster peers: with peers the cluster already splits k, and
-  // the extra planes would lengthen the exchange.)
-  // With cluster peers and small partials, the exchange is an all-gather of
-  // the fp32 partials (one cluster barrier; planes folded locally), which also
-  // lets the k-phase split run under a cluster.
+  // With cluster peers and small fp32 partials, the exchange is an all-gather
+  // (one cluster barrier; each CTA adds the slots itself). Tile-parallel groups
+  // of few tiles also split k over the consumer warps (ksplit k-phases of
+  // kConsumerWarps / ksplit warps each) when there are no peers or the exchange
+  // is an all-gather; with a reduce-scatter the extra planes would lengthen it.
   g.gather = (g.cl > 1 && g.cl * g.rt * (max_rank + 4) * 4 <= kGatherBytes) ? 1 : 0;
   g.ksplit = 1;
   if (!g.group_parallel && (g.cl == 1 || g.gather))
@@ -227,8 +225,8 @@ int lora_bgmv(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_t* base_out,
   return rc ? cuda_fail(rc, "lora_bgmv launch") : ok();
 }
 
-int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_t* base_out,
-                          int64_t out_row_stride, const int32_t* expert_offsets, int32_t num_experts,
+int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, int32_t x_gather,
+                          lora_bf16_t* base_out, int64_t out_row_stride, const int32_t* expert_offsets, int32_t num_experts,
                           const int32_t* sorted_token_ids, int32_t te, const int32_t* row_adapter,
                           int32_t num_tokens, int32_t row_offset, int32_t row_end,
                           const lora_bf16_t* const* a_table, const lora_bf16_t* const* b_table,
@@ -245,8 +243,8 @@ int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_
   if (rc) return rc;
   if (!x || !base_out || !expert_offsets || !a_table || !b_table || !scale_table)
     return fail(LORA_ERR_NULL, "a required pointer is NULL (x, base_out, expert_offsets, a_table, b_table, scale_table)");
-  if (row_adapter && !sorted_token_ids)
-    return fail(LORA_ERR_NULL, "sorted_token_ids is required when row_adapter is given");
+  if ((row_adapter || x_gather) && !sorted_token_ids)
+    return fail(LORA_ERR_NULL, "sorted_token_ids is required with row_adapter or x_gather");
   if (!aligned16(x) || !aligned16(base_out) || (xa && !aligned16(xa)))
     return fail(LORA_ERR_ALIGN, "x, base_out and xa must be 16-byte aligned");
   glora::MoeArgs a{};
@@ -262,6 +260,7 @@ int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_
   a.sorted_token_ids = sorted_token_ids;
   a.row_adapter = row_adapter;
   a.num_tokens = num_tokens;
+  a.x_gather = x_gather ? 1 : 0;
   a.row_offset = row_offset;
   a.row_end = row_end;
   a.a_table = a_table;
@@ -276,6 +275,56 @@ int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_
   return rc ? cuda_fail(rc, "lora_moe_grouped_fold launch") : ok();
 }
 
+int lora_moe_gather_bgmv(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_t* base_out,
+                         int64_t out_row_stride, const int32_t* indices, int32_t n_rows, int32_t top_k,
+                         const int32_t* row_adapter, int32_t num_tokens, int32_t num_experts,
+                         const lora_bf16_t* const* a_table, const lora_bf16_t* const* b_table,
+                         const float* scale_table, int32_t max_loras, int32_t max_rank, int32_t k_in,
+                         int32_t n_out, lora_bf16_t* xa, void* stream) {
+  if (n_rows < 0 || n_rows > LORA_MAX_ROWS) return fail(LORA_ERR_SIZE, "n_rows %d outside [0, %d]", n_rows, LORA_MAX_ROWS);
+  if (top_k < 1) return fail(LORA_ERR_SIZE, "top_k %d < 1", top_k);
+  if (num_tokens < 0) return fail(LORA_ERR_SIZE, "num_tokens %d < 0", num_tokens);
+  if (num_experts < 1 || num_experts > LORA_MAX_EXPERTS)
+    return fail(LORA_ERR_SIZE, "num_experts %d outside [1, %d]", num_experts, LORA_MAX_EXPERTS);
+  if (max_loras < 1 || static_cast<int64_t>(max_loras) * num_experts > LORA_MAX_LORAS)
+    return fail(LORA_ERR_SIZE, "max_loras %d x num_experts %d outside [1, %d] table entries", max_loras,
+                num_experts, LORA_MAX_LORAS);
+  int rc = check_shape(max_rank, k_in, n_out, x_row_stride, out_row_stride);
+  if (rc) return rc;
+  if (n_rows == 0) return ok();
+  if (!x || !base_out || !indices || !a_table || !b_table || !scale_table)
+    return fail(LORA_ERR_NULL, "a required pointer is NULL (x, base_out, indices, a_table, b_table, scale_table)");
+  if (!aligned16(x) || !aligned16(base_out) || (xa && !aligned16(xa)))
+    return fail(LORA_ERR_ALIGN, "x, base_out and xa must be 16-byte aligned");
+  const int tables = max_loras * num_experts;
+  glora::BgmvArgs a{};
+  // Decode MoE rows spread over many (adapter, expert) entries of about one row
+  // each: one CTA per unit (no cluster split) keeps the grid near one wave.
+  if (!make_geometry(false, n_rows, tables, ((n_rows + 3) & ~3) + tables, max_rank, k_in, n_out, a.g, 1))
+    return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory for max_rank %d, k_in %d, n_out %d", max_rank, k_in, n_out);
+  a.x = x;
+  a.x_stride = x_row_stride;
+  a.out = base_out;
+  a.out_stride = out_row_stride;
+  a.seq_slot = nullptr;
+  a.n = n_rows;
+  a.indices = indices;
+  a.row_adapter = row_adapter;
+  a.top_k = top_k;
+  a.num_tokens = num_tokens;
+  a.num_experts = num_experts;
+  a.a_table = a_table;
+  a.b_table = b_table;
+  a.scale_table = scale_table;
+  a.max_loras = tables;
+  a.max_rank = max_rank;
+  a.k_in = k_in;
+  a.n_out = n_out;
+  a.xa = xa;
+  rc = glora::launch_bgmv(a, stream);
+  return rc ? cuda_fail(rc, "lora_moe_gather_bgmv launch") : ok();
+}
+
 int lora_read_device_status(void* stream, uint32_t* status_out, int clear) {
   const int rc = glora::read_device_status(stream, status_out, clear);
   return rc ? cuda_fail(rc, "lora_read_device_status") : ok();
@@ -287,8 +336,10 @@ int lora_launch_geometry(int moe, int32_t rows, int32_t max_loras, int32_t max_r
   int rc = check_shape(max_rank, k_in, n_out, k_in, n_out);
   if (rc) return rc;
   glora::FoldGeometry g{};
-  const int scratch = moe ? LORA_MAX_EXPERTS + 1 : ((rows + 3) & ~3) + max_loras;
-  if (!make_geometry(moe != 0, rows, max_loras, scratch, max_rank, k_in, n_out, g))
+  const bool grouped = moe == 1;
+  const int scratch = grouped ? LORA_MAX_EXPERTS + 1 : ((rows + 3) & ~3) + max_loras;
+  if (!make_geometry(grouped, rows, max_loras, scratch, max_rank, k_in, n_out, g,
+                     moe == 2 ? 1 : GLORA_MAX_CLUSTER))
     return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory");
   const int64_t v[9] = {g.cl, g.rt, g.ksl, g.jsl, g.kch, g.jch, g.ns, g.clusters, g.smem_bytes};
   std::memcpy(out, v, sizeof v);

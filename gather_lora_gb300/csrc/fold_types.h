@@ -8,7 +8,7 @@ namespace glora {
 constexpr int kMaxRows = 64;        // rows (positions) per pass of a work unit
 constexpr int kMaxTileRows = 256;   // sorted rows one MoE work unit scans
 constexpr int kMaxTilesPerWarp = 4; // 16x8 shrink tiles a warp may own: MT * NT <= 32
-constexpr int kPlanBytes = 6144;    // shared memory reserved for the work-unit plan
+constexpr int kPlanBytes = 7168;    // shared memory reserved for the work-unit plan
 constexpr int kConsumerWarps = 8;   // tensor-core / fold warps per CTA
 constexpr int kProducerWarps = 4;   // TMA-issuing warps per CTA (one warpgroup)
 
@@ -45,8 +45,11 @@ struct BgmvArgs {
   long long x_stride;
   uint16_t* out;
   long long out_stride;
-  const int32_t* seq_slot;
+  const int32_t* seq_slot;   // slot per row, or NULL: derived from the MoE decode routing below
   int n;
+  const int32_t* indices;    // MoE decode rows: expert per row
+  const int32_t* row_adapter;  // [num_tokens] adapter per token (NULL: adapter 0)
+  int top_k, num_tokens, num_experts;
   const uint16_t* const* a_table;
   const uint16_t* const* b_table;
   const float* scale_table;
@@ -66,6 +69,7 @@ struct MoeArgs {
   const int32_t* sorted_token_ids;
   const int32_t* row_adapter;
   int num_tokens;
+  int x_gather;     // 1: x is token-major; sorted row r reads row sorted_token_ids[r]
   int row_offset, row_end;
   const uint16_t* const* a_table;
   const uint16_t* const* b_table;

@@ -60,7 +60,8 @@ struct Plan {
   int found_slot, found_tile;      // bgmv planning scratch
   int members[kMaxRows];           // positions, grouped, ascending within a group
   int gstart[kMaxRows + 1];        // group g = members[gstart[g] .. gstart[g+1])
-  int grow[kMaxRows];              // position -> row of x / base_out
+  int grow[kMaxRows];              // position -> row of base_out
+  int xsrc[kMaxRows];              // position -> row of x
   int xarow[kMaxRows];             // position -> row of xa
   int flag[kMaxRows];              // MoE: the expert where a position starts a group, else -1
   unsigned ballots[2];
@@ -69,6 +70,7 @@ struct Plan {
   const uint16_t* gB[kMaxRows];
   int tpos[kMaxTileRows];          // MoE: tile rows routed to this unit's adapter, ascending
   int tkey[kMaxTileRows];          // MoE: their experts
+  int txrow[kMaxTileRows];         // MoE: their rows of x (the token with x_gather)
 };
 
 static_assert(sizeof(Plan) <= kPlanBytes, "plan does not fit its shared-memory reservation");
@@ -189,10 +191,11 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
         const long long stride = set ? stride1 : stride0;
         const uint32_t dst = set ? dst1 : dst0;
         const int n = set ? n1 : n0, bytes = set ? bytes1 : bytes0, pitch = set ? pitch1 : pitch0;
+        const int* rmap = it < n_shrink ? pl.xsrc : pl.grow;   // gathered rows: x (shrink) or base_out
         if (bytes >= kTmaRowBytes) {
 #pragma unroll 1
           for (int q = q0; q < n; q += kP) {
-            const int row = set ? pl.grow[pl.members[m0 + q]] : q;
+            const int row = set ? rmap[pl.members[m0 + q]] : q;
             bulk_g2s(dst + q * pitch, src + row * stride, bytes, full);
           }
         } else {   // short rows: 16-byte cp.async chunks over all producer threads
@@ -200,7 +203,7 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
 #pragma unroll 1
           for (int c = pt; c < n * cpr; c += kP) {
             const int q = c / cpr, ch = c - q * cpr;
-            const int row = set ? pl.grow[pl.members[m0 + q]] : q;
+            const int row = set ? rmap[pl.members[m0 + q]] : q;
             cp_async16(dst + q * pitch + ch * 16, reinterpret_cast<const char*>(src + row * stride) + ch * 16);
           }
         }
@@ -537,6 +540,9 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
 // order. Otherwise units are numbered slot by slot over every slot that has
 // rows. Either way the static grid bound is n/rt + min(n, max_loras) units; a
 // unit that finds no rows, or whose slot has a NULL table entry, does nothing.
+// The decode-path MoE fold runs here too: its "slot" is the table entry
+// a * E + e of the row's expert and its token's adapter, and max_loras is the
+// table count.
 // ============================================================================
 template <int MAXT>
 __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __grid_constant__ BgmvArgs p) {
@@ -563,7 +569,17 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
   // seq_slot (and the per-slot row counts) live in the not-yet-used ring.
   int* ss = reinterpret_cast<int*>(smem + g.off_ring);
   int* cnt = ss + ((p.n + 3) & ~3);
-  for (int i = tid; i < p.n; i += kThreads) ss[i] = p.seq_slot[i];
+  for (int i = tid; i < p.n; i += kThreads) {
+    int sl;
+    if (p.seq_slot) {
+      sl = p.seq_slot[i];
+    } else {   // MoE decode rows: table a * E + e from the row's expert and its token's adapter
+      const int e = p.indices[i], t = i / p.top_k;
+      const int a = p.row_adapter ? (t < p.num_tokens ? p.row_adapter[t] : -1) : 0;
+      sl = (e >= 0 && e < p.num_experts && a >= 0 && a < p.max_loras / p.num_experts) ? a * p.num_experts + e : -1;
+    }
+    ss[i] = sl;
+  }
   if (!first_tile) {
     for (int s = tid; s < p.max_loras; s += kThreads) cnt[s] = 0;
     if (tid == 0) pl.found_slot = -1;
@@ -624,6 +640,7 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
         const int pos = rank - want_lo;
         pl.members[pos] = pos;
         pl.grow[pos] = i;
+        pl.xsrc[pos] = i;
         pl.xarow[pos] = i;
       }
       base += total;
@@ -685,8 +702,10 @@ __global__ void __launch_bounds__(kThreads, 2) lora_moe_fold_kernel(const __grid
   const int T = min(g.tile_rows, p.row_end - r0);
   int* offs = reinterpret_cast<int*>(smem + g.off_ring);  // expert_offsets copy (ring not yet used)
   for (int i = tid; i <= E; i += kThreads) offs[i] = p.expert_offsets[i];
+  // The row's token (the adapter gate; the x row of the gate/up form).
+  const bool need_token = p.row_adapter != nullptr || p.x_gather != 0;
   int token = -1;
-  if (p.row_adapter && tid < T) token = p.sorted_token_ids[r0 + tid];   // overlaps the offsets load
+  if (need_token && tid < T) token = p.sorted_token_ids[r0 + tid];   // overlaps the offsets load
   __syncthreads();
 
   // Per tile row: expert by binary search, then the adapter gate.
@@ -702,8 +721,9 @@ __global__ void __launch_bounds__(kThreads, 2) lora_moe_fold_kernel(const __grid
       if (offs[lo] <= r && r < offs[lo + 1]) {
         int a = 0;
         bool ok = true;
-        if (p.row_adapter) {
-          if (token < 0 || token >= p.num_tokens) ok = false; else a = p.row_adapter[token];
+        if (need_token) {
+          if (token < 0 || token >= p.num_tokens) ok = false;
+          else if (p.row_adapter) a = p.row_adapter[token];
         }
         if (ok && a == adapter) expert = lo;   // a outside [0, max_loras) matches no unit
       }
@@ -725,6 +745,7 @@ __global__ void __launch_bounds__(kThreads, 2) lora_moe_fold_kernel(const __grid
     const int rank = before + __popc(bal & ((1u << lane) - 1u));
     pl.tpos[rank] = tid;
     pl.tkey[rank] = expert;
+    pl.txrow[rank] = p.x_gather ? token : r0 + tid;
   }
   ring_init(pl, g.ns);   // (its barrier also publishes tpos / tkey)
 
@@ -744,6 +765,7 @@ __global__ void __launch_bounds__(kThreads, 2) lora_moe_fold_kernel(const __grid
         const int r = r0 + pl.tpos[base + tid];
         pl.members[tid] = tid;
         pl.grow[tid] = r;
+        pl.xsrc[tid] = pl.txrow[base + tid];
         pl.xarow[tid] = r - p.row_offset;
       }
       const unsigned sb = __ballot_sync(0xffffffffu, start);

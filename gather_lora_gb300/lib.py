@@ -43,8 +43,11 @@ def load():
     lib.lora_bgmv.restype = ctypes.c_int
     lib.lora_bgmv.argtypes = [P, I64, P, I64, P, I32, P, P, P, I32, I32, I32, I32, P, P]
     lib.lora_moe_grouped_fold.restype = ctypes.c_int
-    lib.lora_moe_grouped_fold.argtypes = [P, I64, P, I64, P, I32, P, I32, P, I32, I32, I32,
+    lib.lora_moe_grouped_fold.argtypes = [P, I64, I32, P, I64, P, I32, P, I32, P, I32, I32, I32,
                                           P, P, P, I32, I32, I32, I32, P, P]
+    lib.lora_moe_gather_bgmv.restype = ctypes.c_int
+    lib.lora_moe_gather_bgmv.argtypes = [P, I64, P, I64, P, I32, I32, P, I32, I32,
+                                         P, P, P, I32, I32, I32, I32, P, P]
     lib.lora_last_error.restype = ctypes.c_char_p
     lib.lora_last_error.argtypes = []
     lib.lora_read_device_status.restype = ctypes.c_int
@@ -100,13 +103,25 @@ def lora_bgmv(x, x_row_stride, base_out, out_row_stride, seq_slot, n, a_table, b
 def lora_moe_grouped_fold(x, x_row_stride, base_out, out_row_stride, expert_offsets, num_experts,
                           sorted_token_ids, te, row_adapter, num_tokens, row_offset, row_end,
                           a_table, b_table, scale_table, max_loras, max_rank, k_in, n_out,
-                          xa=None, stream=None):
-    """MoE grouped fold of one window (see lora_moe_grouped_fold in include/gather_lora.h)."""
+                          xa=None, stream=None, x_gather=False):
+    """MoE grouped fold of one window (see lora_moe_grouped_fold in include/gather_lora.h).
+    x_gather: x is token-major and sorted row r reads row sorted_token_ids[r] (gate/up)."""
     return _check(load().lora_moe_grouped_fold(
-        _addr(x), x_row_stride, _addr(base_out), out_row_stride, _addr(expert_offsets),
+        _addr(x), x_row_stride, 1 if x_gather else 0, _addr(base_out), out_row_stride, _addr(expert_offsets),
         num_experts, _addr(sorted_token_ids), te, _addr(row_adapter), num_tokens, row_offset,
         row_end, _addr(a_table), _addr(b_table), _addr(scale_table), max_loras, max_rank, k_in,
         n_out, _addr(xa), _stream(stream)))
+
+
+def lora_moe_gather_bgmv(x, x_row_stride, base_out, out_row_stride, indices, n_rows, top_k,
+                         row_adapter, num_tokens, num_experts, a_table, b_table, scale_table,
+                         max_loras, max_rank, k_in, n_out, xa=None, stream=None):
+    """Decode-path MoE fold over flat (token, slot) rows (see lora_moe_gather_bgmv in
+    include/gather_lora.h)."""
+    return _check(load().lora_moe_gather_bgmv(
+        _addr(x), x_row_stride, _addr(base_out), out_row_stride, _addr(indices), n_rows, top_k,
+        _addr(row_adapter), num_tokens, num_experts, _addr(a_table), _addr(b_table),
+        _addr(scale_table), max_loras, max_rank, k_in, n_out, _addr(xa), _stream(stream)))
 
 
 def lora_last_error() -> str:

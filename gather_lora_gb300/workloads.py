@@ -371,10 +371,30 @@ def moe_down_fold(seed=4):
                     adapter_base_frac=0.20, cap=4096, seed=seed)
 
 
+def moe_gateup_fold(seed=5):
+    """Gate/up form of the MoE fold on the same model: 2048 tokens, top-8 of 128
+    experts, te=16384, token-major x [2048, 2048] ~ N(0,1) gathered per sorted row,
+    n_out=768 (the expert width), 16 adapters at rank 16 (alpha 32), 20% base
+    tokens, windows of 4096."""
+    return make_moe("moe_gateup_fold", num_tokens=2048, top_k=8, num_experts=128, k_in=2048,
+                    n_out=768, max_loras=16, max_rank=16, rank=16, alpha=32.0,
+                    adapter_base_frac=0.20, cap=4096, seed=seed, x_gather=True)
+
+
+def moe_decode_gather(seed=6):
+    """Decode-path MoE down fold: 64 tokens x top-8 of 128 experts = 512 flat rows,
+    x [512, 768] post-SiLU, base_out [512, 2048], 16 adapters at rank 16 (alpha
+    32), 20% base tokens."""
+    return make_moe_gather("moe_decode_gather", num_tokens=64, top_k=8, num_experts=128,
+                           k_in=768, n_out=2048, max_loras=16, max_rank=16, rank=16, alpha=32.0,
+                           adapter_base_frac=0.20, seed=seed)
+
+
 def by_name(name: str, seed=None):
     fn = {"tiny_bgmv": tiny_bgmv, "decode_qproj_bgmv": decode_qproj_bgmv,
           "qkv_kfold_bgmv": qkv_kfold_bgmv, "ffn_down_bgmv": ffn_down_bgmv,
-          "moe_down_fold": moe_down_fold}[name]
+          "moe_down_fold": moe_down_fold, "moe_gateup_fold": moe_gateup_fold,
+          "moe_decode_gather": moe_decode_gather}[name]
     return fn() if seed is None else fn(seed)
 
 
@@ -449,3 +469,30 @@ def moe_to_device(wl: MoeWorkload, device="cuda", xa_rows=None) -> DeviceMoe:
         a_table=_table_of(a_pool, wl.present, device), b_table=_table_of(b_pool, wl.present, device),
         scale=_dev(wl.scale, device),
         xa=torch.zeros((rows, wl.max_rank), dtype=torch.int16, device=device))
+
+
+@dataclass
+class DeviceMoeGather:
+    x: "torch.Tensor"
+    out_buf: "torch.Tensor"
+    indices: "torch.Tensor"
+    row_adapter: "torch.Tensor | None"
+    a_pool: "torch.Tensor"
+    b_pool: "torch.Tensor"
+    a_table: "torch.Tensor"
+    b_table: "torch.Tensor"
+    scale: "torch.Tensor"
+    xa: "torch.Tensor"        # int16 [n_rows, max_rank]
+
+
+def gather_to_device(wl: MoeGatherWorkload, device="cuda") -> DeviceMoeGather:
+    a_pool = _dev(wl.a_pool.view(np.int16), device)
+    b_pool = _dev(wl.b_pool.view(np.int16), device)
+    return DeviceMoeGather(
+        x=_dev(wl.x.view(np.int16), device), out_buf=_dev(wl.out_buf.view(np.int16), device),
+        indices=_dev(wl.indices, device),
+        row_adapter=None if wl.row_adapter is None else _dev(wl.row_adapter, device),
+        a_pool=a_pool, b_pool=b_pool,
+        a_table=_table_of(a_pool, wl.present, device), b_table=_table_of(b_pool, wl.present, device),
+        scale=_dev(wl.scale, device),
+        xa=torch.zeros((max(wl.n_rows, 1), wl.max_rank), dtype=torch.int16, device=device))

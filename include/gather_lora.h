@@ -118,21 +118,25 @@ int lora_bgmv(const lora_bf16_t* x, int64_t x_row_stride,
  * lora_moe_grouped_fold — the fold over expert-sorted MoE rows of one window.
  *
  * Defines: "Module moe_lora_grouped" (atlas rustdoc), the module summary and the
- * `moe_lora_grouped_down`, `MoeExpertRoute` and `MLG_M_TILE` entries (down
- * projection: x is the sorted [te, k_in] activation, x_gather == 0).
+ * `moe_lora_grouped_down`, `MoeExpertRoute` and `MLG_M_TILE` entries. Down
+ * (x_gather == 0): x is the sorted [te, k_in] activation and row r of it feeds
+ * sorted row r. Gate/up (x_gather != 0): x is the token-major [num_tokens, k_in]
+ * expert input and sorted row r reads row sorted_token_ids[r] of it.
  *
  * For every sorted row r in [row_offset, row_end):
  *   e = the expert with expert_offsets[e] <= r < expert_offsets[e+1]
  *       (rows outside [expert_offsets[0], expert_offsets[num_experts]) are skipped);
- *   a = row_adapter ? row_adapter[sorted_token_ids[r]] : 0
- *       (skipped if the token is outside [0, num_tokens) or a is outside [0, max_loras));
+ *   t = sorted_token_ids[r] (read with a row_adapter or x_gather; skipped if t
+ *       is outside [0, num_tokens));
+ *   a = row_adapter ? row_adapter[t] : 0 (skipped if a is outside [0, max_loras));
  *   t = a * num_experts + e (adapter-major tables); skipped if a_table[t] or
  *       b_table[t] is NULL; otherwise the fold of lora_bgmv is applied to
- *       x[r*x_row_stride ..] and base_out[r*out_row_stride ..] with A_t, B_t,
- *       scale_table[t].
+ *       x[xr*x_row_stride ..] (xr = x_gather ? t : r) and
+ *       base_out[r*out_row_stride ..] with A_t, B_t, scale_table[t].
  *
  *   expert_offsets    [num_experts + 1] int32 prefix sum (non-decreasing)
- *   sorted_token_ids  [te] int32 sorted row -> token; may be NULL when row_adapter is NULL
+ *   sorted_token_ids  [te] int32 sorted row -> token; may be NULL when row_adapter is
+ *                     NULL and x_gather == 0
  *   row_adapter       [num_tokens] int32 (< 0 = no delta), or NULL: every row uses adapter 0
  *   a_table, b_table, scale_table   [max_loras * num_experts], index a*num_experts + e
  *   xa                optional [row_end - row_offset, max_rank] BF16 shrink output at the
@@ -143,7 +147,7 @@ int lora_bgmv(const lora_bf16_t* x, int64_t x_row_stride,
  * one adapter in one tile. Calls over windows [0, cap), [cap, 2cap), ... give
  * the same result as one call over [0, te).
  */
-int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride,
+int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, int32_t x_gather,
                           lora_bf16_t* base_out, int64_t out_row_stride,
                           const int32_t* expert_offsets, int32_t num_experts,
                           const int32_t* sorted_token_ids, int32_t te,
@@ -153,6 +157,39 @@ int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride,
                           const float* scale_table, int32_t max_loras,
                           int32_t max_rank, int32_t k_in, int32_t n_out,
                           lora_bf16_t* xa, void* stream);
+
+/*
+ * lora_moe_gather_bgmv — the decode-path MoE fold over flat, unsorted
+ * (token, slot) rows.
+ *
+ * Defines: "Module moe_lora_grouped" (atlas rustdoc), `moe_lora_gather_bgmv`
+ * entry (the unsorted, slot-major analogue of `moe_lora_grouped_down`).
+ *
+ * For every row r in [0, n_rows):
+ *   e = indices[r] (skipped if outside [0, num_experts));
+ *   t = r / top_k (skipped if t >= num_tokens);
+ *   a = row_adapter ? row_adapter[t] : 0 (skipped if outside [0, max_loras));
+ *   entry a * num_experts + e of the adapter-major tables; skipped if its A or B
+ *   pointer is NULL; otherwise the fold of lora_bgmv is applied to
+ *   x[r*x_row_stride ..] and base_out[r*out_row_stride ..].
+ *
+ *   indices      [n_rows] int32 expert per row (row = token * top_k + slot)
+ *   row_adapter  [num_tokens] int32 (< 0 = no delta), or NULL: adapter 0
+ *   a_table, b_table, scale_table  [max_loras * num_experts], index a*num_experts + e
+ *                (max_loras * num_experts <= LORA_MAX_LORAS)
+ *   xa           optional [n_rows, max_rank] BF16 shrink output at row r (routed rows)
+ * Rows of one table entry share a work unit; the launch grid depends only on
+ * n_rows and the table count (capture-safe). Errors, alignment and ownership as
+ * for lora_bgmv.
+ */
+int lora_moe_gather_bgmv(const lora_bf16_t* x, int64_t x_row_stride,
+                         lora_bf16_t* base_out, int64_t out_row_stride,
+                         const int32_t* indices, int32_t n_rows, int32_t top_k,
+                         const int32_t* row_adapter, int32_t num_tokens, int32_t num_experts,
+                         const lora_bf16_t* const* a_table, const lora_bf16_t* const* b_table,
+                         const float* scale_table, int32_t max_loras,
+                         int32_t max_rank, int32_t k_in, int32_t n_out,
+                         lora_bf16_t* xa, void* stream);
 
 /* Text of the last error returned on this host thread ("" if none). */
 const char* lora_last_error(void);
@@ -165,10 +202,12 @@ const char* lora_last_error(void);
 int lora_read_device_status(void* stream, uint32_t* status_out, int clear);
 
 /*
- * Launch geometry that lora_bgmv / lora_moe_grouped_fold would use (for
- * tests and benchmarks). moe == 0: bgmv with `rows` = n; moe != 0: MoE with
- * `rows` = row_end - row_offset and max_loras = the number of adapters the
- * grid covers (max_loras with a row_adapter, 1 without). Writes [cluster,
+ * Launch geometry that lora_bgmv / lora_moe_grouped_fold / lora_moe_gather_bgmv
+ * would use (for tests and benchmarks). moe == 0: bgmv with `rows` = n; moe == 1:
+ * MoE grouped fold with `rows` = row_end - row_offset and max_loras = the number
+ * of adapters the grid covers (max_loras with a row_adapter, 1 without); moe ==
+ * 2: decode gather fold with `rows` = n_rows and max_loras = the table count
+ * (adapters x experts). Writes [cluster,
  * rows_per_tile, k_slice, j_slice, k_chunk, j_chunk, ring_stages, clusters,
  * smem_bytes] to out[0..8].
  */

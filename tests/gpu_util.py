@@ -54,7 +54,7 @@ def gpu_moe(wl: W.MoeWorkload, windows, d: W.DeviceMoe = None, use_row_adapter=T
                                 wl.num_experts, d.sorted_token_ids, wl.te,
                                 d.row_adapter if use_row_adapter else None, wl.num_tokens, lo, hi,
                                 d.a_table, d.b_table, d.scale, wl.max_loras, wl.max_rank,
-                                wl.k_in, wl.n_out, xa=d.xa)
+                                wl.k_in, wl.n_out, xa=d.xa, x_gather=wl.x_gather)
         torch.cuda.synchronize()
         xas.append(to_u16(d.xa)[: hi - lo].copy())
     return to_u16(d.out_buf), xas
@@ -68,7 +68,30 @@ def oracle_moe(wl: W.MoeWorkload, windows, use_row_adapter=True):
         xa, dd = oracle.lora_moe_grouped_fold(
             wl.x, wl.k_in, out, wl.n_out, wl.expert_offsets, wl.sorted_token_ids,
             wl.row_adapter if use_row_adapter else None, wl.num_tokens, lo, hi, wl.a_list(),
-            wl.b_list(), wl.scale, wl.max_rank, wl.k_in, wl.n_out)
+            wl.b_list(), wl.scale, wl.max_rank, wl.k_in, wl.n_out, x_gather=wl.x_gather)
         xas.append(xa)
         d_all[lo:hi] = dd[lo:hi]
     return out, xas, d_all
+
+
+def gpu_gather(wl: W.MoeGatherWorkload, d: W.DeviceMoeGather = None, use_row_adapter=True,
+               indices=None):
+    d = d or W.gather_to_device(wl)
+    if indices is not None:
+        d.indices.copy_(torch.from_numpy(np.ascontiguousarray(indices, dtype=np.int32)))
+    d.xa.zero_()
+    L.lora_moe_gather_bgmv(d.x, wl.k_in, d.out_buf, wl.n_out, d.indices, wl.n_rows, wl.top_k,
+                           d.row_adapter if use_row_adapter else None, wl.num_tokens,
+                           wl.num_experts, d.a_table, d.b_table, d.scale, wl.max_loras,
+                           wl.max_rank, wl.k_in, wl.n_out, xa=d.xa)
+    torch.cuda.synchronize()
+    return to_u16(d.out_buf), to_u16(d.xa)[: wl.n_rows]
+
+
+def oracle_gather(wl: W.MoeGatherWorkload, use_row_adapter=True, indices=None):
+    out = wl.out_buf.copy()
+    xa, dd = oracle.lora_moe_gather_bgmv(
+        wl.x, wl.k_in, out, wl.n_out, wl.indices if indices is None else indices, wl.top_k,
+        wl.row_adapter if use_row_adapter else None, wl.num_tokens, wl.num_experts, wl.a_list(),
+        wl.b_list(), wl.scale, wl.max_rank, wl.k_in, wl.n_out)
+    return out, xa, dd

@@ -120,11 +120,12 @@ def moe_routes(wl: W.MoeWorkload, lo: int, hi: int, offsets=None, sorted_ids=Non
         if not (offs[e] <= r < offs[e + 1]):
             continue
         a = 0
-        if ra is not None:
+        if ra is not None or wl.x_gather:
             t = int(sti[r])
             if t < 0 or t >= wl.num_tokens:
                 continue
-            a = int(ra[t])
+            if ra is not None:
+                a = int(ra[t])
         if a < 0 or a >= wl.max_loras:
             continue
         idx = a * E + e
@@ -147,7 +148,8 @@ def compare_moe(wl: W.MoeWorkload, windows, gpu_out, ora_out, gpu_xas, ora_xas, 
     for (lo, hi), gx, ox in zip(windows, gpu_xas, ora_xas):
         for r, idx in routes:
             if lo <= r < hi:
-                xa_exact += check_xa(gx[r - lo], ox[r - lo], wl.x[r], wl.a_pool[idx])
+                xrow = wl.x[wl.sorted_token_ids[r]] if wl.x_gather else wl.x[r]
+                xa_exact += check_xa(gx[r - lo], ox[r - lo], xrow, wl.a_pool[idx])
     for r, idx in routes:
         # the xa of row r lives in its window's buffer, at the local row
         w = next(k for k, (lo, hi) in enumerate(windows) if lo <= r < hi)
@@ -158,3 +160,44 @@ def compare_moe(wl: W.MoeWorkload, windows, gpu_out, ora_out, gpu_xas, ora_xas, 
     if n_tot:
         assert n_exact / n_tot >= min_exact, f"only {n_exact}/{n_tot} folded values bit-exact"
     return dict(rows=len(routes), exact=n_exact, total=n_tot, xa_exact=xa_exact, worst=worst)
+
+
+def gather_routes(wl: W.MoeGatherWorkload, indices=None, row_adapter="wl"):
+    """(row, table index) of every routed row of a decode-path MoE fold."""
+    idx = wl.indices if indices is None else indices
+    ra = wl.row_adapter if isinstance(row_adapter, str) else row_adapter
+    E = wl.num_experts
+    out = []
+    for r in range(wl.n_rows):
+        e = int(idx[r])
+        t = r // wl.top_k
+        if e < 0 or e >= E or t >= wl.num_tokens:
+            continue
+        a = 0 if ra is None else int(ra[t])
+        if a < 0 or a >= wl.max_loras or not wl.present[a * E + e]:
+            continue
+        out.append((r, a * E + e))
+    return out
+
+
+def compare_gather(wl: W.MoeGatherWorkload, gpu_out, ora_out, gpu_xa, ora_xa, ora_d, routes,
+                   min_exact=0.99):
+    """Full comparison of a decode-path MoE fold (rows in flat (token, slot) order)."""
+    routed = {r for r, _ in routes}
+    mask = np.ones(gpu_out.shape[0], dtype=bool)
+    mask[list(routed)] = False
+    assert np.array_equal(gpu_out[mask], ora_out[mask]), "rows without a delta changed"
+    assert np.array_equal(ora_out[mask], wl.out_buf[mask])
+    n_exact = n_tot = xa_exact = xa_tot = 0
+    worst = 0.0
+    for r, idx in routes:
+        xa_exact += check_xa(gpu_xa[r], ora_xa[r], wl.x[r], wl.a_pool[idx])
+        xa_tot += wl.max_rank
+        e, t, w = check_row_fold(gpu_out[r], ora_out[r], ora_d[r], ora_xa[r], gpu_xa[r],
+                                 wl.b_pool[idx], wl.scale[idx])
+        n_exact, n_tot, worst = n_exact + e, n_tot + t, max(worst, w)
+    if n_tot:
+        assert n_exact / n_tot >= min_exact, f"only {n_exact}/{n_tot} folded values bit-exact"
+    if xa_tot:
+        assert xa_exact / xa_tot >= min_exact, f"only {xa_exact}/{xa_tot} xa values bit-exact"
+    return dict(rows=len(routes), exact=n_exact, total=n_tot, worst=worst)

@@ -33,7 +33,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("lora_bgmv", "lora_moe_grouped_fold", "lora_last_error", "lora_read_device_status",
+    for n in ("lora_bgmv", "lora_moe_grouped_fold", "lora_moe_gather_bgmv", "lora_last_error",
+              "lora_read_device_status",
               "lora_launch_geometry", "lora_grouped_down_wc", "lora_grouped_down_windows",
               "lora_pack_expert_tables"):
         assert n in names
@@ -76,10 +77,10 @@ def test_bgmv_zero_rows_is_a_no_op():
 
 
 def _moe(**kw):
-    a = dict(x=FAKE, xs=768, out=FAKE, os=2048, off=FAKE, E=128, sti=FAKE, te=16384, ra=FAKE,
+    a = dict(x=FAKE, xs=768, xg=0, out=FAKE, os=2048, off=FAKE, E=128, sti=FAKE, te=16384, ra=FAKE,
              nt=2048, lo=0, hi=4096, at=FAKE, bt=FAKE, sc=FAKE, L=16, R=16, k=768, no=2048, xa=FAKE)
     a.update(kw)
-    return L.load().lora_moe_grouped_fold(a["x"], a["xs"], a["out"], a["os"], a["off"], a["E"],
+    return L.load().lora_moe_grouped_fold(a["x"], a["xs"], a["xg"], a["out"], a["os"], a["off"], a["E"],
                                           a["sti"], a["te"], a["ra"], a["nt"], a["lo"], a["hi"],
                                           a["at"], a["bt"], a["sc"], a["L"], a["R"], a["k"], a["no"],
                                           a["xa"], None)
@@ -90,9 +91,33 @@ def _moe(**kw):
     (dict(lo=-1), -5), (dict(lo=10, hi=5), -5), (dict(hi=16385), -5), (dict(R=4), -2),
     (dict(k=770, xs=776), -4), (dict(xs=700), -3), (dict(x=None), -1), (dict(off=None), -1),
     (dict(sti=None), -1), (dict(at=None), -1), (dict(x=FAKE + 2), -4),
+    (dict(sti=None, ra=None, xg=1), -1),
 ])
 def test_moe_rejects_bad_arguments_before_launch(kw, code):
     assert _moe(**kw) == code
+
+
+def _gather(**kw):
+    a = dict(x=FAKE, xs=768, out=FAKE, os=2048, idx=FAKE, n=512, k=8, ra=FAKE, nt=64, E=128,
+             at=FAKE, bt=FAKE, sc=FAKE, L=16, R=16, kin=768, no=2048, xa=FAKE)
+    a.update(kw)
+    return L.load().lora_moe_gather_bgmv(a["x"], a["xs"], a["out"], a["os"], a["idx"], a["n"],
+                                         a["k"], a["ra"], a["nt"], a["E"], a["at"], a["bt"],
+                                         a["sc"], a["L"], a["R"], a["kin"], a["no"], a["xa"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n=-1), -2), (dict(n=8193), -2), (dict(k=0), -2), (dict(nt=-1), -2), (dict(E=0), -2),
+    (dict(E=1025), -2), (dict(L=0), -2), (dict(L=33), -2), (dict(R=4), -2), (dict(xs=700), -3),
+    (dict(x=None), -1), (dict(idx=None), -1), (dict(at=None), -1), (dict(x=FAKE + 2), -4),
+])
+def test_gather_bgmv_rejects_bad_arguments_before_launch(kw, code):
+    assert _gather(**kw) == code
+    assert L.lora_last_error()
+
+
+def test_gather_bgmv_zero_rows_is_a_no_op():
+    assert _gather(n=0, x=None, idx=None) == 0
 
 
 def test_grouped_down_wc():
@@ -158,6 +183,12 @@ def test_bgmv_grid_bounds_every_routing():
         counts = np.bincount(slots[slots >= 0], minlength=L_)
         need = int(np.sum((counts + rt - 1) // rt))
         assert need <= g["clusters"]
+
+
+def test_gather_geometry_has_no_cluster_split():
+    g = L.lora_launch_geometry(2, 512, 2048, 16, 768, 2048)
+    assert g["cluster"] == 1 and g["clusters"] == 512 // 32 + 512
+    assert L.lora_launch_geometry(0, 512, 2048, 16, 768, 2048)["cluster"] == 4
 
 
 def test_moe_geometry_tiles():

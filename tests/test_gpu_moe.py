@@ -1,10 +1,11 @@
 """CUDA lora_moe_grouped_fold against the CPU oracle (-m gpu), through the C ABI.
 
-Covers the MoE down-projection workload at full size over its four windows of
-4096 sorted rows (every element compared), window invariance (one full-window
-call == the windowed calls, bit for bit), small random routings with ragged
-windows, NULL row_adapter, absent (adapter, expert) entries, rows outside the
-expert spans, bad tokens, an empty window, and graph replay with new routing.
+Covers the MoE down-projection workload and its gate/up form (token-major x
+gathered per sorted row) at full size over their four windows of 4096 sorted
+rows (every element compared), window invariance (one full-window call == the
+windowed calls, bit for bit), small random routings with ragged windows, NULL
+row_adapter, absent (adapter, expert) entries, rows outside the expert spans,
+bad tokens, an empty window, and graph replay with new routing.
 """
 from __future__ import annotations
 
@@ -164,3 +165,42 @@ def test_moe_graph_replay_with_new_row_adapter():
         routes = _routes_all(wl, windows)
         g_xas = [to_u16(xa_w[w])[: hi - lo] for w, (lo, hi) in enumerate(windows)]
         compare_moe(wl, windows, to_u16(d.out_buf), o_out, g_xas, o_xas, o_d, routes)
+
+
+# ---------------------------------------------------------- gate/up (x_gather)
+def test_moe_gateup_workload_parity():
+    wl = W.moe_gateup_fold()
+    assert wl.x_gather and wl.x.shape == (wl.num_tokens, wl.k_in)
+    windows = wl.windows()
+    g_out, g_xas = gpu_moe(wl, windows)
+    o_out, o_xas, o_d = oracle_moe(wl, windows)
+    st = compare_moe(wl, windows, g_out, o_out, g_xas, o_xas, o_d, _routes_all(wl, windows))
+    assert st["rows"] > 10000
+    assert L.lora_read_device_status(clear=True) == 0
+
+
+def test_moe_gateup_full_window_equals_windowed():
+    wl = W.moe_gateup_fold()
+    windows = wl.windows()
+    g_out, g_xas = gpu_moe(wl, windows)
+    f_out, (f_xa,) = gpu_moe(wl, [(0, wl.te)])
+    assert np.array_equal(g_out, f_out)
+    assert np.array_equal(np.concatenate(g_xas), f_xa)
+
+
+@pytest.mark.parametrize("use_ra", [True, False])
+def test_moe_gateup_random_and_bad_tokens(use_ra):
+    wl = W.make_moe("gateup_small", num_tokens=150, top_k=4, num_experts=12, k_in=264,
+                    n_out=136, max_loras=3, max_rank=16, rank=16, alpha=16.0,
+                    adapter_base_frac=0.25, cap=230, seed=410 + int(use_ra),
+                    use_row_adapter=use_ra, present_frac=0.8, x_gather=True)
+    wl.sorted_token_ids = wl.sorted_token_ids.copy()
+    wl.sorted_token_ids[5] = wl.num_tokens + 1    # token out of range: row skipped
+    wl.sorted_token_ids[9] = -2
+    windows = wl.windows()
+    g_out, g_xas = gpu_moe(wl, windows, use_row_adapter=use_ra)
+    o_out, o_xas, o_d = oracle_moe(wl, windows, use_row_adapter=use_ra)
+    routes = _routes_all(wl, windows, row_adapter=wl.row_adapter if use_ra else None)
+    compare_moe(wl, windows, g_out, o_out, g_xas, o_xas, o_d, routes, min_exact=0.97)
+    for r in (5, 9):
+        assert np.array_equal(g_out[r], wl.out_buf[r])
