@@ -352,6 +352,23 @@ int32_t lora_grouped_down_wc(int32_t row_offset, int32_t row_end) {
   return static_cast<int32_t>(std::max<int64_t>(1, (span + LORA_MOE_M_TILE - 1) / LORA_MOE_M_TILE));
 }
 
+int32_t lora_gather_row_token(int32_t row, int32_t top_k) {
+  if (row < 0 || top_k < 1) return -1;
+  return row / top_k;
+}
+
+int lora_gather_bgmv_grids(int32_t max_rank, int32_t n_out, int32_t n_slots, int32_t shrink[3],
+                           int32_t expand[3]) {
+  if (max_rank < 1 || n_out < 1 || n_slots < 0 || !shrink || !expand) return -1;
+  shrink[0] = (max_rank + 3) / 4;
+  shrink[1] = n_slots;
+  shrink[2] = 1;
+  expand[0] = static_cast<int32_t>((static_cast<int64_t>(n_out) + 3) / 4);
+  expand[1] = n_slots;
+  expand[2] = 1;
+  return 0;
+}
+
 int32_t lora_grouped_down_windows(int32_t total_rows, int32_t cap, int32_t* starts, int32_t* ends,
                                   int32_t max_windows) {
   if (cap < 1 || total_rows < 0) return -1;

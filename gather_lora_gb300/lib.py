@@ -56,6 +56,10 @@ def load():
     lib.lora_launch_geometry.argtypes = [ctypes.c_int, I32, I32, I32, I32, I32, ctypes.POINTER(I64)]
     lib.lora_grouped_down_wc.restype = I32
     lib.lora_grouped_down_wc.argtypes = [I32, I32]
+    lib.lora_gather_row_token.restype = I32
+    lib.lora_gather_row_token.argtypes = [I32, I32]
+    lib.lora_gather_bgmv_grids.restype = ctypes.c_int
+    lib.lora_gather_bgmv_grids.argtypes = [I32, I32, I32, ctypes.POINTER(I32), ctypes.POINTER(I32)]
     lib.lora_grouped_down_windows.restype = I32
     lib.lora_grouped_down_windows.argtypes = [I32, I32, ctypes.POINTER(I32), ctypes.POINTER(I32), I32]
     lib.lora_pack_expert_tables.restype = ctypes.c_int
@@ -146,6 +150,18 @@ def lora_launch_geometry(moe, rows, max_loras, max_rank, k_in, n_out) -> dict:
 
 def lora_grouped_down_wc(row_offset: int, row_end: int) -> int:
     return int(load().lora_grouped_down_wc(row_offset, row_end))
+
+
+def lora_gather_row_token(row: int, top_k: int) -> int:
+    return int(load().lora_gather_row_token(row, top_k))
+
+
+def lora_gather_bgmv_grids(max_rank: int, n_out: int, n_slots: int):
+    """((shrink grid), (expand grid)) of the pages' decode gather fold, or ValueError."""
+    sh, ex = (ctypes.c_int32 * 3)(), (ctypes.c_int32 * 3)()
+    if load().lora_gather_bgmv_grids(max_rank, n_out, n_slots, sh, ex) != 0:
+        raise ValueError("bad gather grid arguments")
+    return tuple(sh), tuple(ex)
 
 
 def lora_grouped_down_windows(total_rows: int, cap: int):

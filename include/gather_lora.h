@@ -225,6 +225,27 @@ int lora_launch_geometry(int moe, int32_t rows, int32_t max_loras, int32_t max_r
 int32_t lora_grouped_down_wc(int32_t row_offset, int32_t row_end);
 
 /*
+ * lora_gather_row_token — the token owning flat (token, slot) row `row` of the
+ * decode gather fold: row / top_k (the rule lora_moe_gather_bgmv applies).
+ * Returns -1 if row < 0 or top_k < 1.
+ * Defines: "Module moe_lora_grouped" rustdoc, `gather_row_token` entry.
+ */
+int32_t lora_gather_row_token(int32_t row, int32_t top_k);
+
+/*
+ * lora_gather_bgmv_grids — the pages' exact launch grids of their decode gather
+ * fold: shrink = [ceil(max_rank / 4), n_slots, 1], expand = [ceil(n_out / 4),
+ * n_slots, 1], each with a (256, 1, 1) block (one 64-lane group per output, four
+ * outputs per block). Reading: the shrink's outputs are the max_rank xa columns.
+ * This library's own kernel uses lora_launch_geometry's grid instead; the helper
+ * states the pages' arithmetic. Writes shrink[0..2] and expand[0..2]; returns 0,
+ * or -1 if max_rank or n_out < 1, n_slots < 0, or a pointer is NULL.
+ * Defines: "Module moe_lora_grouped" rustdoc, `gather_bgmv_grids` entry.
+ */
+int lora_gather_bgmv_grids(int32_t max_rank, int32_t n_out, int32_t n_slots,
+                           int32_t shrink[3], int32_t expand[3]);
+
+/*
  * lora_grouped_down_windows — contiguous [start, end) windows of `cap` rows
  * covering 0..total_rows (the last may be shorter). Writes up to max_windows
  * pairs into starts/ends (host arrays) and returns the number of windows, or

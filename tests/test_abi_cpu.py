@@ -36,7 +36,7 @@ def test_header_declares_the_entry_points():
     for n in ("lora_bgmv", "lora_moe_grouped_fold", "lora_moe_gather_bgmv", "lora_last_error",
               "lora_read_device_status",
               "lora_launch_geometry", "lora_grouped_down_wc", "lora_grouped_down_windows",
-              "lora_pack_expert_tables"):
+              "lora_pack_expert_tables", "lora_gather_row_token", "lora_gather_bgmv_grids"):
         assert n in names
 
 
@@ -129,6 +129,25 @@ def test_grouped_down_wc():
     assert L.lora_grouped_down_wc(5, 4) == -1
     for lo, hi in [(0, 1), (3, 131), (64, 128), (7, 7000)]:
         assert L.lora_grouped_down_wc(lo, hi) == max(1, -(-(hi - lo) // 64))
+
+
+def test_gather_row_token():
+    assert L.lora_gather_row_token(0, 8) == 0
+    assert L.lora_gather_row_token(7, 8) == 0
+    assert L.lora_gather_row_token(8, 8) == 1
+    assert L.lora_gather_row_token(511, 8) == 63
+    assert L.lora_gather_row_token(5, 1) == 5
+    assert L.lora_gather_row_token(-1, 8) == -1 and L.lora_gather_row_token(3, 0) == -1
+
+
+def test_gather_bgmv_grids():
+    assert L.lora_gather_bgmv_grids(16, 2048, 512) == ((4, 512, 1), (512, 512, 1))
+    assert L.lora_gather_bgmv_grids(24, 1030, 3) == ((6, 3, 1), (258, 3, 1))   # ceil(./4)
+    assert L.lora_gather_bgmv_grids(8, 8, 0) == ((2, 0, 1), (2, 0, 1))
+    with pytest.raises(ValueError):
+        L.lora_gather_bgmv_grids(0, 8, 1)
+    with pytest.raises(ValueError):
+        L.lora_gather_bgmv_grids(8, 8, -1)
 
 
 def test_grouped_down_windows():
