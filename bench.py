@@ -131,6 +131,34 @@ def gather_algorithmic_bytes(wl) -> dict:
                 flops=int(2 * routed * wl.max_rank * (wl.k_in + wl.n_out)))
 
 
+USE_TMAPS = True     # load A as 2-D TMA boxes through host-encoded tensor maps (--no-tmaps: rows)
+
+
+def a_load(wl) -> str:
+    """How the fold loads A for this workload (the library's own choice: the
+    bgmv and gather folds take the maps from LORA_TMAP_MIN_RANK up; the grouped
+    MoE fold loads rows)."""
+    from gather_lora_gb300 import lib as L
+    kind = workload_kind(wl)
+    tiled = 0
+    if USE_TMAPS and kind == "bgmv":
+        tiled = L.lora_launch_geometry(16, wl.n, wl.max_loras, wl.max_rank, wl.k_in, wl.n_out)["a_tiled"]
+    elif USE_TMAPS and kind == "gather":
+        tiled = L.lora_launch_geometry(18, wl.n_rows, wl.max_loras * wl.num_experts, wl.max_rank,
+                                       wl.k_in, wl.n_out)["a_tiled"]
+    return "2-D TMA boxes via tensor maps" if tiled else "one TMA copy per row"
+
+
+def a_maps_for(a_table, max_rank: int, k_in: int):
+    """Device A tensor maps for a device table (encoded once, as at adapter load), or None."""
+    if not USE_TMAPS:
+        return None
+    import torch
+    from gather_lora_gb300 import lib as L
+    maps = L.lora_encode_a_tmaps(a_table.cpu().numpy().astype("uint64"), max_rank, k_in)
+    return torch.from_numpy(maps).to(a_table.device)
+
+
 def workload_kind(wl) -> str:
     from gather_lora_gb300 import workloads as W
     if isinstance(wl, W.MoeGatherWorkload):
@@ -214,6 +242,7 @@ class BgmvRunner:
         self.wl = wl
         base = W.bgmv_to_device(wl, device)
         self.copies = [base] + [self._clone(base, wl) for _ in range(copies - 1)]
+        self.maps = [a_maps_for(d.a_table, wl.max_rank, wl.k_in) for d in self.copies]
         self.launches_per_step = 1
 
     @staticmethod
@@ -238,7 +267,7 @@ class BgmvRunner:
         wl, d = self.wl, self.copies[c]
         L.lora_bgmv(d.x, wl.x_row_stride, d.out_ptr, wl.out_row_stride, d.seq_slot, wl.n,
                     d.a_table, d.b_table, d.scale, wl.max_loras, wl.max_rank, wl.k_in, wl.n_out,
-                    xa=d.xa, stream=stream)
+                    xa=d.xa, stream=stream, a_tmaps=self.maps[c])
 
 
 class MoeRunner:
@@ -247,6 +276,7 @@ class MoeRunner:
         self.wl = wl
         self.windows = wl.windows()
         self.copies = [W.moe_to_device(wl, device, xa_rows=wl.cap) for _ in range(copies)]
+        self.maps = [a_maps_for(d.a_table, wl.max_rank, wl.k_in) for d in self.copies]
         self.launches_per_step = len(self.windows)
 
     def bytes_per_copy(self):
@@ -261,7 +291,7 @@ class MoeRunner:
                                     wl.num_experts, d.sorted_token_ids, wl.te, d.row_adapter,
                                     wl.num_tokens, lo, hi, d.a_table, d.b_table, d.scale,
                                     wl.max_loras, wl.max_rank, wl.k_in, wl.n_out, xa=d.xa,
-                                    stream=stream, x_gather=wl.x_gather)
+                                    stream=stream, x_gather=wl.x_gather, a_tmaps=self.maps[c])
 
 
 class GatherRunner:
@@ -269,6 +299,7 @@ class GatherRunner:
         from gather_lora_gb300 import workloads as W
         self.wl = wl
         self.copies = [W.gather_to_device(wl, device) for _ in range(copies)]
+        self.maps = [a_maps_for(d.a_table, wl.max_rank, wl.k_in) for d in self.copies]
         self.launches_per_step = 1
 
     def bytes_per_copy(self):
@@ -281,7 +312,7 @@ class GatherRunner:
         L.lora_moe_gather_bgmv(d.x, wl.k_in, d.out_buf, wl.n_out, d.indices, wl.n_rows, wl.top_k,
                                d.row_adapter, wl.num_tokens, wl.num_experts, d.a_table, d.b_table,
                                d.scale, wl.max_loras, wl.max_rank, wl.k_in, wl.n_out, xa=d.xa,
-                               stream=stream)
+                               stream=stream, a_tmaps=self.maps[c])
 
 
 RUNNERS = {"bgmv": BgmvRunner, "moe": MoeRunner, "gather": GatherRunner}
@@ -401,6 +432,7 @@ def e2e_bgmv(wl, device, steps, warmup, copies):
     from gather_lora_gb300 import lib as L
     from gather_lora_gb300 import workloads as W
     devs = [W.bgmv_to_device(wl, device) for _ in range(copies)]
+    maps = [a_maps_for(d.a_table, wl.max_rank, wl.k_in) for d in devs]
     hx = torch.from_numpy(wl.x.view(np.int16)).pin_memory()
     hseq = torch.from_numpy(wl.seq_slot).pin_memory()
     hout = torch.from_numpy(wl.out_buf.view(np.int16)).pin_memory()
@@ -414,7 +446,7 @@ def e2e_bgmv(wl, device, steps, warmup, copies):
         d.out_buf.copy_(hout, non_blocking=True)
         L.lora_bgmv(d.x, wl.x_row_stride, d.out_ptr, wl.out_row_stride, d.seq_slot, wl.n,
                     d.a_table, d.b_table, d.scale, wl.max_loras, wl.max_rank, wl.k_in, wl.n_out,
-                    xa=d.xa, stream=stream)
+                    xa=d.xa, stream=stream, a_tmaps=maps[c % copies])
         hres.copy_(d.out_buf, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -533,10 +565,11 @@ def run_ours(args):
         geometry = L.lora_launch_geometry(1, wl.cap, wl.max_loras if wl.row_adapter is not None else 1,
                                           wl.max_rank, wl.k_in, wl.n_out)
     elif head_kind == "gather":
-        geometry = L.lora_launch_geometry(2, wl.n_rows, wl.max_loras * wl.num_experts, wl.max_rank,
+        geometry = L.lora_launch_geometry(18 if USE_TMAPS else 2, wl.n_rows, wl.max_loras * wl.num_experts, wl.max_rank,
                                           wl.k_in, wl.n_out)
     else:
-        geometry = L.lora_launch_geometry(0, wl.n, wl.max_loras, wl.max_rank, wl.k_in, wl.n_out)
+        geometry = L.lora_launch_geometry(16 if USE_TMAPS else 0, wl.n, wl.max_loras, wl.max_rank,
+                                          wl.k_in, wl.n_out)
 
     # the other fold workloads (per-GPU numbers, same timing rules)
     side = {}
@@ -558,7 +591,7 @@ def run_ours(args):
             "rows_per_s": a2["rows"] / (ms2 / 1e3), "routed_rows_per_s": a2["routed_rows"] / (ms2 / 1e3),
             "ms_per_step": ms2, "launches_per_step": r2.launches_per_step, "steps": k2,
             "algorithmic_bytes": a2["bytes"], "achieved_gbs": gbs2, "frac_of_peak": gbs2 / peak,
-            "frac_of_8tbs": gbs2 / 8000.0, "input_copies": len(r2.copies),
+            "frac_of_8tbs": gbs2 / 8000.0, "input_copies": len(r2.copies), "a_load": a_load(w2),
             "traffic": recorded_traffic(name)}
         del r2
         torch.cuda.empty_cache()
@@ -588,7 +621,8 @@ def run_ours(args):
                        "max_rank": wl.max_rank, "distinct_adapters": alg["adapters"],
                        "parallelism": f"replicas{dctx.world}",
                        "l2": f"rotating {C} input copies ({C * runner.bytes_per_copy() / 2**20:.0f} MiB > 2x L2)",
-                       "graph": "CUDA graph replay, programmatic dependent launch"},
+                       "graph": "CUDA graph replay, programmatic dependent launch",
+                       "a_load": a_load(wl)},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": recorded_traffic(head),
                          "peak_kind": peak_kind, "kernel": KERNEL_NAMES[head_kind],
@@ -614,10 +648,13 @@ def main(argv=None):
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-tmaps", action="store_true", help="load A row by row (no tensor maps)")
     p.add_argument("--only", default=None, help="time one named workload alone (profiling runs)")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
+    global USE_TMAPS
+    USE_TMAPS = not args.no_tmaps
     return run_reference(args) if args.impl == "reference" else run_ours(args)
 
 

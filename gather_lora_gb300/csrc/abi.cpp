@@ -3,6 +3,8 @@
 // before any CUDA call, so a rejected call launches nothing.
 #include "../../include/gather_lora.h"
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -78,7 +80,7 @@ int balanced_chunk(int total, int cap) {
 // window), so a row's arithmetic — the k-slices, k-chunks and summation order —
 // is the same in every call with the same (k_in, n_out, max_rank).
 bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_rank, int k_in,
-                   int n_out, glora::FoldGeometry& g, int max_cl = GLORA_MAX_CLUSTER) {
+                   int n_out, glora::FoldGeometry& g, int max_cl = GLORA_MAX_CLUSTER, bool a_tiled = false) {
   g = glora::FoldGeometry{};
   // bgmv: a cluster splits each unit's k (shrink) and n_out (expand); MoE units
   // are many and small, so one CTA folds whole groups.
@@ -104,6 +106,10 @@ bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_
       if (c <= g.ksl && srows * (c * 2 + 16) <= kStageTarget) { kcap = c; break; }
   }
   g.kch = balanced_chunk(g.ksl, kcap);
+  // A as 2-D TMA boxes of 64 columns: k-chunks are whole boxes (a chunk may
+  // reach past its k-slice; those columns are loaded and not used).
+  g.a_tiled = a_tiled ? 1 : 0;
+  if (a_tiled) g.kch = round_up(g.kch, 64);
   // A unit's items either each go to the one consumer warp that owns their
   // ring slot (many small MoE groups whose shrink is a single k-chunk: the
   // latency chains of several items overlap) or are split tile by tile over
@@ -127,12 +133,13 @@ bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_
   }
   g.pitch_k = g.kch * 2 + 16;
   g.pitch_b = max_rank * 2 + (max_rank >= 32 ? 16 : 0);
-  const int shrink_stage = srows * g.pitch_k;
+  const int shrink_stage = a_tiled ? g.mr16 * g.kch * 2 + g.gmax * g.pitch_k : srows * g.pitch_k;
   const int S = std::max(shrink_stage, kMinStage);
   const int jcap = (S - 16 * g.gmax) / (g.pitch_b + 2 * g.gmax);
   g.jch = balanced_chunk(g.jsl, std::min(jcap, g.jsl));
   const int expand_stage = g.jch * g.pitch_b + g.gmax * (g.jch * 2 + 16);
-  g.stage_bytes = round_up(std::max(shrink_stage, expand_stage), 128);
+  // (stages of tiled launches start on the 1024-byte atom of the 128-byte swizzle)
+  g.stage_bytes = round_up(std::max(shrink_stage, expand_stage), a_tiled ? 1024 : 128);
   g.pitch_part = max_rank + 4;
   g.pitch_xa = max_rank * 2 + 16;
   const int planes = g.ksplit + (g.gather ? g.cl : 0);   // partial planes (+ the all-gather slots)
@@ -144,7 +151,7 @@ bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_
   // the ring doubles as planning scratch (bgmv rows + slot counts / MoE offsets)
   while (ns * g.stage_bytes < planner_ints * 4 && ns < kMaxStages) ++ns;
   if (ns * g.stage_bytes < planner_ints * 4)
-    g.stage_bytes = round_up(static_cast<int>(ceil_div(planner_ints * 4, ns)), 128);
+    g.stage_bytes = round_up(static_cast<int>(ceil_div(planner_ints * 4, ns)), a_tiled ? 1024 : 128);
   g.ns = ns;
   g.off_ring = glora::kPlanBytes;
   g.off_out = 0;
@@ -165,6 +172,31 @@ bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_
     g.clusters = rows <= 0 ? 0 : rows / g.rt + std::min(rows, max_loras);
   }
   return true;
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once (NULL without a driver).
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// Launch geometry for a fold call, with A as tensor-map boxes when maps are given
+// and max_rank >= LORA_TMAP_MIN_RANK (falls back to padded A rows otherwise, or
+// when the tiled layout does not fit). Measured on GB300: at rank 16 the boxes
+// (16 rows of 128 bytes) made decode-sized folds about 5% slower than one copy
+// per 512-byte row, while at ranks 64 and 128 they made the folds 6-11% faster.
+bool fold_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_rank, int k_in, int n_out,
+                   glora::FoldGeometry& g, int max_cl, const void* a_tmaps) {
+  if (a_tmaps && max_rank >= LORA_TMAP_MIN_RANK && make_geometry(moe, rows, max_loras, planner_ints, max_rank, k_in, n_out, g, max_cl, true))
+    return true;
+  return make_geometry(moe, rows, max_loras, planner_ints, max_rank, k_in, n_out, g, max_cl, false);
 }
 
 int check_shape(int32_t max_rank, int32_t k_in, int32_t n_out, int64_t xs, int64_t os) {
@@ -193,7 +225,8 @@ const char* lora_last_error(void) { return g_err; }
 int lora_bgmv(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_t* base_out, int64_t out_row_stride,
               const int32_t* seq_slot, int32_t n, const lora_bf16_t* const* a_table,
               const lora_bf16_t* const* b_table, const float* scale_table, int32_t max_loras,
-              int32_t max_rank, int32_t k_in, int32_t n_out, lora_bf16_t* xa, void* stream) {
+              int32_t max_rank, int32_t k_in, int32_t n_out, lora_bf16_t* xa, const void* a_tmaps,
+              void* stream) {
   if (n < 0 || n > LORA_MAX_ROWS) return fail(LORA_ERR_SIZE, "n %d outside [0, %d]", n, LORA_MAX_ROWS);
   if (max_loras < 1 || max_loras > LORA_MAX_LORAS)
     return fail(LORA_ERR_SIZE, "max_loras %d outside [1, %d]", max_loras, LORA_MAX_LORAS);
@@ -205,8 +238,11 @@ int lora_bgmv(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_t* base_out,
   if (!aligned16(x) || !aligned16(base_out) || (xa && !aligned16(xa)))
     return fail(LORA_ERR_ALIGN, "x, base_out and xa must be 16-byte aligned");
   glora::BgmvArgs a{};
-  if (!make_geometry(false, n, max_loras, ((n + 3) & ~3) + max_loras, max_rank, k_in, n_out, a.g))
+  if (a_tmaps && (reinterpret_cast<uintptr_t>(a_tmaps) & 63u))
+    return fail(LORA_ERR_ALIGN, "a_tmaps must be 64-byte aligned");
+  if (!fold_geometry(false, n, max_loras, ((n + 3) & ~3) + max_loras, max_rank, k_in, n_out, a.g, GLORA_MAX_CLUSTER, a_tmaps))
     return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory for max_rank %d, k_in %d, n_out %d", max_rank, k_in, n_out);
+  a.a_maps = a.g.a_tiled ? a_tmaps : nullptr;
   a.x = x;
   a.x_stride = x_row_stride;
   a.out = base_out;
@@ -231,7 +267,7 @@ int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, int32_t x_
                           int32_t num_tokens, int32_t row_offset, int32_t row_end,
                           const lora_bf16_t* const* a_table, const lora_bf16_t* const* b_table,
                           const float* scale_table, int32_t max_loras, int32_t max_rank, int32_t k_in,
-                          int32_t n_out, lora_bf16_t* xa, void* stream) {
+                          int32_t n_out, lora_bf16_t* xa, const void* a_tmaps, void* stream) {
   if (num_experts < 1 || num_experts > LORA_MAX_EXPERTS)
     return fail(LORA_ERR_SIZE, "num_experts %d outside [1, %d]", num_experts, LORA_MAX_EXPERTS);
   if (max_loras < 1 || max_loras > LORA_MAX_LORAS)
@@ -248,6 +284,10 @@ int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, int32_t x_
   if (!aligned16(x) || !aligned16(base_out) || (xa && !aligned16(xa)))
     return fail(LORA_ERR_ALIGN, "x, base_out and xa must be 16-byte aligned");
   glora::MoeArgs a{};
+  if (a_tmaps && (reinterpret_cast<uintptr_t>(a_tmaps) & 63u))
+    return fail(LORA_ERR_ALIGN, "a_tmaps must be 64-byte aligned");
+  // (The grouped fold's A rows span whole k-chunks of 768+ bytes; it loads them
+  // row by row and does not use tensor maps.)
   if (!make_geometry(true, row_end - row_offset, row_adapter ? max_loras : 1, num_experts + 1, max_rank, k_in,
                      n_out, a.g))
     return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory for max_rank %d, k_in %d, n_out %d", max_rank, k_in, n_out);
@@ -261,6 +301,7 @@ int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, int32_t x_
   a.row_adapter = row_adapter;
   a.num_tokens = num_tokens;
   a.x_gather = x_gather ? 1 : 0;
+  a.a_maps = nullptr;
   a.row_offset = row_offset;
   a.row_end = row_end;
   a.a_table = a_table;
@@ -280,7 +321,7 @@ int lora_moe_gather_bgmv(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_t
                          const int32_t* row_adapter, int32_t num_tokens, int32_t num_experts,
                          const lora_bf16_t* const* a_table, const lora_bf16_t* const* b_table,
                          const float* scale_table, int32_t max_loras, int32_t max_rank, int32_t k_in,
-                         int32_t n_out, lora_bf16_t* xa, void* stream) {
+                         int32_t n_out, lora_bf16_t* xa, const void* a_tmaps, void* stream) {
   if (n_rows < 0 || n_rows > LORA_MAX_ROWS) return fail(LORA_ERR_SIZE, "n_rows %d outside [0, %d]", n_rows, LORA_MAX_ROWS);
   if (top_k < 1) return fail(LORA_ERR_SIZE, "top_k %d < 1", top_k);
   if (num_tokens < 0) return fail(LORA_ERR_SIZE, "num_tokens %d < 0", num_tokens);
@@ -300,13 +341,16 @@ int lora_moe_gather_bgmv(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_t
   glora::BgmvArgs a{};
   // Decode MoE rows spread over many (adapter, expert) entries of about one row
   // each: one CTA per unit (no cluster split) keeps the grid near one wave.
-  if (!make_geometry(false, n_rows, tables, ((n_rows + 3) & ~3) + tables, max_rank, k_in, n_out, a.g, 1))
+  if (a_tmaps && (reinterpret_cast<uintptr_t>(a_tmaps) & 63u))
+    return fail(LORA_ERR_ALIGN, "a_tmaps must be 64-byte aligned");
+  if (!fold_geometry(false, n_rows, tables, ((n_rows + 3) & ~3) + tables, max_rank, k_in, n_out, a.g, 1, a_tmaps))
     return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory for max_rank %d, k_in %d, n_out %d", max_rank, k_in, n_out);
   a.x = x;
   a.x_stride = x_row_stride;
   a.out = base_out;
   a.out_stride = out_row_stride;
   a.seq_slot = nullptr;
+  a.a_maps = a.g.a_tiled ? a_tmaps : nullptr;
   a.n = n_rows;
   a.indices = indices;
   a.row_adapter = row_adapter;
@@ -331,17 +375,20 @@ int lora_read_device_status(void* stream, uint32_t* status_out, int clear) {
 }
 
 int lora_launch_geometry(int moe, int32_t rows, int32_t max_loras, int32_t max_rank, int32_t k_in,
-                         int32_t n_out, int64_t out[9]) {
+                         int32_t n_out, int64_t out[10]) {
   if (!out) return fail(LORA_ERR_NULL, "out is NULL");
   int rc = check_shape(max_rank, k_in, n_out, k_in, n_out);
   if (rc) return rc;
   glora::FoldGeometry g{};
-  const bool grouped = moe == 1;
+  const int kind = moe & 15;
+  const bool grouped = kind == 1;
   const int scratch = grouped ? LORA_MAX_EXPERTS + 1 : ((rows + 3) & ~3) + max_loras;
-  if (!make_geometry(grouped, rows, max_loras, scratch, max_rank, k_in, n_out, g,
-                     moe == 2 ? 1 : GLORA_MAX_CLUSTER))
+  // stands for a tensor-map array (only its presence matters); the grouped fold ignores maps
+  static const char kAnyMaps = 0;
+  if (!fold_geometry(grouped, rows, max_loras, scratch, max_rank, k_in, n_out, g,
+                     kind == 2 ? 1 : GLORA_MAX_CLUSTER, (moe & 16) && !grouped ? &kAnyMaps : nullptr))
     return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory");
-  const int64_t v[9] = {g.cl, g.rt, g.ksl, g.jsl, g.kch, g.jch, g.ns, g.clusters, g.smem_bytes};
+  const int64_t v[10] = {g.cl, g.rt, g.ksl, g.jsl, g.kch, g.jch, g.ns, g.clusters, g.smem_bytes, g.a_tiled};
   std::memcpy(out, v, sizeof v);
   return ok();
 }
@@ -367,6 +414,35 @@ int lora_gather_bgmv_grids(int32_t max_rank, int32_t n_out, int32_t n_slots, int
   expand[1] = n_slots;
   expand[2] = 1;
   return 0;
+}
+
+int lora_encode_a_tmaps(const uint64_t* a_ptrs, int32_t count, int32_t max_rank, int32_t k_in,
+                        void* maps_out) {
+  if (count < 0) return fail(LORA_ERR_SIZE, "count %d < 0", count);
+  if (max_rank < 8 || max_rank > LORA_MAX_RANK) return fail(LORA_ERR_SIZE, "max_rank %d outside [8, %d]", max_rank, LORA_MAX_RANK);
+  if (k_in < 8 || k_in > LORA_MAX_K_IN) return fail(LORA_ERR_SIZE, "k_in %d outside [8, %d]", k_in, LORA_MAX_K_IN);
+  if (k_in % 8) return fail(LORA_ERR_ALIGN, "k_in %d must be a multiple of 8", k_in);
+  if (count == 0) return ok();
+  if (!a_ptrs || !maps_out) return fail(LORA_ERR_NULL, "a_ptrs and maps_out are required");
+  if (reinterpret_cast<uintptr_t>(maps_out) & 63u) return fail(LORA_ERR_ALIGN, "maps_out must be 64-byte aligned");
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = encode_tiled();
+  if (!enc) return fail(LORA_ERR_CUDA, "cuTensorMapEncodeTiled is not available (no CUDA driver)");
+  const int mr16 = (max_rank + 15) / 16 * 16;
+  auto* maps = static_cast<CUtensorMap*>(maps_out);
+  for (int32_t i = 0; i < count; ++i) {
+    std::memset(&maps[i], 0, sizeof(CUtensorMap));
+    if (a_ptrs[i] == 0) continue;
+    if (a_ptrs[i] & 15u) return fail(LORA_ERR_ALIGN, "A pointer %d is not 16-byte aligned", i);
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k_in), static_cast<cuuint64_t>(max_rank)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(k_in) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(mr16)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(&maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, reinterpret_cast<void*>(a_ptrs[i]), dims,
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(LORA_ERR_CUDA, "cuTensorMapEncodeTiled failed for A pointer %d (%d)", i, static_cast<int>(r));
+  }
+  return ok();
 }
 
 int32_t lora_grouped_down_windows(int32_t total_rows, int32_t cap, int32_t* starts, int32_t* ends,

@@ -102,6 +102,20 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src, uin
                ::"r"(dst_smem), "l"(src), "r"(bytes), "r"(bar)
                : "memory");
 }
+// 2-D TMA tile load: the box of the tensor map `map` (a CUtensorMap in global or
+// parameter memory) at coordinates (c0 innermost, c1) into shared memory at dst,
+// completing on mbarrier `bar`. c0 * element size must be a multiple of 16 bytes;
+// out-of-range parts of the box are filled with zeros and still count as bytes.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst_smem, const void* map, int c0, int c1, uint32_t bar) {
+  asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n"
+               ::"r"(dst_smem), "l"(map), "r"(c0), "r"(c1), "r"(bar)
+               : "memory");
+}
+// Start fetching a tensor map (in global memory) into the descriptor cache
+// ahead of its first use by tma_load_2d.
+__device__ __forceinline__ void prefetch_tensormap(const void* map) {
+  asm volatile("prefetch.tensormap [%0];\n" ::"l"(map) : "memory");
+}
 // Order this thread's generic-proxy shared-memory accesses before later
 // async-proxy (TMA) accesses of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -29,6 +29,8 @@ struct FoldGeometry {
   int ksplit;       // tile-parallel: k-phases the consumer warps form (1, 2, 4, 8; partial planes of part_s)
   int direct;       // bgmv: unit s < max_loras is tile 0 of slot s (max_loras <= rows)
   int gather;       // exchange by all-gather of fp32 partials into cl planes after the k-phase planes
+  int a_tiled;      // shrink stages hold A as 2-D TMA boxes (kch/64 boxes of mr16 rows x 128 B,
+                    // 128-byte swizzle) ahead of the padded x rows; 0: padded A rows
   int mr16;         // max_rank rounded up to 16
   int pitch_k;      // bytes per A or x row in a shrink stage (kch*2 + 16)
   int pitch_b;      // bytes per B row in an expand stage
@@ -45,6 +47,7 @@ struct BgmvArgs {
   long long x_stride;
   uint16_t* out;
   long long out_stride;
+  const void* a_maps;        // [max_loras] 128-byte A tensor maps (a_tiled), or NULL
   const int32_t* seq_slot;   // slot per row, or NULL: derived from the MoE decode routing below
   int n;
   const int32_t* indices;    // MoE decode rows: expert per row
@@ -70,6 +73,7 @@ struct MoeArgs {
   const int32_t* row_adapter;
   int num_tokens;
   int x_gather;     // 1: x is token-major; sorted row r reads row sorted_token_ids[r]
+  const void* a_maps;  // [max_loras * num_experts] 128-byte A tensor maps (a_tiled), or NULL
   int row_offset, row_end;
   const uint16_t* const* a_table;
   const uint16_t* const* b_table;

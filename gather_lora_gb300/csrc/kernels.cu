@@ -68,6 +68,7 @@ struct Plan {
   float gscale[kMaxRows];
   const uint16_t* gA[kMaxRows];
   const uint16_t* gB[kMaxRows];
+  const void* gmap[kMaxRows];      // the group's A tensor map (a_tiled launches)
   int tpos[kMaxTileRows];          // MoE: tile rows routed to this unit's adapter, ascending
   int tkey[kMaxTileRows];          // MoE: their experts
   int txrow[kMaxTileRows];         // MoE: their rows of x (the token with x_gather)
@@ -89,6 +90,15 @@ __device__ __forceinline__ void record_timeout(Plan& pl) {
   pl.failed = 1;
 }
 
+// Launches with A as swizzled TMA boxes need the ring on a 1024-byte boundary
+// (the 128-byte swizzle atom). If the dynamic shared memory were placed
+// otherwise, fold nothing and report it instead of issuing the copies.
+__device__ __forceinline__ bool tiled_smem_ok(const FoldGeometry& g, const unsigned char* smem) {
+  if (!g.a_tiled || ((smem_u32(smem) + g.off_ring) & 1023u) == 0) return true;
+  if (threadIdx.x == 0) atomicOr(&g_lora_status, kDevMisaligned);
+  return false;
+}
+
 // The ring's mbarriers, initialized once per CTA; passes of a work unit keep
 // counting ring items from where the previous pass stopped. Called by all threads.
 __device__ __forceinline__ void ring_init(Plan& pl, int ns) {
@@ -108,8 +118,9 @@ __device__ __forceinline__ void ring_init(Plan& pl, int ns) {
 // Called by all kThreads threads of every CTA of the cluster, after
 // ring_init(); `it0` ring items were used by earlier passes. Returns the ring
 // items this pass used. MAXT bounds the 16x8 shrink tiles one consumer warp
-// owns (MT * ceil(group rows / 8) <= 8 * MAXT).
-template <int MAXT>
+// owns (MT * ceil(group rows / 8) <= 8 * MAXT). TILED: A comes as TMA boxes
+// (launches with g.a_tiled); each instance has one A layout.
+template <int MAXT, bool TILED>
 __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeometry& g, Plan& pl,
                                            unsigned char* smem, const cg::cluster_group& cluster,
                                            int crank, int it0) {
@@ -163,13 +174,21 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
       long long stride0, stride1;
       uint32_t dst0, dst1;
       int n0, bytes0, pitch0, n1, bytes1, pitch1, m0;
+      const void* amap = nullptr;   // a_tiled shrink item: A comes as kch/64 boxes of this map
+      int k0 = 0;
       if (it < n_shrink) {
         const int gi = it / nk, kc = it - gi * nk;
-        const int k0 = k_lo + kc * g.kch, bytes = min(g.kch, k_hi - k0) * 2;
+        k0 = k_lo + kc * g.kch;
+        const int bytes = min(g.kch, k_hi - k0) * 2;
         m0 = pl.gstart[gi];
         src0 = pl.gA[gi] + k0; stride0 = p.k_in; dst0 = st; n0 = p.max_rank; bytes0 = bytes; pitch0 = g.pitch_k;
         src1 = p.x + k0; stride1 = p.x_stride; dst1 = st + g.mr16 * g.pitch_k; n1 = pl.gstart[gi + 1] - m0;
         bytes1 = bytes; pitch1 = g.pitch_k;
+        if (TILED && g.a_tiled) {
+          amap = pl.gmap[gi];
+          n0 = 0;
+          dst1 = st + g.mr16 * g.kch * 2;
+        }
       } else {
         const int e = it - n_shrink, gi = e / nj, jc = e - gi * nj;
         const int j0 = j_lo + jc * g.jch, jlen = min(g.jch, j_hi - j0);
@@ -183,8 +202,13 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
       // TMA bytes this thread issues (rows q0, q0 + kP, ... of each TMA set)
       const int mine0 = bytes0 >= kTmaRowBytes && q0 < n0 ? (n0 - 1 - q0) / kP + 1 : 0;
       const int mine1 = bytes1 >= kTmaRowBytes && q0 < n1 ? (n1 - 1 - q0) / kP + 1 : 0;
-      const int tx = mine0 * bytes0 + mine1 * bytes1;
+      const int nbox = g.kch >> 6, a_box = g.mr16 * 128;
+      const int tx = mine0 * bytes0 + mine1 * bytes1 + (amap && pt == 0 ? nbox * a_box : 0);
       if (tx) mbar_expect_tx(full, static_cast<uint32_t>(tx));
+      if (amap && pt == 0) {
+#pragma unroll 1
+        for (int b = 0; b < nbox; ++b) tma_load_2d(st + b * a_box, amap, k0 + 64 * b, 0, full);
+      }
 #pragma unroll 1
       for (int set = 0; set < 2; ++set) {
         const uint16_t* src = set ? src1 : src0;
@@ -242,7 +266,8 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
   const int t_first = gpar ? 0 : warp % TW, t_step = gpar ? 1 : TW;
   const int MT = g.mr16 >> 4;
   const int plane = g.rt * g.pitch_part;         // floats per k-phase plane of part_s
-  for (int gi = g_first; gi < G && nk > 0 && !idle; gi += g_step) {
+  // The shrink of one group, compiled per A layout (padded rows, or swizzled TMA boxes).
+  auto shrink_group = [&](int gi, auto tiled_c) {
     const int m0 = pl.gstart[gi], R = pl.gstart[gi + 1] - m0, NT = (R + 7) >> 3, ntiles = MT * NT;
     // Independent accumulator chains per tile (k-steps dealt round-robin over
     // the chains within each chunk) when a warp holds few tiles, so consecutive
@@ -251,48 +276,66 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
     // warp stride is a multiple of MT), its A fragment is loaded once per k-step.
     constexpr int kChains = MAXT == 1 ? 4 : (MAXT == 2 ? 2 : 1);
     const bool share_a = !gpar && (TW % MT) == 0;
+    // A fragment rows: padded rows (pitch_k), or 128-byte swizzled rows of
+    // 64-column TMA boxes (a_tiled: 16-byte chunk c of row r sits at chunk
+    // c ^ (r & 7)); the x rows follow the A region, padded.
+    constexpr bool tiled = decltype(tiled_c)::value;
+    const int a_box = g.mr16 * 128;                  // bytes per A box
+    const uint32_t x_base = tiled ? g.mr16 * g.kch * 2 : g.mr16 * g.pitch_k;
+    int a_row[MAXT];
     uint32_t a_off[MAXT], x_off[MAXT];
     float acc[kChains][MAXT][4];
 #pragma unroll
     for (int i = 0; i < MAXT; ++i) {
       const int t = t_first + i * t_step;
       const int mt = t % MT, nt = t / MT;
-      a_off[i] = (mt * 16 + (lane & 15)) * g.pitch_k;
-      x_off[i] = (g.mr16 + nt * 8 + (lane & 7)) * g.pitch_k;
+      a_row[i] = mt * 16 + (lane & 15);
+      a_off[i] = a_row[i] * (tiled ? 128 : g.pitch_k);
+      x_off[i] = x_base + (nt * 8 + (lane & 7)) * g.pitch_k;
 #pragma unroll
       for (int ch = 0; ch < kChains; ++ch) acc[ch][i][0] = acc[ch][i][1] = acc[ch][i][2] = acc[ch][i][3] = 0.f;
     }
+    // this lane's ldmatrix address of A tile i at k-step kk (x4 for k16: lanes
+    // 16..31 take the second 8 columns; x2 for the k8 tail)
+    auto a_addr = [&](uint32_t st, int i, int kk, bool k16) -> uint32_t {
+      if constexpr (tiled) {
+        const int c = ((kk & 63) >> 3) + (k16 ? (lane >> 4) : 0);
+        return st + (kk >> 6) * a_box + a_off[i] + ((c ^ (a_row[i] & 7)) << 4);
+      } else {
+        return st + a_off[i] + kk * 2 + (k16 ? ((lane >> 4) << 4) : 0);
+      }
+    };
     // one k-step (16, or an 8-wide tail) of every tile of this warp into chain `ch`
     auto step = [&](uint32_t st, int kk, int kstep, float (&ac)[MAXT][4]) {
-      if (share_a) {
-        if (kstep == 16) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4(st + a_off[0] + kk * 2 + ((lane >> 4) << 4), a0, a1, a2, a3);
-#pragma unroll
-          for (int i = 0; i < MAXT; ++i) {
-            if (t_first + i * t_step < ntiles) {
-              uint32_t b0, b1;
-              ldsm_x2(st + x_off[i] + kk * 2 + (((lane >> 3) & 1) << 4), b0, b1);
-              mma_k16(ac[i], a0, a1, a2, a3, b0, b1);
-            }
-          }
-        } else {
-          uint32_t a0, a1;
-          ldsm_x2(st + a_off[0] + kk * 2, a0, a1);
-#pragma unroll
-          for (int i = 0; i < MAXT; ++i) {
-            if (t_first + i * t_step < ntiles) {
-              uint32_t b0;
-              ldsm_x1(st + x_off[i] + kk * 2, b0);
-              mma_k8(ac[i], a0, a1, b0);
-            }
-          }
-        }
-      } else {
+      if (!tiled && !share_a) {
 #pragma unroll
         for (int i = 0; i < MAXT; ++i) {
           if (t_first + i * t_step < ntiles)
             mma_step(ac[i], st + a_off[i] + kk * 2, st + x_off[i] + kk * 2, kstep, lane);
+        }
+      } else if (kstep == 16) {
+        uint32_t a0, a1, a2, a3;
+        if (share_a) ldsm_x4(a_addr(st, 0, kk, true), a0, a1, a2, a3);
+#pragma unroll
+        for (int i = 0; i < MAXT; ++i) {
+          if (t_first + i * t_step < ntiles) {
+            if (!share_a) ldsm_x4(a_addr(st, i, kk, true), a0, a1, a2, a3);
+            uint32_t b0, b1;
+            ldsm_x2(st + x_off[i] + kk * 2 + (((lane >> 3) & 1) << 4), b0, b1);
+            mma_k16(ac[i], a0, a1, a2, a3, b0, b1);
+          }
+        }
+      } else {
+        uint32_t a0, a1;
+        if (share_a) ldsm_x2(a_addr(st, 0, kk, false), a0, a1);
+#pragma unroll
+        for (int i = 0; i < MAXT; ++i) {
+          if (t_first + i * t_step < ntiles) {
+            if (!share_a) ldsm_x2(a_addr(st, i, kk, false), a0, a1);
+            uint32_t b0;
+            ldsm_x1(st + x_off[i] + kk * 2, b0);
+            mma_k8(ac[i], a0, a1, b0);
+          }
         }
       }
     };
@@ -331,6 +374,9 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
         }
       }
     }
+  };
+  for (int gi = g_first; gi < G && nk > 0 && !idle; gi += g_step) {
+    shrink_group(gi, std::integral_constant<bool, TILED>{});
   }
   if (nk == 0) {  // empty k-slice: the partials are zero
     for (int e = tid; e < KS * NV * p.max_rank; e += kConsumerWarps * 32) {
@@ -544,7 +590,7 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
 // a * E + e of the row's expert and its token's adapter, and max_loras is the
 // table count.
 // ============================================================================
-template <int MAXT>
+template <int MAXT, bool TILED>
 __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __grid_constant__ BgmvArgs p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const FoldGeometry& g = p.g;
@@ -555,13 +601,17 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
   Plan& pl = *reinterpret_cast<Plan*>(smem);
 
   pdl_wait_then_release();
+  if (!tiled_smem_ok(g, smem)) return;
 
   const bool first_tile = g.direct && unit < p.max_loras;
   int slot = first_tile ? unit : -1, tile = 0;
   const uint16_t* tab_a = nullptr;  // table entries: the loads overlap the scans below
   const uint16_t* tab_b = nullptr;
   float tab_s = 0.f;
+  // the slot's A tensor map (a_tiled launches); its descriptor fetch overlaps the scans
+  auto a_map = [&](int s) { return static_cast<const char*>(p.a_maps) + 128 * static_cast<long long>(s); };
   if (first_tile && tid == 0) {
+    if (TILED) prefetch_tensormap(a_map(slot));
     tab_a = p.a_table[slot];
     tab_b = p.b_table[slot];
     tab_s = p.scale_table[slot];
@@ -610,6 +660,7 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
     if (slot < 0) return;  // every CTA of the cluster takes this branch together
     tile = pl.found_tile;
     if (tid == 0) {
+      if (TILED) prefetch_tensormap(a_map(slot));
       tab_a = p.a_table[slot];
       tab_b = p.b_table[slot];
       tab_s = p.scale_table[slot];
@@ -651,6 +702,7 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
   if (R <= 0) return;  // no rows for this unit (every thread computed the same count)
   if (tid == 0) {
     pl.gA[0] = tab_a;
+    pl.gmap[0] = TILED ? a_map(slot) : nullptr;
     pl.gB[0] = tab_b;
     pl.gscale[0] = tab_s;
     const uintptr_t a = reinterpret_cast<uintptr_t>(tab_a), b = reinterpret_cast<uintptr_t>(tab_b);
@@ -671,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
 
   ring_init(pl, g.ns);
   const EngineArgs ea{p.x, p.x_stride, p.out, p.out_stride, p.xa, p.max_rank, p.k_in, p.n_out};
-  fold_engine<MAXT>(ea, g, pl, smem, cluster, crank, 0);
+  fold_engine<MAXT, TILED>(ea, g, pl, smem, cluster, crank, 0);
 }
 
 // ============================================================================
@@ -820,7 +872,7 @@ __global__ void __launch_bounds__(kThreads, 2) lora_moe_fold_kernel(const __grid
       pl.NV = nvk;
     }
     __syncthreads();
-    if (pl.G > 0) it0 += fold_engine<MAXT>(ea, g, pl, smem, cluster, crank, it0);
+    if (pl.G > 0) it0 += fold_engine<MAXT, false>(ea, g, pl, smem, cluster, crank, it0);
     __syncthreads();   // the next pass rewrites the plan
   }
 }
@@ -858,10 +910,18 @@ static int launch_fold(void (*kernel)(Args), const Args& a, void* stream) {
 }
 
 int launch_bgmv(const BgmvArgs& a, void* stream) {
+  if (a.g.a_tiled) {
+    switch (a.g.maxt) {
+      case 1: return launch_fold(lora_bgmv_fold_kernel<1, true>, a, stream);
+      case 2: return launch_fold(lora_bgmv_fold_kernel<2, true>, a, stream);
+      case 4: return launch_fold(lora_bgmv_fold_kernel<4, true>, a, stream);
+      default: return static_cast<int>(cudaErrorInvalidValue);
+    }
+  }
   switch (a.g.maxt) {
-    case 1: return launch_fold(lora_bgmv_fold_kernel<1>, a, stream);
-    case 2: return launch_fold(lora_bgmv_fold_kernel<2>, a, stream);
-    case 4: return launch_fold(lora_bgmv_fold_kernel<4>, a, stream);
+    case 1: return launch_fold(lora_bgmv_fold_kernel<1, false>, a, stream);
+    case 2: return launch_fold(lora_bgmv_fold_kernel<2, false>, a, stream);
+    case 4: return launch_fold(lora_bgmv_fold_kernel<4, false>, a, stream);
     default: return static_cast<int>(cudaErrorInvalidValue);
   }
 }

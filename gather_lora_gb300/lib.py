@@ -20,6 +20,7 @@ STATUS_NAMES = {-1: "LORA_ERR_NULL", -2: "LORA_ERR_SIZE", -3: "LORA_ERR_STRIDE",
                 -7: "LORA_ERR_UNSUPPORTED"}
 LORA_DEV_MISALIGNED = 0x1
 MOE_M_TILE = 64
+TMAP_MIN_RANK = 32         # LORA_TMAP_MIN_RANK: a_tmaps are used from this max_rank up
 
 
 class LoraError(RuntimeError):
@@ -41,13 +42,15 @@ def load():
     lib = ctypes.CDLL(LIB_PATH)
     P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
     lib.lora_bgmv.restype = ctypes.c_int
-    lib.lora_bgmv.argtypes = [P, I64, P, I64, P, I32, P, P, P, I32, I32, I32, I32, P, P]
+    lib.lora_bgmv.argtypes = [P, I64, P, I64, P, I32, P, P, P, I32, I32, I32, I32, P, P, P]
     lib.lora_moe_grouped_fold.restype = ctypes.c_int
     lib.lora_moe_grouped_fold.argtypes = [P, I64, I32, P, I64, P, I32, P, I32, P, I32, I32, I32,
-                                          P, P, P, I32, I32, I32, I32, P, P]
+                                          P, P, P, I32, I32, I32, I32, P, P, P]
     lib.lora_moe_gather_bgmv.restype = ctypes.c_int
     lib.lora_moe_gather_bgmv.argtypes = [P, I64, P, I64, P, I32, I32, P, I32, I32,
-                                         P, P, P, I32, I32, I32, I32, P, P]
+                                         P, P, P, I32, I32, I32, I32, P, P, P]
+    lib.lora_encode_a_tmaps.restype = ctypes.c_int
+    lib.lora_encode_a_tmaps.argtypes = [P, I32, I32, I32, P]
     lib.lora_last_error.restype = ctypes.c_char_p
     lib.lora_last_error.argtypes = []
     lib.lora_read_device_status.restype = ctypes.c_int
@@ -96,36 +99,51 @@ def _check(rc: int) -> int:
 
 
 def lora_bgmv(x, x_row_stride, base_out, out_row_stride, seq_slot, n, a_table, b_table,
-              scale_table, max_loras, max_rank, k_in, n_out, xa=None, stream=None):
+              scale_table, max_loras, max_rank, k_in, n_out, xa=None, stream=None, a_tmaps=None):
     """Routed bgmv fold (see lora_bgmv in include/gather_lora.h)."""
     return _check(load().lora_bgmv(_addr(x), x_row_stride, _addr(base_out), out_row_stride,
                                    _addr(seq_slot), n, _addr(a_table), _addr(b_table),
                                    _addr(scale_table), max_loras, max_rank, k_in, n_out,
-                                   _addr(xa), _stream(stream)))
+                                   _addr(xa), _addr(a_tmaps), _stream(stream)))
 
 
 def lora_moe_grouped_fold(x, x_row_stride, base_out, out_row_stride, expert_offsets, num_experts,
                           sorted_token_ids, te, row_adapter, num_tokens, row_offset, row_end,
                           a_table, b_table, scale_table, max_loras, max_rank, k_in, n_out,
-                          xa=None, stream=None, x_gather=False):
+                          xa=None, stream=None, x_gather=False, a_tmaps=None):
     """MoE grouped fold of one window (see lora_moe_grouped_fold in include/gather_lora.h).
     x_gather: x is token-major and sorted row r reads row sorted_token_ids[r] (gate/up)."""
     return _check(load().lora_moe_grouped_fold(
         _addr(x), x_row_stride, 1 if x_gather else 0, _addr(base_out), out_row_stride, _addr(expert_offsets),
         num_experts, _addr(sorted_token_ids), te, _addr(row_adapter), num_tokens, row_offset,
         row_end, _addr(a_table), _addr(b_table), _addr(scale_table), max_loras, max_rank, k_in,
-        n_out, _addr(xa), _stream(stream)))
+        n_out, _addr(xa), _addr(a_tmaps), _stream(stream)))
 
 
 def lora_moe_gather_bgmv(x, x_row_stride, base_out, out_row_stride, indices, n_rows, top_k,
                          row_adapter, num_tokens, num_experts, a_table, b_table, scale_table,
-                         max_loras, max_rank, k_in, n_out, xa=None, stream=None):
+                         max_loras, max_rank, k_in, n_out, xa=None, stream=None, a_tmaps=None):
     """Decode-path MoE fold over flat (token, slot) rows (see lora_moe_gather_bgmv in
     include/gather_lora.h)."""
     return _check(load().lora_moe_gather_bgmv(
         _addr(x), x_row_stride, _addr(base_out), out_row_stride, _addr(indices), n_rows, top_k,
         _addr(row_adapter), num_tokens, num_experts, _addr(a_table), _addr(b_table),
-        _addr(scale_table), max_loras, max_rank, k_in, n_out, _addr(xa), _stream(stream)))
+        _addr(scale_table), max_loras, max_rank, k_in, n_out, _addr(xa), _addr(a_tmaps),
+        _stream(stream)))
+
+
+def lora_encode_a_tmaps(a_ptrs, max_rank: int, k_in: int):
+    """Host-encoded A tensor maps (see lora_encode_a_tmaps): returns a uint8 numpy
+    array of len(a_ptrs) * 128 bytes to copy to (64-byte aligned) device memory."""
+    import numpy as np
+    ptrs = np.ascontiguousarray(np.asarray(a_ptrs, dtype=np.uint64))
+    n = int(ptrs.shape[0])
+    buf = np.zeros(n * 128 + 64, dtype=np.uint8)
+    off = (-buf.ctypes.data) % 64
+    maps = buf[off:off + n * 128]
+    _check(load().lora_encode_a_tmaps(ptrs.ctypes.data if n else None, n, max_rank, k_in,
+                                      maps.ctypes.data if n else None))
+    return maps.copy()
 
 
 def lora_last_error() -> str:
@@ -139,11 +157,11 @@ def lora_read_device_status(stream=None, clear=True) -> int:
 
 
 GEOMETRY_KEYS = ("cluster", "rows_per_tile", "k_slice", "j_slice", "k_chunk", "j_chunk",
-                 "ring_stages", "clusters", "smem_bytes")
+                 "ring_stages", "clusters", "smem_bytes", "a_tiled")
 
 
 def lora_launch_geometry(moe, rows, max_loras, max_rank, k_in, n_out) -> dict:
-    out = (ctypes.c_int64 * 9)()
+    out = (ctypes.c_int64 * 10)()
     _check(load().lora_launch_geometry(int(moe), rows, max_loras, max_rank, k_in, n_out, out))
     return dict(zip(GEOMETRY_KEYS, list(out)))
 

@@ -75,6 +75,7 @@ enum lora_status {
 #define LORA_MAX_ROWS 8192         /* n of lora_bgmv in [0, 8192] */
 #define LORA_MAX_LORAS 4096        /* max_loras of lora_bgmv in [1, 4096] */
 #define LORA_MAX_EXPERTS 1024      /* num_experts of the MoE fold in [1, 1024] */
+#define LORA_TMAP_MIN_RANK 32      /* a_tmaps are used from this max_rank up */
 #define LORA_MOE_M_TILE 64         /* sorted rows per MoE tile (static grid unit) */
 
 /*
@@ -104,6 +105,15 @@ enum lora_status {
  *   scale_table  [max_loras] f32 per-slot scale (alpha/r, or alpha/sqrt(r) for rsLoRA)
  *   xa           optional [n, max_rank] BF16 output of the shrink (routed rows only
  *                are written); NULL skips it
+ *   a_tmaps      optional device array of [max_loras] 128-byte TMA tensor maps of the
+ *                A matrices, written by lora_encode_a_tmaps for the same a_table
+ *                pointers, max_rank and k_in, 64-byte aligned. Given and max_rank >=
+ *                LORA_TMAP_MIN_RANK, A is loaded as 2-D boxes (far fewer copy
+ *                requests); NULL, or a smaller max_rank, loads A row by row (boxes
+ *                of under 32 rows measured slower than the row copies on GB300).
+ *                The results are the same bits either way. The caller keeps the
+ *                maps in step with a_table (adapters are load-time fixed); an entry
+ *                used by a routed row must describe that adapter.
  *   n == 0 is a no-op (returns LORA_OK, nothing launched).
  */
 int lora_bgmv(const lora_bf16_t* x, int64_t x_row_stride,
@@ -112,7 +122,7 @@ int lora_bgmv(const lora_bf16_t* x, int64_t x_row_stride,
               const lora_bf16_t* const* a_table, const lora_bf16_t* const* b_table,
               const float* scale_table, int32_t max_loras,
               int32_t max_rank, int32_t k_in, int32_t n_out,
-              lora_bf16_t* xa, void* stream);
+              lora_bf16_t* xa, const void* a_tmaps, void* stream);
 
 /*
  * lora_moe_grouped_fold — the fold over expert-sorted MoE rows of one window.
@@ -139,6 +149,9 @@ int lora_bgmv(const lora_bf16_t* x, int64_t x_row_stride,
  *                     NULL and x_gather == 0
  *   row_adapter       [num_tokens] int32 (< 0 = no delta), or NULL: every row uses adapter 0
  *   a_table, b_table, scale_table   [max_loras * num_experts], index a*num_experts + e
+ *   a_tmaps           accepted for symmetry with the other folds and not used: the
+ *                     grouped fold copies whole 768+-byte A row chunks, which the
+ *                     maps would not reduce much (checked for 64-byte alignment)
  *   xa                optional [row_end - row_offset, max_rank] BF16 shrink output at the
  *                     LOCAL row r - row_offset (routed rows only); NULL skips it
  * The window must satisfy 0 <= row_offset <= row_end <= te. The launch grid is
@@ -156,7 +169,7 @@ int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, int32_t x_
                           const lora_bf16_t* const* a_table, const lora_bf16_t* const* b_table,
                           const float* scale_table, int32_t max_loras,
                           int32_t max_rank, int32_t k_in, int32_t n_out,
-                          lora_bf16_t* xa, void* stream);
+                          lora_bf16_t* xa, const void* a_tmaps, void* stream);
 
 /*
  * lora_moe_gather_bgmv — the decode-path MoE fold over flat, unsorted
@@ -178,6 +191,7 @@ int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, int32_t x_
  *   a_table, b_table, scale_table  [max_loras * num_experts], index a*num_experts + e
  *                (max_loras * num_experts <= LORA_MAX_LORAS)
  *   xa           optional [n_rows, max_rank] BF16 shrink output at row r (routed rows)
+ *   a_tmaps      optional [max_loras * num_experts] A tensor maps, as for lora_bgmv
  * Rows of one table entry share a work unit; the launch grid depends only on
  * n_rows and the table count (capture-safe). Errors, alignment and ownership as
  * for lora_bgmv.
@@ -189,7 +203,20 @@ int lora_moe_gather_bgmv(const lora_bf16_t* x, int64_t x_row_stride,
                          const lora_bf16_t* const* a_table, const lora_bf16_t* const* b_table,
                          const float* scale_table, int32_t max_loras,
                          int32_t max_rank, int32_t k_in, int32_t n_out,
-                         lora_bf16_t* xa, void* stream);
+                         lora_bf16_t* xa, const void* a_tmaps, void* stream);
+
+/*
+ * lora_encode_a_tmaps — host helper run once when adapters are loaded: writes,
+ * for each of `count` A matrices ([max_rank, k_in] row-major BF16 at the device
+ * address a_ptrs[i]; 0 = none), the 128-byte TMA tensor map the folds use to
+ * load 64-column boxes of all its rank rows (128-byte swizzle). maps_out is
+ * HOST memory of count * 128 bytes, 64-byte aligned; entries of 0 pointers are
+ * zeroed. Copy it to device memory and pass it as a_tmaps. Needs the CUDA driver
+ * (no GPU work is done); returns LORA_ERR_CUDA without one.
+ * No counterpart in the pages: it prepares the TMA copies of this library.
+ */
+int lora_encode_a_tmaps(const uint64_t* a_ptrs, int32_t count, int32_t max_rank, int32_t k_in,
+                        void* maps_out);
 
 /* Text of the last error returned on this host thread ("" if none). */
 const char* lora_last_error(void);
@@ -207,12 +234,13 @@ int lora_read_device_status(void* stream, uint32_t* status_out, int clear);
  * MoE grouped fold with `rows` = row_end - row_offset and max_loras = the number
  * of adapters the grid covers (max_loras with a row_adapter, 1 without); moe ==
  * 2: decode gather fold with `rows` = n_rows and max_loras = the table count
- * (adapters x experts). Writes [cluster,
+ * (adapters x experts). Add 16 to `moe` for the geometry of a call given
+ * a_tmaps. Writes [cluster,
  * rows_per_tile, k_slice, j_slice, k_chunk, j_chunk, ring_stages, clusters,
- * smem_bytes] to out[0..8].
+ * smem_bytes, a_tiled (1 when A is loaded through the tensor maps)] to out[0..9].
  */
 int lora_launch_geometry(int moe, int32_t rows, int32_t max_loras, int32_t max_rank,
-                         int32_t k_in, int32_t n_out, int64_t out[9]);
+                         int32_t k_in, int32_t n_out, int64_t out[10]);
 
 /* ---- pure host helpers (no GPU) ------------------------------------------ */
 

@@ -95,3 +95,13 @@ def oracle_gather(wl: W.MoeGatherWorkload, use_row_adapter=True, indices=None):
         wl.row_adapter if use_row_adapter else None, wl.num_tokens, wl.num_experts, wl.a_list(),
         wl.b_list(), wl.scale, wl.max_rank, wl.k_in, wl.n_out)
     return out, xa, dd
+
+
+def device_a_tmaps(a_table: torch.Tensor, max_rank: int, k_in: int) -> torch.Tensor:
+    """Encode the A tensor maps of a device table (read back once, as at adapter
+    load) and place them in device memory."""
+    ptrs = a_table.cpu().numpy().astype(np.uint64)
+    maps = L.lora_encode_a_tmaps(ptrs, max_rank, k_in)
+    t = torch.from_numpy(maps).to(a_table.device)
+    assert t.data_ptr() % 64 == 0
+    return t

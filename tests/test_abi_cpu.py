@@ -52,10 +52,10 @@ def test_library_exports_every_declared_symbol():
 
 def _bgmv(**kw):
     a = dict(x=FAKE, xs=4096, out=FAKE, os=4096, seq=FAKE, n=4, at=FAKE, bt=FAKE, sc=FAKE, L=8,
-             R=16, k=4096, no=4096, xa=FAKE)
+             R=16, k=4096, no=4096, xa=FAKE, maps=None)
     a.update(kw)
     return L.load().lora_bgmv(a["x"], a["xs"], a["out"], a["os"], a["seq"], a["n"], a["at"],
-                              a["bt"], a["sc"], a["L"], a["R"], a["k"], a["no"], a["xa"], None)
+                              a["bt"], a["sc"], a["L"], a["R"], a["k"], a["no"], a["xa"], a["maps"], None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -64,7 +64,7 @@ def _bgmv(**kw):
     (dict(no=4097, os=8192), -4), (dict(xs=4088), -3), (dict(os=100, no=128), -3),
     (dict(xs=4100), -4), (dict(x=None), -1), (dict(out=None), -1), (dict(seq=None), -1),
     (dict(at=None), -1), (dict(bt=None), -1), (dict(sc=None), -1), (dict(x=FAKE + 2), -4),
-    (dict(out=FAKE + 8), -4), (dict(xa=FAKE + 4), -4),
+    (dict(out=FAKE + 8), -4), (dict(xa=FAKE + 4), -4), (dict(maps=FAKE + 32), -4),
 ])
 def test_bgmv_rejects_bad_arguments_before_launch(kw, code):
     assert _bgmv(**kw) == code
@@ -78,12 +78,13 @@ def test_bgmv_zero_rows_is_a_no_op():
 
 def _moe(**kw):
     a = dict(x=FAKE, xs=768, xg=0, out=FAKE, os=2048, off=FAKE, E=128, sti=FAKE, te=16384, ra=FAKE,
-             nt=2048, lo=0, hi=4096, at=FAKE, bt=FAKE, sc=FAKE, L=16, R=16, k=768, no=2048, xa=FAKE)
+             nt=2048, lo=0, hi=4096, at=FAKE, bt=FAKE, sc=FAKE, L=16, R=16, k=768, no=2048, xa=FAKE,
+             maps=None)
     a.update(kw)
     return L.load().lora_moe_grouped_fold(a["x"], a["xs"], a["xg"], a["out"], a["os"], a["off"], a["E"],
                                           a["sti"], a["te"], a["ra"], a["nt"], a["lo"], a["hi"],
                                           a["at"], a["bt"], a["sc"], a["L"], a["R"], a["k"], a["no"],
-                                          a["xa"], None)
+                                          a["xa"], a["maps"], None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -99,11 +100,12 @@ def test_moe_rejects_bad_arguments_before_launch(kw, code):
 
 def _gather(**kw):
     a = dict(x=FAKE, xs=768, out=FAKE, os=2048, idx=FAKE, n=512, k=8, ra=FAKE, nt=64, E=128,
-             at=FAKE, bt=FAKE, sc=FAKE, L=16, R=16, kin=768, no=2048, xa=FAKE)
+             at=FAKE, bt=FAKE, sc=FAKE, L=16, R=16, kin=768, no=2048, xa=FAKE, maps=None)
     a.update(kw)
     return L.load().lora_moe_gather_bgmv(a["x"], a["xs"], a["out"], a["os"], a["idx"], a["n"],
                                          a["k"], a["ra"], a["nt"], a["E"], a["at"], a["bt"],
-                                         a["sc"], a["L"], a["R"], a["kin"], a["no"], a["xa"], None)
+                                         a["sc"], a["L"], a["R"], a["kin"], a["no"], a["xa"],
+                                         a["maps"], None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -129,6 +131,23 @@ def test_grouped_down_wc():
     assert L.lora_grouped_down_wc(5, 4) == -1
     for lo, hi in [(0, 1), (3, 131), (64, 128), (7, 7000)]:
         assert L.lora_grouped_down_wc(lo, hi) == max(1, -(-(hi - lo) // 64))
+
+
+def test_encode_a_tmaps_checks_arguments():
+    enc = L.load().lora_encode_a_tmaps
+    assert enc(None, 0, 16, 4096, None) == 0                   # nothing to encode
+    assert enc(None, -1, 16, 4096, None) == -2
+    assert enc(None, 2, 4, 4096, None) == -2                   # max_rank out of range
+    assert enc(None, 2, 16, 4100, None) == -4                  # k_in not a multiple of 8
+    assert enc(None, 2, 16, 4096, None) == -1                  # pointers required
+    ptrs = (ctypes.c_uint64 * 2)(0x10000, 0x20000)
+    buf = ctypes.create_string_buffer(2 * 128 + 64)
+    base = ctypes.addressof(buf)
+    aligned = base + (-base) % 64
+    assert enc(ptrs, 2, 16, 4096, aligned + 16) == -4          # maps_out not 64-byte aligned
+    bad = (ctypes.c_uint64 * 2)(0x10000, 0x20008)
+    rc = enc(bad, 2, 16, 4096, aligned)
+    assert rc in (-4, -6)     # misaligned A pointer; or no CUDA driver on this machine
 
 
 def test_gather_row_token():
@@ -220,3 +239,19 @@ def test_moe_geometry_tiles():
     assert L.lora_launch_geometry(1, 100, 1, 16, 768, 2048)["clusters"] == 2
     assert L.lora_launch_geometry(1, 0, 1, 16, 768, 2048)["clusters"] == 1
     assert L.lora_launch_geometry(1, 0, 16, 16, 768, 2048)["clusters"] == 16
+
+
+def test_tensor_maps_only_from_the_minimum_rank():
+    m = re.search(r"#define LORA_TMAP_MIN_RANK (\d+)", open(HEADER).read())
+    assert m and int(m.group(1)) == L.TMAP_MIN_RANK
+    for mode, rows, tables in ((0, 64, 32), (2, 512, 2048)):
+        for rank in (8, 16, L.TMAP_MIN_RANK - 8):
+            args = (rows, tables, rank, 4096, 4096)
+            assert L.lora_launch_geometry(mode + 16, *args) == L.lora_launch_geometry(mode, *args)
+            assert L.lora_launch_geometry(mode + 16, *args)["a_tiled"] == 0
+        for rank in (L.TMAP_MIN_RANK, 64, 128):
+            g = L.lora_launch_geometry(mode + 16, rows, tables, rank, 4104, 4096)
+            assert g["a_tiled"] == 1 and g["k_chunk"] % 64 == 0
+            assert L.lora_launch_geometry(mode, rows, tables, rank, 4104, 4096)["a_tiled"] == 0
+    # the grouped MoE fold loads A rows whatever it is given
+    assert L.lora_launch_geometry(17, 4096, 16, 64, 768, 2048) == L.lora_launch_geometry(1, 4096, 16, 64, 768, 2048)
