@@ -127,6 +127,28 @@ class MoeWorkload:
         return [self.b_pool[i] if self.present[i] else None for i in range(len(self.present))]
 
 
+@dataclass
+class DeltaWorkload:
+    """One single-adapter delta problem (lora_delta.rs page, apply_lora_delta):
+    every one of the m rows is adapted by the same pair. Layout of ``out_buf`` as
+    for BgmvWorkload (the folded segment of row i starts at ``out_offset``)."""
+    name: str
+    m: int
+    k_in: int
+    n_out: int
+    max_rank: int
+    rank: int
+    x_row_stride: int
+    out_row_stride: int
+    out_offset: int
+    x: np.ndarray            # uint16 [m, x_row_stride]
+    out_buf: np.ndarray      # uint16 [m, out_row_stride]
+    a: np.ndarray            # uint16 [max_rank, k_in], rows >= rank zero
+    b: np.ndarray            # uint16 [n_out, max_rank], columns >= rank zero
+    scale: np.float32
+    meta: dict = field(default_factory=dict)
+
+
 def _pack_pool(rng, count, present, ranks, max_rank, k_in, n_out, a_bound, b_std):
     """Zeroed pool, then each present adapter's true-rank A rows / B columns."""
     a_pool = np.zeros((count, max_rank, k_in), dtype=np.uint16)
@@ -204,6 +226,32 @@ def make_bgmv(name, *, n, k_in, n_out, max_loras, max_rank, rank_choices, alpha,
     return BgmvWorkload(name, n, k_in, n_out, max_loras, max_rank, xs, os_, out_offset,
                         x, out_buf, seq, ranks, present, a_pool, b_pool, scale,
                         meta=dict(seed=seed, slot_law=slot_law, alpha=alpha, rslora=rslora))
+
+
+def make_delta(name, *, m, k_in, n_out, max_rank, rank, alpha, rslora, seed, x_law="normal",
+               x_row_stride=None, out_row_stride=None, out_offset=0, a_bound=None,
+               b_std=0.02) -> DeltaWorkload:
+    """Draw one single-adapter delta problem: x ~ N(0,1) (or SiLU(N)*N), base_out ~
+    N(0,1), A ~ U(+-1/sqrt(k_in)) in its first ``rank`` rows, B ~ N(0, b_std) in
+    its first ``rank`` columns, zeros elsewhere; scale as for the pool."""
+    rng = np.random.default_rng(seed)
+    xs = x_row_stride or k_in
+    os_ = out_row_stride or (out_offset + n_out)
+    if x_law == "normal":
+        xf = rng.standard_normal((m, xs), dtype=np.float32)
+    elif x_law == "silu_gate":
+        g = rng.standard_normal((m, xs), dtype=np.float32)
+        u = rng.standard_normal((m, xs), dtype=np.float32)
+        xf = (g / (1.0 + np.exp(-g))) * u
+    else:
+        raise ValueError(x_law)
+    x = to_bf16_bits(xf)
+    out_buf = to_bf16_bits(rng.standard_normal((m, os_), dtype=np.float32))
+    a_pool, b_pool = _pack_pool(rng, 1, np.ones(1, dtype=bool), np.array([rank]), max_rank, k_in,
+                                n_out, a_bound if a_bound is not None else 1.0 / math.sqrt(k_in), b_std)
+    return DeltaWorkload(name, m, k_in, n_out, max_rank, rank, xs, os_, out_offset, x, out_buf,
+                         a_pool[0], b_pool[0], lora_scale(alpha, rank, rslora),
+                         meta=dict(seed=seed, alpha=alpha, rslora=rslora, x_law=x_law))
 
 
 def make_moe(name, *, num_tokens, top_k, num_experts, k_in, n_out, max_loras, max_rank,
@@ -390,11 +438,26 @@ def moe_decode_gather(seed=6):
                            adapter_base_frac=0.20, seed=seed)
 
 
+def prefill_qproj_delta(seed=7):
+    """Prefill with one active adapter on the decode q_proj's model: m=4096 rows,
+    k_in=n_out=4096, x ~ N(0,1), the adapter at rank 16 (alpha 32)."""
+    return make_delta("prefill_qproj_delta", m=4096, k_in=4096, n_out=4096, max_rank=16, rank=16,
+                      alpha=32.0, rslora=False, seed=seed)
+
+
+def prefill_down_delta(seed=8):
+    """Prefill with one active adapter on the FFN down_proj's model: m=4096 rows,
+    k_in=12288, n_out=4096, post-SiLU x, the adapter at rank 128 (rsLoRA, alpha 64)."""
+    return make_delta("prefill_down_delta", m=4096, k_in=12288, n_out=4096, max_rank=128, rank=128,
+                      alpha=64.0, rslora=True, seed=seed, x_law="silu_gate")
+
+
 def by_name(name: str, seed=None):
     fn = {"tiny_bgmv": tiny_bgmv, "decode_qproj_bgmv": decode_qproj_bgmv,
           "qkv_kfold_bgmv": qkv_kfold_bgmv, "ffn_down_bgmv": ffn_down_bgmv,
           "moe_down_fold": moe_down_fold, "moe_gateup_fold": moe_gateup_fold,
-          "moe_decode_gather": moe_decode_gather}[name]
+          "moe_decode_gather": moe_decode_gather, "prefill_qproj_delta": prefill_qproj_delta,
+          "prefill_down_delta": prefill_down_delta}[name]
     return fn() if seed is None else fn(seed)
 
 
@@ -439,6 +502,24 @@ def bgmv_to_device(wl: BgmvWorkload, device="cuda") -> DeviceBgmv:
         a_table=_table_of(a_pool, wl.present, device), b_table=_table_of(b_pool, wl.present, device),
         scale=_dev(wl.scale, device),
         xa=torch.zeros((max(wl.n, 1), wl.max_rank), dtype=torch.int16, device=device))
+
+
+@dataclass
+class DeviceDelta:
+    x: "torch.Tensor"         # int16 [m, x_row_stride]
+    out_buf: "torch.Tensor"   # int16 [m, out_row_stride]
+    out_ptr: int              # address of out_buf[0, out_offset]
+    a: "torch.Tensor"         # int16 [max_rank, k_in]
+    b: "torch.Tensor"         # int16 [n_out, max_rank]
+    xa: "torch.Tensor"        # int16 [m, max_rank]
+
+
+def delta_to_device(wl: DeltaWorkload, device="cuda") -> DeviceDelta:
+    out = _dev(wl.out_buf.view(np.int16), device)
+    return DeviceDelta(x=_dev(wl.x.view(np.int16), device), out_buf=out,
+                       out_ptr=out.data_ptr() + 2 * wl.out_offset,
+                       a=_dev(wl.a.view(np.int16), device), b=_dev(wl.b.view(np.int16), device),
+                       xa=torch.zeros((max(wl.m, 1), wl.max_rank), dtype=torch.int16, device=device))
 
 
 @dataclass

@@ -55,6 +55,12 @@ def _bind(lib):
         u16p, u16p, u16p, ctypes.c_int32,
         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
         u16p, u16p, ctypes.c_int32]
+    lib.ora_lora_delta.restype = ctypes.c_int
+    lib.ora_lora_delta.argtypes = [
+        u16p, ctypes.c_int64, u16p, ctypes.c_int64, ctypes.c_int32,
+        u16p, u16p, ctypes.c_float,
+        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+        u16p, u16p, ctypes.c_int32]
     lib.ora_lora_moe_grouped_fold.restype = ctypes.c_int
     lib.ora_lora_moe_grouped_fold.argtypes = [
         u16p, ctypes.c_int64, ctypes.c_int32, u16p, ctypes.c_int64,
@@ -141,6 +147,30 @@ def lora_bgmv(x, x_row_stride, base_out, out_row_stride, seq_slot, a_list, b_lis
     if rc != 0:
         raise ValueError(f"oracle lora_bgmv rejected its arguments (rc={rc})")
     return xa[:n], d[:n]
+
+
+def lora_delta(x, x_row_stride, base_out, out_row_stride, m, a, b, scale, max_rank, k_in,
+               n_out, mode=0, lib=None):
+    """Fold one adapter pair into all m rows of base_out in place ("lora_delta.rs",
+    apply_lora_delta).
+
+    x: uint16 array holding m rows at ``x_row_stride`` elements; base_out: uint16
+    array (modified in place) of m rows at ``out_row_stride`` elements, the first
+    n_out of each folded; a: uint16 [max_rank, k_in]; b: uint16 [n_out, max_rank];
+    scale: the f32 scale. Returns (xa [m, max_rank], d [m, n_out]) as uint16.
+    """
+    lib = lib or load()
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    assert base_out.dtype == np.uint16 and base_out.flags.c_contiguous
+    a = np.ascontiguousarray(a, dtype=np.uint16)
+    b = np.ascontiguousarray(b, dtype=np.uint16)
+    xa = np.zeros((max(m, 1), max_rank), dtype=np.uint16)
+    d = np.zeros((max(m, 1), n_out), dtype=np.uint16)
+    rc = lib.ora_lora_delta(_ptr(x), x_row_stride, _ptr(base_out), out_row_stride, m, _ptr(a), _ptr(b),
+                            float(np.float32(scale)), max_rank, k_in, n_out, _ptr(xa), _ptr(d), mode)
+    if rc != 0:
+        raise ValueError(f"oracle lora_delta rejected its arguments (rc={rc})")
+    return xa[:m], d[:m]
 
 
 def lora_moe_grouped_fold(x, x_row_stride, base_out, out_row_stride, expert_offsets,

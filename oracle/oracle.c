@@ -27,6 +27,9 @@
  *   Same page, moe_lora_gather_bgmv entry: the decode-path twin over flat,
  *     unsorted (token, slot) rows; expert from indices[row], adapter gate from
  *     row_adapter[row / top_k].
+ *   lora_delta.rs page, apply_lora_delta: one LoraPair over all m rows
+ *     (base_out[m, n_out] += scale * (x @ a^T) @ b^T), every row adapted; the
+ *     same per-row fold as the bgmv.
  *
  * Readings where the pages are silent:
  *   - fp32 -> BF16 is round-to-nearest-even.
@@ -171,6 +174,31 @@ int ora_lora_bgmv(const uint16_t* x, int64_t x_row_stride,
         uint16_t* d_row = d_out ? d_out + (int64_t)i * n_out : NULL;
         fold_one_row(x + (int64_t)i * x_row_stride, base_out + (int64_t)i * out_row_stride,
                      A, B, scale_table[s], max_rank, k_in, n_out, xa_row, d_row, mode);
+    }
+    return 0;
+}
+
+/* ---- one adapter pair over every row ---------------------------------------
+ * "lora_delta.rs", apply_lora_delta: base_out[m, n_out] += scale * (x @ a^T) @ b^T
+ * for one LoraPair, with the same rounding points as the routed fold (xa and the
+ * delta rounded to BF16, then one fp32 fma and a BF16 rounding). Every row is
+ * adapted; there is no routing. */
+int ora_lora_delta(const uint16_t* x, int64_t x_row_stride,
+                   uint16_t* base_out, int64_t out_row_stride, int32_t m,
+                   const uint16_t* a, const uint16_t* b, float scale,
+                   int32_t max_rank, int32_t k_in, int32_t n_out,
+                   uint16_t* xa, uint16_t* d_out, int32_t mode)
+{
+    if (m < 0 || max_rank <= 0 || k_in <= 0 || n_out <= 0) return -1;
+    if (x_row_stride < k_in || out_row_stride < n_out || a == NULL || b == NULL) return -1;
+    uint16_t xa_tmp[4096];
+    if (max_rank > 4096) return -1;
+    for (int32_t row = 0; row < m; ++row) {
+        uint16_t* xa_row = xa ? xa + (int64_t)row * max_rank : xa_tmp;
+        uint16_t* d_row = d_out ? d_out + (int64_t)row * n_out : NULL;
+        const uint16_t* x_row = x + (int64_t)row * x_row_stride;
+        uint16_t* out_row = base_out + (int64_t)row * out_row_stride;
+        fold_one_row(x_row, out_row, a, b, scale, max_rank, k_in, n_out, xa_row, d_row, mode);
     }
     return 0;
 }

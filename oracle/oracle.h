@@ -27,6 +27,13 @@ int ora_lora_bgmv(const uint16_t* x, int64_t x_row_stride,
                   int32_t max_rank, int32_t k_in, int32_t n_out,
                   uint16_t* xa, uint16_t* d_out, int32_t mode);
 
+/* One adapter pair (a [max_rank, k_in], b [n_out, max_rank], scale) over all m rows. */
+int ora_lora_delta(const uint16_t* x, int64_t x_row_stride,
+                   uint16_t* base_out, int64_t out_row_stride, int32_t m,
+                   const uint16_t* a, const uint16_t* b, float scale,
+                   int32_t max_rank, int32_t k_in, int32_t n_out,
+                   uint16_t* xa, uint16_t* d_out, int32_t mode);
+
 /* x_gather != 0: x is token-major [num_tokens, .] and sorted row r reads row
    sorted_token_ids[r] of it (gate/up); 0: x is [te, .] at row r (down). */
 int ora_lora_moe_grouped_fold(const uint16_t* x, int64_t x_row_stride, int32_t x_gather,

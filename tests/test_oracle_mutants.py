@@ -39,6 +39,10 @@ MUTANTS = {
     "gather_token_of_row": ("const int32_t t = r / top_k;", "const int32_t t = r % top_k;"),
     "gather_table_expert_major": ("const int64_t entry = (int64_t)a * num_experts + e;",
                                   "const int64_t entry = (int64_t)e * max_loras + a;"),
+    "delta_out_stride": ("uint16_t* out_row = base_out + (int64_t)row * out_row_stride;",
+                         "uint16_t* out_row = base_out + (int64_t)row * n_out;"),
+    "delta_x_stride": ("const uint16_t* x_row = x + (int64_t)row * x_row_stride;",
+                       "const uint16_t* x_row = x + (int64_t)row * k_in;"),
     "last_k_dropped": ("for (int32_t k = 0; k < k_in; ++k)\n                acc = acc + ora_f32_of_bf16(xrow[k])",
                        "for (int32_t k = 0; k < k_in - 1; ++k)\n                acc = acc + ora_f32_of_bf16(xrow[k])"),
 }

@@ -478,3 +478,70 @@ def test_gather_bgmv_null_row_adapter_is_adapter_zero():
     o1, _, _ = _run_gather(wl, row_adapter=None)
     o2, _, _ = _run_gather(wl, row_adapter=np.zeros(wl.num_tokens, np.int32))
     assert np.array_equal(o1, o2)
+
+
+# ------------------------------------------------ single-adapter delta
+def _int_delta(seed, m=6, k_in=24, n_out=20, max_rank=16, rank=11, xs_pad=8, out_offset=8, out_pad=8):
+    """Small-integer single-adapter delta where every fp32 and BF16 step is exact."""
+    rng = np.random.default_rng(seed)
+    xs, os_ = k_in + xs_pad, out_offset + n_out + out_pad
+    x = rng.integers(-1, 2, size=(m, xs))
+    base = rng.integers(-6, 7, size=(m, os_))
+    a_int = np.zeros((max_rank, k_in), dtype=np.int64)
+    b_int = np.zeros((n_out, max_rank), dtype=np.int64)
+    a_int[:rank] = rng.integers(-1, 2, size=(rank, k_in))
+    b_int[:, :rank] = rng.integers(-1, 2, size=(n_out, rank))
+    wl = W.DeltaWorkload("int_delta", m, k_in, n_out, max_rank, rank, xs, os_, out_offset,
+                         _int_bits(x), _int_bits(base), _int_bits(a_int), _int_bits(b_int),
+                         np.float32(2.0))
+    return wl, x, base, a_int, b_int
+
+
+def _run_delta(wl: W.DeltaWorkload, mode=0):
+    out = wl.out_buf.copy()
+    seg = out.reshape(-1)[wl.out_offset:]
+    xa, d = oracle.lora_delta(wl.x.reshape(-1), wl.x_row_stride, seg, wl.out_row_stride, wl.m,
+                              wl.a, wl.b, wl.scale, wl.max_rank, wl.k_in, wl.n_out, mode=mode)
+    return out, xa, d
+
+
+@pytest.mark.parametrize("seed", [31, 32, 33])
+def test_delta_exact_integer_case(seed):
+    """lora_delta.rs, apply_lora_delta on small integers: every row equals the
+    integer product out + scale * (x @ A^T) @ B^T exactly; bytes outside each
+    row's [out_offset, out_offset + n_out) stay."""
+    wl, x, base, a_int, b_int = _int_delta(seed)
+    out, xa, d = _run_delta(wl)
+    want = base.astype(np.float64).copy()
+    seg = slice(wl.out_offset, wl.out_offset + wl.n_out)
+    for i in range(wl.m):
+        xa_i = a_int @ x[i, :wl.k_in]                      # int64 matmul (library)
+        d_i = b_int @ xa_i
+        assert np.abs(xa_i).max() <= 256 and np.abs(d_i).max() <= 256
+        want[i, seg] = base[i, seg] + float(wl.scale) * d_i
+        assert np.array_equal(W.bf16_bits_to_f32(xa[i]), xa_i.astype(np.float32))
+    assert np.abs(want).max() <= 256
+    assert np.array_equal(out, _int_bits(want))
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_delta_equals_bgmv_with_one_slot(mode):
+    """apply_lora_delta over m rows == apply_lora_bgmv with every row on one slot
+    holding the same pair (the routed fold's definition, pinned above)."""
+    wl = W.make_delta("d", m=9, k_in=72, n_out=40, max_rank=16, rank=12, alpha=16.0, rslora=False,
+                      seed=41, x_row_stride=80, out_row_stride=56, out_offset=8)
+    out_d, xa_d, d_d = _run_delta(wl, mode)
+    bg = W.BgmvWorkload("b", wl.m, wl.k_in, wl.n_out, 1, wl.max_rank, wl.x_row_stride,
+                        wl.out_row_stride, wl.out_offset, wl.x, wl.out_buf.copy(),
+                        np.zeros(wl.m, dtype=np.int32), np.array([wl.rank], np.int32),
+                        np.ones(1, dtype=bool), wl.a[None], wl.b[None],
+                        np.array([wl.scale], dtype=np.float32))
+    out_b, xa_b, d_b = _run_bgmv(bg, mode)
+    assert np.array_equal(out_d, out_b) and np.array_equal(xa_d, xa_b) and np.array_equal(d_d, d_b)
+    assert not np.array_equal(out_d, wl.out_buf)
+
+
+def test_delta_zero_rows_is_a_no_op():
+    wl = W.make_delta("z", m=0, k_in=16, n_out=16, max_rank=8, rank=8, alpha=8.0, rslora=False, seed=1)
+    out, xa, d = _run_delta(wl)
+    assert out.shape == (0, 16) and xa.shape == (0, 8)
