@@ -37,10 +37,10 @@ if ROOT not in sys.path:
 METRIC = "routed LoRA fold rows/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 HEADLINE = "decode_qproj_bgmv"
 SIDE_WORKLOADS = ("qkv_kfold_bgmv", "ffn_down_bgmv", "moe_down_fold", "moe_gateup_fold",
-                  "moe_decode_gather")
+                  "moe_decode_gather", "prefill_qproj_delta", "prefill_down_delta")
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_NAMES = {"bgmv": "lora_bgmv_fold_kernel", "moe": "lora_moe_fold_kernel",
-                "gather": "lora_bgmv_fold_kernel"}
+                "gather": "lora_bgmv_fold_kernel", "delta": "lora_dense_fold_kernel"}
 
 
 # ----------------------------------------------------------------- helpers
@@ -92,6 +92,17 @@ def bgmv_algorithmic_bytes(wl) -> dict:
                 flops=int(2 * len(routed) * wl.max_rank * (wl.k_in + wl.n_out)))
 
 
+def delta_algorithmic_bytes(wl) -> dict:
+    """Bytes of one single-adapter delta: every row's x row, out row read+write and
+    xa row write+read (as for the routed fold), plus the pair's A and B once."""
+    per_row = wl.k_in * 2 + wl.n_out * 2 * 2 + wl.max_rank * 2 * 2
+    per_adapter = wl.max_rank * wl.k_in * 2 + wl.n_out * wl.max_rank * 2
+    total = wl.m * per_row + per_adapter
+    return dict(bytes=int(total), routed_rows=int(wl.m), rows=int(wl.m), adapters=1,
+                per_row=per_row, per_adapter=per_adapter,
+                flops=int(2 * wl.m * wl.max_rank * (wl.k_in + wl.n_out)))
+
+
 def moe_algorithmic_bytes(wl) -> dict:
     E = wl.num_experts
     routed, pairs = 0, set()
@@ -140,6 +151,10 @@ def a_load(wl) -> str:
     MoE fold loads rows)."""
     from gather_lora_gb300 import lib as L
     kind = workload_kind(wl)
+    if kind == "delta":
+        dense = L.lora_delta_geometry(wl.m, wl.max_rank, wl.k_in, wl.n_out)["dense"]
+        return ("2-D TMA boxes into tcgen05 tensor cores (tensor maps encoded per call)" if dense
+                else "one TMA copy per row")
     tiled = 0
     if USE_TMAPS and kind == "bgmv":
         tiled = L.lora_launch_geometry(16, wl.n, wl.max_loras, wl.max_rank, wl.k_in, wl.n_out)["a_tiled"]
@@ -163,13 +178,15 @@ def workload_kind(wl) -> str:
     from gather_lora_gb300 import workloads as W
     if isinstance(wl, W.MoeGatherWorkload):
         return "gather"
+    if isinstance(wl, W.DeltaWorkload):
+        return "delta"
     return "moe" if isinstance(wl, W.MoeWorkload) else "bgmv"
 
 
 def algorithmic_bytes(wl) -> dict:
     k = workload_kind(wl)
     return {"bgmv": bgmv_algorithmic_bytes, "moe": moe_algorithmic_bytes,
-            "gather": gather_algorithmic_bytes}[k](wl)
+            "gather": gather_algorithmic_bytes, "delta": delta_algorithmic_bytes}[k](wl)
 
 
 class ClockSampler:
@@ -315,7 +332,25 @@ class GatherRunner:
                                stream=stream, a_tmaps=self.maps[c])
 
 
-RUNNERS = {"bgmv": BgmvRunner, "moe": MoeRunner, "gather": GatherRunner}
+class DeltaRunner:
+    def __init__(self, wl, copies, device):
+        from gather_lora_gb300 import workloads as W
+        self.wl = wl
+        self.copies = [W.delta_to_device(wl, device) for _ in range(copies)]
+        self.launches_per_step = 1
+
+    def bytes_per_copy(self):
+        d = self.copies[0]
+        return sum(t.numel() * t.element_size() for t in (d.x, d.out_buf, d.a, d.b))
+
+    def step(self, c, stream):
+        from gather_lora_gb300 import lib as L
+        wl, d = self.wl, self.copies[c]
+        L.lora_delta(d.x, wl.x_row_stride, d.out_ptr, wl.out_row_stride, wl.m, d.a, d.b, wl.scale,
+                     wl.max_rank, wl.k_in, wl.n_out, xa=d.xa, stream=stream)
+
+
+RUNNERS = {"bgmv": BgmvRunner, "moe": MoeRunner, "gather": GatherRunner, "delta": DeltaRunner}
 
 
 def copies_needed(bytes_per_copy, l2_bytes):
@@ -564,6 +599,8 @@ def run_ours(args):
     if head_moe:
         geometry = L.lora_launch_geometry(1, wl.cap, wl.max_loras if wl.row_adapter is not None else 1,
                                           wl.max_rank, wl.k_in, wl.n_out)
+    elif head_kind == "delta":
+        geometry = L.lora_delta_geometry(wl.m, wl.max_rank, wl.k_in, wl.n_out)
     elif head_kind == "gather":
         geometry = L.lora_launch_geometry(18 if USE_TMAPS else 2, wl.n_rows, wl.max_loras * wl.num_experts, wl.max_rank,
                                           wl.k_in, wl.n_out)

@@ -18,7 +18,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgather_lora.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-Xcompiler", "-Wall"]
-SOURCES = ["kernels.cu", "abi.cpp"]
+SOURCES = ["kernels.cu", "dense.cu", "abi.cpp"]
 
 
 def nvcc() -> str:

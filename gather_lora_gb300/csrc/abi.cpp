@@ -12,6 +12,7 @@
 #include <cstdio>
 #include <cstring>
 
+#include "dense_types.h"
 #include "fold_types.h"
 
 namespace {
@@ -216,6 +217,66 @@ int cuda_fail(int err, const char* what) {
   return fail(LORA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(static_cast<cudaError_t>(err)));
 }
 
+// ---- dense single-adapter delta ----------------------------------------------
+static_assert(glora::idesc_bf16_f32(128, 64) == 0x08100490u, "instruction descriptor bit layout");
+
+// Ranks the tensor-core path takes: the expand's K (= max_rank) is one 32- or
+// 64-byte swizzle row, or whole 64-column atoms of the 128-byte swizzle, and the
+// shrink's N (= max_rank) fits the TMEM partial (128 columns).
+bool dense_rank(int r) { return r == 16 || r == 32 || r == 64 || r == 128; }
+
+struct DenseGeom {
+  int dense, cl, ns, stage, smem;
+  long long ctas;
+};
+
+// The tensor-core launch for m rows, or false (the routed engine takes the call).
+// cl: the largest power of two <= 8 with tiles * cl <= the SM count (one CTA
+// per SM) and at least one k-chunk per CTA; the ring takes what shared memory
+// is left (at most kDenseMaxRing stages).
+bool dense_geometry(int m, int r, int k_in, int sms, DenseGeom& g) {
+  g = DenseGeom{};
+  if (!dense_rank(r) || m < LORA_DELTA_DENSE_MIN_ROWS) return false;
+  const long long tiles = ceil_div(m, glora::kDenseRows);
+  const int nkc = static_cast<int>(ceil_div(k_in, glora::kDenseKChunk));
+  int cl = 1;
+  while (cl < 8 && tiles * cl * 2 <= std::max(sms, 1) && cl * 2 <= nkc) cl *= 2;
+  const int stage = glora::dense_stage_bytes(r);
+  const int fixed = 2 * glora::kDenseOutStage + glora::kDenseRows * r * 2 + glora::kDenseControl + 1024;
+  const int ns = std::min(glora::kDenseMaxRing, (227 * 1024 - fixed) / stage);
+  if (ns < 2) return false;
+  g.dense = 1;
+  g.cl = cl;
+  g.ns = ns;
+  g.stage = stage;
+  g.smem = fixed + ns * stage;
+  g.ctas = tiles * cl;
+  return true;
+}
+
+int device_sm_count() {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return v;
+}
+
+// One 2-D BF16 tensor map: `inner` x `outer` elements, rows `row_bytes` apart.
+int encode_map(glora::TensorMapBytes* out, const void* ptr, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+               uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz, const char* what) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = encode_tiled();
+  if (!enc) return fail(LORA_ERR_CUDA, "cuTensorMapEncodeTiled is not available (no CUDA driver)");
+  static_assert(sizeof(glora::TensorMapBytes) == sizeof(CUtensorMap), "tensor map size");
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(reinterpret_cast<CUtensorMap*>(out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr),
+                         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? LORA_OK : fail(LORA_ERR_CUDA, "cuTensorMapEncodeTiled failed for %s (%d)", what, static_cast<int>(r));
+}
+
 }  // namespace
 
 extern "C" {
@@ -369,8 +430,96 @@ int lora_moe_gather_bgmv(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_t
   return rc ? cuda_fail(rc, "lora_moe_gather_bgmv launch") : ok();
 }
 
+int lora_delta(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_t* base_out, int64_t out_row_stride,
+               int32_t m, const lora_bf16_t* a, const lora_bf16_t* b, float scale, int32_t max_rank,
+               int32_t k_in, int32_t n_out, lora_bf16_t* xa, void* stream) {
+  if (m < 0 || m > LORA_MAX_DELTA_ROWS) return fail(LORA_ERR_SIZE, "m %d outside [0, %d]", m, LORA_MAX_DELTA_ROWS);
+  int rc = check_shape(max_rank, k_in, n_out, x_row_stride, out_row_stride);
+  if (rc) return rc;
+  if (m == 0) return ok();
+  if (!x || !base_out || !a || !b) return fail(LORA_ERR_NULL, "a required pointer is NULL (x, base_out, a, b)");
+  if (!aligned16(x) || !aligned16(base_out) || !aligned16(a) || !aligned16(b) || (xa && !aligned16(xa)))
+    return fail(LORA_ERR_ALIGN, "x, base_out, a, b and xa must be 16-byte aligned");
+  DenseGeom dg;
+  if (dense_geometry(m, max_rank, k_in, device_sm_count(), dg)) {
+    glora::DenseArgs d{};
+    const CUtensorMapSwizzle bswz = max_rank >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                    : (max_rank == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+    if ((rc = encode_map(&d.map_x, x, k_in, m, x_row_stride * 2, 64, glora::kDenseRows, CU_TENSOR_MAP_SWIZZLE_128B, "x")) ||
+        (rc = encode_map(&d.map_a, a, k_in, max_rank, static_cast<uint64_t>(k_in) * 2, 64, max_rank,
+                         CU_TENSOR_MAP_SWIZZLE_128B, "A")) ||
+        (rc = encode_map(&d.map_b, b, max_rank, n_out, static_cast<uint64_t>(max_rank) * 2, std::min(max_rank, 64),
+                         glora::kDenseJChunk, bswz, "B")) ||
+        (rc = encode_map(&d.map_out, base_out, n_out, m, out_row_stride * 2, 64, glora::kDenseRows,
+                         CU_TENSOR_MAP_SWIZZLE_128B, "base_out")))
+      return rc;
+    d.xa = xa;
+    d.scale = scale;
+    d.m = m;
+    d.k_in = k_in;
+    d.n_out = n_out;
+    d.max_rank = max_rank;
+    d.cl = dg.cl;
+    d.ns = dg.ns;
+    d.stage_bytes = dg.stage;
+    d.smem_bytes = dg.smem;
+    rc = glora::launch_dense(d, stream);
+    return rc ? cuda_fail(rc, "lora_delta launch") : ok();
+  }
+  // Small m, or a rank the tensor-core path does not take: the routed engine
+  // with every row on one slot (one launch per LORA_MAX_ROWS rows).
+  for (int32_t r0 = 0; r0 < m; r0 += LORA_MAX_ROWS) {
+    const int32_t n = std::min<int32_t>(LORA_MAX_ROWS, m - r0);
+    glora::BgmvArgs g{};
+    if (!fold_geometry(false, n, 1, ((n + 3) & ~3) + 1, max_rank, k_in, n_out, g.g, GLORA_MAX_CLUSTER, nullptr))
+      return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory for max_rank %d, k_in %d, n_out %d", max_rank, k_in, n_out);
+    g.x = x + static_cast<long long>(r0) * x_row_stride;
+    g.x_stride = x_row_stride;
+    g.out = base_out + static_cast<long long>(r0) * out_row_stride;
+    g.out_stride = out_row_stride;
+    g.single = 1;
+    g.one_a = a;
+    g.one_b = b;
+    g.one_scale = scale;
+    g.n = n;
+    g.max_loras = 1;
+    g.max_rank = max_rank;
+    g.k_in = k_in;
+    g.n_out = n_out;
+    g.xa = xa ? xa + static_cast<long long>(r0) * max_rank : nullptr;
+    rc = glora::launch_bgmv(g, stream);
+    if (rc) return cuda_fail(rc, "lora_delta launch");
+  }
+  return ok();
+}
+
+int lora_delta_geometry(int32_t m, int32_t max_rank, int32_t k_in, int32_t n_out, int32_t sm_count, int64_t out[6]) {
+  if (!out) return fail(LORA_ERR_NULL, "out is NULL");
+  if (m < 0 || m > LORA_MAX_DELTA_ROWS) return fail(LORA_ERR_SIZE, "m %d outside [0, %d]", m, LORA_MAX_DELTA_ROWS);
+  const int rc = check_shape(max_rank, k_in, n_out, k_in, n_out);
+  if (rc) return rc;
+  DenseGeom dg;
+  const int sms = sm_count > 0 ? sm_count : device_sm_count();
+  int64_t v[6] = {0, 0, 0, 0, 0, 0};
+  if (dense_geometry(m, max_rank, k_in, sms, dg)) {
+    v[0] = 1; v[1] = dg.cl; v[2] = dg.ns; v[3] = dg.stage; v[4] = dg.smem; v[5] = dg.ctas;
+  } else {
+    glora::FoldGeometry g{};
+    const int n = std::max(1, std::min<int32_t>(m, LORA_MAX_ROWS));
+    if (!fold_geometry(false, n, 1, ((n + 3) & ~3) + 1, max_rank, k_in, n_out, g, GLORA_MAX_CLUSTER, nullptr))
+      return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory");
+    v[1] = g.cl; v[2] = g.ns; v[3] = g.stage_bytes; v[4] = g.smem_bytes; v[5] = static_cast<int64_t>(g.clusters) * g.cl;
+  }
+  std::memcpy(out, v, sizeof v);
+  return ok();
+}
+
 int lora_read_device_status(void* stream, uint32_t* status_out, int clear) {
-  const int rc = glora::read_device_status(stream, status_out, clear);
+  if (!status_out) return fail(LORA_ERR_NULL, "status_out is NULL");
+  uint32_t a = 0, b = 0;
+  int rc = glora::read_device_status(stream, &a, clear);
+  if (!rc) rc = glora::read_dense_status(stream, &b, clear);
+  *status_out = a | b;
   return rc ? cuda_fail(rc, "lora_read_device_status") : ok();
 }
 

@@ -49,6 +49,10 @@ struct BgmvArgs {
   long long out_stride;
   const void* a_maps;        // [max_loras] 128-byte A tensor maps (a_tiled), or NULL
   const int32_t* seq_slot;   // slot per row, or NULL: derived from the MoE decode routing below
+  int single;                // 1: every row uses slot 0, whose entries are one_a / one_b / one_scale
+  const uint16_t* one_a;
+  const uint16_t* one_b;
+  float one_scale;
   int n;
   const int32_t* indices;    // MoE decode rows: expert per row
   const int32_t* row_adapter;  // [num_tokens] adapter per token (NULL: adapter 0)

@@ -588,7 +588,8 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
 // unit that finds no rows, or whose slot has a NULL table entry, does nothing.
 // The decode-path MoE fold runs here too: its "slot" is the table entry
 // a * E + e of the row's expert and its token's adapter, and max_loras is the
-// table count.
+// table count. So does the single-adapter delta at small m (`single`): every
+// row is slot 0 of a one-entry table passed by value.
 // ============================================================================
 template <int MAXT, bool TILED>
 __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __grid_constant__ BgmvArgs p) {
@@ -612,16 +613,18 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
   auto a_map = [&](int s) { return static_cast<const char*>(p.a_maps) + 128 * static_cast<long long>(s); };
   if (first_tile && tid == 0) {
     if (TILED) prefetch_tensormap(a_map(slot));
-    tab_a = p.a_table[slot];
-    tab_b = p.b_table[slot];
-    tab_s = p.scale_table[slot];
+    tab_a = p.single ? p.one_a : p.a_table[slot];
+    tab_b = p.single ? p.one_b : p.b_table[slot];
+    tab_s = p.single ? p.one_scale : p.scale_table[slot];
   }
   // seq_slot (and the per-slot row counts) live in the not-yet-used ring.
   int* ss = reinterpret_cast<int*>(smem + g.off_ring);
   int* cnt = ss + ((p.n + 3) & ~3);
   for (int i = tid; i < p.n; i += kThreads) {
     int sl;
-    if (p.seq_slot) {
+    if (p.single) {
+      sl = 0;
+    } else if (p.seq_slot) {
       sl = p.seq_slot[i];
     } else {   // MoE decode rows: table a * E + e from the row's expert and its token's adapter
       const int e = p.indices[i], t = i / p.top_k;
@@ -661,9 +664,9 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
     tile = pl.found_tile;
     if (tid == 0) {
       if (TILED) prefetch_tensormap(a_map(slot));
-      tab_a = p.a_table[slot];
-      tab_b = p.b_table[slot];
-      tab_s = p.scale_table[slot];
+      tab_a = p.single ? p.one_a : p.a_table[slot];
+      tab_b = p.single ? p.one_b : p.b_table[slot];
+      tab_s = p.single ? p.one_scale : p.scale_table[slot];
     }
   } else {
     __syncthreads();

@@ -21,6 +21,7 @@ STATUS_NAMES = {-1: "LORA_ERR_NULL", -2: "LORA_ERR_SIZE", -3: "LORA_ERR_STRIDE",
 LORA_DEV_MISALIGNED = 0x1
 MOE_M_TILE = 64
 TMAP_MIN_RANK = 32         # LORA_TMAP_MIN_RANK: a_tmaps are used from this max_rank up
+DELTA_DENSE_MIN_ROWS = 256  # LORA_DELTA_DENSE_MIN_ROWS: lora_delta's tensor-core path from this m up
 
 
 class LoraError(RuntimeError):
@@ -49,6 +50,10 @@ def load():
     lib.lora_moe_gather_bgmv.restype = ctypes.c_int
     lib.lora_moe_gather_bgmv.argtypes = [P, I64, P, I64, P, I32, I32, P, I32, I32,
                                          P, P, P, I32, I32, I32, I32, P, P, P]
+    lib.lora_delta.restype = ctypes.c_int
+    lib.lora_delta.argtypes = [P, I64, P, I64, I32, P, P, ctypes.c_float, I32, I32, I32, P, P]
+    lib.lora_delta_geometry.restype = ctypes.c_int
+    lib.lora_delta_geometry.argtypes = [I32, I32, I32, I32, I32, ctypes.POINTER(I64)]
     lib.lora_encode_a_tmaps.restype = ctypes.c_int
     lib.lora_encode_a_tmaps.argtypes = [P, I32, I32, I32, P]
     lib.lora_last_error.restype = ctypes.c_char_p
@@ -105,6 +110,23 @@ def lora_bgmv(x, x_row_stride, base_out, out_row_stride, seq_slot, n, a_table, b
                                    _addr(seq_slot), n, _addr(a_table), _addr(b_table),
                                    _addr(scale_table), max_loras, max_rank, k_in, n_out,
                                    _addr(xa), _addr(a_tmaps), _stream(stream)))
+
+
+def lora_delta(x, x_row_stride, base_out, out_row_stride, m, a, b, scale, max_rank, k_in, n_out,
+               xa=None, stream=None):
+    """One adapter pair folded into all m rows (see lora_delta in include/gather_lora.h)."""
+    return _check(load().lora_delta(_addr(x), x_row_stride, _addr(base_out), out_row_stride, m,
+                                    _addr(a), _addr(b), float(scale), max_rank, k_in, n_out,
+                                    _addr(xa), _stream(stream)))
+
+
+DELTA_GEOMETRY_KEYS = ("dense", "cluster", "ring_stages", "stage_bytes", "smem_bytes", "ctas")
+
+
+def lora_delta_geometry(m, max_rank, k_in, n_out, sm_count=0) -> dict:
+    out = (ctypes.c_int64 * 6)()
+    _check(load().lora_delta_geometry(m, max_rank, k_in, n_out, sm_count, out))
+    return dict(zip(DELTA_GEOMETRY_KEYS, list(out)))
 
 
 def lora_moe_grouped_fold(x, x_row_stride, base_out, out_row_stride, expert_offsets, num_experts,

@@ -76,6 +76,8 @@ enum lora_status {
 #define LORA_MAX_LORAS 4096        /* max_loras of lora_bgmv in [1, 4096] */
 #define LORA_MAX_EXPERTS 1024      /* num_experts of the MoE fold in [1, 1024] */
 #define LORA_TMAP_MIN_RANK 32      /* a_tmaps are used from this max_rank up */
+#define LORA_MAX_DELTA_ROWS (1 << 20)      /* m of lora_delta in [0, 2^20] */
+#define LORA_DELTA_DENSE_MIN_ROWS 256      /* lora_delta takes the tensor-core path from this m up */
 #define LORA_MOE_M_TILE 64         /* sorted rows per MoE tile (static grid unit) */
 
 /*
@@ -204,6 +206,45 @@ int lora_moe_gather_bgmv(const lora_bf16_t* x, int64_t x_row_stride,
                          const float* scale_table, int32_t max_loras,
                          int32_t max_rank, int32_t k_in, int32_t n_out,
                          lora_bf16_t* xa, const void* a_tmaps, void* stream);
+
+/*
+ * lora_delta — one adapter pair folded into every row: the pages' apply_lora_delta
+ * ("lora_delta.rs", apply_lora_delta; "Module lora_delta", LoraPair), for m rows
+ *   xa[i, :]  = bf16( x[i, :] @ a^T )                          fp32 accumulate
+ *   out[i, :] = bf16( fma(scale, bf16( xa[i, :] @ b^T ), out[i, :]) ),  i < m.
+ * Pages' m == 1 GEMV, small-m per-row and large-m tensor-core GEMM paths are one
+ * call here, with the same rounding points as lora_bgmv:
+ *   - m >= LORA_DELTA_DENSE_MIN_ROWS and max_rank in {16, 32, 64, 128}: one
+ *     launch of the tcgen05 tensor-core kernel (tiles of 128 rows, a cluster of
+ *     CTAs splits k_in and n_out; TMA tensor maps are encoded on the host per call);
+ *   - otherwise the routed engine of lora_bgmv with every row on one slot (one
+ *     launch per LORA_MAX_ROWS rows).
+ * The fp32 summation order depends on (k_in, max_rank) and, on the tensor-core
+ * path, on the cluster size, which follows the number of 128-row tiles: unlike
+ * lora_bgmv, results may differ in the last bit between calls of different m
+ * (each within the oracle's tolerance).
+ *   x         [m, x_row_stride] BF16 rows (k_in used), 16-byte aligned
+ *   base_out  [m, out_row_stride] BF16, columns [0, n_out) folded in place; other
+ *             bytes are not touched
+ *   a         [max_rank, k_in] row-major BF16 (rank-padded with zero rows)
+ *   b         [n_out, max_rank] row-major BF16 (rank-padded with zero columns)
+ *   scale     f32 (alpha/r, or alpha/sqrt(r) for rsLoRA)
+ *   xa        optional [m, max_rank] BF16 output of the shrink; NULL skips it
+ * Shapes, strides and alignment as for lora_bgmv (a and b 16-byte aligned, too);
+ * m == 0 is a no-op. No allocation, no synchronization: capture-safe.
+ */
+int lora_delta(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_t* base_out, int64_t out_row_stride,
+               int32_t m, const lora_bf16_t* a, const lora_bf16_t* b, float scale, int32_t max_rank,
+               int32_t k_in, int32_t n_out, lora_bf16_t* xa, void* stream);
+
+/*
+ * lora_delta_geometry — the launch lora_delta would make for m rows on a device
+ * with sm_count SMs (0: the current device). Writes [dense (1: tensor-core
+ * kernel, 0: routed engine), cluster, ring_stages, stage_bytes, smem_bytes, ctas
+ * (of one launch)] to out[0..5]. No counterpart in the pages (tests, benchmarks).
+ */
+int lora_delta_geometry(int32_t m, int32_t max_rank, int32_t k_in, int32_t n_out, int32_t sm_count,
+                        int64_t out[6]);
 
 /*
  * lora_encode_a_tmaps — host helper run once when adapters are loaded: writes,

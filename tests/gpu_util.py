@@ -105,3 +105,29 @@ def device_a_tmaps(a_table: torch.Tensor, max_rank: int, k_in: int) -> torch.Ten
     t = torch.from_numpy(maps).to(a_table.device)
     assert t.data_ptr() % 64 == 0
     return t
+
+
+def gpu_delta(wl: W.DeltaWorkload, d: W.DeviceDelta = None, with_xa=True, stream=None):
+    """Run lora_delta on the device copy of wl. Returns (out_buf, xa [m, max_rank]) as uint16."""
+    d = d or W.delta_to_device(wl)
+    L.lora_delta(d.x, wl.x_row_stride, d.out_ptr, wl.out_row_stride, wl.m, d.a, d.b, wl.scale,
+                 wl.max_rank, wl.k_in, wl.n_out, xa=d.xa if with_xa else None, stream=stream)
+    torch.cuda.synchronize()
+    return to_u16(d.out_buf), to_u16(d.xa)[: wl.m]
+
+
+def oracle_delta(wl: W.DeltaWorkload):
+    out = wl.out_buf.copy()
+    seg = out.reshape(-1)[wl.out_offset:]
+    xa, dd = oracle.lora_delta(wl.x.reshape(-1), wl.x_row_stride, seg, wl.out_row_stride, wl.m,
+                               wl.a, wl.b, wl.scale, wl.max_rank, wl.k_in, wl.n_out)
+    return out, xa, dd
+
+
+def delta_rows(wl: W.DeltaWorkload, rows) -> W.DeltaWorkload:
+    """The same problem restricted to the given rows (for oracle samples of a full-size run)."""
+    rows = np.asarray(rows)
+    return W.DeltaWorkload(wl.name, len(rows), wl.k_in, wl.n_out, wl.max_rank, wl.rank,
+                           wl.x_row_stride, wl.out_row_stride, wl.out_offset,
+                           np.ascontiguousarray(wl.x[rows]), np.ascontiguousarray(wl.out_buf[rows]),
+                           wl.a, wl.b, wl.scale, wl.meta)

@@ -201,3 +201,17 @@ def compare_gather(wl: W.MoeGatherWorkload, gpu_out, ora_out, gpu_xa, ora_xa, or
     if xa_tot:
         assert xa_exact / xa_tot >= min_exact, f"only {xa_exact}/{xa_tot} xa values bit-exact"
     return dict(rows=len(routes), exact=n_exact, total=n_tot, worst=worst)
+
+
+def delta_as_bgmv(wl: W.DeltaWorkload) -> W.BgmvWorkload:
+    """The single-adapter delta as a routed fold with every row on slot 0 (its
+    definition, lora_delta.rs apply_lora_delta), for the bgmv comparison rules."""
+    return W.BgmvWorkload(wl.name, wl.m, wl.k_in, wl.n_out, 1, wl.max_rank, wl.x_row_stride,
+                          wl.out_row_stride, wl.out_offset, wl.x, wl.out_buf,
+                          np.zeros(wl.m, dtype=np.int32), np.array([wl.rank], np.int32),
+                          np.ones(1, dtype=bool), wl.a[None], wl.b[None],
+                          np.array([wl.scale], dtype=np.float32))
+
+
+def compare_delta(wl: W.DeltaWorkload, gpu_out, ora_out, gpu_xa, ora_xa, ora_d, min_exact=0.99):
+    return compare_bgmv(delta_as_bgmv(wl), gpu_out, ora_out, gpu_xa, ora_xa, ora_d, min_exact)

@@ -255,3 +255,46 @@ def test_tensor_maps_only_from_the_minimum_rank():
             assert L.lora_launch_geometry(mode, rows, tables, rank, 4104, 4096)["a_tiled"] == 0
     # the grouped MoE fold loads A rows whatever it is given
     assert L.lora_launch_geometry(17, 4096, 16, 64, 768, 2048) == L.lora_launch_geometry(1, 4096, 16, 64, 768, 2048)
+
+
+def _delta(**kw):
+    a = dict(x=FAKE, xs=4096, out=FAKE, os=4096, m=512, a=FAKE, b=FAKE, sc=1.0, R=64, k=4096, no=4096,
+             xa=None)
+    a.update(kw)
+    return L.load().lora_delta(a["x"], a["xs"], a["out"], a["os"], a["m"], a["a"], a["b"], a["sc"],
+                               a["R"], a["k"], a["no"], a["xa"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(m=-1), -2), (dict(m=(1 << 20) + 1), -2), (dict(R=0), -2), (dict(R=264), -2), (dict(R=12), -4),
+    (dict(k=4100, xs=4104), -4), (dict(xs=4088), -3), (dict(os=100, no=128), -3), (dict(x=None), -1),
+    (dict(out=None), -1), (dict(a=None), -1), (dict(b=None), -1), (dict(a=FAKE + 8), -4),
+    (dict(b=FAKE + 2), -4), (dict(xa=FAKE + 4), -4), (dict(out=FAKE + 8), -4),
+])
+def test_delta_rejects_bad_arguments_before_launch(kw, code):
+    assert _delta(**kw) == code
+    assert L.lora_last_error()
+
+
+def test_delta_zero_rows_is_a_no_op():
+    assert _delta(m=0, x=None, out=None) == 0
+
+
+def test_delta_geometry():
+    g = L.lora_delta_geometry(4096, 16, 4096, 4096, 152)
+    assert g["dense"] == 1 and g["cluster"] == 4 and g["ctas"] == 128 and g["ring_stages"] == 8
+    g = L.lora_delta_geometry(4096, 128, 12288, 4096, 152)
+    assert g["dense"] == 1 and g["cluster"] == 4 and g["ring_stages"] == 4
+    assert L.lora_delta_geometry(16384, 64, 4096, 4096, 152)["cluster"] == 1    # 128 tiles fill the SMs
+    assert L.lora_delta_geometry(1024, 64, 4096, 4096, 152)["cluster"] == 8
+    assert L.lora_delta_geometry(4096, 64, 64, 4096, 152)["cluster"] == 1       # one k-chunk
+    for r, ns in ((16, 8), (32, 7), (64, 6), (128, 4)):
+        g = L.lora_delta_geometry(L.DELTA_DENSE_MIN_ROWS, r, 4096, 4096, 152)
+        assert g["dense"] == 1 and g["ring_stages"] == ns and 116 * 1024 < g["smem_bytes"] <= 227 * 1024
+        assert g["stage_bytes"] % 1024 == 0
+    # small m or a rank the tensor-core path does not take: the routed engine
+    assert L.lora_delta_geometry(L.DELTA_DENSE_MIN_ROWS - 1, 64, 4096, 4096, 152)["dense"] == 0
+    for r in (8, 24, 48, 256):
+        assert L.lora_delta_geometry(4096, r, 4096, 4096, 152)["dense"] == 0
+    m = re.search(r"#define LORA_DELTA_DENSE_MIN_ROWS (\d+)", open(HEADER).read())
+    assert m and int(m.group(1)) == L.DELTA_DENSE_MIN_ROWS

@@ -1,0 +1,112 @@
+"""Single-adapter delta (lora_delta) on the GPU against the CPU oracle (-m gpu).
+
+lora_delta.rs page, apply_lora_delta: one adapter pair folded into every row.
+From LORA_DELTA_DENSE_MIN_ROWS rows up, ranks 16/32/64/128 run on the tcgen05
+tensor-core kernel; smaller m and other ranks run on the routed engine with
+every row on one slot. Both must match the oracle under the fold's rule
+(tests/parity.py), leave bytes outside [out_offset, out_offset + n_out) of each
+row untouched, and write the BF16 xa of every row.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from gather_lora_gb300 import lib as L
+from gather_lora_gb300 import workloads as W
+from gpu_util import delta_rows, gpu_delta, oracle_delta, require_gpu, to_u16
+from parity import compare_delta
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _gpu():
+    require_gpu()
+    L.lora_read_device_status(clear=True)
+
+
+CASES = [
+    # m, k_in, n_out, max_rank, rank, x pad, out offset, expected path (1 = tensor cores)
+    (300, 1000, 520, 16, 16, 24, 8, 1),     # 3 tiles, ragged rows, k-chunk and output chunk
+    (300, 1000, 520, 32, 24, 0, 0, 1),
+    (513, 2056, 1032, 64, 40, 8, 16, 1),    # 5 tiles, last one a single row
+    (260, 4104, 264, 128, 128, 0, 8, 1),
+    (1024, 64, 136, 64, 64, 0, 0, 1),       # one k-chunk: cluster of one CTA
+    (2176, 520, 200, 16, 12, 0, 0, 1),      # 17 tiles
+    (40, 1000, 520, 16, 16, 24, 8, 0),      # small m: routed engine
+    (300, 1000, 520, 24, 24, 0, 0, 0),      # rank outside the tensor-core set
+    (700, 512, 256, 256, 200, 0, 0, 0),
+]
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_delta_matches_oracle(case):
+    m, k_in, n_out, R, rank, xpad, off, path = CASES[case]
+    wl = W.make_delta(f"delta{case}", m=m, k_in=k_in, n_out=n_out, max_rank=R, rank=rank, alpha=32.0,
+                      rslora=False, seed=700 + case, x_row_stride=k_in + xpad, out_offset=off,
+                      out_row_stride=off + n_out + (8 if off else 0))
+    assert L.lora_delta_geometry(m, R, k_in, n_out)["dense"] == path
+    g_out, g_xa = gpu_delta(wl)
+    o_out, o_xa, o_d = oracle_delta(wl)
+    compare_delta(wl, g_out, o_out, g_xa, o_xa, o_d, min_exact=0.97)
+    assert L.lora_read_device_status(clear=True) == 0
+
+
+def test_delta_without_xa_gives_the_same_fold():
+    wl = W.make_delta("noxa", m=384, k_in=2048, n_out=1024, max_rank=64, rank=64, alpha=16.0,
+                      rslora=False, seed=720)
+    o1, _ = gpu_delta(wl)
+    o2, _ = gpu_delta(wl, with_xa=False)
+    assert np.array_equal(o1, o2)
+
+
+def test_delta_is_deterministic():
+    wl = W.make_delta("det", m=640, k_in=4096, n_out=2048, max_rank=128, rank=128, alpha=64.0,
+                      rslora=True, seed=721, x_law="silu_gate")
+    d = W.delta_to_device(wl)
+    o1, x1 = gpu_delta(wl, d)
+    d2 = W.delta_to_device(wl)
+    o2, x2 = gpu_delta(wl, d2)
+    assert np.array_equal(o1, o2) and np.array_equal(x1, x2)
+
+
+@pytest.mark.parametrize("name", ["prefill_qproj_delta", "prefill_down_delta"])
+def test_delta_full_size_sampled(name):
+    """The benchmarked workloads at full size, checked on rows sampled from the
+    first, middle and last tiles (the oracle runs on those rows only)."""
+    wl = W.by_name(name)
+    g_out, g_xa = gpu_delta(wl)
+    rng = np.random.default_rng(5)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, wl.m // 2, wl.m - 1],
+                                     rng.integers(0, wl.m, size=18)]))
+    sub = delta_rows(wl, rows)
+    o_out, o_xa, o_d = oracle_delta(sub)
+    compare_delta(sub, g_out[rows], o_out, g_xa[rows], o_xa, o_d)
+    assert L.lora_read_device_status(clear=True) == 0
+
+
+def test_delta_graph_replay_reads_new_inputs():
+    """Captured once, replayed after the inputs changed in place: the replay folds
+    the new inputs (no host-side state is baked into the launch)."""
+    wl = W.make_delta("graph", m=512, k_in=1024, n_out=512, max_rank=32, rank=32, alpha=32.0,
+                      rslora=False, seed=722)
+    wl2 = W.make_delta("graph2", m=512, k_in=1024, n_out=512, max_rank=32, rank=32, alpha=32.0,
+                       rslora=False, seed=723)
+    d = W.delta_to_device(wl)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            L.lora_delta(d.x, wl.x_row_stride, d.out_ptr, wl.out_row_stride, wl.m, d.a, d.b, wl.scale,
+                         wl.max_rank, wl.k_in, wl.n_out, xa=d.xa, stream=s)
+    d.x.copy_(torch.from_numpy(wl2.x.view(np.int16)))
+    d.out_buf.copy_(torch.from_numpy(wl2.out_buf.view(np.int16)))
+    d.a.copy_(torch.from_numpy(wl2.a.view(np.int16)))
+    d.b.copy_(torch.from_numpy(wl2.b.view(np.int16)))
+    g.replay()
+    torch.cuda.synchronize()
+    wl2.scale = wl.scale            # the scale is a launch argument, captured by value
+    o_out, o_xa, o_d = oracle_delta(wl2)
+    compare_delta(wl2, to_u16(d.out_buf), o_out, to_u16(d.xa)[: wl2.m], o_xa, o_d)
