@@ -654,7 +654,7 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": head, "rows": alg["rows"], "routed_rows": alg["routed_rows"],
-                       "k_in": wl.k_in, "n_out": wl.n_out, "max_loras": wl.max_loras,
+                       "k_in": wl.k_in, "n_out": wl.n_out, "max_loras": getattr(wl, "max_loras", 1),
                        "max_rank": wl.max_rank, "distinct_adapters": alg["adapters"],
                        "parallelism": f"replicas{dctx.world}",
                        "l2": f"rotating {C} input copies ({C * runner.bytes_per_copy() / 2**20:.0f} MiB > 2x L2)",
