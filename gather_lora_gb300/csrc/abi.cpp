@@ -533,6 +533,13 @@ int lora_delta_geometry(int32_t m, int32_t max_rank, int32_t k_in, int32_t n_out
   return ok();
 }
 
+int lora_selftest_wait_timeout(int64_t limit_cycles, void* stream) {
+  if (limit_cycles < 1 || limit_cycles > (int64_t{1} << 32))
+    return fail(LORA_ERR_SIZE, "limit_cycles %lld outside [1, 2^32]", static_cast<long long>(limit_cycles));
+  const int rc = glora::launch_wait_selftest(limit_cycles, stream);
+  return rc ? cuda_fail(rc, "lora_selftest_wait_timeout launch") : ok();
+}
+
 int lora_read_device_status(void* stream, uint32_t* status_out, int clear) {
   if (!status_out) return fail(LORA_ERR_NULL, "status_out is NULL");
   uint32_t a = 0, b = 0;

@@ -82,17 +82,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uin
       : "memory");
   return done != 0;
 }
-// Wait for phase `parity` of an mbarrier; false after kWaitLimitCycles SM
-// clocks without it. The limit is measured with the SM-local cycle counter:
-// reading the global nanosecond timer costs about half a microsecond.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for phase `parity` of an mbarrier; false after `limit` SM clocks
+// (kWaitLimitCycles for the folds) without it. The limit is measured with the
+// SM-local cycle counter: reading the global nanosecond timer costs about half
+// a microsecond.
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, long long limit) {
   constexpr uint32_t kHintNs = 1000000;
   if (mbar_try_wait(bar, parity, kHintNs)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity, kHintNs)) {
-    if (clock64() - t0 > kWaitLimitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   }
   return true;
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  return mbar_wait_limit(bar, parity, kWaitLimitCycles);
 }
 
 // 1-D TMA copy of `bytes` (multiple of 16, both addresses 16-byte aligned)

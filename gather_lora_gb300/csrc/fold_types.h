@@ -92,5 +92,6 @@ struct MoeArgs {
 int launch_bgmv(const BgmvArgs& a, void* stream);
 int launch_moe(const MoeArgs& a, void* stream);
 int read_device_status(void* stream, uint32_t* out, int clear);
+int launch_wait_selftest(long long limit_cycles, void* stream);
 
 }  // namespace glora

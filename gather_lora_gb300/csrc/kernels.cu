@@ -937,6 +937,24 @@ int launch_moe(const MoeArgs& a, void* stream) {
   }
 }
 
+// Self-test of the bounded wait every fold relies on: one thread waits on an
+// mbarrier that nothing arrives at, with a limit of `limit_cycles` SM clocks;
+// giving up sets the timeout bit of the device status word, as in the folds.
+__global__ void lora_wait_selftest_kernel(long long limit_cycles) {
+  __shared__ __align__(8) unsigned long long bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait_limit(smem_u32(&bar), 0, limit_cycles)) atomicOr(&g_lora_status, kDevTimeout);
+}
+
+int launch_wait_selftest(long long limit_cycles, void* stream) {
+  lora_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_cycles);
+  return static_cast<int>(cudaGetLastError());
+}
+
 int read_device_status(void* stream, uint32_t* out, int clear) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned int v = 0;

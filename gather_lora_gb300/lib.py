@@ -56,6 +56,8 @@ def load():
     lib.lora_delta_geometry.argtypes = [I32, I32, I32, I32, I32, ctypes.POINTER(I64)]
     lib.lora_encode_a_tmaps.restype = ctypes.c_int
     lib.lora_encode_a_tmaps.argtypes = [P, I32, I32, I32, P]
+    lib.lora_selftest_wait_timeout.restype = ctypes.c_int
+    lib.lora_selftest_wait_timeout.argtypes = [I64, P]
     lib.lora_last_error.restype = ctypes.c_char_p
     lib.lora_last_error.argtypes = []
     lib.lora_read_device_status.restype = ctypes.c_int
@@ -170,6 +172,11 @@ def lora_encode_a_tmaps(a_ptrs, max_rank: int, k_in: int):
 
 def lora_last_error() -> str:
     return load().lora_last_error().decode()
+
+
+def lora_selftest_wait_timeout(limit_cycles, stream=None):
+    """Diagnostic: one bounded wait that runs out (see include/gather_lora.h)."""
+    return _check(load().lora_selftest_wait_timeout(int(limit_cycles), _stream(stream)))
 
 
 def lora_read_device_status(stream=None, clear=True) -> int:

@@ -259,6 +259,16 @@ int lora_delta_geometry(int32_t m, int32_t max_rank, int32_t k_in, int32_t n_out
 int lora_encode_a_tmaps(const uint64_t* a_ptrs, int32_t count, int32_t max_rank, int32_t k_in,
                         void* maps_out);
 
+/*
+ * lora_selftest_wait_timeout — diagnostic: launches one CTA whose thread waits on
+ * an mbarrier that nothing arrives at, through the same bounded wait the folds
+ * use, with a limit of limit_cycles SM clocks (in [1, 2^32]); giving up sets
+ * LORA_DEV_TIMEOUT in the device status word, as a fold that timed out would.
+ * The kernel then returns normally: the context stays usable. No counterpart in
+ * the pages (it tests the failure path of this library without a GPU fault).
+ */
+int lora_selftest_wait_timeout(int64_t limit_cycles, void* stream);
+
 /* Text of the last error returned on this host thread ("" if none). */
 const char* lora_last_error(void);
 

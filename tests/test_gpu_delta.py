@@ -35,6 +35,8 @@ CASES = [
     (260, 4104, 264, 128, 128, 0, 8, 1),
     (1024, 64, 136, 64, 64, 0, 0, 1),       # one k-chunk: cluster of one CTA
     (2176, 520, 200, 16, 12, 0, 0, 1),      # 17 tiles
+    (300, 8, 8, 16, 16, 0, 0, 1),           # k_in and n_out far below one box
+    (256, 24, 40, 128, 96, 8, 8, 1),        # exactly two tiles, boxes mostly outside the tensors
     (40, 1000, 520, 16, 16, 24, 8, 0),      # small m: routed engine
     (300, 1000, 520, 24, 24, 0, 0, 0),      # rank outside the tensor-core set
     (700, 512, 256, 256, 200, 0, 0, 0),
