@@ -53,6 +53,9 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 #ifndef GLORA_MOE_STAGE_TARGET
 #define GLORA_MOE_STAGE_TARGET (56 * 1024)
 #endif
+#ifndef GLORA_TC_SHRINK
+#define GLORA_TC_SHRINK 1
+#endif
 #ifndef GLORA_MIN_STAGE
 #define GLORA_MIN_STAGE (24 * 1024)
 #endif
@@ -139,6 +142,9 @@ bool make_geometry_at(bool moe, int rows, int max_loras, int planner_ints, int m
   } else {
     while (g.maxt * (glora::kConsumerWarps / g.ksplit) < tiles) g.maxt *= 2;
   }
+  // The bgmv shrink runs on tcgen05 when A comes as TMA boxes of 128 rows and
+  // a unit has at most 16 rows: M = 128 (A rows), N = 16 (the unit's x rows).
+  g.tc = (!moe && a_tiled && g.mr16 == 128 && g.gmax == 16 && g.ksplit == 1 && !g.group_parallel) ? GLORA_TC_SHRINK : 0;
   g.pitch_k = g.kch * 2 + 16;
   g.pitch_b = max_rank * 2 + (max_rank >= 32 ? 16 : 0);
   const int shrink_stage = a_tiled ? g.mr16 * g.kch * 2 + g.gmax * g.pitch_k : srows * g.pitch_k;
@@ -550,7 +556,7 @@ int lora_read_device_status(void* stream, uint32_t* status_out, int clear) {
 }
 
 int lora_launch_geometry(int moe, int32_t rows, int32_t max_loras, int32_t max_rank, int32_t k_in,
-                         int32_t n_out, int64_t out[10]) {
+                         int32_t n_out, int64_t out[11]) {
   if (!out) return fail(LORA_ERR_NULL, "out is NULL");
   int rc = check_shape(max_rank, k_in, n_out, k_in, n_out);
   if (rc) return rc;
@@ -563,7 +569,7 @@ int lora_launch_geometry(int moe, int32_t rows, int32_t max_loras, int32_t max_r
   if (!fold_geometry(grouped, rows, max_loras, scratch, max_rank, k_in, n_out, g,
                      kind == 2 ? 1 : GLORA_MAX_CLUSTER, (moe & 16) && !grouped ? &kAnyMaps : nullptr))
     return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory");
-  const int64_t v[10] = {g.cl, g.rt, g.ksl, g.jsl, g.kch, g.jch, g.ns, g.clusters, g.smem_bytes, g.a_tiled};
+  const int64_t v[11] = {g.cl, g.rt, g.ksl, g.jsl, g.kch, g.jch, g.ns, g.clusters, g.smem_bytes, g.a_tiled, g.tc};
   std::memcpy(out, v, sizeof v);
   return ok();
 }

@@ -29,6 +29,11 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 __device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst_smem), "l"(src) : "memory");
 }
+// 16 zero bytes into shared memory through the same asynchronous path (no
+// global read: the source size is 0).
+__device__ __forceinline__ void cp_async16_zero(uint32_t dst_smem, const void* any_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, 0;\n" ::"r"(dst_smem), "l"(any_src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;\n" ::: "memory");
 }

@@ -31,6 +31,8 @@ struct FoldGeometry {
   int gather;       // exchange by all-gather of fp32 partials into cl planes after the k-phase planes
   int a_tiled;      // shrink stages hold A as 2-D TMA boxes (kch/64 boxes of mr16 rows x 128 B,
                     // 128-byte swizzle) ahead of the padded x rows; 0: padded A rows
+  int tc;           // bgmv shrink on tcgen05 (a_tiled, mr16 == 128, gmax == 16): the x rows are
+                    // placed as 128-byte-swizzled 64-column atoms of gmax rows after the A boxes
   int mr16;         // max_rank rounded up to 16
   int pitch_k;      // bytes per A or x row in a shrink stage (kch*2 + 16)
   int pitch_b;      // bytes per B row in an expand stage

@@ -33,6 +33,7 @@
 #include <limits.h>
 
 #include "common.cuh"
+#include "tc05.cuh"
 
 #include <type_traits>
 #include "fold_types.h"
@@ -69,6 +70,8 @@ struct Plan {
   const uint16_t* gA[kMaxRows];
   const uint16_t* gB[kMaxRows];
   const void* gmap[kMaxRows];      // the group's A tensor map (a_tiled launches)
+  unsigned long long tc_done;      // tcgen05 shrink: the unit's partial is in TMEM
+  uint32_t tmem;                   // tcgen05 shrink: TMEM base address
   int tpos[kMaxTileRows];          // MoE: tile rows routed to this unit's adapter, ascending
   int tkey[kMaxTileRows];          // MoE: their experts
   int txrow[kMaxTileRows];         // MoE: their rows of x (the token with x_gather)
@@ -119,8 +122,10 @@ __device__ __forceinline__ void ring_init(Plan& pl, int ns) {
 // ring_init(); `it0` ring items were used by earlier passes. Returns the ring
 // items this pass used. MAXT bounds the 16x8 shrink tiles one consumer warp
 // owns (MT * ceil(group rows / 8) <= 8 * MAXT). TILED: A comes as TMA boxes
-// (launches with g.a_tiled); each instance has one A layout.
-template <int MAXT, bool TILED>
+// (launches with g.a_tiled); each instance has one A layout. TC: the shrink
+// runs on tcgen05 (launches with g.tc; one group per pass, TMEM allocated by
+// the caller at pl.tmem).
+template <int MAXT, bool TILED, bool TC = false>
 __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeometry& g, Plan& pl,
                                            unsigned char* smem, const cg::cluster_group& cluster,
                                            int crank, int it0) {
@@ -201,7 +206,7 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
       }
       // TMA bytes this thread issues (rows q0, q0 + kP, ... of each TMA set)
       const int mine0 = bytes0 >= kTmaRowBytes && q0 < n0 ? (n0 - 1 - q0) / kP + 1 : 0;
-      const int mine1 = bytes1 >= kTmaRowBytes && q0 < n1 ? (n1 - 1 - q0) / kP + 1 : 0;
+      const int mine1 = bytes1 >= kTmaRowBytes && q0 < n1 && !(TC && it < n_shrink) ? (n1 - 1 - q0) / kP + 1 : 0;
       const int nbox = g.kch >> 6, a_box = g.mr16 * 128;
       const int tx = mine0 * bytes0 + mine1 * bytes1 + (amap && pt == 0 ? nbox * a_box : 0);
       if (tx) mbar_expect_tx(full, static_cast<uint32_t>(tx));
@@ -216,7 +221,19 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
         const uint32_t dst = set ? dst1 : dst0;
         const int n = set ? n1 : n0, bytes = set ? bytes1 : bytes0, pitch = set ? pitch1 : pitch0;
         const int* rmap = it < n_shrink ? pl.xsrc : pl.grow;   // gathered rows: x (shrink) or base_out
-        if (bytes >= kTmaRowBytes) {
+        if (TC && set == 1 && it < n_shrink) {
+          // x rows for the tensor core: 16-byte chunk ch of row q goes to atom
+          // ch / 8 (gmax rows x 128 B), chunk (ch % 8) ^ (q % 8); the chunks of
+          // the last 16-wide k-step past the data are zeros.
+          const int cpr = bytes >> 4, cpr16 = ((bytes + 31) >> 5) << 1;
+#pragma unroll 1
+          for (int c = pt; c < n * cpr16; c += kP) {
+            const int q = c / cpr16, ch = c - q * cpr16;
+            const uint32_t d = dst + (ch >> 3) * (g.gmax * 128) + q * 128 + (((ch & 7) ^ (q & 7)) << 4);
+            const char* srow = reinterpret_cast<const char*>(src + static_cast<long long>(rmap[pl.members[m0 + q]]) * stride);
+            if (ch < cpr) cp_async16(d, srow + ch * 16); else cp_async16_zero(d, srow);
+          }
+        } else if (bytes >= kTmaRowBytes) {
 #pragma unroll 1
           for (int q = q0; q < n; q += kP) {
             const int row = set ? rmap[pl.members[m0 + q]] : q;
@@ -375,8 +392,54 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
       }
     }
   };
-  for (int gi = g_first; gi < G && nk > 0 && !idle; gi += g_step) {
-    shrink_group(gi, std::integral_constant<bool, TILED>{});
+  if constexpr (TC) {
+    // tcgen05 shrink of the pass's one group: consumer warp 0 issues the MMAs
+    // D[A rows (rank) x x rows] += A x^T into TMEM (M = 128, N = gmax = 16),
+    // and releases each stage through the commit plus the other seven
+    // consumer arrivals; warps 0-3 then move the fp32 partial from their TMEM
+    // lanes (lane = rank index, column = row) to part_s. One pass per launch:
+    // tc_done completes once (phase 0).
+    if (nk > 0) {
+      const int m0 = pl.gstart[0], R = pl.gstart[1] - m0;
+      if (warp == 0 && lane == 0) {
+        const uint32_t idesc = idesc_bf16_f32(128, 16);
+        const int a_box = g.mr16 * 128, x_atom = g.gmax * 128;
+        for (int kc = 0; kc < nk; ++kc) {
+          const int ri = it0 + kc, s = ri % ns;
+          if (!mbar_wait(smem_u32(&pl.full[s]), (ri / ns) & 1)) record_timeout(pl);
+          tc_fence_after();
+          const uint32_t st = ring_u32 + s * g.stage_bytes, xt = st + g.mr16 * g.kch * 2;
+          const int klen = min(g.kch, k_hi - (k_lo + kc * g.kch)), nst = (klen + 15) >> 4;
+          for (int s16 = 0; s16 < nst; ++s16) {
+            const uint32_t off = (s16 & 3) * 32;
+            umma_bf16(pl.tmem, smem_desc(st + (s16 >> 2) * a_box + off, 1024, Swz::k128),
+                      smem_desc(xt + (s16 >> 2) * x_atom + off, 1024, Swz::k128), idesc, (kc | s16) != 0);
+          }
+          umma_commit(smem_u32(&pl.empty[s]));
+          mbar_arrive_count(smem_u32(&pl.empty[s]), kConsumerWarps - 1);   // the phase still waits for the commit
+        }
+        umma_commit(smem_u32(&pl.tc_done));
+      }
+      __syncwarp();
+      if (!mbar_wait(smem_u32(&pl.tc_done), 0) && lane == 0) record_timeout(pl);
+      tc_fence_after();
+      if (warp < 4) {
+        uint32_t v[16];
+        tmem_ld16(pl.tmem + (static_cast<uint32_t>(warp * 32) << 16), v);
+        tmem_ld_wait();
+        const int c = warp * 32 + lane;
+        if (c < p.max_rank) {
+#pragma unroll
+          for (int r = 0; r < 16; ++r)
+            if (r < R) part_s[pl.members[m0 + r] * g.pitch_part + c] = __uint_as_float(v[r]);
+        }
+      }
+      tc_fence_before();
+    }
+  } else {
+    for (int gi = g_first; gi < G && nk > 0 && !idle; gi += g_step) {
+      shrink_group(gi, std::integral_constant<bool, TILED>{});
+    }
   }
   if (nk == 0) {  // empty k-slice: the partials are zero
     for (int e = tid; e < KS * NV * p.max_rank; e += kConsumerWarps * 32) {
@@ -591,7 +654,7 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
 // table count. So does the single-adapter delta at small m (`single`): every
 // row is slot 0 of a one-entry table passed by value.
 // ============================================================================
-template <int MAXT, bool TILED>
+template <int MAXT, bool TILED, bool TC>
 __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __grid_constant__ BgmvArgs p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const FoldGeometry& g = p.g;
@@ -724,9 +787,26 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
   __syncthreads();
   if (pl.G == 0) return;  // NULL or misaligned adapter: rows stay unchanged
 
+  if constexpr (TC) {   // the shrink's accumulator: 32 TMEM columns (16 used)
+    if (warp == 0) {
+      tmem_alloc(smem_u32(&pl.tmem), 32);
+      tmem_relinquish();
+    }
+    if (tid == 0) mbar_init(smem_u32(&pl.tc_done), 1);   // ring_init fences and synchronizes
+    tc_fence_before();
+  }
   ring_init(pl, g.ns);
+  if constexpr (TC) tc_fence_after();
   const EngineArgs ea{p.x, p.x_stride, p.out, p.out_stride, p.xa, p.max_rank, p.k_in, p.n_out};
-  fold_engine<MAXT, TILED>(ea, g, pl, smem, cluster, crank, 0);
+  fold_engine<MAXT, TILED, TC>(ea, g, pl, smem, cluster, crank, 0);
+  if constexpr (TC) {
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+      tc_fence_after();
+      tmem_dealloc(pl.tmem, 32);
+    }
+  }
 }
 
 // ============================================================================
@@ -913,18 +993,26 @@ static int launch_fold(void (*kernel)(Args), const Args& a, void* stream) {
 }
 
 int launch_bgmv(const BgmvArgs& a, void* stream) {
+  if (a.g.tc) {
+    switch (a.g.maxt) {
+      case 1: return launch_fold(lora_bgmv_fold_kernel<1, true, true>, a, stream);
+      case 2: return launch_fold(lora_bgmv_fold_kernel<2, true, true>, a, stream);
+      case 4: return launch_fold(lora_bgmv_fold_kernel<4, true, true>, a, stream);
+      default: return static_cast<int>(cudaErrorInvalidValue);
+    }
+  }
   if (a.g.a_tiled) {
     switch (a.g.maxt) {
-      case 1: return launch_fold(lora_bgmv_fold_kernel<1, true>, a, stream);
-      case 2: return launch_fold(lora_bgmv_fold_kernel<2, true>, a, stream);
-      case 4: return launch_fold(lora_bgmv_fold_kernel<4, true>, a, stream);
+      case 1: return launch_fold(lora_bgmv_fold_kernel<1, true, false>, a, stream);
+      case 2: return launch_fold(lora_bgmv_fold_kernel<2, true, false>, a, stream);
+      case 4: return launch_fold(lora_bgmv_fold_kernel<4, true, false>, a, stream);
       default: return static_cast<int>(cudaErrorInvalidValue);
     }
   }
   switch (a.g.maxt) {
-    case 1: return launch_fold(lora_bgmv_fold_kernel<1, false>, a, stream);
-    case 2: return launch_fold(lora_bgmv_fold_kernel<2, false>, a, stream);
-    case 4: return launch_fold(lora_bgmv_fold_kernel<4, false>, a, stream);
+    case 1: return launch_fold(lora_bgmv_fold_kernel<1, false, false>, a, stream);
+    case 2: return launch_fold(lora_bgmv_fold_kernel<2, false, false>, a, stream);
+    case 4: return launch_fold(lora_bgmv_fold_kernel<4, false, false>, a, stream);
     default: return static_cast<int>(cudaErrorInvalidValue);
   }
 }

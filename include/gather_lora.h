@@ -288,10 +288,11 @@ int lora_read_device_status(void* stream, uint32_t* status_out, int clear);
  * (adapters x experts). Add 16 to `moe` for the geometry of a call given
  * a_tmaps. Writes [cluster,
  * rows_per_tile, k_slice, j_slice, k_chunk, j_chunk, ring_stages, clusters,
- * smem_bytes, a_tiled (1 when A is loaded through the tensor maps)] to out[0..9].
+ * smem_bytes, a_tiled (1 when A is loaded through the tensor maps), tc (1 when the shrink
+ * runs on the tcgen05 tensor cores)] to out[0..10].
  */
 int lora_launch_geometry(int moe, int32_t rows, int32_t max_loras, int32_t max_rank,
-                         int32_t k_in, int32_t n_out, int64_t out[10]);
+                         int32_t k_in, int32_t n_out, int64_t out[11]);
 
 /* ---- pure host helpers (no GPU) ------------------------------------------ */
 

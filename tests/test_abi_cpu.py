@@ -298,3 +298,12 @@ def test_delta_geometry():
         assert L.lora_delta_geometry(4096, r, 4096, 4096, 152)["dense"] == 0
     m = re.search(r"#define LORA_DELTA_DENSE_MIN_ROWS (\d+)", open(HEADER).read())
     assert m and int(m.group(1)) == L.DELTA_DENSE_MIN_ROWS
+
+
+def test_tcgen05_shrink_geometry():
+    """The bgmv shrink moves to tcgen05 only with A tensor maps at max_rank 128 (units of 16 rows)."""
+    assert L.lora_launch_geometry(16, 512, 64, 128, 12288, 4096)["tc"] == 1
+    assert L.lora_launch_geometry(0, 512, 64, 128, 12288, 4096)["tc"] == 0     # no maps
+    assert L.lora_launch_geometry(16, 256, 128, 64, 4096, 1024)["tc"] == 0     # rank 64
+    assert L.lora_launch_geometry(17, 4096, 16, 128, 768, 2048)["tc"] == 0     # grouped MoE
+    assert L.lora_launch_geometry(18, 512, 2048, 128, 768, 2048)["tc"] == 1    # decode gather fold

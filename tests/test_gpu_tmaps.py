@@ -1,9 +1,11 @@
 """A loaded as 2-D TMA boxes (lora_encode_a_tmaps + a_tmaps) on the GPU (-m gpu).
 
-The maps change only how A reaches shared memory (64-column boxes with the
-128-byte swizzle instead of one copy per row), not the arithmetic: every fold
-must give the same bits with and without them, and match the CPU oracle on
-random shapes.
+The maps change how A reaches shared memory (64-column boxes with the 128-byte
+swizzle instead of one copy per row). Where the shrink stays on mma.sync the
+arithmetic is unchanged and the fold must give the same bits with and without
+them; at max_rank 128 with units of at most 16 rows the shrink moves to the
+tcgen05 tensor cores (another fp32 summation order), and every result must
+match the CPU oracle.
 """
 from __future__ import annotations
 
@@ -45,9 +47,10 @@ def test_bgmv_maps_give_the_same_bits(name):
         assert g == L.lora_launch_geometry(0, wl.n, wl.max_loras, wl.max_rank, wl.k_in, wl.n_out)
     o1, x1 = _bgmv_run(wl)
     o2, x2 = _bgmv_run(wl, maps=True)
-    assert np.array_equal(o1, o2)
-    routed = [i for i in range(wl.n) if 0 <= wl.seq_slot[i] < wl.max_loras and wl.present[wl.seq_slot[i]]]
-    assert np.array_equal(x1[routed], x2[routed])
+    if not g["tc"]:     # same arithmetic, other loads: the same bits
+        assert np.array_equal(o1, o2)
+        routed = [i for i in range(wl.n) if 0 <= wl.seq_slot[i] < wl.max_loras and wl.present[wl.seq_slot[i]]]
+        assert np.array_equal(x1[routed], x2[routed])
     o_out, o_xa, o_d = oracle_bgmv(wl)
     compare_bgmv(wl, o2, o_out, x2, o_xa, o_d)
     assert L.lora_read_device_status(clear=True) == 0
@@ -100,7 +103,7 @@ def test_moe_maps_give_the_same_bits(name):
     assert L.lora_read_device_status(clear=True) == 0
 
 
-@pytest.mark.parametrize("max_rank", [16, 64])
+@pytest.mark.parametrize("max_rank", [16, 64, 128])
 def test_gather_maps_give_the_same_bits(max_rank):
     wl = W.make_moe_gather("tmg", num_tokens=64, top_k=8, num_experts=128, k_in=768, n_out=2048,
                            max_loras=16, max_rank=max_rank, rank=max_rank, alpha=32.0,
@@ -115,6 +118,9 @@ def test_gather_maps_give_the_same_bits(max_rank):
                                a_tmaps=m)
         torch.cuda.synchronize()
         res.append((to_u16(d.out_buf), to_u16(d.xa)[: wl.n_rows]))
-    assert np.array_equal(res[0][0], res[1][0])
+    g = L.lora_launch_geometry(18, wl.n_rows, wl.max_loras * wl.num_experts, wl.max_rank, wl.k_in, wl.n_out)
+    assert g["tc"] == (1 if max_rank == 128 else 0)
+    if not g["tc"]:
+        assert np.array_equal(res[0][0], res[1][0])
     o_out, o_xa, o_d = oracle_gather(wl)
     compare_gather(wl, res[1][0], o_out, res[1][1], o_xa, o_d, gather_routes(wl))
