@@ -71,6 +71,11 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 constexpr int kBudgetTwoPerSm = GLORA_BUDGET_TWO_PER_SM;
 constexpr int kBudgetOnePerSm = 225 * 1024;
 constexpr int kStageTarget = GLORA_STAGE_TARGET;
+#ifndef GLORA_CLUSTER_CAP_HIGH_RANK
+#define GLORA_CLUSTER_CAP_HIGH_RANK 4
+#endif
+constexpr int kClusterCapRank = 64;
+constexpr int kClusterCapHighRank = GLORA_CLUSTER_CAP_HIGH_RANK;
 // MoE groups are small and many: larger items (a whole k_in of 768 in one shrink
 // item, which also lets each consumer warp own whole groups) measured 7% faster
 // on the MoE down fold; the bgmv folds measured best at kStageTarget.
@@ -95,6 +100,12 @@ bool make_geometry_at(bool moe, int rows, int max_loras, int planner_ints, int m
   g = glora::FoldGeometry{};
   // bgmv: a cluster splits each unit's k (shrink) and n_out (expand); MoE units
   // are many and small, so one CTA folds whole groups.
+  // Clusters of at most 4 from max_rank 64 up: per k-slice a CTA then moves
+  // more adapter bytes per fixed cost (planning, exchange). Measured on GB300:
+  // qkv (rank 64) 33.5 -> 28.4 us and ffn (rank 128) 69.4 -> 63.4 us at 4
+  // instead of 8, decode (rank 16) 10.2 -> 12.3 us. The cap depends on the
+  // shapes only (a row's k-split never depends on the batch).
+  if (max_rank >= kClusterCapRank) max_cl = std::min(max_cl, kClusterCapHighRank);
   g.cl = moe ? 1 : pow2_floor(std::min(max_cl, std::max(1, std::max(k_in, n_out) / 512)));
   g.mr16 = round_up(max_rank, 16);
   const int mt = g.mr16 / 16;
