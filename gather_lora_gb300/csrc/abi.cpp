@@ -53,6 +53,15 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 #ifndef GLORA_MOE_STAGE_TARGET
 #define GLORA_MOE_STAGE_TARGET (56 * 1024)
 #endif
+#ifndef GLORA_UNIT_ROWS
+#define GLORA_UNIT_ROWS 16
+#endif
+#ifndef GLORA_GATHER_UNIT_ROWS
+#define GLORA_GATHER_UNIT_ROWS 8
+#endif
+#ifndef GLORA_GATHER_MAX_CL
+#define GLORA_GATHER_MAX_CL 1
+#endif
 #ifndef GLORA_TC_SHRINK
 #define GLORA_TC_SHRINK 1
 #endif
@@ -75,6 +84,11 @@ constexpr int kStageTarget = GLORA_STAGE_TARGET;
 #define GLORA_CLUSTER_CAP_HIGH_RANK 4
 #endif
 constexpr int kClusterCapRank = 64;
+// Rows per bgmv work unit. Measured on GB300 against 32 (rank <= 64) and 8:
+// decode q_proj 10.2 -> 8.5 us, qkv 28.3 -> 25.1 us at 16; the decode gather
+// fold, whose table entries hold about one row each, 27.9 -> 22.8 us at 8.
+constexpr int kUnitRows = GLORA_UNIT_ROWS;
+constexpr int kGatherUnitRows = GLORA_GATHER_UNIT_ROWS;
 constexpr int kClusterCapHighRank = GLORA_CLUSTER_CAP_HIGH_RANK;
 // MoE groups are small and many: larger items (a whole k_in of 768 in one shrink
 // item, which also lets each consumer warp own whole groups) measured 7% faster
@@ -96,7 +110,7 @@ int balanced_chunk(int total, int cap) {
 // window), so a row's arithmetic — the k-slices, k-chunks and summation order —
 // is the same in every call with the same (k_in, n_out, max_rank).
 bool make_geometry_at(bool moe, int rows, int max_loras, int planner_ints, int max_rank, int k_in,
-                      int n_out, glora::FoldGeometry& g, int max_cl, bool a_tiled, int target) {
+                      int n_out, glora::FoldGeometry& g, int max_cl, bool a_tiled, int target, int unit_rows) {
   g = glora::FoldGeometry{};
   // bgmv: a cluster splits each unit's k (shrink) and n_out (expand); MoE units
   // are many and small, so one CTA folds whole groups.
@@ -114,7 +128,7 @@ bool make_geometry_at(bool moe, int rows, int max_loras, int planner_ints, int m
     g.rt = LORA_MOE_M_TILE;
     g.gmax = std::min(std::min(GLORA_MOE_GROUP_ROWS, 32), tile_rows_cap);
   } else {
-    g.rt = max_rank <= 64 ? 32 : 16;
+    g.rt = unit_rows;
     g.gmax = std::min(g.rt, tile_rows_cap);
   }
   g.ksl = round_up(static_cast<int>(ceil_div(k_in, g.cl)), 16);
@@ -202,13 +216,14 @@ bool make_geometry_at(bool moe, int rows, int max_loras, int planner_ints, int m
 // MoE takes the larger stage target when its geometry still fits two CTAs per
 // SM (the gate/up form at k_in 2048 would drop to one and measured slower).
 bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_rank, int k_in,
-                   int n_out, glora::FoldGeometry& g, int max_cl = GLORA_MAX_CLUSTER, bool a_tiled = false) {
+                   int n_out, glora::FoldGeometry& g, int max_cl = GLORA_MAX_CLUSTER, bool a_tiled = false,
+                   int unit_rows = kUnitRows) {
   if (moe && make_geometry_at(moe, rows, max_loras, planner_ints, max_rank, k_in, n_out, g, max_cl, a_tiled,
-                              kMoeStageTarget) &&
+                              kMoeStageTarget, unit_rows) &&
       g.smem_bytes <= kBudgetTwoPerSm)
     return true;
   return make_geometry_at(moe, rows, max_loras, planner_ints, max_rank, k_in, n_out, g, max_cl, a_tiled,
-                          kStageTarget);
+                          kStageTarget, unit_rows);
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once (NULL without a driver).
@@ -230,10 +245,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
 // (16 rows of 128 bytes) made decode-sized folds about 5% slower than one copy
 // per 512-byte row, while at ranks 64 and 128 they made the folds 6-11% faster.
 bool fold_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_rank, int k_in, int n_out,
-                   glora::FoldGeometry& g, int max_cl, const void* a_tmaps) {
-  if (a_tmaps && max_rank >= LORA_TMAP_MIN_RANK && make_geometry(moe, rows, max_loras, planner_ints, max_rank, k_in, n_out, g, max_cl, true))
+                   glora::FoldGeometry& g, int max_cl, const void* a_tmaps, int unit_rows = kUnitRows) {
+  if (a_tmaps && max_rank >= LORA_TMAP_MIN_RANK &&
+      make_geometry(moe, rows, max_loras, planner_ints, max_rank, k_in, n_out, g, max_cl, true, unit_rows))
     return true;
-  return make_geometry(moe, rows, max_loras, planner_ints, max_rank, k_in, n_out, g, max_cl, false);
+  return make_geometry(moe, rows, max_loras, planner_ints, max_rank, k_in, n_out, g, max_cl, false, unit_rows);
 }
 
 int check_shape(int32_t max_rank, int32_t k_in, int32_t n_out, int64_t xs, int64_t os) {
@@ -440,7 +456,8 @@ int lora_moe_gather_bgmv(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_t
   // each: one CTA per unit (no cluster split) keeps the grid near one wave.
   if (a_tmaps && (reinterpret_cast<uintptr_t>(a_tmaps) & 63u))
     return fail(LORA_ERR_ALIGN, "a_tmaps must be 64-byte aligned");
-  if (!fold_geometry(false, n_rows, tables, ((n_rows + 3) & ~3) + tables, max_rank, k_in, n_out, a.g, 1, a_tmaps))
+  if (!fold_geometry(false, n_rows, tables, ((n_rows + 3) & ~3) + tables, max_rank, k_in, n_out, a.g, GLORA_GATHER_MAX_CL, a_tmaps,
+                     kGatherUnitRows))
     return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory for max_rank %d, k_in %d, n_out %d", max_rank, k_in, n_out);
   a.x = x;
   a.x_stride = x_row_stride;
@@ -578,7 +595,8 @@ int lora_launch_geometry(int moe, int32_t rows, int32_t max_loras, int32_t max_r
   // stands for a tensor-map array (only its presence matters); the grouped fold ignores maps
   static const char kAnyMaps = 0;
   if (!fold_geometry(grouped, rows, max_loras, scratch, max_rank, k_in, n_out, g,
-                     kind == 2 ? 1 : GLORA_MAX_CLUSTER, (moe & 16) && !grouped ? &kAnyMaps : nullptr))
+                     kind == 2 ? GLORA_GATHER_MAX_CL : GLORA_MAX_CLUSTER, (moe & 16) && !grouped ? &kAnyMaps : nullptr,
+                     kind == 2 ? kGatherUnitRows : kUnitRows))
     return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory");
   const int64_t v[11] = {g.cl, g.rt, g.ksl, g.jsl, g.kch, g.jch, g.ns, g.clusters, g.smem_bytes, g.a_tiled, g.tc};
   std::memcpy(out, v, sizeof v);

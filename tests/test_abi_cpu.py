@@ -225,7 +225,7 @@ def test_bgmv_grid_bounds_every_routing():
 
 def test_gather_geometry_has_no_cluster_split():
     g = L.lora_launch_geometry(2, 512, 2048, 16, 768, 2048)
-    assert g["cluster"] == 1 and g["clusters"] == 512 // 32 + 512
+    assert g["cluster"] == 1 and g["clusters"] == 512 // 8 + 512 and g["rows_per_tile"] == 8
     assert L.lora_launch_geometry(0, 512, 2048, 16, 768, 2048)["cluster"] == 4
 
 
@@ -306,4 +306,4 @@ def test_tcgen05_shrink_geometry():
     assert L.lora_launch_geometry(0, 512, 64, 128, 12288, 4096)["tc"] == 0     # no maps
     assert L.lora_launch_geometry(16, 256, 128, 64, 4096, 1024)["tc"] == 0     # rank 64
     assert L.lora_launch_geometry(17, 4096, 16, 128, 768, 2048)["tc"] == 0     # grouped MoE
-    assert L.lora_launch_geometry(18, 512, 2048, 128, 768, 2048)["tc"] == 1    # decode gather fold
+    assert L.lora_launch_geometry(18, 512, 2048, 128, 768, 2048)["tc"] == 0    # gather units: 8 rows

@@ -119,7 +119,6 @@ def test_gather_maps_give_the_same_bits(max_rank):
         torch.cuda.synchronize()
         res.append((to_u16(d.out_buf), to_u16(d.xa)[: wl.n_rows]))
     g = L.lora_launch_geometry(18, wl.n_rows, wl.max_loras * wl.num_experts, wl.max_rank, wl.k_in, wl.n_out)
-    assert g["tc"] == (1 if max_rank == 128 else 0)
     if not g["tc"]:
         assert np.array_equal(res[0][0], res[1][0])
     o_out, o_xa, o_d = oracle_gather(wl)
