@@ -62,6 +62,9 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 #ifndef GLORA_GATHER_MAX_CL
 #define GLORA_GATHER_MAX_CL 1
 #endif
+#ifndef GLORA_TMAP_MIN_RANK
+#define GLORA_TMAP_MIN_RANK LORA_TMAP_MIN_RANK
+#endif
 #ifndef GLORA_TC_SHRINK
 #define GLORA_TC_SHRINK 1
 #endif
@@ -246,7 +249,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
 // per 512-byte row, while at ranks 64 and 128 they made the folds 6-11% faster.
 bool fold_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_rank, int k_in, int n_out,
                    glora::FoldGeometry& g, int max_cl, const void* a_tmaps, int unit_rows = kUnitRows) {
-  if (a_tmaps && max_rank >= LORA_TMAP_MIN_RANK &&
+  if (a_tmaps && max_rank >= GLORA_TMAP_MIN_RANK &&
       make_geometry(moe, rows, max_loras, planner_ints, max_rank, k_in, n_out, g, max_cl, true, unit_rows))
     return true;
   return make_geometry(moe, rows, max_loras, planner_ints, max_rank, k_in, n_out, g, max_cl, false, unit_rows);
