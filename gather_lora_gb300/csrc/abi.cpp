@@ -92,6 +92,9 @@ constexpr int kClusterCapRank = 64;
 // fold, whose table entries hold about one row each, 27.9 -> 22.8 us at 8.
 constexpr int kUnitRows = GLORA_UNIT_ROWS;
 constexpr int kGatherUnitRows = GLORA_GATHER_UNIT_ROWS;
+static_assert(kUnitRows <= glora::kMaxGroupRows && kGatherUnitRows <= glora::kMaxGroupRows &&
+                  GLORA_MOE_GROUP_ROWS <= glora::kMaxGroupRows,
+              "groups wider than the kernels' row tiles (kMaxGroupRows)");
 constexpr int kClusterCapHighRank = GLORA_CLUSTER_CAP_HIGH_RANK;
 // MoE groups are small and many: larger items (a whole k_in of 768 in one shrink
 // item, which also lets each consumer warp own whole groups) measured 7% faster
@@ -129,7 +132,7 @@ bool make_geometry_at(bool moe, int rows, int max_loras, int planner_ints, int m
   const int tile_rows_cap = 8 * (glora::kMaxTilesPerWarp * glora::kConsumerWarps / mt);
   if (moe) {
     g.rt = LORA_MOE_M_TILE;
-    g.gmax = std::min(std::min(GLORA_MOE_GROUP_ROWS, 32), tile_rows_cap);
+    g.gmax = std::min(std::min(GLORA_MOE_GROUP_ROWS, glora::kMaxGroupRows), tile_rows_cap);
   } else {
     g.rt = unit_rows;
     g.gmax = std::min(g.rt, tile_rows_cap);

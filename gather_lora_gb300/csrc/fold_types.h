@@ -5,6 +5,7 @@
 
 namespace glora {
 
+constexpr int kMaxGroupRows = 16;  // rows of one group (one adapter's rows folded together)
 constexpr int kMaxRows = 64;        // rows (positions) per pass of a work unit
 constexpr int kMaxTileRows = 256;   // sorted rows one MoE work unit scans
 constexpr int kMaxTilesPerWarp = 4; // 16x8 shrink tiles a warp may own: MT * NT <= 32

@@ -541,19 +541,20 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
     // last one), and for rows gq + 8 * hh the offset of the staged old values
     // inside a stage (rows past R read the last row, in bounds) and the output
     // row (NULL past R).
-    uint32_t a_row[2], rowoff[4];
-    uint16_t* obase[4];
+    constexpr int kRT = (kMaxGroupRows + 15) / 16;   // 16-row tiles of a group
+    uint32_t a_row[kRT], rowoff[2 * kRT];
+    uint16_t* obase[2 * kRT];
 #pragma unroll
-    for (int mr = 0; mr < 2; ++mr) a_row[mr] = xa_base + pl.members[m0 + min(mr * 16 + (lane & 15), R - 1)] * g.pitch_xa;
+    for (int mr = 0; mr < kRT; ++mr) a_row[mr] = xa_base + pl.members[m0 + min(mr * 16 + (lane & 15), R - 1)] * g.pitch_xa;
 #pragma unroll
-    for (int hh = 0; hh < 4; ++hh) {
+    for (int hh = 0; hh < 2 * kRT; ++hh) {
       const int r = hh * 8 + gq;
       rowoff[hh] = out_region + min(r, R - 1) * pitch_o + 4 * q;
       obase[hh] = r < R ? p.out + (long long)pl.grow[pl.members[m0 + r]] * p.out_stride + scol : nullptr;
     }
-    // The group's expand items, compiled per row-tile count MR (1, 2) and per
-    // KS, the k16 steps whose xa fragments stay in registers (1: max_rank 16,
-    // 2: max_rank 32; 0: any max_rank, fragments loaded per step, k8 tail).
+    // The group's expand items, compiled per row-tile count MR (up to kRT) and
+    // per KS, the k16 steps whose xa fragments stay in registers (1: max_rank
+    // 16, 2: max_rank 32; 0: any max_rank, fragments loaded per step, k8 tail).
     auto items = [&](auto mr_c, auto ks_c) {
       constexpr int MR = decltype(mr_c)::value, KS = decltype(ks_c)::value;
       uint32_t af[MR][KS > 0 ? KS : 1][4];
@@ -640,9 +641,16 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
     using I1 = std::integral_constant<int, 1>;
     using I2 = std::integral_constant<int, 2>;
     using I0 = std::integral_constant<int, 0>;
-    if (p.max_rank == 16) { if (R <= 16) items(I1{}, I1{}); else items(I2{}, I1{}); }
-    else if (p.max_rank == 32) { if (R <= 16) items(I1{}, I2{}); else items(I2{}, I2{}); }
-    else { if (R <= 16) items(I1{}, I0{}); else items(I2{}, I0{}); }
+    auto by_rank = [&](auto mr_c) {
+      if (p.max_rank == 16) items(mr_c, I1{});
+      else if (p.max_rank == 32) items(mr_c, I2{});
+      else items(mr_c, I0{});
+    };
+    if constexpr (kRT > 1) {
+      if (R <= 16) by_rank(I1{}); else by_rank(I2{});
+    } else {
+      by_rank(I1{});
+    }
   }
   return n_items;
 }
