@@ -342,13 +342,10 @@ __global__ void __launch_bounds__(kDenseThreads, 1) lora_dense_fold_kernel(const
 }
 
 int launch_dense(const DenseArgs& a, void* stream) {
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(lora_dense_fold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               227 * 1024);
-    if (e != cudaSuccess) return static_cast<int>(e);
-    configured = true;
-  }
+  // (set on every call: the attribute belongs to the current device, like the launch)
+  const cudaError_t set = cudaFuncSetAttribute(lora_dense_fold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               a.smem_bytes);
+  if (set != cudaSuccess) return static_cast<int>(set);
   const int tiles = (a.m + kDenseRows - 1) / kDenseRows;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(tiles * a.cl), 1, 1);
