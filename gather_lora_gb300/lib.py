@@ -186,11 +186,11 @@ def lora_read_device_status(stream=None, clear=True) -> int:
 
 
 GEOMETRY_KEYS = ("cluster", "rows_per_tile", "k_slice", "j_slice", "k_chunk", "j_chunk",
-                 "ring_stages", "clusters", "smem_bytes", "a_tiled", "tc")
+                 "ring_stages", "clusters", "smem_bytes", "a_tiled", "tc", "direct")
 
 
 def lora_launch_geometry(moe, rows, max_loras, max_rank, k_in, n_out) -> dict:
-    out = (ctypes.c_int64 * 11)()
+    out = (ctypes.c_int64 * 12)()
     _check(load().lora_launch_geometry(int(moe), rows, max_loras, max_rank, k_in, n_out, out))
     return dict(zip(GEOMETRY_KEYS, list(out)))
 

@@ -307,3 +307,15 @@ def test_tcgen05_shrink_geometry():
     assert L.lora_launch_geometry(16, 256, 128, 64, 4096, 1024)["tc"] == 0     # rank 64
     assert L.lora_launch_geometry(17, 4096, 16, 128, 768, 2048)["tc"] == 0     # grouped MoE
     assert L.lora_launch_geometry(18, 512, 2048, 128, 768, 2048)["tc"] == 0    # gather units: 8 rows
+
+
+def test_unit_numbering_rule():
+    """Direct numbering unless the grid is more than one wave of CTAs and the slots
+    are many for the rows (152 SMs without a device)."""
+    assert L.lora_launch_geometry(0, 64, 32, 16, 4096, 4096)["direct"] == 1      # one wave
+    assert L.lora_launch_geometry(16, 512, 64, 128, 12288, 4096)["direct"] == 1  # few slots per row
+    assert L.lora_launch_geometry(16, 256, 128, 64, 4096, 1024)["direct"] == 0   # many sparse slots
+    assert L.lora_launch_geometry(0, 16, 128, 16, 4096, 4096)["direct"] == 0     # more slots than rows
+    for args in [(0, 64, 32, 16, 4096, 4096), (16, 256, 128, 64, 4096, 1024)]:
+        g = L.lora_launch_geometry(*args)
+        assert g["clusters"] == args[1] // g["rows_per_tile"] + min(args[1], args[2])
