@@ -57,7 +57,9 @@ def measured_peaks():
 def kernel_source_digest() -> str:
     h = hashlib.sha256()
     for rel in ("gather_lora_gb300/csrc/kernels.cu", "gather_lora_gb300/csrc/common.cuh",
-                "gather_lora_gb300/csrc/fold_types.h", "gather_lora_gb300/csrc/abi.cpp"):
+                "gather_lora_gb300/csrc/fold_types.h", "gather_lora_gb300/csrc/abi.cpp",
+                "gather_lora_gb300/csrc/dense.cu", "gather_lora_gb300/csrc/dense_types.h",
+                "gather_lora_gb300/csrc/tc05.cuh"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
