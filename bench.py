@@ -15,8 +15,8 @@ a device synchronize; with several ranks the time is the max over ranks.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
---impl reference times the CPU oracle (the reference arm of this comparison)
-on the host cores for the same workload and metric.
+--impl reference times the CPU oracle (the reference arm of this comparison),
+unchanged, on all host cores (disjoint rows per thread) for the same workload and metric.
 """
 from __future__ import annotations
 
@@ -504,31 +504,76 @@ def e2e_bgmv(wl, device, steps, warmup, copies):
 
 
 # ------------------------------------------------------------ CPU oracle
-def oracle_rows_per_s(wl, budget_s: float, rows_per_call=None):
-    """Time the single-threaded oracle on the host over a bounded sample of the
-    batch's rows; returns (rows/s, rows timed, seconds)."""
-    import numpy as np
+def host_threads() -> int:
+    """Host cores this process may run on."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def oracle_fold(wl, idx) -> None:
+    """Fold the batch rows `idx` with the oracle, into a copy of their out rows."""
     import oracle
-    rows_per_call = rows_per_call or wl.n
+    out = wl.out_buf[idx].copy()
+    seg = out.reshape(-1)[wl.out_offset:]
+    oracle.lora_bgmv(wl.x[idx].reshape(-1), wl.x_row_stride, seg, wl.out_row_stride,
+                     wl.seq_slot[idx], wl.a_list(), wl.b_list(), wl.scale, wl.max_rank,
+                     wl.k_in, wl.n_out)
+
+
+def oracle_rows_per_s(wl, budget_s: float, rows_per_call=None, threads: int = 1):
+    """Time the oracle on the host over a bounded sample of the batch's rows.
+
+    Each of `threads` host threads folds its own rotating rows, rows_per_call
+    at a time, until budget_s has passed (the oracle is a C call that releases
+    the interpreter lock, so the threads run in parallel; the oracle itself is
+    unchanged). Returns (rows/s over all threads, rows timed, seconds)."""
+    import threading
+    import numpy as np
+    rows_per_call = rows_per_call or max(1, wl.n // threads)
+    done = [0] * threads
     t0 = time.perf_counter()
-    done = 0
-    i0 = 0
-    while True:
-        idx = np.arange(i0, i0 + rows_per_call) % wl.n
-        out = wl.out_buf[idx].copy()
-        seg = out.reshape(-1)[wl.out_offset:]
-        oracle.lora_bgmv(wl.x[idx].reshape(-1), wl.x_row_stride, seg, wl.out_row_stride,
-                         wl.seq_slot[idx], wl.a_list(), wl.b_list(), wl.scale, wl.max_rank,
-                         wl.k_in, wl.n_out)
-        done += rows_per_call
-        i0 = (i0 + rows_per_call) % wl.n
-        el = time.perf_counter() - t0
-        if el >= budget_s:
-            return done / el, done, el
+
+    def work(t):
+        i0 = (t * rows_per_call) % wl.n
+        while True:
+            oracle_fold(wl, np.arange(i0, i0 + rows_per_call) % wl.n)
+            done[t] += rows_per_call
+            i0 = (i0 + threads * rows_per_call) % wl.n
+            if time.perf_counter() - t0 >= budget_s:
+                return
+
+    if threads == 1:
+        work(0)
+    else:
+        pool = [threading.Thread(target=work, args=(t,)) for t in range(threads)]
+        for th in pool:
+            th.start()
+        for th in pool:
+            th.join()
+    el = time.perf_counter() - t0
+    return sum(done) / el, sum(done), el
+
+
+def cpu_baseline(wl, seconds: float) -> dict:
+    """The oracle on all host cores (rows partitioned over threads), with its
+    one-thread figure beside it; `seconds` of wall time in all."""
+    threads = host_threads()
+    v1, n1, s1 = oracle_rows_per_s(wl, seconds / 2)
+    vt, nt, st = oracle_rows_per_s(wl, seconds / 2, threads=threads)
+    return {"value": vt, "unit": "rows/s", "cores": threads, "kind": "oracle",
+            "sample": f"{nt} decode rows of the {HEADLINE} batch, {threads} host threads on "
+                      f"disjoint rows ({st:.1f} s)",
+            "single_thread": {"value": v1, "cores": 1,
+                              "sample": f"{n1} decode rows, 1 host thread ({s1:.1f} s)"}}
 
 
 def run_reference(args):
-    """CPU oracle arm: same workload, metric and unit, on the host cores."""
+    """CPU oracle arm: same workload, metric and unit, on the host cores (each
+    step's rows partitioned over all host threads)."""
+    from concurrent.futures import ThreadPoolExecutor
+    import numpy as np
     dctx = DistCtx()
     if dctx.rank != 0:
         dctx.close()
@@ -537,19 +582,31 @@ def run_reference(args):
     import oracle
     wl = W.by_name(HEADLINE)
     oracle.load()
-    # calibrate: seconds per row
+    threads = host_threads()
+    # calibrate: seconds per row on one thread
     _, n_cal, s_cal = oracle_rows_per_s(wl, 0.5, rows_per_call=4)
     t_row = s_cal / n_cal
     budget = 150.0
-    rows_per_step = int(max(1, min(wl.n, budget / max(args.steps + args.warmup, 1) / t_row)))
-    for _ in range(args.warmup):
-        oracle_rows_per_s(wl, 0.0, rows_per_call=rows_per_step)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle_rows_per_s(wl, 0.0, rows_per_call=rows_per_step)
-    el = time.perf_counter() - t0
+    rows_per_step = int(max(min(threads, wl.n),
+                            min(wl.n, budget * threads / max(args.steps + args.warmup, 1) / t_row)))
+    chunks = [c for c in np.array_split(np.arange(rows_per_step), min(threads, rows_per_step)) if c.size]
+    state = {"i0": 0}
+
+    def step(ex):
+        i0 = state["i0"]
+        list(ex.map(lambda c: oracle_fold(wl, (c + i0) % wl.n), chunks))
+        state["i0"] = (i0 + rows_per_step) % wl.n
+
+    with ThreadPoolExecutor(len(chunks)) as ex:
+        for _ in range(args.warmup):
+            step(ex)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            step(ex)
+        el = time.perf_counter() - t0
     value = rows_per_step * args.steps / el
-    sample = f"{rows_per_step} of the {wl.n} decode rows per step (rotating), oracle on 1 host thread"
+    sample = (f"{rows_per_step} of the {wl.n} decode rows per step (rotating), split over "
+              f"{len(chunks)} host threads")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -557,7 +614,7 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": HEADLINE, "n": wl.n, "k_in": wl.k_in, "n_out": wl.n_out,
                    "max_loras": wl.max_loras, "max_rank": wl.max_rank},
-        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": len(chunks), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -645,9 +702,7 @@ def run_ours(args):
 
     cpu = None
     if dctx.rank == 0 and not args.no_cpu_baseline and head_kind == "bgmv":
-        v, n_rows, secs = oracle_rows_per_s(wl, args.cpu_seconds)
-        cpu = {"value": v, "unit": "rows/s", "cores": 1, "kind": "oracle",
-               "sample": f"{n_rows} decode rows of the {HEADLINE} batch ({secs:.1f} s, 1 host thread)"}
+        cpu = cpu_baseline(wl, args.cpu_seconds)
 
     if dctx.rank == 0:
         line = {
