@@ -1,0 +1,51 @@
+"""The CPU arms of bench.py: `--impl reference` and the threaded oracle baseline.
+
+Both time the unchanged oracle on host threads that fold disjoint rows. This
+checks, without a GPU, that the reference arm prints one JSON line with the
+contract's keys, and that the threaded timing returns rows from every thread.
+"""
+from __future__ import annotations
+
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+
+def test_reference_arm_prints_contract_line():
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "4", "--warmup", "3"], capture_output=True, text=True,
+                       timeout=600, env=env, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config"):
+        assert key in d, key
+    assert d["steps"] == 4 and d["warmup"] == 3 and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["unit"] == "rows/s"
+    cpu = d["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["value"] == d["value"] and cpu["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": "rows/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"] == "decode_qproj_bgmv"
+
+
+def test_threaded_oracle_baseline_counts_every_thread():
+    import bench
+    import oracle
+    from gather_lora_gb300 import workloads as W
+    oracle.load()
+    wl = W.by_name(bench.HEADLINE)
+    rows_per_s, rows, secs = bench.oracle_rows_per_s(wl, 0.0, rows_per_call=2, threads=3)
+    # a zero budget still lets each thread fold one call's rows
+    assert rows == 3 * 2 and secs > 0 and rows_per_s > 0
+    base = bench.cpu_baseline(wl, 0.0)
+    assert base["cores"] == bench.host_threads() and base["kind"] == "oracle"
+    assert base["single_thread"]["cores"] == 1 and base["single_thread"]["value"] > 0
