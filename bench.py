@@ -3,9 +3,11 @@
 
 Headline workload: the decode q_proj routed bgmv (64 decode rows, k_in = n_out
 = 4096, 32 adapters at max_rank 16, Zipf(1.1) slots with 10% base rows). A step
-is one lora_bgmv call over one batch. The other three fold workloads (strided K
-fold into an interleaved QKV row, dense FFN down_proj, MoE grouped down fold)
-are measured the same way and reported under "workloads".
+is one lora_bgmv call over one batch. The other fold workloads (strided K fold
+into an interleaved QKV row, dense FFN down_proj, the MoE grouped down and
+gate/up folds in windows of 4096 sorted rows and as one call over all rows, the
+decode-path MoE gather fold, single-adapter prefill deltas) are measured the
+same way and reported under "workloads".
 
 Timing: inputs are resident in HBM; consecutive steps rotate through enough
 independent copies of every input (adapter pools included) to exceed 2x the L2
@@ -37,6 +39,7 @@ if ROOT not in sys.path:
 METRIC = "routed LoRA fold rows/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 HEADLINE = "decode_qproj_bgmv"
 SIDE_WORKLOADS = ("qkv_kfold_bgmv", "ffn_down_bgmv", "moe_down_fold", "moe_gateup_fold",
+                  "moe_down_fold_one_launch", "moe_gateup_fold_one_launch",
                   "moe_decode_gather", "prefill_qproj_delta", "prefill_down_delta")
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_NAMES = {"bgmv": "lora_bgmv_fold_kernel", "moe": "lora_moe_fold_kernel",

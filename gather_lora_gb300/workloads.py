@@ -25,7 +25,7 @@ fp32 samples, done by torch's CPU conversion).
 from __future__ import annotations
 
 import math
-from dataclasses import dataclass, field
+from dataclasses import dataclass, field, replace
 
 import numpy as np
 import torch
@@ -452,7 +452,15 @@ def prefill_down_delta(seed=8):
                       alpha=64.0, rslora=True, seed=seed, x_law="silu_gate")
 
 
+def one_launch(wl: MoeWorkload) -> MoeWorkload:
+    """The same MoE problem folded by one call over all te sorted rows: one
+    window of cap = te, so the xa output holds every row."""
+    return replace(wl, name=wl.name + "_one_launch", cap=wl.te)
+
+
 def by_name(name: str, seed=None):
+    if name.endswith("_one_launch"):
+        return one_launch(by_name(name[: -len("_one_launch")], seed))
     fn = {"tiny_bgmv": tiny_bgmv, "decode_qproj_bgmv": decode_qproj_bgmv,
           "qkv_kfold_bgmv": qkv_kfold_bgmv, "ffn_down_bgmv": ffn_down_bgmv,
           "moe_down_fold": moe_down_fold, "moe_gateup_fold": moe_gateup_fold,

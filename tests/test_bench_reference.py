@@ -49,3 +49,21 @@ def test_threaded_oracle_baseline_counts_every_thread():
     base = bench.cpu_baseline(wl, 0.0)
     assert base["cores"] == bench.host_threads() and base["kind"] == "oracle"
     assert base["single_thread"]["cores"] == 1 and base["single_thread"]["value"] > 0
+
+
+def test_one_launch_moe_workload_is_the_same_problem():
+    import numpy as np
+    import bench
+    from gather_lora_gb300 import workloads as W
+    a = W.by_name("moe_down_fold")
+    b = W.by_name("moe_down_fold_one_launch")
+    assert b.name == "moe_down_fold_one_launch" and b.cap == b.te == a.te
+    assert b.windows() == [(0, a.te)] and len(a.windows()) == 4
+    for f in ("x", "out_buf", "expert_offsets", "sorted_token_ids", "row_adapter", "present",
+              "a_pool", "b_pool", "scale"):
+        assert np.array_equal(getattr(a, f), getattr(b, f)), f
+    ba, bb = bench.algorithmic_bytes(a), bench.algorithmic_bytes(b)
+    # same routed rows; an (adapter, expert) pair split by a window boundary is counted once
+    assert ba["routed_rows"] == bb["routed_rows"] and bb["adapters"] <= ba["adapters"]
+    assert bb["bytes"] < ba["bytes"]
+    assert "moe_down_fold_one_launch" in bench.SIDE_WORKLOADS
