@@ -536,16 +536,20 @@ def oracle_rows_per_s(wl, budget_s: float, rows_per_call=None, threads: int = 1)
     import numpy as np
     rows_per_call = rows_per_call or max(1, wl.n // threads)
     done = [0] * threads
+    errors = []
     t0 = time.perf_counter()
 
     def work(t):
-        i0 = (t * rows_per_call) % wl.n
-        while True:
-            oracle_fold(wl, np.arange(i0, i0 + rows_per_call) % wl.n)
-            done[t] += rows_per_call
-            i0 = (i0 + threads * rows_per_call) % wl.n
-            if time.perf_counter() - t0 >= budget_s:
-                return
+        try:
+            i0 = (t * rows_per_call) % wl.n
+            while True:
+                oracle_fold(wl, np.arange(i0, i0 + rows_per_call) % wl.n)
+                done[t] += rows_per_call
+                i0 = (i0 + threads * rows_per_call) % wl.n
+                if time.perf_counter() - t0 >= budget_s:
+                    return
+        except BaseException as e:   # re-raised below: a failed thread must not shorten the count silently
+            errors.append(e)
 
     if threads == 1:
         work(0)
@@ -555,6 +559,8 @@ def oracle_rows_per_s(wl, budget_s: float, rows_per_call=None, threads: int = 1)
             th.start()
         for th in pool:
             th.join()
+    if errors:
+        raise errors[0]
     el = time.perf_counter() - t0
     return sum(done) / el, sum(done), el
 

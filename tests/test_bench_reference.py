@@ -67,3 +67,17 @@ def test_one_launch_moe_workload_is_the_same_problem():
     assert ba["routed_rows"] == bb["routed_rows"] and bb["adapters"] <= ba["adapters"]
     assert bb["bytes"] < ba["bytes"]
     assert "moe_down_fold_one_launch" in bench.SIDE_WORKLOADS
+
+
+def test_threaded_oracle_baseline_propagates_a_thread_failure(monkeypatch):
+    import pytest
+    import bench
+    from gather_lora_gb300 import workloads as W
+    wl = W.by_name("tiny_bgmv")
+
+    def boom(wl, idx):
+        raise RuntimeError("oracle call failed")
+
+    monkeypatch.setattr(bench, "oracle_fold", boom)
+    with pytest.raises(RuntimeError, match="oracle call failed"):
+        bench.oracle_rows_per_s(wl, 0.0, rows_per_call=1, threads=2)
