@@ -43,6 +43,24 @@ MUTANTS = {
                          "uint16_t* out_row = base_out + (int64_t)row * n_out;"),
     "delta_x_stride": ("const uint16_t* x_row = x + (int64_t)row * x_row_stride;",
                        "const uint16_t* x_row = x + (int64_t)row * k_in;"),
+    "xa_truncated": ("            xa_row[c] = ora_bf16_of_f32(acc);",
+                     "            { uint32_t u; memcpy(&u, &acc, sizeof u); xa_row[c] = (uint16_t)(u >> 16); }"),
+    "delta_truncated": ("            d = ora_bf16_of_f32(acc);",
+                        "            { uint32_t u; memcpy(&u, &acc, sizeof u); d = (uint16_t)(u >> 16); }"),
+    "fold_rounds_twice": ("float folded = fmaf(scale, ora_f32_of_bf16(d), ora_f32_of_bf16(orow[j]));",
+                          "float folded = ora_f32_of_bf16(ora_bf16_of_f32(scale * ora_f32_of_bf16(d)))"
+                          " + ora_f32_of_bf16(orow[j]);"),
+    "last_rank_dropped": ("for (int32_t c = 0; c < max_rank; ++c)\n                acc = acc + ora_f32_of_bf16(xa_row[c])",
+                          "for (int32_t c = 0; c < max_rank - 1; ++c)\n                acc = acc + ora_f32_of_bf16(xa_row[c])"),
+    "window_first_row_skipped": ("for (int32_t r = row_offset; r < row_end; ++r) {",
+                                 "for (int32_t r = row_offset + 1; r < row_end; ++r) {"),
+    "moe_adapter_gate_ignored": ("int32_t a = row_adapter ? row_adapter[t] : 0;\n        if (a < 0 || a >= max_loras) continue;\n        int64_t ti",
+                                 "int32_t a = 0;\n        if (a < 0 || a >= max_loras) continue;\n        int64_t ti"),
+    "moe_d_at_window_row": ("uint16_t* d_row = d_out ? d_out + (int64_t)r * n_out : NULL;\n        const int64_t xr",
+                            "uint16_t* d_row = d_out ? d_out + local * n_out : NULL;\n        const int64_t xr"),
+    "gather_expert_zero_skipped": ("if (e < 0 || e >= num_experts) continue;",
+                                   "if (e < 1 || e >= num_experts) continue;"),
+    "gather_last_token_skipped": ("if (t >= num_tokens) continue;", "if (t >= num_tokens - 1) continue;"),
     "last_k_dropped": ("for (int32_t k = 0; k < k_in; ++k)\n                acc = acc + ora_f32_of_bf16(xrow[k])",
                        "for (int32_t k = 0; k < k_in - 1; ++k)\n                acc = acc + ora_f32_of_bf16(xrow[k])"),
 }

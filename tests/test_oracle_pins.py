@@ -311,6 +311,28 @@ def test_moe_full_window_equals_sub_windows():
     assert np.array_equal(np.concatenate(xas), xa_full)
 
 
+def test_moe_delta_rows_are_sorted_rows_in_every_window():
+    """The d output of a window sits at the sorted row index r (as base_out
+    does), so each window's d equals the full call's d on its rows and is zero
+    elsewhere; xa alone is window-local."""
+    wl = _small_moe()
+
+    def run_d(lo, hi):
+        out = wl.out_buf.copy()
+        _, d = oracle.lora_moe_grouped_fold(
+            wl.x, wl.k_in, out, wl.n_out, wl.expert_offsets, wl.sorted_token_ids, wl.row_adapter,
+            wl.num_tokens, lo, hi, wl.a_list(), wl.b_list(), wl.scale, wl.max_rank, wl.k_in,
+            wl.n_out)
+        return d
+
+    d_full = run_d(0, wl.te)
+    assert d_full.any()
+    for lo, hi in [(0, 17), (17, 40), (40, wl.te)]:
+        d = run_d(lo, hi)
+        assert np.array_equal(d[lo:hi], d_full[lo:hi])
+        assert not d[:lo].any() and not d[hi:].any()
+
+
 def test_moe_group_equals_bgmv_on_same_rows():
     """The fold of the rows of one (adapter, expert) group equals the bgmv of the
     same rows with that adapter in slot 0."""
