@@ -157,10 +157,14 @@ int lora_bgmv(const lora_bf16_t* x, int64_t x_row_stride,
  *   xa                optional [row_end - row_offset, max_rank] BF16 shrink output at the
  *                     LOCAL row r - row_offset (routed rows only); NULL skips it
  * The window must satisfy 0 <= row_offset <= row_end <= te. The launch grid is
- * ceil((row_end - row_offset) / LORA_MOE_M_TILE) tiles (at least 1) times the
- * adapters (max_loras with a row_adapter, else 1); each CTA folds the rows of
+ * ceil((row_end - row_offset) / T) tiles of T sorted rows (at least 1) times the
+ * adapters (max_loras with a row_adapter, else 1), T in {64, 128, 256} the
+ * largest that still gives 128 such units (64 otherwise), so the grid depends
+ * only on the window size and the adapter count; each CTA folds the rows of
  * one adapter in one tile. Calls over windows [0, cap), [cap, 2cap), ... give
- * the same result as one call over [0, te).
+ * the same base_out as one call over [0, te). The fold never reads xa back, so
+ * a caller whose xa holds all te rows, or who passes NULL, can make that one
+ * call: it also spares the wait of each window for the previous one's last CTA.
  */
 int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, int32_t x_gather,
                           lora_bf16_t* base_out, int64_t out_row_stride,
