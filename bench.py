@@ -27,6 +27,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -57,14 +58,23 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def code_only(text: str) -> str:
+    """C/C++/CUDA source without its comments, trailing blanks and blank lines."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip())
+
+
 def kernel_source_digest() -> str:
+    """Digest of the kernel and launcher code (comments excluded: they do not
+    change what runs), which keys the recorded ncu counters."""
     h = hashlib.sha256()
     for rel in ("gather_lora_gb300/csrc/kernels.cu", "gather_lora_gb300/csrc/common.cuh",
                 "gather_lora_gb300/csrc/fold_types.h", "gather_lora_gb300/csrc/abi.cpp",
                 "gather_lora_gb300/csrc/dense.cu", "gather_lora_gb300/csrc/dense_types.h",
                 "gather_lora_gb300/csrc/tc05.cuh"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
