@@ -7,21 +7,26 @@
 // per token by moe_row_adapter.
 //
 // GB300 design (one launch per call, no global scratch):
-//   * A cluster of `cl` CTAs owns one WORK UNIT: up to 64 rows split into
-//     groups that share one adapter (bgmv: rows of one slot; MoE: the
-//     (adapter, expert) groups of a 64-row tile of sorted rows). Every CTA of
-//     the cluster builds the same plan from the routing data.
-//   * A producer warpgroup per CTA streams the unit's data with 1-D TMA bulk
-//     copies into a ring of shared-memory stages (full / empty mbarriers);
-//     each item's copies are spread over its four warps, because the request
-//     rate of one issuing warp, not HBM, limits small copies:
-//     first [group, k-chunk] items (A rows of this CTA's k-slice and the
-//     group's x rows), then [group, j-chunk] items (B rows of this CTA's
-//     j-slice and the matching out-row segments).
-//   * Eight consumer warps contract each shrink item on the tensor cores
-//     (mma.sync BF16, fp32 accumulate). The fp32 partials of the cl k-slices
-//     are reduced in distributed shared memory in rank order (reduce-scatter),
-//     rounded to BF16 once, and the BF16 xa is pushed to every CTA.
+//   * A cluster of `cl` CTAs owns one WORK UNIT: bgmv, up to 16 rows of one
+//     slot (8 for the decode gather fold); MoE, the rows of one adapter in a
+//     tile of 64-256 sorted rows, folded in passes and split into groups of
+//     one expert. CTA c of the cluster takes k-slice c of the shrink and
+//     j-slice c of the expand; every CTA builds the same plan from the routing
+//     data.
+//   * A producer warpgroup per CTA streams the unit's data into a ring of
+//     shared-memory stages (full / empty mbarriers): rows by 1-D TMA bulk
+//     copies (16-byte cp.async below kTmaRowBytes), A as 2-D swizzled TMA
+//     boxes when tensor maps are given. Each item's copies are spread over
+//     the four warps, because the request rate of one issuing warp, not HBM,
+//     limits small copies: first [group, k-chunk] items (A of this CTA's
+//     k-slice and the group's x rows), then [group, j-chunk] items (B rows of
+//     this CTA's j-slice and the matching out-row segments).
+//   * Eight consumer warps contract each shrink item on the tensor cores:
+//     mma.sync BF16 with fp32 accumulation, or (A boxes of 128 rows, units of
+//     at most 16 rows) one tcgen05.mma per k-step into TMEM. The fp32
+//     partials of the cl k-slices are combined in distributed shared memory
+//     in rank order (an all-gather when they are small, else a reduce-scatter
+//     whose BF16 result is pushed to every CTA) and rounded to BF16 once.
 //   * For each expand item the consumers compute d = bf16(xa @ B^T), fold
 //     out = bf16(fma(scale, d, out)) against the staged out segment in
 //     registers, and store the result straight to global memory (the stage is
@@ -522,7 +527,8 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
   // ---- expand + fold over this CTA's j-slice ---------------------------------
   // Work comes in 16-column blocks of two 16x8 tensor-core tiles (16 group rows
   // x 8 consecutive output columns each), with the xa rows as the A operand:
-  // their fragments are loaded once per item (max_rank <= 32). Lane (g, q)
+  // their fragments are loaded once per group at max_rank 16 and 32, per
+  // block at other ranks. Lane (g, q)
   // holds columns 2q, 2q+1 of each tile for rows g and g + 8; it folds them
   // with the staged old values in registers, and one exchange with lane q ^ 1
   // leaves it four adjacent columns, so each row leaves as one full 32-byte
