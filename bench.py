@@ -602,26 +602,35 @@ def run_reference(args):
     wl = W.by_name(HEADLINE)
     oracle.load()
     threads = host_threads()
-    # calibrate: seconds per row on one thread
-    _, n_cal, s_cal = oracle_rows_per_s(wl, 0.5, rows_per_call=4)
-    t_row = s_cal / n_cal
-    budget = 150.0
-    rows_per_step = int(max(min(threads, wl.n),
-                            min(wl.n, budget * threads / max(args.steps + args.warmup, 1) / t_row)))
-    chunks = [c for c in np.array_split(np.arange(rows_per_step), min(threads, rows_per_step)) if c.size]
     state = {"i0": 0}
 
-    def step(ex):
+    def split(rows):
+        return [c for c in np.array_split(np.arange(rows), min(threads, rows)) if c.size]
+
+    def step(ex, chunks, rows):
         i0 = state["i0"]
         list(ex.map(lambda c: oracle_fold(wl, (c + i0) % wl.n), chunks))
-        state["i0"] = (i0 + rows_per_step) % wl.n
+        state["i0"] = (i0 + rows) % wl.n
 
-    with ThreadPoolExecutor(len(chunks)) as ex:
+    with ThreadPoolExecutor(threads) as ex:
+        # calibrate on parallel steps of the whole batch: seconds per row as the
+        # threads actually share it (the second of two steps; the first starts them)
+        cal = split(wl.n)
+        for _ in range(2):
+            t0 = time.perf_counter()
+            step(ex, cal, wl.n)
+            t_row = (time.perf_counter() - t0) / wl.n
+        # rows per step: all warm-up and timed steps within about `budget` seconds,
+        # at least one row per thread
+        budget = 150.0
+        rows_per_step = int(max(min(threads, wl.n),
+                                min(wl.n, budget / max(args.steps + args.warmup, 1) / t_row)))
+        chunks = split(rows_per_step)
         for _ in range(args.warmup):
-            step(ex)
+            step(ex, chunks, rows_per_step)
         t0 = time.perf_counter()
         for _ in range(args.steps):
-            step(ex)
+            step(ex, chunks, rows_per_step)
         el = time.perf_counter() - t0
     value = rows_per_step * args.steps / el
     sample = (f"{rows_per_step} of the {wl.n} decode rows per step (rotating), split over "
