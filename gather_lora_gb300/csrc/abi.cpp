@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -224,7 +225,9 @@ bool make_geometry_at(bool moe, int rows, int max_loras, int planner_ints, int m
     g.tile_rows = LORA_MOE_M_TILE;
     for (int tr = glora::kMaxTileRows; tr > LORA_MOE_M_TILE; tr /= 2)
       if (ceil_div(rows, tr) * max_loras >= kMoeMinUnits) { g.tile_rows = tr; break; }
-    g.clusters = static_cast<int>(std::max(1LL, ceil_div(rows, g.tile_rows)) * max_loras);
+    const long long clusters = std::max(1LL, ceil_div(rows, g.tile_rows)) * max_loras;
+    if (clusters * g.cl > INT_MAX) return false;   // the grid would not fit a launch
+    g.clusters = static_cast<int>(clusters);
   } else {
     g.tile_rows = g.rt;
     // Direct numbering (unit s = tile 0 of slot s) plans fastest, but its empty
@@ -429,7 +432,9 @@ int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, int32_t x_
   // row by row and does not use tensor maps.)
   if (!make_geometry(true, row_end - row_offset, row_adapter ? max_loras : 1, num_experts + 1, max_rank, k_in,
                      n_out, a.g))
-    return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory for max_rank %d, k_in %d, n_out %d", max_rank, k_in, n_out);
+    return fail(LORA_ERR_SIZE, "no launch geometry for a window of %d rows x %d adapters at max_rank %d, k_in %d, "
+                "n_out %d (shared memory or grid size)", row_end - row_offset, row_adapter ? max_loras : 1, max_rank,
+                k_in, n_out);
   a.x = x;
   a.x_stride = x_row_stride;
   a.out = base_out;
@@ -623,7 +628,7 @@ int lora_launch_geometry(int moe, int32_t rows, int32_t max_loras, int32_t max_r
   if (!fold_geometry(grouped, rows, max_loras, scratch, max_rank, k_in, n_out, g,
                      kind == 2 ? GLORA_GATHER_MAX_CL : GLORA_MAX_CLUSTER, (moe & 16) && !grouped ? &kAnyMaps : nullptr,
                      kind == 2 ? kGatherUnitRows : kUnitRows))
-    return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory");
+    return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory and the grid size");
   const int64_t v[12] = {g.cl, g.rt, g.ksl, g.jsl, g.kch, g.jch, g.ns, g.clusters, g.smem_bytes, g.a_tiled, g.tc, g.direct};
   std::memcpy(out, v, sizeof v);
   return ok();

@@ -98,6 +98,18 @@ def test_moe_rejects_bad_arguments_before_launch(kw, code):
     assert _moe(**kw) == code
 
 
+def test_moe_grid_that_overflows_a_launch_is_rejected():
+    """A window whose tiles x adapters grid would not fit one launch is refused
+    with an error (not folded partially or skipped)."""
+    big = 2 ** 31 - 1
+    assert _moe(te=big, lo=0, hi=big, L=4096, xa=None) == -2
+    assert "grid size" in L.lora_last_error()
+    with pytest.raises(L.LoraError, match="grid size"):
+        L.lora_launch_geometry(1, big, 4096, 16, 768, 2048)
+    # the same window with 16 adapters still fits: 2^23 tiles of 256 rows x 16
+    assert L.lora_launch_geometry(1, big, 16, 16, 768, 2048)["clusters"] == (2 ** 23) * 16
+
+
 def _gather(**kw):
     a = dict(x=FAKE, xs=768, out=FAKE, os=2048, idx=FAKE, n=512, k=8, ra=FAKE, nt=64, E=128,
              at=FAKE, bt=FAKE, sc=FAKE, L=16, R=16, kin=768, no=2048, xa=FAKE, maps=None)
