@@ -156,7 +156,9 @@ int lora_bgmv(const lora_bf16_t* x, int64_t x_row_stride,
  *                     maps would not reduce much (checked for 64-byte alignment)
  *   xa                optional [row_end - row_offset, max_rank] BF16 shrink output at the
  *                     LOCAL row r - row_offset (routed rows only); NULL skips it
- * The window must satisfy 0 <= row_offset <= row_end <= te. The launch grid is
+ * The window must satisfy 0 <= row_offset <= row_end <= te (else LORA_ERR_WINDOW);
+ * a window whose grid (below) would exceed one launch's 2^31 - 1 CTAs gives
+ * LORA_ERR_SIZE and launches nothing. The launch grid is
  * ceil((row_end - row_offset) / T) tiles of T sorted rows (at least 1) times the
  * adapters (max_loras with a row_adapter, else 1), T in {64, 128, 256} the
  * largest that still gives 128 such units (64 otherwise), so the grid depends
