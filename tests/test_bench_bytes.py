@@ -81,3 +81,12 @@ def test_delta_bytes():
                          np.zeros((N, R), np.uint16), np.float32(1.0))
     got = bench.algorithmic_bytes(wl)
     assert got["bytes"] == 3 * 96 + (R * K * 2 + N * R * 2) == 672
+
+
+def test_counter_digest_follows_code_not_comments():
+    src = 'int f(int a) {  // add one\n  /* block\n     comment */ return a + 1;\n}\n'
+    assert bench.code_only(src) == bench.code_only(src.replace("add one", "increment"))
+    assert bench.code_only(src) == bench.code_only(src.replace("block", "other text"))
+    assert bench.code_only(src) != bench.code_only(src.replace("a + 1", "a + 2"))
+    assert "//" not in bench.code_only(src) and "/*" not in bench.code_only(src)
+    assert len(bench.kernel_source_digest()) == 16
