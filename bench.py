@@ -1,13 +1,14 @@
 #!/usr/bin/env python3
 """Benchmark of the routed LoRA fold on GB300 (one JSON line on stdout).
 
-Headline workload: the decode q_proj routed bgmv (64 decode rows, k_in = n_out
-= 4096, 32 adapters at max_rank 16, Zipf(1.1) slots with 10% base rows). A step
-is one lora_bgmv call over one batch. The other fold workloads (strided K fold
-into an interleaved QKV row, dense FFN down_proj, the MoE grouped down and
-gate/up folds in windows of 4096 sorted rows and as one call over all rows, the
-decode-path MoE gather fold, single-adapter prefill deltas) are measured the
-same way and reported under "workloads".
+Headline workload: the MoE grouped down fold (2048 tokens x top-8 of 128
+experts = 16384 expert-sorted rows, k_in 768, n_out 2048, 16 adapters x 128
+experts at max_rank 16, 20% of tokens without an adapter), folded in its four
+windows of 4096 sorted rows: a step is the four lora_moe_grouped_fold calls over
+one batch. The other fold workloads (decode q_proj, strided K fold into an
+interleaved QKV row, dense FFN down_proj, the MoE gate/up form, both MoE folds
+as one call over all rows, the decode-path MoE gather fold, single-adapter
+prefill deltas) are measured the same way and reported under "workloads".
 
 Timing: inputs are resident in HBM; consecutive steps rotate through enough
 independent copies of every input (adapter pools included) to exceed 2x the L2
@@ -18,7 +19,8 @@ a device synchronize; with several ranks the time is the max over ranks.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 --impl reference times the CPU oracle (the reference arm of this comparison),
-unchanged, on all host cores (disjoint rows per thread) for the same workload and metric.
+unchanged, on all host cores (disjoint rows per thread) for the same workload,
+metric, unit and config.
 """
 from __future__ import annotations
 
@@ -38,8 +40,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "routed LoRA fold rows/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
-HEADLINE = "decode_qproj_bgmv"
-SIDE_WORKLOADS = ("qkv_kfold_bgmv", "ffn_down_bgmv", "moe_down_fold", "moe_gateup_fold",
+HEADLINE = "moe_down_fold"
+SIDE_WORKLOADS = ("decode_qproj_bgmv", "qkv_kfold_bgmv", "ffn_down_bgmv", "moe_gateup_fold",
                   "moe_down_fold_one_launch", "moe_gateup_fold_one_launch",
                   "moe_decode_gather", "prefill_qproj_delta", "prefill_down_delta")
 FALLBACK_HBM_GBS = 6800.0
@@ -308,7 +310,6 @@ class MoeRunner:
         self.wl = wl
         self.windows = wl.windows()
         self.copies = [W.moe_to_device(wl, device, xa_rows=wl.cap) for _ in range(copies)]
-        self.maps = [a_maps_for(d.a_table, wl.max_rank, wl.k_in) for d in self.copies]
         self.launches_per_step = len(self.windows)
 
     def bytes_per_copy(self):
@@ -323,7 +324,7 @@ class MoeRunner:
                                     wl.num_experts, d.sorted_token_ids, wl.te, d.row_adapter,
                                     wl.num_tokens, lo, hi, d.a_table, d.b_table, d.scale,
                                     wl.max_loras, wl.max_rank, wl.k_in, wl.n_out, xa=d.xa,
-                                    stream=stream, x_gather=wl.x_gather, a_tmaps=self.maps[c])
+                                    stream=stream, x_gather=wl.x_gather)
 
 
 class GatherRunner:
@@ -473,30 +474,62 @@ def aggregate(rows_per_rank: float, ms_max: float, steps: int, n_ranks: int):
 
 
 # --------------------------------------------------------------- e2e
-def e2e_bgmv(wl, device, steps, warmup, copies):
-    """Same metric through the C ABI with host buffers: every step copies x,
-    seq_slot and base_out from pinned host memory, calls lora_bgmv, and reads
-    base_out back into pinned host memory; all inside the timed region."""
+def _pinned(a):
     import numpy as np
+    import torch
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).pin_memory()
+
+
+def e2e_run(wl, device, steps, warmup, copies):
+    """The headline metric through the C ABI with host buffers. Every step copies
+    the step's inputs from pinned host memory (bgmv: x, seq_slot, base_out; MoE:
+    x, expert_offsets, sorted_token_ids, row_adapter, base_out), makes the fold's
+    calls (MoE: one per window), and reads base_out back into pinned host memory,
+    all inside the timed region. Returns (rows/s, H2D bytes, D2H bytes) per step."""
     import torch
     from gather_lora_gb300 import lib as L
     from gather_lora_gb300 import workloads as W
-    devs = [W.bgmv_to_device(wl, device) for _ in range(copies)]
-    maps = [a_maps_for(d.a_table, wl.max_rank, wl.k_in) for d in devs]
-    hx = torch.from_numpy(wl.x.view(np.int16)).pin_memory()
-    hseq = torch.from_numpy(wl.seq_slot).pin_memory()
-    hout = torch.from_numpy(wl.out_buf.view(np.int16)).pin_memory()
-    hres = torch.empty_like(hout).pin_memory()
+    kind = workload_kind(wl)
     stream = torch.cuda.Stream(device=device)
+    if kind == "bgmv":
+        devs = [W.bgmv_to_device(wl, device) for _ in range(copies)]
+        maps = [a_maps_for(d.a_table, wl.max_rank, wl.k_in) for d in devs]
+        pairs = lambda d: [(d.x, _pinned(wl.x)), (d.seq_slot, _pinned(wl.seq_slot)),
+                           (d.out_buf, _pinned(wl.out_buf))]
 
-    def one(c):
-        d = devs[c % copies]
-        d.x.copy_(hx, non_blocking=True)
-        d.seq_slot.copy_(hseq, non_blocking=True)
-        d.out_buf.copy_(hout, non_blocking=True)
-        L.lora_bgmv(d.x, wl.x_row_stride, d.out_ptr, wl.out_row_stride, d.seq_slot, wl.n,
-                    d.a_table, d.b_table, d.scale, wl.max_loras, wl.max_rank, wl.k_in, wl.n_out,
-                    xa=d.xa, stream=stream, a_tmaps=maps[c % copies])
+        def call(c, d):
+            L.lora_bgmv(d.x, wl.x_row_stride, d.out_ptr, wl.out_row_stride, d.seq_slot, wl.n,
+                        d.a_table, d.b_table, d.scale, wl.max_loras, wl.max_rank, wl.k_in, wl.n_out,
+                        xa=d.xa, stream=stream, a_tmaps=maps[c])
+        rows = wl.n
+    elif kind == "moe":
+        devs = [W.moe_to_device(wl, device, xa_rows=wl.cap) for _ in range(copies)]
+        pairs = lambda d: [(d.x, _pinned(wl.x)), (d.expert_offsets, _pinned(wl.expert_offsets)),
+                           (d.sorted_token_ids, _pinned(wl.sorted_token_ids)),
+                           (d.row_adapter, _pinned(wl.row_adapter)), (d.out_buf, _pinned(wl.out_buf))]
+
+        def call(c, d):
+            for lo, hi in wl.windows():
+                L.lora_moe_grouped_fold(d.x, wl.k_in, d.out_buf, wl.n_out, d.expert_offsets,
+                                        wl.num_experts, d.sorted_token_ids, wl.te, d.row_adapter,
+                                        wl.num_tokens, lo, hi, d.a_table, d.b_table, d.scale,
+                                        wl.max_loras, wl.max_rank, wl.k_in, wl.n_out, xa=d.xa,
+                                        stream=stream, x_gather=wl.x_gather)
+        rows = wl.te
+    else:
+        raise ValueError(f"no end-to-end run for {kind}")
+    host = [pairs(d) for d in devs]
+    hres = _pinned(wl.out_buf).clone().pin_memory()
+
+    def one(i):
+        c = i % copies
+        d = devs[c]
+        for dst, src in host[c]:
+            dst.copy_(src, non_blocking=True)
+        call(c, d)
         hres.copy_(d.out_buf, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -511,9 +544,9 @@ def e2e_bgmv(wl, device, steps, warmup, copies):
         end.record(stream)
     torch.cuda.synchronize(device)
     ms = start.elapsed_time(end)
-    h2d = hx.numel() * 2 + hseq.numel() * 4 + hout.numel() * 2
-    d2h = hres.numel() * 2
-    return wl.n * steps / (ms / 1e3), h2d, d2h
+    h2d = sum(src.numel() * src.element_size() for _, src in host[0])
+    d2h = hres.numel() * hres.element_size()
+    return rows * steps / (ms / 1e3), h2d, d2h
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -523,6 +556,25 @@ def host_threads() -> int:
         return max(1, len(os.sched_getaffinity(0)))
     except AttributeError:
         return max(1, os.cpu_count() or 1)
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the baseline line."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
 
 
 def oracle_fold(wl, idx) -> None:
@@ -535,27 +587,62 @@ def oracle_fold(wl, idx) -> None:
                      wl.k_in, wl.n_out)
 
 
+def oracle_fold_moe(wl, lo: int, hi: int) -> None:
+    """Fold sorted rows [lo, hi) of an MoE workload with the oracle, into a copy of
+    their out rows. The rows are handed over as the same problem on fewer rows:
+    their x (or, for gate/up, the token-major x itself) and out rows, their token
+    ids, and the expert offsets shifted by lo and clipped to [0, hi - lo], so every
+    row keeps its expert, token and adapter."""
+    import numpy as np
+    import oracle
+    offs = np.clip(wl.expert_offsets.astype(np.int64) - lo, 0, hi - lo).astype(np.int32)
+    out = wl.out_buf[lo:hi].copy()
+    x = wl.x if wl.x_gather else wl.x[lo:hi]
+    oracle.lora_moe_grouped_fold(x, wl.k_in, out, wl.n_out, offs, wl.sorted_token_ids[lo:hi],
+                                 wl.row_adapter, wl.num_tokens, 0, hi - lo, wl.a_list(), wl.b_list(),
+                                 wl.scale, wl.max_rank, wl.k_in, wl.n_out, x_gather=wl.x_gather)
+
+
+def oracle_total_rows(wl) -> int:
+    return int(wl.te) if workload_kind(wl) == "moe" else int(wl.n)
+
+
+def oracle_fold_rows(wl, start: int, count: int) -> None:
+    """Fold `count` consecutive rows of the workload from `start` (wrapping)."""
+    import numpy as np
+    total = oracle_total_rows(wl)
+    if workload_kind(wl) == "moe":
+        lo = start % total
+        hi = min(total, lo + count)
+        oracle_fold_moe(wl, lo, hi)
+        if lo + count > total:
+            oracle_fold_moe(wl, 0, lo + count - total)
+    else:
+        oracle_fold(wl, np.arange(start, start + count) % total)
+
+
 def oracle_rows_per_s(wl, budget_s: float, rows_per_call=None, threads: int = 1):
-    """Time the oracle on the host over a bounded sample of the batch's rows.
+    """Time the oracle on the host over a bounded sample of the workload's rows.
 
     Each of `threads` host threads folds its own rotating rows, rows_per_call
     at a time, until budget_s has passed (the oracle is a C call that releases
     the interpreter lock, so the threads run in parallel; the oracle itself is
     unchanged). Returns (rows/s over all threads, rows timed, seconds)."""
     import threading
-    import numpy as np
-    rows_per_call = rows_per_call or max(1, wl.n // threads)
+    total = oracle_total_rows(wl)
+    default = 256 if workload_kind(wl) == "moe" else max(1, total // threads)
+    rows_per_call = rows_per_call or default
     done = [0] * threads
     errors = []
     t0 = time.perf_counter()
 
     def work(t):
         try:
-            i0 = (t * rows_per_call) % wl.n
+            i0 = (t * rows_per_call) % total
             while True:
-                oracle_fold(wl, np.arange(i0, i0 + rows_per_call) % wl.n)
+                oracle_fold_rows(wl, i0, rows_per_call)
                 done[t] += rows_per_call
-                i0 = (i0 + threads * rows_per_call) % wl.n
+                i0 = (i0 + threads * rows_per_call) % total
                 if time.perf_counter() - t0 >= budget_s:
                     return
         except BaseException as e:   # re-raised below: a failed thread must not shorten the count silently
@@ -575,6 +662,10 @@ def oracle_rows_per_s(wl, budget_s: float, rows_per_call=None, threads: int = 1)
     return sum(done) / el, sum(done), el
 
 
+def _rows_word(wl) -> str:
+    return "expert-sorted rows" if workload_kind(wl) == "moe" else "decode rows"
+
+
 def cpu_baseline(wl, seconds: float) -> dict:
     """The oracle on all host cores (rows partitioned over threads), with its
     one-thread figure beside it; `seconds` of wall time in all."""
@@ -582,15 +673,29 @@ def cpu_baseline(wl, seconds: float) -> dict:
     v1, n1, s1 = oracle_rows_per_s(wl, seconds / 2)
     vt, nt, st = oracle_rows_per_s(wl, seconds / 2, threads=threads)
     return {"value": vt, "unit": "rows/s", "cores": threads, "kind": "oracle",
-            "sample": f"{nt} decode rows of the {HEADLINE} batch, {threads} host threads on "
+            "cpu_model": cpu_model(),
+            "sample": f"{nt} {_rows_word(wl)} of the {wl.name} batch, {threads} host threads on "
                       f"disjoint rows ({st:.1f} s)",
             "single_thread": {"value": v1, "cores": 1,
-                              "sample": f"{n1} decode rows, 1 host thread ({s1:.1f} s)"}}
+                              "sample": f"{n1} {_rows_word(wl)}, 1 host thread ({s1:.1f} s)"}}
+
+
+def workload_config(wl, alg) -> dict:
+    """The `config` object of the JSON line: the workload and its shapes (both arms)."""
+    kind = workload_kind(wl)
+    cfg = {"workload": wl.name, "rows": alg["rows"], "routed_rows": alg["routed_rows"],
+           "k_in": wl.k_in, "n_out": wl.n_out, "max_loras": getattr(wl, "max_loras", 1),
+           "max_rank": wl.max_rank, "distinct_adapters": alg["adapters"]}
+    if kind == "moe":
+        cfg.update(num_experts=wl.num_experts, num_tokens=wl.num_tokens, te=wl.te,
+                   windows=len(wl.windows()), window_rows=wl.cap, x_gather=bool(wl.x_gather))
+    cfg["l2"] = "inputs rotate through device copies totalling more than 2x L2 between steps"
+    return cfg
 
 
 def run_reference(args):
-    """CPU oracle arm: same workload, metric and unit, on the host cores (each
-    step's rows partitioned over all host threads)."""
+    """CPU oracle arm: same workload, metric, unit and config, on the host cores
+    (each step's rows partitioned over all host threads)."""
     from concurrent.futures import ThreadPoolExecutor
     import numpy as np
     dctx = DistCtx()
@@ -602,29 +707,32 @@ def run_reference(args):
     wl = W.by_name(HEADLINE)
     oracle.load()
     threads = host_threads()
+    total = oracle_total_rows(wl)
     state = {"i0": 0}
 
     def split(rows):
-        return [c for c in np.array_split(np.arange(rows), min(threads, rows)) if c.size]
+        per = max(1, -(-rows // threads))
+        return [(o, min(per, rows - o)) for o in range(0, rows, per)]
 
     def step(ex, chunks, rows):
         i0 = state["i0"]
-        list(ex.map(lambda c: oracle_fold(wl, (c + i0) % wl.n), chunks))
-        state["i0"] = (i0 + rows) % wl.n
+        list(ex.map(lambda c: oracle_fold_rows(wl, i0 + c[0], c[1]), chunks))
+        state["i0"] = (i0 + rows) % total
 
     with ThreadPoolExecutor(threads) as ex:
-        # calibrate on parallel steps of the whole batch: seconds per row as the
+        # calibrate on parallel steps of a part of the batch: seconds per row as the
         # threads actually share it (the second of two steps; the first starts them)
-        cal = split(wl.n)
+        cal_rows = min(total, 64 * threads)
+        cal = split(cal_rows)
         for _ in range(2):
             t0 = time.perf_counter()
-            step(ex, cal, wl.n)
-            t_row = (time.perf_counter() - t0) / wl.n
+            step(ex, cal, cal_rows)
+            t_row = (time.perf_counter() - t0) / cal_rows
         # rows per step: all warm-up and timed steps within about `budget` seconds,
         # at least one row per thread
         budget = 150.0
-        rows_per_step = int(max(min(threads, wl.n),
-                                min(wl.n, budget / max(args.steps + args.warmup, 1) / t_row)))
+        rows_per_step = int(max(min(threads, total),
+                                min(total, budget / max(args.steps + args.warmup, 1) / t_row)))
         chunks = split(rows_per_step)
         for _ in range(args.warmup):
             step(ex, chunks, rows_per_step)
@@ -633,17 +741,17 @@ def run_reference(args):
             step(ex, chunks, rows_per_step)
         el = time.perf_counter() - t0
     value = rows_per_step * args.steps / el
-    sample = (f"{rows_per_step} of the {wl.n} decode rows per step (rotating), split over "
+    sample = (f"{rows_per_step} of the {total} {_rows_word(wl)} per step (rotating), split over "
               f"{len(chunks)} host threads")
+    alg = algorithmic_bytes(wl)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": HEADLINE, "n": wl.n, "k_in": wl.k_in, "n_out": wl.n_out,
-                   "max_loras": wl.max_loras, "max_rank": wl.max_rank},
+        "config": workload_config(wl, alg),
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": len(chunks), "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -652,6 +760,20 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------- main
+def geometry_of(L, wl):
+    kind = workload_kind(wl)
+    if kind == "moe":
+        return L.lora_launch_geometry(1, wl.cap, wl.max_loras if wl.row_adapter is not None else 1,
+                                      wl.max_rank, wl.k_in, wl.n_out)
+    if kind == "delta":
+        return L.lora_delta_geometry(wl.m, wl.max_rank, wl.k_in, wl.n_out)
+    if kind == "gather":
+        return L.lora_launch_geometry(18 if USE_TMAPS else 2, wl.n_rows, wl.max_loras * wl.num_experts,
+                                      wl.max_rank, wl.k_in, wl.n_out)
+    return L.lora_launch_geometry(16 if USE_TMAPS else 0, wl.n, wl.max_loras, wl.max_rank,
+                                  wl.k_in, wl.n_out)
+
+
 def run_ours(args):
     import torch
     from gather_lora_gb300 import lib as L
@@ -668,7 +790,6 @@ def run_ours(args):
     head = args.only or HEADLINE
     wl = W.by_name(head)
     head_kind = workload_kind(wl)
-    head_moe = head_kind == "moe"
     alg = algorithmic_bytes(wl)
     mk = RUNNERS[head_kind]
     probe = mk(wl, 1, device)
@@ -683,17 +804,7 @@ def run_ours(args):
     achieved = bytes_per_launch / (kernel_ms / 1e3) / 1e9
     clocks = sampler.summary() if sampler else None
     launches = args.steps * runner.launches_per_step
-    if head_moe:
-        geometry = L.lora_launch_geometry(1, wl.cap, wl.max_loras if wl.row_adapter is not None else 1,
-                                          wl.max_rank, wl.k_in, wl.n_out)
-    elif head_kind == "delta":
-        geometry = L.lora_delta_geometry(wl.m, wl.max_rank, wl.k_in, wl.n_out)
-    elif head_kind == "gather":
-        geometry = L.lora_launch_geometry(18 if USE_TMAPS else 2, wl.n_rows, wl.max_loras * wl.num_experts, wl.max_rank,
-                                          wl.k_in, wl.n_out)
-    else:
-        geometry = L.lora_launch_geometry(16 if USE_TMAPS else 0, wl.n, wl.max_loras, wl.max_rank,
-                                          wl.k_in, wl.n_out)
+    geometry = geometry_of(L, wl)
 
     # the other fold workloads (per-GPU numbers, same timing rules)
     side = {}
@@ -717,34 +828,40 @@ def run_ours(args):
             "algorithmic_bytes": a2["bytes"], "achieved_gbs": gbs2, "frac_of_peak": gbs2 / peak,
             "frac_of_8tbs": gbs2 / 8000.0, "input_copies": len(r2.copies), "a_load": a_load(w2),
             "traffic": recorded_traffic(name)}
+        if dctx.rank == 0 and not args.no_cpu_baseline and workload_kind(w2) in ("bgmv", "moe") \
+                and not name.endswith("_one_launch"):
+            vt, nt, st = oracle_rows_per_s(w2, 1.0, threads=host_threads())
+            side[name]["cpu_oracle_rows_per_s"] = vt
+            side[name]["cpu_oracle_sample"] = f"{nt} rows, {host_threads()} host threads ({st:.1f} s)"
         del r2
         torch.cuda.empty_cache()
 
     # e2e through the C ABI with host buffers
     e2e = None
-    if head_kind == "bgmv":
-        e2e_steps = max(50, min(args.steps, 2000))
-        e2e_val, h2d, d2h = e2e_bgmv(wl, device, e2e_steps, 10, C)
+    if head_kind in ("bgmv", "moe"):
+        e2e_steps = max(50, min(args.steps, 2000 if head_kind == "bgmv" else 400))
+        e2e_val, h2d, d2h = e2e_run(wl, device, e2e_steps, 10, C)
         e2e = {"value": dctx.sum(e2e_val), "unit": "rows/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": e2e_steps}
 
     cpu = None
-    if dctx.rank == 0 and not args.no_cpu_baseline and head_kind == "bgmv":
+    if dctx.rank == 0 and not args.no_cpu_baseline and head_kind in ("bgmv", "moe"):
         cpu = cpu_baseline(wl, args.cpu_seconds)
 
     if dctx.rank == 0:
+        config = workload_config(wl, alg)
+        config["parallelism"] = f"replicas{dctx.world}"
         line = {
             "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": dctx.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": head, "rows": alg["rows"], "routed_rows": alg["routed_rows"],
-                       "k_in": wl.k_in, "n_out": wl.n_out, "max_loras": getattr(wl, "max_loras", 1),
-                       "max_rank": wl.max_rank, "distinct_adapters": alg["adapters"],
-                       "parallelism": f"replicas{dctx.world}",
-                       "l2": f"rotating {C} input copies ({C * runner.bytes_per_copy() / 2**20:.0f} MiB > 2x L2)",
+            "config": config,
+            "timing": {"input_copies": C,
+                       "copies_mib": round(C * runner.bytes_per_copy() / 2 ** 20),
+                       "l2_mib": round(l2 / 2 ** 20),
                        "graph": "CUDA graph replay, programmatic dependent launch",
-                       "a_load": a_load(wl)},
+                       "launches_per_step": runner.launches_per_step, "a_load": a_load(wl)},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": recorded_traffic(head),
                          "peak_kind": peak_kind, "kernel": KERNEL_NAMES[head_kind],

@@ -409,7 +409,7 @@ int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, int32_t x_
                           int32_t num_tokens, int32_t row_offset, int32_t row_end,
                           const lora_bf16_t* const* a_table, const lora_bf16_t* const* b_table,
                           const float* scale_table, int32_t max_loras, int32_t max_rank, int32_t k_in,
-                          int32_t n_out, lora_bf16_t* xa, const void* a_tmaps, void* stream) {
+                          int32_t n_out, lora_bf16_t* xa, int32_t xa_rows, void* stream) {
   if (num_experts < 1 || num_experts > LORA_MAX_EXPERTS)
     return fail(LORA_ERR_SIZE, "num_experts %d outside [1, %d]", num_experts, LORA_MAX_EXPERTS);
   if (max_loras < 1 || max_loras > LORA_MAX_LORAS)
@@ -423,13 +423,12 @@ int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, int32_t x_
     return fail(LORA_ERR_NULL, "a required pointer is NULL (x, base_out, expert_offsets, a_table, b_table, scale_table)");
   if ((row_adapter || x_gather) && !sorted_token_ids)
     return fail(LORA_ERR_NULL, "sorted_token_ids is required with row_adapter or x_gather");
+  if (xa && (xa_rows < 0 || xa_rows < row_end - row_offset))
+    return fail(LORA_ERR_SIZE, "xa holds %d rows, the window [%d, %d) writes %d", xa_rows, row_offset, row_end,
+                row_end - row_offset);
   if (!aligned16(x) || !aligned16(base_out) || (xa && !aligned16(xa)))
     return fail(LORA_ERR_ALIGN, "x, base_out and xa must be 16-byte aligned");
   glora::MoeArgs a{};
-  if (a_tmaps && (reinterpret_cast<uintptr_t>(a_tmaps) & 63u))
-    return fail(LORA_ERR_ALIGN, "a_tmaps must be 64-byte aligned");
-  // (The grouped fold's A rows span whole k-chunks of 768+ bytes; it loads them
-  // row by row and does not use tensor maps.)
   if (!make_geometry(true, row_end - row_offset, row_adapter ? max_loras : 1, num_experts + 1, max_rank, k_in,
                      n_out, a.g))
     return fail(LORA_ERR_SIZE, "no launch geometry for a window of %d rows x %d adapters at max_rank %d, k_in %d, "
@@ -445,7 +444,6 @@ int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, int32_t x_
   a.row_adapter = row_adapter;
   a.num_tokens = num_tokens;
   a.x_gather = x_gather ? 1 : 0;
-  a.a_maps = nullptr;
   a.row_offset = row_offset;
   a.row_end = row_end;
   a.a_table = a_table;

@@ -18,6 +18,7 @@ namespace glora {
 constexpr int kThreads = (kConsumerWarps + kProducerWarps) * 32;
 constexpr int kWarps = kThreads / 32;
 constexpr long long kWaitLimitCycles = 4000000000LL;  // give up on an mbarrier after ~2 s
+constexpr long long kDrainLimitCycles = 200000000LL;  // ~0.1 s for in-flight copies after a give-up
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -80,7 +80,6 @@ struct MoeArgs {
   const int32_t* row_adapter;
   int num_tokens;
   int x_gather;     // 1: x is token-major; sorted row r reads row sorted_token_ids[r]
-  const void* a_maps;  // [max_loras * num_experts] 128-byte A tensor maps (a_tiled), or NULL
   int row_offset, row_end;
   const uint16_t* const* a_table;
   const uint16_t* const* b_table;

@@ -173,11 +173,17 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
     const int pt = tid - kConsumerWarps * 32;          // 0 .. 127
     constexpr int kP = kProducerWarps * 32;
     const int q0 = pw + kProducerWarps * lane;         // this thread's first TMA copy
+    bool dead = false;   // this thread gave up on a stage: it issues no further copies
     auto produce = [&](int it) {
       const int ri = it0 + it, s = ri % ns;   // ring item
       const uint32_t full = smem_u32(&pl.full[s]);
-      if (ri >= ns && !mbar_wait(smem_u32(&pl.empty[s]), ((ri / ns) - 1) & 1)) {
+      if (!dead && ri >= ns && !mbar_wait(smem_u32(&pl.empty[s]), ((ri / ns) - 1) & 1)) {
         if (lane == 0) record_timeout(pl);
+        dead = true;
+      }
+      if (dead) {   // no copies into a stage that may still be read; the phase completes
+        cp_async_arrive_noinc(full);
+        return;
       }
       const uint32_t st = ring_u32 + s * g.stage_bytes;
       // An item is two row sets. Set 0: the adapter rows (A rows of this
@@ -270,6 +276,15 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
     unit_sync();
     if (!g.gather) unit_sync();
     for (int it = pre; it < n_items; ++it) produce(it);
+    if (*reinterpret_cast<volatile int*>(&pl.failed)) {
+      // A wait gave up somewhere: before the CTA can exit, let this thread's own
+      // copies land (cp.async groups; TMA bytes complete the stages' full phases).
+      cp_async_wait(0);
+      for (int it = max(0, n_items - ns); it < n_items; ++it) {
+        const int ri = it0 + it;
+        mbar_wait_limit(smem_u32(&pl.full[ri % ns]), (ri / ns) & 1, kDrainLimitCycles);
+      }
+    }
     return n_items;
   }
 

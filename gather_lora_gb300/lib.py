@@ -46,7 +46,7 @@ def load():
     lib.lora_bgmv.argtypes = [P, I64, P, I64, P, I32, P, P, P, I32, I32, I32, I32, P, P, P]
     lib.lora_moe_grouped_fold.restype = ctypes.c_int
     lib.lora_moe_grouped_fold.argtypes = [P, I64, I32, P, I64, P, I32, P, I32, P, I32, I32, I32,
-                                          P, P, P, I32, I32, I32, I32, P, P, P]
+                                          P, P, P, I32, I32, I32, I32, P, I32, P]
     lib.lora_moe_gather_bgmv.restype = ctypes.c_int
     lib.lora_moe_gather_bgmv.argtypes = [P, I64, P, I64, P, I32, I32, P, I32, I32,
                                          P, P, P, I32, I32, I32, I32, P, P, P]
@@ -134,14 +134,22 @@ def lora_delta_geometry(m, max_rank, k_in, n_out, sm_count=0) -> dict:
 def lora_moe_grouped_fold(x, x_row_stride, base_out, out_row_stride, expert_offsets, num_experts,
                           sorted_token_ids, te, row_adapter, num_tokens, row_offset, row_end,
                           a_table, b_table, scale_table, max_loras, max_rank, k_in, n_out,
-                          xa=None, stream=None, x_gather=False, a_tmaps=None):
+                          xa=None, stream=None, x_gather=False, xa_rows=None):
     """MoE grouped fold of one window (see lora_moe_grouped_fold in include/gather_lora.h).
-    x_gather: x is token-major and sorted row r reads row sorted_token_ids[r] (gate/up)."""
+    x_gather: x is token-major and sorted row r reads row sorted_token_ids[r] (gate/up).
+    xa_rows: rows allocated for xa; taken from the tensor's size (numel // max_rank) when
+    xa is a tensor and xa_rows is not given."""
+    if xa is None:
+        xa_rows = 0
+    elif xa_rows is None:
+        if isinstance(xa, int):
+            raise ValueError("xa given as a raw address needs xa_rows")
+        xa_rows = xa.numel() // max_rank
     return _check(load().lora_moe_grouped_fold(
         _addr(x), x_row_stride, 1 if x_gather else 0, _addr(base_out), out_row_stride, _addr(expert_offsets),
         num_experts, _addr(sorted_token_ids), te, _addr(row_adapter), num_tokens, row_offset,
         row_end, _addr(a_table), _addr(b_table), _addr(scale_table), max_loras, max_rank, k_in,
-        n_out, _addr(xa), _addr(a_tmaps), _stream(stream)))
+        n_out, _addr(xa), int(xa_rows), _stream(stream)))
 
 
 def lora_moe_gather_bgmv(x, x_row_stride, base_out, out_row_stride, indices, n_rows, top_k,

@@ -151,11 +151,13 @@ int lora_bgmv(const lora_bf16_t* x, int64_t x_row_stride,
  *                     NULL and x_gather == 0
  *   row_adapter       [num_tokens] int32 (< 0 = no delta), or NULL: every row uses adapter 0
  *   a_table, b_table, scale_table   [max_loras * num_experts], index a*num_experts + e
- *   a_tmaps           accepted for symmetry with the other folds and not used: the
- *                     grouped fold copies whole 768+-byte A row chunks, which the
- *                     maps would not reduce much (checked for 64-byte alignment)
- *   xa                optional [row_end - row_offset, max_rank] BF16 shrink output at the
+ *   xa                optional [xa_rows, max_rank] BF16 shrink output, written at the
  *                     LOCAL row r - row_offset (routed rows only); NULL skips it
+ *   xa_rows           rows the caller allocated for xa. The window writes local rows
+ *                     [0, row_end - row_offset), so xa != NULL with xa_rows < row_end -
+ *                     row_offset (or < 0) is rejected with LORA_ERR_SIZE before any
+ *                     launch; ignored when xa is NULL ("Module moe_lora_grouped",
+ *                     `moe_lora_grouped_down`: the caller needs at least the window's rows)
  * The window must satisfy 0 <= row_offset <= row_end <= te (else LORA_ERR_WINDOW);
  * a window whose grid (below) would exceed one launch's 2^31 - 1 CTAs gives
  * LORA_ERR_SIZE and launches nothing. The launch grid is
@@ -177,7 +179,7 @@ int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, int32_t x_
                           const lora_bf16_t* const* a_table, const lora_bf16_t* const* b_table,
                           const float* scale_table, int32_t max_loras,
                           int32_t max_rank, int32_t k_in, int32_t n_out,
-                          lora_bf16_t* xa, const void* a_tmaps, void* stream);
+                          lora_bf16_t* xa, int32_t xa_rows, void* stream);
 
 /*
  * lora_moe_gather_bgmv — the decode-path MoE fold over flat, unsorted

@@ -4,27 +4,44 @@ Index and routing work is compared bit-exactly: every row the oracle leaves
 alone, and every element outside a row's folded segment, must be byte-identical
 on the GPU.
 
-Floating point: the GPU sums the same BF16 products in another fixed order
-(tensor-core steps of 16, k-slices reduced in rank order), so each fp32 sum may
-differ from the oracle's sequential one by the standard summation bound. With
-u = 2^-24 and gamma_m = m*u / (1 - m*u), for a sum of m products:
-    |S_gpu - S_oracle| <= 2 * gamma_m * sum |terms|        (both orders' errors)
-A BF16 rounding after the sum adds at most one ulp of the result. So
-  * xa:    |xa_gpu - xa_ora| <= ulp + 2*gamma_{k_in} * sum_k |x_k A_ck|;
-  * delta: the expand sum moves by sum_c |xa_gpu_c - xa_ora_c| |B_jc| (the
-           observed xa difference, itself checked above) plus
-           2*gamma_{max_rank} * sum_c |xa_c| |B_jc|, then one BF16 rounding;
-  * fold:  |scale| times the delta change, plus one ulp of the result.
-Where no intermediate rounding flips, this is the 1-ulp rule of the method.
-A floor on the fraction of bit-exact elements is checked too.
+Floating point. The GPU sums the same BF16 products as the oracle (each product
+is exact in fp32) in another fixed order: tensor-core steps of 16, k-slices
+reduced in rank order. The rule ("Function apply_lora_bgmv" summary: fp32
+accumulate, xa rounded to BF16, the delta rounded to BF16, then one fp32 fold)
+is checked in three parts, with u = 2^-24:
+
+  xa     |xa_gpu - xa_ora| <= ulp + 2 * LAMBDA * sqrt(k_in) * u * sum_k |x_k A_ck|.
+         The second term is the probabilistic bound on two fp32 summation
+         orders of k_in terms (each error at most LAMBDA * sqrt(m) * u * sum|t|,
+         failing with probability below 2 exp(-LAMBDA^2 / 2) ~ 3e-8 per value).
+         Where it is below one ulp this is the one-ulp rule; more than one ulp
+         is only allowed where the sum cancels so far that the two orders can
+         straddle several BF16 values.
+  fold   every folded value must be the fold of the GPU's own xa up to the
+         expand's summation order: with S' the oracle-order fp32 expand sum of
+         the GPU's xa and delta = 2 * gamma_{max_rank} * sum_c |xa_c B_jc|
+         (the worst case of two orders, gamma_m = m*u / (1 - m*u)), the GPU value
+         must lie between bf16(fma(scale, bf16(S' -+ delta), base)). A fold that
+         is off by even one ulp for any other reason fails.
+  stated the folded value is within one ulp of the oracle's wherever neither
+         the row's xa nor the element's delta differs from the oracle's; beyond
+         one ulp only where one of them flipped (the relative error is then the
+         flip's, at most 2^-7 of the delta term for a delta flip).
+A floor on the fraction of bit-exact elements is checked too, and the largest
+ulp distance of xa and of the folded values is reported.
 """
 from __future__ import annotations
+
+import math
+from collections import defaultdict
 
 import numpy as np
 
 from gather_lora_gb300 import workloads as W
 
 F = W.bf16_bits_to_f32
+U = 2.0 ** -24
+LAMBDA = 6.0
 
 
 def bf16_ulp(bits: np.ndarray) -> np.ndarray:
@@ -38,37 +55,147 @@ def ulp_of_value(v: np.ndarray) -> np.ndarray:
     return np.ldexp(1.0, np.floor(np.log2(v)).astype(np.int64) - 7)
 
 
-def gamma(m: int, u: float = 2.0 ** -24) -> float:
+def gamma(m: int, u: float = U) -> float:
     return m * u / (1.0 - m * u)
 
 
+def ulp_distance(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
+    """Distance in BF16 steps between two arrays of BF16 patterns (sign-aware)."""
+    def key(b):
+        b = np.asarray(b, dtype=np.uint16).astype(np.int64)
+        return np.where(b & 0x8000, -(b & 0x7FFF), b)
+    return np.abs(key(a_bits) - key(b_bits))
+
+
+def _f64_to_f32_odd(v: np.ndarray) -> np.ndarray:
+    """float64 -> float32 rounded to odd (exact values stay; an inexact one takes
+    the neighbour with an odd last bit). Rounding that to BF16 (RNE) gives the
+    correctly rounded BF16 of v, since 24 >= 8 + 2."""
+    v = np.asarray(v, dtype=np.float64)
+    r = v.astype(np.float32)
+    inexact = r.astype(np.float64) != v
+    even = (r.view(np.uint32) & 1) == 0
+    toward = np.where(v > r.astype(np.float64), np.float32(np.inf), np.float32(-np.inf))
+    return np.where(inexact & even, np.nextafter(r, toward), r)
+
+
+def bf16_of_f64(v: np.ndarray) -> np.ndarray:
+    """Round float64 values to BF16 bit patterns (round to nearest even)."""
+    return W.to_bf16_bits(_f64_to_f32_odd(v))
+
+
+def fmaf32(a: np.ndarray, b: np.ndarray, c: np.ndarray) -> np.ndarray:
+    """fp32 fma(a, b, c) with one rounding, for float32 a and c and b holding BF16
+    values: a*b is exact in float64; the sum is made exact by TwoSum and rounded
+    to odd in float64, then rounded to float32 (53 >= 24 + 2)."""
+    p = np.asarray(a, np.float64) * np.asarray(b, np.float64)
+    q = np.asarray(c, np.float64)
+    s = p + q
+    bb = s - p
+    err = (p - (s - bb)) + (q - bb)
+    even = (s.view(np.int64) & 1) == 0
+    s = np.where((err != 0) & even, np.nextafter(s, np.where(err > 0, np.inf, -np.inf)), s)
+    return s.astype(np.float32)
+
+
+def fold_bits(scale: float, d_bits: np.ndarray, base_bits: np.ndarray) -> np.ndarray:
+    """The method's fold of BF16 deltas into BF16 base values: bf16(fma(scale, d, base))."""
+    r = fmaf32(np.float32(scale), F(d_bits), F(base_bits))
+    return W.to_bf16_bits(r)
+
+
 def check_xa(gpu_xa_row, ora_xa_row, x_row, A):
-    """xa within one ulp plus both summation errors of the k_in-term sums."""
+    """xa within one ulp plus the probabilistic bound of two k_in-term summation
+    orders. Returns (bit-exact count, largest ulp distance)."""
     g, o = F(gpu_xa_row).astype(np.float64), F(ora_xa_row).astype(np.float64)
     mag = np.abs(F(A).astype(np.float64)) @ np.abs(F(x_row).astype(np.float64))
-    bound = np.maximum(bf16_ulp(gpu_xa_row), bf16_ulp(ora_xa_row)) + 2.0 * gamma(A.shape[1]) * mag
+    k_in = A.shape[1]
+    bound = (np.maximum(bf16_ulp(gpu_xa_row), bf16_ulp(ora_xa_row))
+             + 2.0 * LAMBDA * math.sqrt(k_in) * U * mag)
     err = np.abs(g - o)
     if not np.all(err <= bound):
         c = int(np.argmax(err / bound))
         raise AssertionError(f"xa[{c}] gpu {g[c]!r} oracle {o[c]!r} err {err[c]:.3g} > bound {bound[c]:.3g}")
-    return int(np.sum(gpu_xa_row == ora_xa_row))
+    dist = ulp_distance(gpu_xa_row, ora_xa_row)
+    return int(np.sum(gpu_xa_row == ora_xa_row)), int(dist.max()) if dist.size else 0
 
 
-def check_row_fold(gpu_row, ora_row, d_row, ora_xa_row, gpu_xa_row, B, scale):
-    """Compare one routed row's folded segment; returns (n_exact, n, worst err/bound)."""
-    Bf = np.abs(F(B).astype(np.float64))
-    xo, xg = F(ora_xa_row).astype(np.float64), F(gpu_xa_row).astype(np.float64)
-    dT = Bf @ np.abs(xg - xo) + 2.0 * gamma(B.shape[1]) * (Bf @ np.abs(xo))
-    d = np.abs(F(d_row).astype(np.float64))
-    d_change = dT + np.maximum(bf16_ulp(d_row), ulp_of_value(d + dT))
-    gf, of = F(gpu_row).astype(np.float64), F(ora_row).astype(np.float64)
-    err = np.abs(gf - of)
-    bound = np.maximum(bf16_ulp(ora_row), bf16_ulp(gpu_row)) + abs(float(scale)) * d_change
-    worst = float(np.max(err / bound)) if err.size else 0.0
-    if not np.all(err <= bound):
-        j = int(np.argmax(err / bound))
-        raise AssertionError(f"fold[{j}] gpu {gf[j]!r} oracle {of[j]!r} err {err[j]:.3g} > bound {bound[j]:.3g}")
-    return int(np.sum(gpu_row == ora_row)), int(gpu_row.size), worst
+def expand_oracle_order(xa_bits: np.ndarray, B: np.ndarray) -> np.ndarray:
+    """fp32 expand sums of rows xa [R, max_rank] against B [n_out, max_rank], summed
+    term by term in rank order as the oracle does (float32 arrays, no fma)."""
+    xa = F(xa_bits).astype(np.float32)
+    Bf = F(B).astype(np.float32)
+    S = np.zeros((xa.shape[0], Bf.shape[0]), dtype=np.float32)
+    for c in range(Bf.shape[1]):
+        S = S + xa[:, c:c + 1] * Bf[None, :, c]
+    return S
+
+
+def check_fold_group(gpu_rows, ora_rows, base_rows, ora_d, ora_xa, gpu_xa, B, scale):
+    """All routed rows of one adapter table entry: [R, n_out] BF16 folded segments of
+    the GPU and the oracle, the original base values, the oracle's deltas and both
+    xa [R, max_rank]. Returns (bit-exact count, total, largest ulp distance, values
+    beyond one ulp)."""
+    gpu_rows, ora_rows = np.atleast_2d(gpu_rows), np.atleast_2d(ora_rows)
+    R = gpu_rows.shape[0]
+    if R == 0:
+        return 0, 0, 0, 0
+    # fold: the GPU value must be the fold of a delta its own xa allows
+    S = expand_oracle_order(gpu_xa, B).astype(np.float64)
+    mag = np.abs(F(gpu_xa).astype(np.float64)) @ np.abs(F(B).astype(np.float64)).T
+    delta = 2.0 * gamma(B.shape[1]) * mag
+    f_lo = fold_bits(scale, bf16_of_f64(S - delta), base_rows)
+    f_hi = fold_bits(scale, bf16_of_f64(S + delta), base_rows)
+    lo = np.minimum(F(f_lo).astype(np.float64), F(f_hi).astype(np.float64))
+    hi = np.maximum(F(f_lo).astype(np.float64), F(f_hi).astype(np.float64))
+    g = F(gpu_rows).astype(np.float64)
+    bad = ~((g >= lo) & (g <= hi))
+    if bad.any():
+        r, j = map(int, np.argwhere(bad)[0])
+        raise AssertionError(f"fold[{r},{j}] gpu {g[r, j]!r} is not the fold of its own xa: "
+                             f"allowed [{lo[r, j]!r}, {hi[r, j]!r}] (oracle {F(ora_rows)[r, j]!r})")
+    # stated rule: one ulp, beyond it only where xa or the delta flipped
+    dist = ulp_distance(gpu_rows, ora_rows)
+    beyond = dist > 1
+    if beyond.any():
+        xa_flip = np.any(gpu_xa != ora_xa, axis=1)[:, None]
+        d_flip = np.zeros_like(beyond)
+        for step in (-1, 1):   # the oracle's fold with its delta one BF16 step away
+            d_alt = (ora_d.astype(np.int64) + np.where(ora_d & 0x8000, -step, step)).astype(np.uint16)
+            d_flip |= fold_bits(scale, d_alt, base_rows) == gpu_rows
+        unexplained = beyond & ~(xa_flip | d_flip)
+        if unexplained.any():
+            r, j = map(int, np.argwhere(unexplained)[0])
+            raise AssertionError(f"fold[{r},{j}] gpu {g[r, j]!r} oracle {F(ora_rows)[r, j]!r}: "
+                                 f"{int(dist[r, j])} ulps with no xa or delta flip")
+    return (int(np.sum(gpu_rows == ora_rows)), int(gpu_rows.size), int(dist.max()),
+            int(beyond.sum()))
+
+
+def _fold_groups(groups, stats):
+    """groups: {table: [(gpu_row, ora_row, base_row, ora_d, ora_xa, gpu_xa), ...]} with the
+    table's (B, scale) in groups[table].meta. Accumulates into stats."""
+    for (B, scale), items in groups.values():
+        cols = list(zip(*items))
+        e, t, dmax, beyond = check_fold_group(*(np.stack(c) for c in cols), B, scale)
+        stats["exact"] += e
+        stats["total"] += t
+        stats["max_ulps"] = max(stats["max_ulps"], dmax)
+        stats["beyond_1ulp"] += beyond
+
+
+def _finish(stats, xa_exact, xa_tot, xa_max, min_exact):
+    n_exact, n_tot = stats["exact"], stats["total"]
+    if n_tot:
+        assert n_exact / n_tot >= min_exact, f"only {n_exact}/{n_tot} folded values bit-exact"
+    if xa_tot:
+        assert xa_exact / xa_tot >= min_exact, f"only {xa_exact}/{xa_tot} xa values bit-exact"
+    return dict(exact=n_exact, total=n_tot, xa_exact=xa_exact, xa_total=xa_tot,
+                max_ulps=stats["max_ulps"], xa_max_ulps=xa_max, beyond_1ulp=stats["beyond_1ulp"])
+
+
+def _new_stats():
+    return dict(exact=0, total=0, max_ulps=0, beyond_1ulp=0)
 
 
 def routed_bgmv_rows(wl: W.BgmvWorkload):
@@ -90,20 +217,18 @@ def compare_bgmv(wl: W.BgmvWorkload, gpu_out, ora_out, gpu_xa, ora_xa, ora_d, mi
         mask[i, seg] = False
     assert np.array_equal(gpu_out[mask], ora_out[mask]), "bytes outside the folded segments changed"
     assert np.array_equal(ora_out[mask], wl.out_buf[mask])
-    n_exact = n_tot = xa_exact = xa_tot = 0
-    worst = 0.0
+    xa_exact = xa_tot = xa_max = 0
+    groups = {}
     for i, s in routed:
-        xa_exact += check_xa(gpu_xa[i], ora_xa[i], wl.x[i, :wl.k_in], wl.a_pool[s])
-        xa_tot += wl.max_rank
-        e, t, w = check_row_fold(gpu_out[i, seg], ora_out[i, seg], ora_d[i], ora_xa[i], gpu_xa[i],
-                                 wl.b_pool[s], wl.scale[s])
-        n_exact, n_tot, worst = n_exact + e, n_tot + t, max(worst, w)
-    if n_tot:
-        assert n_exact / n_tot >= min_exact, f"only {n_exact}/{n_tot} folded values bit-exact"
-    if xa_tot:
-        assert xa_exact / xa_tot >= min_exact, f"only {xa_exact}/{xa_tot} xa values bit-exact"
-    return dict(rows=len(routed), exact=n_exact, total=n_tot, xa_exact=xa_exact, xa_total=xa_tot,
-                worst=worst)
+        e, m = check_xa(gpu_xa[i], ora_xa[i], wl.x[i, :wl.k_in], wl.a_pool[s])
+        xa_exact, xa_tot, xa_max = xa_exact + e, xa_tot + wl.max_rank, max(xa_max, m)
+        groups.setdefault(s, ((wl.b_pool[s], wl.scale[s]), []))[1].append(
+            (gpu_out[i, seg], ora_out[i, seg], wl.out_buf[i, seg], ora_d[i], ora_xa[i], gpu_xa[i]))
+    stats = _new_stats()
+    _fold_groups(groups, stats)
+    res = _finish(stats, xa_exact, xa_tot, xa_max, min_exact)
+    res["rows"] = len(routed)
+    return res
 
 
 def moe_routes(wl: W.MoeWorkload, lo: int, hi: int, offsets=None, sorted_ids=None, row_adapter="wl"):
@@ -143,23 +268,23 @@ def compare_moe(wl: W.MoeWorkload, windows, gpu_out, ora_out, gpu_xas, ora_xas, 
     mask[list(routed)] = False
     assert np.array_equal(gpu_out[mask], ora_out[mask]), "rows without a delta changed"
     assert np.array_equal(ora_out[mask], wl.out_buf[mask])
-    n_exact = n_tot = xa_exact = 0
-    worst = 0.0
-    for (lo, hi), gx, ox in zip(windows, gpu_xas, ora_xas):
-        for r, idx in routes:
-            if lo <= r < hi:
-                xrow = wl.x[wl.sorted_token_ids[r]] if wl.x_gather else wl.x[r]
-                xa_exact += check_xa(gx[r - lo], ox[r - lo], xrow, wl.a_pool[idx])
+    xa_exact = xa_tot = xa_max = 0
+    groups = {}
     for r, idx in routes:
         # the xa of row r lives in its window's buffer, at the local row
         w = next(k for k, (lo, hi) in enumerate(windows) if lo <= r < hi)
         lr = r - windows[w][0]
-        e, t, wst = check_row_fold(gpu_out[r], ora_out[r], ora_d[r], ora_xas[w][lr],
-                                   gpu_xas[w][lr], wl.b_pool[idx], wl.scale[idx])
-        n_exact, n_tot, worst = n_exact + e, n_tot + t, max(worst, wst)
-    if n_tot:
-        assert n_exact / n_tot >= min_exact, f"only {n_exact}/{n_tot} folded values bit-exact"
-    return dict(rows=len(routes), exact=n_exact, total=n_tot, xa_exact=xa_exact, worst=worst)
+        gx, ox = gpu_xas[w][lr], ora_xas[w][lr]
+        xrow = wl.x[wl.sorted_token_ids[r]] if wl.x_gather else wl.x[r]
+        e, m = check_xa(gx, ox, xrow, wl.a_pool[idx])
+        xa_exact, xa_tot, xa_max = xa_exact + e, xa_tot + wl.max_rank, max(xa_max, m)
+        groups.setdefault(idx, ((wl.b_pool[idx], wl.scale[idx]), []))[1].append(
+            (gpu_out[r], ora_out[r], wl.out_buf[r], ora_d[r], ox, gx))
+    stats = _new_stats()
+    _fold_groups(groups, stats)
+    res = _finish(stats, xa_exact, xa_tot, xa_max, min_exact)
+    res["rows"] = len(routes)
+    return res
 
 
 def gather_routes(wl: W.MoeGatherWorkload, indices=None, row_adapter="wl"):
@@ -188,19 +313,18 @@ def compare_gather(wl: W.MoeGatherWorkload, gpu_out, ora_out, gpu_xa, ora_xa, or
     mask[list(routed)] = False
     assert np.array_equal(gpu_out[mask], ora_out[mask]), "rows without a delta changed"
     assert np.array_equal(ora_out[mask], wl.out_buf[mask])
-    n_exact = n_tot = xa_exact = xa_tot = 0
-    worst = 0.0
+    xa_exact = xa_tot = xa_max = 0
+    groups = {}
     for r, idx in routes:
-        xa_exact += check_xa(gpu_xa[r], ora_xa[r], wl.x[r], wl.a_pool[idx])
-        xa_tot += wl.max_rank
-        e, t, w = check_row_fold(gpu_out[r], ora_out[r], ora_d[r], ora_xa[r], gpu_xa[r],
-                                 wl.b_pool[idx], wl.scale[idx])
-        n_exact, n_tot, worst = n_exact + e, n_tot + t, max(worst, w)
-    if n_tot:
-        assert n_exact / n_tot >= min_exact, f"only {n_exact}/{n_tot} folded values bit-exact"
-    if xa_tot:
-        assert xa_exact / xa_tot >= min_exact, f"only {xa_exact}/{xa_tot} xa values bit-exact"
-    return dict(rows=len(routes), exact=n_exact, total=n_tot, worst=worst)
+        e, m = check_xa(gpu_xa[r], ora_xa[r], wl.x[r], wl.a_pool[idx])
+        xa_exact, xa_tot, xa_max = xa_exact + e, xa_tot + wl.max_rank, max(xa_max, m)
+        groups.setdefault(idx, ((wl.b_pool[idx], wl.scale[idx]), []))[1].append(
+            (gpu_out[r], ora_out[r], wl.out_buf[r], ora_d[r], ora_xa[r], gpu_xa[r]))
+    stats = _new_stats()
+    _fold_groups(groups, stats)
+    res = _finish(stats, xa_exact, xa_tot, xa_max, min_exact)
+    res["rows"] = len(routes)
+    return res
 
 
 def delta_as_bgmv(wl: W.DeltaWorkload) -> W.BgmvWorkload:

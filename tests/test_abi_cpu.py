@@ -79,12 +79,12 @@ def test_bgmv_zero_rows_is_a_no_op():
 def _moe(**kw):
     a = dict(x=FAKE, xs=768, xg=0, out=FAKE, os=2048, off=FAKE, E=128, sti=FAKE, te=16384, ra=FAKE,
              nt=2048, lo=0, hi=4096, at=FAKE, bt=FAKE, sc=FAKE, L=16, R=16, k=768, no=2048, xa=FAKE,
-             maps=None)
+             xa_rows=4096)
     a.update(kw)
     return L.load().lora_moe_grouped_fold(a["x"], a["xs"], a["xg"], a["out"], a["os"], a["off"], a["E"],
                                           a["sti"], a["te"], a["ra"], a["nt"], a["lo"], a["hi"],
                                           a["at"], a["bt"], a["sc"], a["L"], a["R"], a["k"], a["no"],
-                                          a["xa"], a["maps"], None)
+                                          a["xa"], a["xa_rows"], None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -93,9 +93,19 @@ def _moe(**kw):
     (dict(k=770, xs=776), -4), (dict(xs=700), -3), (dict(x=None), -1), (dict(off=None), -1),
     (dict(sti=None), -1), (dict(at=None), -1), (dict(x=FAKE + 2), -4),
     (dict(sti=None, ra=None, xg=1), -1),
+    (dict(xa_rows=4095), -2), (dict(xa_rows=-1), -2), (dict(lo=100, hi=5000, xa_rows=4899), -2),
 ])
 def test_moe_rejects_bad_arguments_before_launch(kw, code):
     assert _moe(**kw) == code
+
+
+def test_moe_xa_rows_cover_the_window():
+    """xa needs the window's rows (written at the local row r - row_offset), not te's;
+    with xa NULL the count is not looked at. The check runs before any launch."""
+    assert _moe(lo=100, hi=5000, xa_rows=4899) == -2
+    assert "xa holds 4899 rows" in L.lora_last_error()
+    assert _moe(lo=0, hi=0, xa_rows=0, x=FAKE + 2) == -4      # reaches the alignment check
+    assert _moe(xa=None, xa_rows=-5, x=FAKE + 2) == -4         # xa_rows ignored without xa
 
 
 def test_moe_grid_that_overflows_a_launch_is_rejected():

@@ -11,6 +11,8 @@ import os
 import subprocess
 import sys
 
+import pytest
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
 
@@ -34,21 +36,49 @@ def test_reference_arm_prints_contract_line():
     assert cpu["kind"] == "oracle" and cpu["value"] == d["value"] and cpu["cores"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": "rows/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
-    assert d["config"]["workload"] == "decode_qproj_bgmv"
+    import bench
+    from gather_lora_gb300 import workloads as W
+    wl = W.by_name(bench.HEADLINE)
+    assert d["config"] == bench.workload_config(wl, bench.algorithmic_bytes(wl))
+    assert d["config"]["workload"] == "moe_down_fold" and d["config"]["windows"] == 4
+    assert cpu["cpu_model"]
 
 
-def test_threaded_oracle_baseline_counts_every_thread():
+@pytest.mark.parametrize("name", ["moe_down_fold", "decode_qproj_bgmv"])
+def test_threaded_oracle_baseline_counts_every_thread(name):
     import bench
     import oracle
     from gather_lora_gb300 import workloads as W
     oracle.load()
-    wl = W.by_name(bench.HEADLINE)
+    wl = W.by_name(name)
     rows_per_s, rows, secs = bench.oracle_rows_per_s(wl, 0.0, rows_per_call=2, threads=3)
     # a zero budget still lets each thread fold one call's rows
     assert rows == 3 * 2 and secs > 0 and rows_per_s > 0
     base = bench.cpu_baseline(wl, 0.0)
     assert base["cores"] == bench.host_threads() and base["kind"] == "oracle"
     assert base["single_thread"]["cores"] == 1 and base["single_thread"]["value"] > 0
+
+
+def test_moe_oracle_sample_equals_the_window_fold():
+    """The baseline folds sorted rows [lo, hi) as the same problem on fewer rows;
+    its results must be the rows the oracle gives over the whole window."""
+    import numpy as np
+    import oracle
+    from gather_lora_gb300 import workloads as W
+    from gpu_util import oracle_moe
+    oracle.load()
+    wl = W.make_moe("sample_eq", num_tokens=96, top_k=4, num_experts=12, k_in=64, n_out=48,
+                    max_loras=3, max_rank=8, rank=8, alpha=16.0, adapter_base_frac=0.2, cap=384,
+                    seed=12)
+    full, _, _ = oracle_moe(wl, wl.windows())
+    lo, hi = 37, 211
+    offs = np.clip(wl.expert_offsets.astype(np.int64) - lo, 0, hi - lo).astype(np.int32)
+    out = wl.out_buf[lo:hi].copy()
+    oracle.lora_moe_grouped_fold(wl.x[lo:hi], wl.k_in, out, wl.n_out, offs,
+                                 wl.sorted_token_ids[lo:hi], wl.row_adapter, wl.num_tokens, 0,
+                                 hi - lo, wl.a_list(), wl.b_list(), wl.scale, wl.max_rank, wl.k_in,
+                                 wl.n_out)
+    assert np.array_equal(out, full[lo:hi])
 
 
 def test_one_launch_moe_workload_is_the_same_problem():

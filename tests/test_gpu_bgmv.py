@@ -14,7 +14,7 @@ import torch
 
 from gather_lora_gb300 import lib as L
 from gather_lora_gb300 import workloads as W
-from gpu_util import gpu_bgmv, oracle_bgmv, require_gpu, to_u16
+from gpu_util import device_a_tmaps, gpu_bgmv, oracle_bgmv, require_gpu, to_u16
 from parity import compare_bgmv
 
 pytestmark = pytest.mark.gpu
@@ -107,24 +107,64 @@ def test_bgmv_units_numbered_slot_by_slot():
     compare_bgmv(wl, g_out, o_out, g_xa, o_xa, o_d)
 
 
-@pytest.mark.parametrize("name", ["decode_qproj_bgmv", "qkv_kfold_bgmv", "ffn_down_bgmv"])
-def test_bgmv_batch_invariance(name):
-    """Each row folded alone (n = 1 per call) is bit-identical to the batched call."""
-    wl = W.by_name(name)
-    d = W.bgmv_to_device(wl)
-    g_out, g_xa = gpu_bgmv(wl, d)
-    d1 = W.bgmv_to_device(wl)
-    rows = range(wl.n) if wl.n <= 64 else list(range(0, wl.n, 3))
+def _one_row_calls(wl, d, rows, maps):
+    """Fold each of `rows` alone (n = 1 per call) on device copy d."""
     for i in rows:
-        L.lora_bgmv(d1.x[i], wl.x_row_stride, d1.out_buf[i].data_ptr() + 2 * wl.out_offset,
-                    wl.out_row_stride, d1.seq_slot[i:i + 1], 1, d1.a_table, d1.b_table, d1.scale,
-                    wl.max_loras, wl.max_rank, wl.k_in, wl.n_out, xa=d1.xa[i])
+        L.lora_bgmv(d.x[i], wl.x_row_stride, d.out_buf[i].data_ptr() + 2 * wl.out_offset,
+                    wl.out_row_stride, d.seq_slot[i:i + 1], 1, d.a_table, d.b_table, d.scale,
+                    wl.max_loras, wl.max_rank, wl.k_in, wl.n_out, xa=d.xa[i], a_tmaps=maps)
     torch.cuda.synchronize()
-    s_out, s_xa = to_u16(d1.out_buf), to_u16(d1.xa)
+    return to_u16(d.out_buf), to_u16(d.xa)
+
+
+def _batch_invariant(wl, rows, maps: bool):
+    """The batched call and one call per row give the same bits (out and xa);
+    both with A tensor maps when `maps` (the launch geometry then follows them)."""
+    d = W.bgmv_to_device(wl)
+    m = device_a_tmaps(d.a_table, wl.max_rank, wl.k_in) if maps else None
+    L.lora_bgmv(d.x, wl.x_row_stride, d.out_ptr, wl.out_row_stride, d.seq_slot, wl.n, d.a_table,
+                d.b_table, d.scale, wl.max_loras, wl.max_rank, wl.k_in, wl.n_out, xa=d.xa, a_tmaps=m)
+    torch.cuda.synchronize()
+    g_out, g_xa = to_u16(d.out_buf), to_u16(d.xa)
+    d1 = W.bgmv_to_device(wl)
+    m1 = device_a_tmaps(d1.a_table, wl.max_rank, wl.k_in) if maps else None
+    s_out, s_xa = _one_row_calls(wl, d1, rows, m1)
     rows = list(rows)
     assert np.array_equal(s_out[rows], g_out[rows])
-    routed = [i for i in rows if wl.seq_slot[i] >= 0]
+    routed = [i for i in rows if 0 <= wl.seq_slot[i] < wl.max_loras and wl.present[wl.seq_slot[i]]]
     assert np.array_equal(s_xa[routed], g_xa[routed])
+    return g_out, g_xa
+
+
+@pytest.mark.parametrize("name,maps", [("decode_qproj_bgmv", False), ("qkv_kfold_bgmv", False),
+                                       ("qkv_kfold_bgmv", True), ("ffn_down_bgmv", False),
+                                       ("ffn_down_bgmv", True)])
+def test_bgmv_batch_invariance(name, maps):
+    """Each row folded alone (n = 1 per call) is bit-identical to the batched call
+    ("Function apply_lora_bgmv", BYTE-IDENTICAL paragraph), on every shrink path a
+    routed call can take: mma.sync with A rows or A boxes, and the tcgen05 shrink
+    (ffn_down_bgmv with maps)."""
+    wl = W.by_name(name)
+    g = L.lora_launch_geometry(16 if maps else 0, wl.n, wl.max_loras, wl.max_rank, wl.k_in, wl.n_out)
+    if name == "ffn_down_bgmv":
+        assert g["tc"] == int(maps)
+    rows = range(wl.n) if wl.n <= 64 else list(range(0, wl.n, 3))
+    _batch_invariant(wl, rows, maps)
+
+
+def test_bgmv_tc_shrink_small_units_batch_invariant():
+    """tcgen05 shrink with units of fewer than 16 rows (the N = 16 atom then holds
+    x columns past the unit's rows): parity with the oracle and bit-identity with
+    one row per call."""
+    wl = W.make_bgmv("tc_small", n=45, k_in=2056, n_out=520, max_loras=7, max_rank=128,
+                     rank_choices=(128, 96), alpha=16.0, rslora=True, slot_law="uniform",
+                     slot_base_frac=0.1, seed=77)
+    assert L.lora_launch_geometry(16, wl.n, wl.max_loras, wl.max_rank, wl.k_in, wl.n_out)["tc"] == 1
+    counts = np.bincount(wl.seq_slot[wl.seq_slot >= 0], minlength=wl.max_loras)
+    assert counts.max() < 16
+    g_out, g_xa = _batch_invariant(wl, range(wl.n), maps=True)
+    o_out, o_xa, o_d = oracle_bgmv(wl)
+    compare_bgmv(wl, g_out, o_out, g_xa, o_xa, o_d, min_exact=0.97)
 
 
 def test_bgmv_graph_replay_with_new_routing():

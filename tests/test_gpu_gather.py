@@ -14,7 +14,7 @@ import torch
 
 from gather_lora_gb300 import lib as L
 from gather_lora_gb300 import workloads as W
-from gpu_util import gpu_gather, oracle_gather, require_gpu, to_u16
+from gpu_util import device_a_tmaps, gpu_gather, oracle_gather, require_gpu, to_u16
 from parity import compare_gather, gather_routes
 
 pytestmark = pytest.mark.gpu
@@ -90,6 +90,39 @@ def test_gather_per_token_calls_equal_batched():
     assert np.array_equal(to_u16(d.out_buf), g_out)
     routed = [r for r, _ in gather_routes(wl)]
     assert np.array_equal(to_u16(d.xa)[routed], g_xa[routed])
+
+
+@pytest.mark.parametrize("max_rank,maps", [(16, False), (64, True), (128, True)])
+def test_gather_decode_shape_per_token_calls_equal_batched(max_rank, maps):
+    """The decode workload (64 tokens x top-8 of 128 experts, k_in 768, n_out 2048;
+    at ranks 64 and 128 the same rows over 32 experts x 8 adapters, to keep the
+    adapter pool small): one token's rows per call give the same bits as the batched
+    call, with A row copies (rank 16) and with A tensor maps (ranks 64, 128)."""
+    wl = (W.moe_decode_gather() if max_rank == 16 else
+          W.make_moe_gather("g_inv_full", num_tokens=64, top_k=8, num_experts=32, k_in=768,
+                            n_out=2048, max_loras=8, max_rank=max_rank, rank=max_rank, alpha=32.0,
+                            adapter_base_frac=0.2, seed=560 + max_rank))
+    res = []
+    for per_token in (False, True):
+        d = W.gather_to_device(wl)
+        m = device_a_tmaps(d.a_table, wl.max_rank, wl.k_in) if maps else None
+        k = wl.top_k
+        calls = ([(slice(t * k, (t + 1) * k), t) for t in range(wl.num_tokens)] if per_token
+                 else [(slice(0, wl.n_rows), None)])
+        for rows, t in calls:
+            n = rows.stop - rows.start
+            ra = d.row_adapter if t is None else d.row_adapter[t:t + 1]
+            L.lora_moe_gather_bgmv(d.x[rows], wl.k_in, d.out_buf[rows], wl.n_out, d.indices[rows], n, k,
+                                   ra, wl.num_tokens if t is None else 1, wl.num_experts, d.a_table,
+                                   d.b_table, d.scale, wl.max_loras, wl.max_rank, wl.k_in, wl.n_out,
+                                   xa=d.xa[rows], a_tmaps=m)
+        torch.cuda.synchronize()
+        res.append((to_u16(d.out_buf), to_u16(d.xa)[: wl.n_rows]))
+    assert np.array_equal(res[0][0], res[1][0])
+    routed = [r for r, _ in gather_routes(wl)]
+    assert np.array_equal(res[0][1][routed], res[1][1][routed])
+    o_out, o_xa, o_d = oracle_gather(wl)
+    compare_gather(wl, res[0][0], o_out, res[0][1], o_xa, o_d, gather_routes(wl))
 
 
 def test_gather_graph_replay_with_new_routing():

@@ -74,6 +74,8 @@ def test_moe_writes_stay_inside(name, one_call):
     res = []
     for guard in (False, True):
         d = W.moe_to_device(wl, xa_rows=max(hi - lo for lo, hi in windows))
+        # xa holds exactly the largest window's rows: its band starts at row xa_rows
+        assert d.xa.shape[0] == max(hi - lo for lo, hi in windows)
         d, bands = _guard(d, guard, "out_buf", "xa")
         for lo, hi in windows:
             L.lora_moe_grouped_fold(d.x, wl.k_in, d.out_buf, wl.n_out, d.expert_offsets,
@@ -119,3 +121,17 @@ def test_delta_writes_stay_inside(name, rows):
         res.append((to_u16(d.out_buf), to_u16(d.xa)))
     assert np.array_equal(res[0][0], res[1][0]) and np.array_equal(res[0][1], res[1][1])
 
+
+
+def test_moe_undersized_xa_is_rejected_before_launch():
+    """An xa of fewer rows than the window is refused on the host; nothing runs."""
+    wl = W.moe_down_fold()
+    lo, hi = wl.windows()[0]
+    d = W.moe_to_device(wl, xa_rows=hi - lo)
+    with pytest.raises(L.LoraError, match="LORA_ERR_SIZE"):
+        L.lora_moe_grouped_fold(d.x, wl.k_in, d.out_buf, wl.n_out, d.expert_offsets, wl.num_experts,
+                                d.sorted_token_ids, wl.te, d.row_adapter, wl.num_tokens, lo, hi,
+                                d.a_table, d.b_table, d.scale, wl.max_loras, wl.max_rank, wl.k_in,
+                                wl.n_out, xa=d.xa, xa_rows=hi - lo - 1)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_u16(d.out_buf), wl.out_buf)

@@ -2,8 +2,9 @@
 
 The oracle's own result, offered as the GPU result, must pass; each kind of
 mistake a kernel could make must be rejected: a changed byte outside a folded
-segment or in a row without a delta, a folded value far off, a wrong xa, and
-too many values that are each within the bound but not bit-exact.
+segment or in a row without a delta, a folded value far off, a wrong xa, a few
+values a few ulps off, an xa (and the fold made from it) missing the last k
+terms of a row, and too many values that are each one ulp off.
 """
 from __future__ import annotations
 
@@ -13,8 +14,8 @@ import pytest
 import oracle
 from gather_lora_gb300 import workloads as W
 from gpu_util import oracle_bgmv, oracle_delta, oracle_gather, oracle_moe
-from parity import (compare_bgmv, compare_delta, compare_gather, compare_moe, gather_routes,
-                    moe_routes, routed_bgmv_rows)
+from parity import (bf16_of_f64, compare_bgmv, compare_delta, compare_gather, compare_moe,
+                    expand_oracle_order, fold_bits, gather_routes, moe_routes, routed_bgmv_rows)
 
 F = W.bf16_bits_to_f32
 
@@ -42,16 +43,45 @@ def test_oracle_result_passes(bg):
     assert st["rows"] > 5 and st["exact"] == st["total"] > 0
 
 
-def test_one_ulp_passes_and_a_sign_flip_fails(bg):
+def _consistent_row(wl, i, s, xa_row):
+    """Row i's folded segment as a correct kernel would give it from `xa_row`: the
+    expand in the oracle's order, the BF16 delta, one fp32 fma and BF16 rounding."""
+    S = expand_oracle_order(xa_row[None], wl.b_pool[s])[0]
+    d = bf16_of_f64(S.astype(np.float64))
+    seg = wl.out_buf[i, wl.out_offset:wl.out_offset + wl.n_out]
+    return fold_bits(wl.scale[s], d, seg)
+
+
+def test_xa_flip_and_its_fold_pass_and_a_sign_flip_fails(bg):
+    """An xa value one ulp off (a summation-order flip), with the fold made from it,
+    passes; the same magnitude with the other sign in the output fails."""
+    wl, out, xa, d = bg
+    i, s = routed_bgmv_rows(wl)[0]
+    c = int(np.argmax(np.abs(F(xa[i]))))
+    gx = xa.copy()
+    gx[i, c] = xa[i, c] + 1
+    g = out.copy()
+    seg = slice(wl.out_offset, wl.out_offset + wl.n_out)
+    g[i, seg] = _consistent_row(wl, i, s, gx[i])
+    st = compare_bgmv(wl, g, out, gx, xa, d, min_exact=0.0)
+    assert st["xa_max_ulps"] == 1
+    j = _big_element(wl, out, i)
+    g = out.copy()
+    g[i, j] = out[i, j] ^ 0x8000                 # same magnitude, other sign
+    with pytest.raises(AssertionError, match="fold"):
+        compare_bgmv(wl, g, out, xa, xa, d)
+
+
+def test_a_one_ulp_fold_change_without_a_flip_fails(bg):
+    """With xa equal to the oracle's and the expand sum away from a rounding
+    boundary, a folded value one ulp off is not a summation-order effect."""
     wl, out, xa, d = bg
     i, _ = routed_bgmv_rows(wl)[0]
     j = _big_element(wl, out, i)
     g = out.copy()
-    g[i, j] = out[i, j] + 1                      # the next BF16 value: one ulp away
-    compare_bgmv(wl, g, out, xa, xa, d)
-    g[i, j] = out[i, j] ^ 0x8000                 # same magnitude, other sign
+    g[i, j] = out[i, j] + 1
     with pytest.raises(AssertionError, match="fold"):
-        compare_bgmv(wl, g, out, xa, xa, d)
+        compare_bgmv(wl, g, out, xa, xa, d, min_exact=0.0)
 
 
 def test_bytes_outside_the_segment_and_base_rows_are_exact(bg):
@@ -83,15 +113,17 @@ def test_wrong_xa_fails(bg):
 
 
 def test_too_many_inexact_values_fail(bg):
+    """Three rows whose every xa value is one ulp off (folds made from them): each
+    value passes the rules, but the bit-exact floor rejects that many."""
     wl, out, xa, d = bg
-    g = out.copy()
+    g, gx = out.copy(), xa.copy()
     seg = slice(wl.out_offset, wl.out_offset + wl.n_out)
-    routed = [i for i, _ in routed_bgmv_rows(wl)]
-    for i in routed[:3]:                         # every value of three rows one ulp off
-        g[i, seg] = out[i, seg] + 1
+    for i, s in routed_bgmv_rows(wl)[:3]:
+        gx[i] = xa[i] + 1
+        g[i, seg] = _consistent_row(wl, i, s, gx[i])
     with pytest.raises(AssertionError, match="bit-exact"):
-        compare_bgmv(wl, g, out, xa, xa, d)
-    compare_bgmv(wl, g, out, xa, xa, d, min_exact=0.0)   # each value is within the bound
+        compare_bgmv(wl, g, out, gx, xa, d)
+    compare_bgmv(wl, g, out, gx, xa, d, min_exact=0.0)   # each value is within the rules
 
 
 def test_moe_rule_passes_oracle_and_rejects_mistakes():
@@ -143,3 +175,63 @@ def test_delta_rule_passes_oracle_and_rejects_mistakes():
     g[3, wl.out_offset + wl.n_out] ^= 1          # a byte after the folded segment
     with pytest.raises(AssertionError, match="outside the folded segments"):
         compare_delta(wl, g, out, xa, xa, d)
+
+
+def test_few_values_a_few_ulps_off_fail(bg):
+    """+3 ulps on 0.5% of the folded values (at least one) is not a summation-order
+    effect: the fold is no longer the fold of the row's own xa."""
+    wl, out, xa, d = bg
+    seg = slice(wl.out_offset, wl.out_offset + wl.n_out)
+    routed = [i for i, _ in routed_bgmv_rows(wl)]
+    rng = np.random.default_rng(0)
+    n_bad = max(1, int(0.005 * len(routed) * wl.n_out))
+    g = out.copy()
+    for _ in range(n_bad):
+        i = int(rng.choice(routed))
+        j = wl.out_offset + int(rng.integers(wl.n_out))
+        g[i, j] = out[i, j] + 3
+    with pytest.raises(AssertionError, match="fold"):
+        compare_bgmv(wl, g, out, xa, xa, d, min_exact=0.0)
+
+
+def test_one_xa_value_three_ulps_off_fails(bg):
+    wl, out, xa, d = bg
+    i, _ = routed_bgmv_rows(wl)[0]
+    c = int(np.argmax(np.abs(F(xa[i]))))        # a large, well-conditioned value
+    gx = xa.copy()
+    gx[i, c] = xa[i, c] + 3
+    with pytest.raises(AssertionError, match="xa"):
+        compare_bgmv(wl, out, out, gx, xa, d, min_exact=0.0)
+
+
+def test_dropped_k_tail_on_one_row_fails(bg):
+    """A kernel that drops the last 16 k terms of one row (and folds consistently
+    from that wrong xa) is caught by the xa rule."""
+    wl, out, xa, d = bg
+    i, _ = routed_bgmv_rows(wl)[1]
+    bad = W.BgmvWorkload(**{**wl.__dict__})
+    bad.x = wl.x.copy()
+    bad.x[i, wl.k_in - 16:wl.k_in] = 0
+    b_out, b_xa, b_d = oracle_bgmv(bad)
+    g, gx = out.copy(), xa.copy()
+    g[i], gx[i] = b_out[i], b_xa[i]
+    assert not np.array_equal(gx[i], xa[i])
+    with pytest.raises(AssertionError, match="xa"):
+        compare_bgmv(wl, g, out, gx, xa, d, min_exact=0.0)
+
+
+def test_reported_ulp_distances(bg):
+    wl, out, xa, d = bg
+    st = compare_bgmv(wl, out.copy(), out, xa.copy(), xa, d)
+    assert st["max_ulps"] == 0 and st["xa_max_ulps"] == 0 and st["beyond_1ulp"] == 0
+
+
+def test_fold_helpers_against_the_oracle(bg):
+    """The rule's own fp32 fma and BF16 rounding reproduce the oracle's folded
+    values from the oracle's deltas bit for bit."""
+    wl, out, xa, d = bg
+    seg = slice(wl.out_offset, wl.out_offset + wl.n_out)
+    for i, s in routed_bgmv_rows(wl):
+        assert np.array_equal(fold_bits(wl.scale[s], d[i], wl.out_buf[i, seg]), out[i, seg])
+        S = expand_oracle_order(xa[i][None], wl.b_pool[s])[0]
+        assert np.array_equal(bf16_of_f64(S.astype(np.float64)), d[i])
