@@ -89,11 +89,11 @@ int device_sm_count_or(int fallback) {
 #ifndef GLORA_MAX_CLUSTER
 #define GLORA_MAX_CLUSTER 8
 #endif
+#ifndef GLORA_MOE_TILE_SHRINK
+#define GLORA_MOE_TILE_SHRINK 0
+#endif
 #ifndef GLORA_MOE_GROUP_ROWS
 #define GLORA_MOE_GROUP_ROWS 16
-#endif
-#ifndef GLORA_MOE_MIN_UNITS
-#define GLORA_MOE_MIN_UNITS 128
 #endif
 constexpr int kBudgetTwoPerSm = GLORA_BUDGET_TWO_PER_SM;
 constexpr int kBudgetOnePerSm = 225 * 1024;
@@ -117,7 +117,6 @@ constexpr int kClusterCapHighRank = GLORA_CLUSTER_CAP_HIGH_RANK;
 constexpr int kMoeStageTarget = GLORA_MOE_STAGE_TARGET;
 constexpr int kMinStage = GLORA_MIN_STAGE;
 constexpr int kMaxStages = 8;
-constexpr long long kMoeMinUnits = GLORA_MOE_MIN_UNITS;  // MoE work units that keep the GPU busy
 constexpr int kGatherBytes = 24 * 1024;                  // largest all-gather buffer of the exchange
 
 // Split `total` into equal chunks of at most `cap` (multiples of 16).
@@ -172,7 +171,7 @@ bool make_geometry_at(bool moe, int rows, int max_loras, int planner_ints, int m
   // latency chains of several items overlap) or are split tile by tile over
   // all consumer warps in order (one bgmv group, or larger groups).
   const int tiles = mt * static_cast<int>(ceil_div(g.gmax, 8));
-  g.group_parallel = (moe && tiles <= 4 && g.kch >= g.ksl) ? 1 : 0;
+  g.group_parallel = (moe && !GLORA_MOE_TILE_SHRINK && tiles <= 4 && g.kch >= g.ksl) ? 1 : 0;
   // With cluster peers and small fp32 partials, the exchange is an all-gather
   // (one cluster barrier; each CTA adds the slots itself). Tile-parallel groups
   // of few tiles also split k over the consumer warps (ksplit k-phases of
@@ -220,16 +219,8 @@ bool make_geometry_at(bool moe, int rows, int max_loras, int planner_ints, int m
   g.smem_bytes = g.off_xa + g.rt * g.pitch_xa;
   if (g.smem_bytes > kBudgetOnePerSm + 2048) return false;
   if (moe) {
-    // MoE (max_loras = adapters the grid covers): the largest scan tile that
-    // still gives kMoeMinUnits work units; at least one tile.
-    g.tile_rows = LORA_MOE_M_TILE;
-    for (int tr = glora::kMaxTileRows; tr > LORA_MOE_M_TILE; tr /= 2)
-      if (ceil_div(rows, tr) * max_loras >= kMoeMinUnits) { g.tile_rows = tr; break; }
-    const long long clusters = std::max(1LL, ceil_div(rows, g.tile_rows)) * max_loras;
-    if (clusters * g.cl > INT_MAX) return false;   // the grid would not fit a launch
-    g.clusters = static_cast<int>(clusters);
+    g.clusters = 0;   // the persistent grid and layout: moe_geometry()
   } else {
-    g.tile_rows = g.rt;
     // Direct numbering (unit s = tile 0 of slot s) plans fastest, but its empty
     // units (slots without rows) sit between the real ones in launch order.
     // When the grid is more than one wave of CTAs (two per SM) and slots are
@@ -258,6 +249,38 @@ bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_
     return true;
   return make_geometry_at(moe, rows, max_loras, planner_ints, max_rank, k_in, n_out, g, max_cl, a_tiled,
                           kStageTarget, unit_rows);
+}
+
+// The MoE fold's launch: the arithmetic (k chunks, shrink mode, row tiles) from
+// the shapes alone, as for every fold, so a row's bits never depend on the
+// window; then the persistent layout: the CTA's plan (MoePlan) before the ring,
+// as many ring stages as fit kMoeCtasPerSm CTAs per SM, and a grid of one such
+// CTA set per SM (fewer for small windows, at least 16 rows per CTA). Each CTA
+// plans its units in the ring before its first fold (offsets, its units, the
+// counts of their groups).
+bool moe_geometry(int window, int adapters, int num_experts, int max_rank, int k_in, int n_out, int sms,
+                  glora::FoldGeometry& g) {
+  if (!make_geometry(true, window, adapters, 0, max_rank, k_in, n_out, g)) return false;
+  const int budget = glora::kMoeCtasPerSm == 1 ? kBudgetOnePerSm : kBudgetTwoPerSm;
+  const int planes = g.ksplit + (g.gather ? g.cl : 0);
+  const int tail = planes * g.rt * g.pitch_part * 4 + g.rt * g.pitch_xa;
+  g.off_mplan = glora::kPlanBytes;
+  g.off_ring = round_up(g.off_mplan + static_cast<int>(sizeof(glora::MoePlan)), 1024);
+  const int ns = std::min(kMaxStages, (budget - g.off_ring - tail) / g.stage_bytes);
+  if (ns < 2) return false;
+  g.ns = ns;
+  g.off_part = g.off_ring + ns * g.stage_bytes;
+  g.off_xa = g.off_part + planes * g.rt * g.pitch_part * 4;
+  g.smem_bytes = g.off_xa + g.rt * g.pitch_xa;
+  const long long bins = static_cast<long long>(num_experts) * adapters;
+  // planner scratch: offsets, four unit arrays, the groups of a round
+  const long long scratch = ((num_experts + 4) & ~3) * 4LL + (4LL * 64 + 4) * 4 +
+                            static_cast<long long>(std::max(glora::kMoeMaxDesc, adapters)) * 4;
+  const long long ring = static_cast<long long>(ns) * g.stage_bytes;
+  if (bins > glora::kMoeMaxBins || scratch > ring) return false;
+  g.clusters = static_cast<int>(std::max<long long>(1, std::min<long long>(static_cast<long long>(sms) * glora::kMoeCtasPerSm,
+                                                                            ceil_div(window, 16))));
+  return true;
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once (NULL without a driver).
@@ -414,6 +437,9 @@ int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, int32_t x_
     return fail(LORA_ERR_SIZE, "num_experts %d outside [1, %d]", num_experts, LORA_MAX_EXPERTS);
   if (max_loras < 1 || max_loras > LORA_MAX_LORAS)
     return fail(LORA_ERR_SIZE, "max_loras %d outside [1, %d]", max_loras, LORA_MAX_LORAS);
+  if (static_cast<int64_t>(max_loras) * num_experts > LORA_MAX_LORAS)
+    return fail(LORA_ERR_SIZE, "max_loras %d x num_experts %d outside [1, %d] table entries", max_loras,
+                num_experts, LORA_MAX_LORAS);
   if (te < 0 || num_tokens < 0) return fail(LORA_ERR_SIZE, "te %d and num_tokens %d must be >= 0", te, num_tokens);
   if (row_offset < 0 || row_end < row_offset || row_end > te)
     return fail(LORA_ERR_WINDOW, "window [%d, %d) outside [0, te=%d]", row_offset, row_end, te);
@@ -429,11 +455,11 @@ int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, int32_t x_
   if (!aligned16(x) || !aligned16(base_out) || (xa && !aligned16(xa)))
     return fail(LORA_ERR_ALIGN, "x, base_out and xa must be 16-byte aligned");
   glora::MoeArgs a{};
-  if (!make_geometry(true, row_end - row_offset, row_adapter ? max_loras : 1, num_experts + 1, max_rank, k_in,
-                     n_out, a.g))
-    return fail(LORA_ERR_SIZE, "no launch geometry for a window of %d rows x %d adapters at max_rank %d, k_in %d, "
-                "n_out %d (shared memory or grid size)", row_end - row_offset, row_adapter ? max_loras : 1, max_rank,
-                k_in, n_out);
+  const int adapters = row_adapter ? max_loras : 1;
+  if (!moe_geometry(row_end - row_offset, adapters, num_experts, max_rank, k_in, n_out, device_sm_count_or(152), a.g))
+    return fail(LORA_ERR_SIZE, "no launch geometry for %d experts x %d adapters at max_rank %d, k_in %d, n_out %d "
+                "(shared memory)", num_experts, adapters, max_rank, k_in, n_out);
+  a.adapters = adapters;
   a.x = x;
   a.x_stride = x_row_stride;
   a.out = base_out;
@@ -620,12 +646,12 @@ int lora_launch_geometry(int moe, int32_t rows, int32_t max_loras, int32_t max_r
   glora::FoldGeometry g{};
   const int kind = moe & 15;
   const bool grouped = kind == 1;
-  const int scratch = grouped ? LORA_MAX_EXPERTS + 1 : ((rows + 3) & ~3) + max_loras;
-  // stands for a tensor-map array (only its presence matters); the grouped fold ignores maps
+  // stands for a tensor-map array (only its presence matters); the grouped fold takes none
   static const char kAnyMaps = 0;
-  if (!fold_geometry(grouped, rows, max_loras, scratch, max_rank, k_in, n_out, g,
-                     kind == 2 ? GLORA_GATHER_MAX_CL : GLORA_MAX_CLUSTER, (moe & 16) && !grouped ? &kAnyMaps : nullptr,
-                     kind == 2 ? kGatherUnitRows : kUnitRows))
+  if (grouped ? !moe_geometry(std::max(rows, 0), max_loras, 1, max_rank, k_in, n_out, device_sm_count_or(152), g)
+              : !fold_geometry(false, rows, max_loras, ((rows + 3) & ~3) + max_loras, max_rank, k_in, n_out, g,
+                               kind == 2 ? GLORA_GATHER_MAX_CL : GLORA_MAX_CLUSTER,
+                               (moe & 16) ? &kAnyMaps : nullptr, kind == 2 ? kGatherUnitRows : kUnitRows))
     return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory and the grid size");
   const int64_t v[12] = {g.cl, g.rt, g.ksl, g.jsl, g.kch, g.jch, g.ns, g.clusters, g.smem_bytes, g.a_tiled, g.tc, g.direct};
   std::memcpy(out, v, sizeof v);

@@ -7,9 +7,11 @@ namespace glora {
 
 constexpr int kMaxGroupRows = 16;  // rows of one group (one adapter's rows folded together)
 constexpr int kMaxRows = 64;        // rows (positions) per pass of a work unit
-constexpr int kMaxTileRows = 256;   // sorted rows one MoE work unit scans
 constexpr int kMaxTilesPerWarp = 4; // 16x8 shrink tiles a warp may own: MT * NT <= 32
-constexpr int kPlanBytes = 7168;    // shared memory reserved for the work-unit plan
+constexpr int kPlanBytes = 4096;    // shared memory reserved for the work-unit plan
+constexpr int kMoeMaxDesc = 128;    // MoE: (expert, adapter) groups (runs) one CTA plans per round
+constexpr int kMoeMaxPos = 1024;    // MoE: rows one CTA scans (so at most folds) per round
+constexpr int kMoeMaxBins = 4096;   // MoE: (expert, adapter) groups of a window (num_experts * adapters)
 constexpr int kConsumerWarps = 8;   // tensor-core / fold warps per CTA
 constexpr int kProducerWarps = 4;   // TMA-issuing warps per CTA (one warpgroup)
 
@@ -20,7 +22,6 @@ constexpr int kProducerWarps = 4;   // TMA-issuing warps per CTA (one warpgroup)
 struct FoldGeometry {
   int cl;           // CTAs per cluster
   int rt;           // rows per pass of a work unit (<= kMaxRows)
-  int tile_rows;    // MoE: sorted rows scanned per work unit (64, 128 or 256)
   int ksl, jsl;     // k-slice / j-slice per CTA (multiples of 16)
   int kch, jch;     // k columns / B rows per ring stage (multiples of 16)
   int ns;           // ring depth (>= 2)
@@ -42,6 +43,7 @@ struct FoldGeometry {
   int pitch_xa;     // bytes per xa row (max_rank*2 + 16)
   int stage_bytes;
   int off_ring, off_out, off_part, off_xa, smem_bytes;
+  int off_mplan;    // MoE: the CTA's planned row runs and rows (MoePlan), before the ring
   int clusters;     // grid = clusters * cl CTAs
 };
 
@@ -81,6 +83,7 @@ struct MoeArgs {
   int num_tokens;
   int x_gather;     // 1: x is token-major; sorted row r reads row sorted_token_ids[r]
   int row_offset, row_end;
+  int adapters;     // adapters the routing distinguishes: max_loras with a row_adapter, else 1
   const uint16_t* const* a_table;
   const uint16_t* const* b_table;
   const float* scale_table;
@@ -89,6 +92,29 @@ struct MoeArgs {
   uint16_t* xa;
   FoldGeometry g;
 };
+
+// MoE fold: one run of an (expert, adapter) group's rows planned for a CTA, and
+// the CTA's plan of one round (its runs and their rows, run after run).
+struct MoeDesc {
+  int e, a;                // expert, adapter
+  int i_lo, n;             // the run's rows: n rows of the group
+  int pos0;                // first position of the run in the CTA's row list
+  float scale;
+  const uint16_t* A;       // NULL: entry NULL or misaligned (the rows stay unchanged)
+  const uint16_t* B;
+};
+struct MoePlan {
+  int nd, npos, more;
+  MoeDesc desc[kMoeMaxDesc];
+  int pos_row[kMoeMaxPos];     // sorted row of each position
+  int pos_tok[kMoeMaxPos];     // its token (the x row of the gate/up form)
+  short pos_desc[kMoeMaxPos];  // its run
+};
+
+#ifndef GLORA_MOE_CTAS_PER_SM
+#define GLORA_MOE_CTAS_PER_SM 1
+#endif
+constexpr int kMoeCtasPerSm = GLORA_MOE_CTAS_PER_SM;   // resident MoE CTAs per SM (the persistent grid)
 
 // Launchers (kernels.cu). Return 0 or a cudaError_t value.
 int launch_bgmv(const BgmvArgs& a, void* stream);

@@ -83,9 +83,6 @@ struct Plan {
   const void* gmap[kMaxRows];      // the group's A tensor map (a_tiled launches)
   unsigned long long tc_done;      // tcgen05 shrink: the unit's partial is in TMEM
   uint32_t tmem;                   // tcgen05 shrink: TMEM base address
-  int tpos[kMaxTileRows];          // MoE: tile rows routed to this unit's adapter, ascending
-  int tkey[kMaxTileRows];          // MoE: their experts
-  int txrow[kMaxTileRows];         // MoE: their rows of x (the token with x_gather)
 };
 
 static_assert(sizeof(Plan) <= kPlanBytes, "plan does not fit its shared-memory reservation");
@@ -155,9 +152,11 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
   const int n_shrink = G * nk, n_items = G * (nk + nj);
   const int out_region = g.jch * g.pitch_b;   // byte offset of the out rows inside an expand stage
   const int pitch_o = g.jch * 2 + 16;
-  // CTA-wide barrier of the exchange (a cluster barrier when the cluster has peers)
+  // Barrier of the exchange: a cluster barrier when the cluster has peers;
+  // otherwise only the consumer warps take part (the producer never touches
+  // the partials or xa, so it keeps filling the ring meanwhile).
   auto unit_sync = [&]() {
-    if (g.cl > 1) cluster.sync(); else __syncthreads();
+    if (g.cl > 1) cluster.sync(); else consumer_sync();
   };
 
   if (warp >= kConsumerWarps) {
@@ -271,10 +270,12 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
     // Items whose stage is freed by shrink work can be issued before the
     // cluster exchange; the rest only after it (their stages are released by
     // expand work, which needs the exchanged xa).
-    const int pre = min(n_items, n_shrink + ns);
+    const int pre = g.cl > 1 ? min(n_items, n_shrink + ns) : n_items;
     for (int it = 0; it < pre; ++it) produce(it);
-    unit_sync();
-    if (!g.gather) unit_sync();
+    if (g.cl > 1) {
+      cluster.sync();
+      if (!g.gather) cluster.sync();
+    }
     for (int it = pre; it < n_items; ++it) produce(it);
     if (*reinterpret_cast<volatile int*>(&pl.failed)) {
       // A wait gave up somewhere: before the CTA can exit, let this thread's own
@@ -592,8 +593,8 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
         const uint32_t st = ring_u32 + s * g.stage_bytes;
         const int j0 = j_lo + jc * g.jch, jlen = min(g.jch, j_hi - j0), NCB = (jlen + 15) >> 4;
         const bool store = pl.failed == 0;
-        for (int cb = warp; cb < NCB; cb += kConsumerWarps) {
-          float d[MR][2][4];
+        // One 16-column block: both 16x8 tiles of every 16-row tile of the group.
+        auto block_mma = [&](int cb, float (&d)[MR][2][4]) {
 #pragma unroll
           for (int mr = 0; mr < MR; ++mr)
 #pragma unroll
@@ -635,25 +636,60 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
               }
             }
           }
+        };
+        // The staged old values of a block's rows (rows past R read the last
+        // row: in bounds, never stored).
+        auto block_old = [&](int cb, uint32_t (&o)[2 * MR][2]) {
+          const int c0 = cb * 16;
+#pragma unroll
+          for (int hh = 0; hh < 2 * MR; ++hh) {
+            if (hh == 0 || hh * 8 < R) {                // warp-uniform: this row half has rows
+              asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(o[hh][0]) : "r"(st + rowoff[hh] + c0 * 2));
+              asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(o[hh][1]) : "r"(st + rowoff[hh] + c0 * 2 + 16));
+            }
+          }
+        };
+        // Fold and store a block: lane (g, q) folds columns 2q, 2q+1 of both
+        // tiles for rows g and g + 8; one exchange with lane q ^ 1 leaves it
+        // four adjacent columns (a full 8-byte store; each row's 32 bytes
+        // leave as one sector).
+        auto block_fold = [&](int cb, const float (&d)[MR][2][4], const uint32_t (&o)[2 * MR][2]) {
           const int c0 = cb * 16;
           const bool col_ok = c0 + scol < jlen;         // the last block may hold only 8 columns
 #pragma unroll
           for (int hh = 0; hh < 2 * MR; ++hh) {
             const int mr = hh >> 1, h = hh & 1;
-            if (hh == 0 || hh * 8 < R) {                // warp-uniform: this row half has rows
-              uint32_t o0, o1;
-              asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(o0) : "r"(st + rowoff[hh] + c0 * 2));
-              asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(o1) : "r"(st + rowoff[hh] + c0 * 2 + 16));
-              const uint32_t f0 = fold_pair(d[mr][0][2 * h], d[mr][0][2 * h + 1], scale, o0);
-              const uint32_t f1 = fold_pair(d[mr][1][2 * h], d[mr][1][2 * h + 1], scale, o1);
+            if (hh == 0 || hh * 8 < R) {
+              const uint32_t f0 = fold_pair(d[mr][0][2 * h], d[mr][0][2 * h + 1], scale, o[hh][0]);
+              const uint32_t f1 = fold_pair(d[mr][1][2 * h], d[mr][1][2 * h + 1], scale, o[hh][1]);
               const uint32_t recv = __shfl_xor_sync(0xffffffffu, odd ? f0 : f1, 1);
-              uint16_t* o = obase[hh];
-              if (o && store && col_ok) {
+              uint16_t* ob = obase[hh];
+              if (ob && store && col_ok) {
                 const uint32_t lo = odd ? recv : f0, hi = odd ? f1 : recv;
-                asm volatile("st.global.v2.b32 [%0], {%1, %2};\n" ::"l"(o + j0 + c0), "r"(lo), "r"(hi) : "memory");
+                asm volatile("st.global.v2.b32 [%0], {%1, %2};\n" ::"l"(ob + j0 + c0), "r"(lo), "r"(hi) : "memory");
               }
             }
           }
+        };
+        // Two blocks per step (cb and cb + 8): both blocks' loads and MMAs are
+        // issued before either block's dependent fold.
+        int cb = warp;
+        for (; cb + kConsumerWarps < NCB; cb += 2 * kConsumerWarps) {
+          float da[MR][2][4], db[MR][2][4];
+          uint32_t oa[2 * MR][2], ob2[2 * MR][2];
+          block_mma(cb, da);
+          block_mma(cb + kConsumerWarps, db);
+          block_old(cb, oa);
+          block_old(cb + kConsumerWarps, ob2);
+          block_fold(cb, da, oa);
+          block_fold(cb + kConsumerWarps, db, ob2);
+        }
+        if (cb < NCB) {
+          float da[MR][2][4];
+          uint32_t oa[2 * MR][2];
+          block_mma(cb, da);
+          block_old(cb, oa);
+          block_fold(cb, da, oa);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&pl.empty[s]));
@@ -845,153 +881,292 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
 }
 
 // ============================================================================
-// MoE grouped fold: work unit = the rows of one adapter within one tile of
-// tile_rows sorted rows of the window. grid = ceil(window / tile_rows) tiles
-// (>= 1) x (max_loras, or 1 without a row_adapter). The unit's rows, in sorted
-// order, are folded in passes of up to kMaxRows rows; a pass is split into
-// runs of one expert of at most gmax rows (the rows are sorted by expert, so
-// each run belongs to one (adapter, expert) group), and every group is folded
-// over the full k_in and n_out.
+// MoE grouped fold: persistent CTAs over units of the window's (expert,
+// adapter) groups.
+//
+// The rows of a window are sorted by expert; the rows of one (expert e,
+// adapter a) group share A and B, so each group should be read once. A unit
+// is one expert of the window and a chunk of `ac` adapters: its groups are
+// (e, a) for a in the chunk. The chunk size follows the window's expert count
+// (about kMoeUnitsPerCta units per CTA), and CTA b of G takes units b, b + G,
+// ... A CTA plans only its own units: it reads the expert offsets, then the
+// token and adapter of each row of its units' experts (two memory round trips,
+// the units' table entries loaded beside them), and numbers each routed row
+// within its group with one shared-memory atomic. Which rows share a group of
+// the fold never changes a row's arithmetic, so that order may vary.
+// Rows are taken kMoeRoundRows at a time (rounds) from the CTA's units' rows,
+// folded in passes of up to kMaxRows rows, split into groups of at most gmax
+// rows of one (expert, adapter) pair, each folded over the full k_in and n_out.
 // ============================================================================
+constexpr int kMoeUnitsPerCta = 2;
+constexpr int kMoeRoundRows = kMoeMaxPos;    // rows of the units' experts scanned per round
+constexpr int kMoeRowsPerThread = (kMoeRoundRows + kThreads - 1) / kThreads;
+constexpr int kMoeMaxMyUnits = 64;           // units of one CTA planned per round
+
 template <int MAXT>
-__global__ void __launch_bounds__(kThreads, 2) lora_moe_fold_kernel(const __grid_constant__ MoeArgs p) {
+__global__ void __launch_bounds__(kThreads, kMoeCtasPerSm) lora_moe_fold_kernel(const __grid_constant__ MoeArgs p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const FoldGeometry& g = p.g;
   const cg::cluster_group cluster = cg::this_cluster();
-  const int crank = static_cast<int>(cluster.block_rank());
-  const int adapters = p.row_adapter ? p.max_loras : 1;
-  const int unit = static_cast<int>(blockIdx.x) / g.cl;
-  const int tile = unit / adapters, adapter = unit - tile * adapters;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   Plan& pl = *reinterpret_cast<Plan*>(smem);
-  const int E = p.num_experts;
+  MoePlan& mp = *reinterpret_cast<MoePlan*>(smem + g.off_mplan);
+  const int E = p.num_experts, A = p.adapters;
+  const bool need_token = p.row_adapter != nullptr || p.x_gather != 0;
+  const int G = gridDim.x, b = blockIdx.x;
+
+  // Planning scratch in the ring (free until the first fold): the expert
+  // offsets and, per round, the CTA's units (expert, first adapter, rows) and
+  // the counts of their groups.
+  unsigned char* ring = smem + g.off_ring;
+  int* offs = reinterpret_cast<int*>(ring);
+  int* u_e = offs + ((E + 4) & ~3);            // [kMoeMaxMyUnits] expert of each unit of the round
+  int* u_a0 = u_e + kMoeMaxMyUnits;            // first adapter of its chunk
+  int* u_lo = u_a0 + kMoeMaxMyUnits;           // its rows in the window: [u_lo, u_hi)
+  int* u_row0 = u_lo + kMoeMaxMyUnits;         // prefix of the units' rows (+1 entry)
+  int* bcnt = u_row0 + kMoeMaxMyUnits + 4;     // [units * ac] rows of each group in the round
 
   pdl_wait_then_release();
 
-  const int r0 = p.row_offset + tile * g.tile_rows;
-  const int T = min(g.tile_rows, p.row_end - r0);
-  int* offs = reinterpret_cast<int*>(smem + g.off_ring);  // expert_offsets copy (ring not yet used)
-  for (int i = tid; i <= E; i += kThreads) offs[i] = p.expert_offsets[i];
-  // The row's token (the adapter gate; the x row of the gate/up form).
-  const bool need_token = p.row_adapter != nullptr || p.x_gather != 0;
-  int token = -1;
-  if (need_token && tid < T) token = p.sorted_token_ids[r0 + tid];   // overlaps the offsets load
-  __syncthreads();
-
-  // Per tile row: expert by binary search, then the adapter gate.
-  int expert = -1;
-  if (tid < T) {
-    const int r = r0 + tid;
-    if (r >= offs[0] && r < offs[E]) {
-      int lo = 0, hi = E;  // largest e in [0, E) with offs[e] <= r
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (offs[mid] <= r) lo = mid; else hi = mid;
-      }
-      if (offs[lo] <= r && r < offs[lo + 1]) {
-        int a = 0;
-        bool ok = true;
-        if (need_token) {
-          if (token < 0 || token >= p.num_tokens) ok = false;
-          else if (p.row_adapter) a = p.row_adapter[token];
-        }
-        if (ok && a == adapter) expert = lo;   // a outside [0, max_loras) matches no unit
-      }
+  // Expert of sorted row r (-1 outside the spans): the largest e with offs[e] <= r.
+  auto expert_of = [&](int r) -> int {
+    if (r < offs[0] || r >= offs[E]) return -1;
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (offs[mid] <= r) lo = mid; else hi = mid;
     }
-  }
-  // Ordered compaction of this adapter's rows (one ballot per warp).
-  const unsigned bal = __ballot_sync(0xffffffffu, expert >= 0);
-  if (lane == 0) pl.warp_sums[warp] = __popc(bal);
+    return (offs[lo] <= r && r < offs[lo + 1]) ? lo : -1;
+  };
+
+  for (int i = tid; i <= E; i += kThreads) offs[i] = p.expert_offsets[i];
   __syncthreads();
-  int before = 0, npos = 0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    const int c = pl.warp_sums[w];
-    before += (w < warp) ? c : 0;
-    npos += c;
-  }
-  if (npos == 0) return;  // nothing for this adapter in this tile
-  if (expert >= 0) {
-    const int rank = before + __popc(bal & ((1u << lane) - 1u));
-    pl.tpos[rank] = tid;
-    pl.tkey[rank] = expert;
-    pl.txrow[rank] = p.x_gather ? token : r0 + tid;
-  }
-  ring_init(pl, g.ns);   // (its barrier also publishes tpos / tkey)
+  const int lo_w = max(p.row_offset, offs[0]), hi_w = min(p.row_end, offs[E]);
+  if (hi_w <= lo_w) return;                      // every thread agrees
+  int e_first = expert_of(lo_w), e_last = expert_of(hi_w - 1);
+  if (e_first < 0 || e_last < e_first) { e_first = 0; e_last = E - 1; }   // offsets out of order: all experts
+  const int E_w = e_last - e_first + 1;
+  const int n_chunks0 = min(A, max(1, (kMoeUnitsPerCta * G) / E_w));
+  const int ac = (A + n_chunks0 - 1) / n_chunks0, n_chunks = (A + ac - 1) / ac;
+  const long long n_units = static_cast<long long>(E_w) * n_chunks;
+  const int my_units = n_units > b ? static_cast<int>((n_units - b + G - 1) / G) : 0;
 
   const EngineArgs ea{p.x, p.x_stride, p.out, p.out_stride, p.xa, p.max_rank, p.k_in, p.n_out};
   int it0 = 0;
-  for (int base = 0; base < npos; base += kMaxRows) {
-    const int P = min(kMaxRows, npos - base);
-    // Groups: a new group where the expert changes, and every gmax rows of a run.
-    if (tid < kMaxRows) {
-      bool start = false;
-      int e = -1;
+  bool ring_ready = false;
+  // Rounds over the CTA's units: units [v0, v1) of its list and, within their
+  // concatenated rows, rows [row_cur, row_cur + kMoeRoundRows).
+  int v0 = 0, row_cur = 0;
+  // Rows scanned per round: kMoeRoundRows, or kMoeMaxDesc when one unit's chunk
+  // alone has more groups than a round holds runs (each row at most one run).
+  const int round_rows = ac > kMoeMaxDesc ? kMoeMaxDesc : kMoeRoundRows;
+  while (v0 < my_units) {
+    if (ring_ready) {   // the ring holds the last round's stages: reload the offsets
+      for (int i = tid; i <= E; i += kThreads) offs[i] = p.expert_offsets[i];
+      __syncthreads();
+    }
+    // at most kMoeMaxDesc groups (so runs) per round, or one unit
+    const int v1 = min(my_units, v0 + min(kMoeMaxMyUnits, max(1, kMoeMaxDesc / ac)));
+    const int nu = v1 - v0;
+    if (tid < nu) {
+      const long long u = b + static_cast<long long>(v0 + tid) * G;
+      const int e = e_first + static_cast<int>(u / n_chunks);
+      u_e[tid] = e;
+      u_a0[tid] = static_cast<int>(u % n_chunks) * ac;
+      u_lo[tid] = max(offs[e], lo_w);
+      u_row0[tid] = max(0, min(offs[e + 1], hi_w) - max(offs[e], lo_w));
+    }
+    for (int i = tid; i < nu * ac; i += kThreads) bcnt[i] = 0;
+    __syncthreads();
+    if (tid == 0) {   // prefix of the units' rows
+      int run = 0;
+      for (int v = 0; v < nu; ++v) {
+        const int c = u_row0[v];
+        u_row0[v] = run;
+        run += c;
+      }
+      u_row0[nu] = run;
+    }
+    __syncthreads();
+    const int rows_all = u_row0[nu];
+    // this round: rows [row_cur, row_end) of the units' concatenated rows
+    const int row_end = min(rows_all, row_cur + round_rows);
+    // Each thread takes up to kMoeRowsPerThread rows of the round: their unit,
+    // token and adapter (all token loads, then all adapter loads); a routed row
+    // of its unit's chunk takes a rank in its group.
+    int rr[kMoeRowsPerThread], tk[kMoeRowsPerThread], grp[kMoeRowsPerThread], rank[kMoeRowsPerThread];
+    int uv[kMoeRowsPerThread];
+#pragma unroll
+    for (int j = 0; j < kMoeRowsPerThread; ++j) {
+      const int q = row_cur + tid + j * kThreads;
+      rr[j] = -1;
+      tk[j] = 0;
+      uv[j] = 0;
+      if (q < row_end) {
+        int v = 0;
+        while (u_row0[v + 1] <= q) ++v;
+        uv[j] = v;
+        rr[j] = u_lo[v] + (q - u_row0[v]);
+        tk[j] = need_token ? p.sorted_token_ids[rr[j]] : 0;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kMoeRowsPerThread; ++j) {
+      grp[j] = -1;
+      rank[j] = 0;
+      if (rr[j] >= 0) {
+        const int v = uv[j], t = tk[j];
+        const bool tok_ok = !need_token || (t >= 0 && t < p.num_tokens);
+        const int a = (tok_ok && p.row_adapter) ? p.row_adapter[t] : 0;
+        if (tok_ok && expert_of(rr[j]) == u_e[v] && a >= u_a0[v] && a < min(A, u_a0[v] + ac)) {
+          grp[j] = v * ac + (a - u_a0[v]);
+          rank[j] = atomicAdd(&bcnt[grp[j]], 1);
+        }
+      }
+    }
+    __syncthreads();
+    // Groups with rows become the round's runs (in group order); positions follow.
+    if (warp == 0) {
+      int carry_pos = 0, carry_run = 0;
+      for (int c0 = 0; c0 < nu * ac; c0 += 32) {
+        const int k = c0 + lane;
+        const int n = k < nu * ac ? bcnt[k] : 0;
+        int incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += t;
+        }
+        const unsigned has = __ballot_sync(0xffffffffu, n > 0);
+        const int d = carry_run + __popc(has & ((1u << lane) - 1u));
+        if (n > 0) {
+          MoeDesc& dd = mp.desc[d];
+          const int v = k / ac;
+          dd.e = u_e[v];
+          dd.a = u_a0[v] + (k - v * ac);
+          dd.i_lo = 0;
+          dd.n = n;
+          dd.pos0 = carry_pos + incl - n;
+          bcnt[k] = (d << 16) | 0;   // the run of group k (positions are pos0 + rank)
+        }
+        carry_pos += __shfl_sync(0xffffffffu, incl, 31);
+        carry_run += __popc(has);
+      }
+      if (lane == 0) {
+        mp.nd = carry_run;
+        mp.npos = carry_pos;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kMoeRowsPerThread; ++j) {
+      if (grp[j] >= 0) {
+        const int d = bcnt[grp[j]] >> 16;
+        const int qpos = mp.desc[d].pos0 + rank[j];
+        mp.pos_row[qpos] = rr[j];
+        mp.pos_tok[qpos] = p.x_gather ? tk[j] : rr[j];
+        mp.pos_desc[qpos] = static_cast<short>(d);
+      }
+    }
+    const int nd = mp.nd, npos = mp.npos;
+    // table entries of the runs
+    for (int k = tid; k < nd; k += kThreads) {
+      MoeDesc& d = mp.desc[k];
+      const int idx = d.a * E + d.e;
+      const uint16_t* Ap = p.a_table[idx];
+      const uint16_t* Bp = p.b_table[idx];
+      const uintptr_t ua = reinterpret_cast<uintptr_t>(Ap), ub = reinterpret_cast<uintptr_t>(Bp);
+      const bool usable = ua != 0 && ub != 0 && ((ua | ub) & 15u) == 0;
+      if (ua != 0 && ub != 0 && !usable) atomicOr(&g_lora_status, kDevMisaligned);
+      d.A = usable ? Ap : nullptr;
+      d.B = Bp;
+      d.scale = usable ? p.scale_table[idx] : 0.f;
+    }
+    // next round
+    if (row_end >= rows_all) {
+      v0 = v1;
+      row_cur = 0;
+    } else {
+      row_cur = row_end;
+    }
+    __syncthreads();
+    if (!ring_ready) {
+      ring_init(pl, g.ns);   // (fences the planner's generic writes before the ring's TMA writes)
+      ring_ready = true;
+    } else {
+      fence_proxy_async_smem();
+      __syncthreads();
+    }
+
+    // ---- passes of up to kMaxRows positions ----
+    for (int P0 = 0; P0 < npos; P0 += kMaxRows) {
+      const int P = min(kMaxRows, npos - P0);
+      if (tid < kMaxRows) {
+        bool start = false;
+        int k = -1;
+        if (tid < P) {
+          const int q = P0 + tid;
+          k = mp.pos_desc[q];
+          const int run = q - max(P0, mp.desc[k].pos0);   // rows of the run before this one in the pass
+          start = (run % g.gmax) == 0;
+          const int r = mp.pos_row[q];
+          pl.members[tid] = tid;
+          pl.grow[tid] = r;
+          pl.xsrc[tid] = mp.pos_tok[q];
+          pl.xarow[tid] = r - p.row_offset;
+        }
+        const unsigned sb = __ballot_sync(0xffffffffu, start);
+        if (lane == 0) pl.ballots[tid >> 5] = sb;
+        pl.flag[tid] = start ? k : -1;
+      }
+      __syncthreads();
       if (tid < P) {
-        e = pl.tkey[base + tid];
-        int run = 0;  // rows of the same expert before this one in the pass
-        for (int u = tid - 1; u >= 0 && pl.tkey[base + u] == e; --u) ++run;
-        start = (run % g.gmax) == 0;
-        const int r = r0 + pl.tpos[base + tid];
-        pl.members[tid] = tid;
-        pl.grow[tid] = r;
-        pl.xsrc[tid] = pl.txrow[base + tid];
-        pl.xarow[tid] = r - p.row_offset;
+        const unsigned s0 = pl.ballots[0], s1 = pl.ballots[1];
+        const unsigned below = tid < 32 ? (s0 & ((1u << tid) - 1u)) : s0;
+        const int gid = __popc(below) + (tid < 32 ? 0 : __popc(s1 & ((1u << (tid - 32)) - 1u)));
+        const int k = pl.flag[tid];
+        if (k >= 0) {
+          const MoeDesc& d = mp.desc[k];
+          pl.gstart[gid] = tid;
+          pl.gA[gid] = d.A;
+          pl.gB[gid] = d.B;
+          pl.gscale[gid] = d.scale;
+        }
+        if (tid == 0) {
+          const int G0 = __popc(s0) + __popc(s1);
+          pl.G = G0;
+          pl.gstart[G0] = P;
+        }
       }
-      const unsigned sb = __ballot_sync(0xffffffffu, start);
-      if (lane == 0) pl.ballots[tid >> 5] = sb;
-      pl.flag[tid] = start ? e : -1;
-    }
-    __syncthreads();
-    if (tid < P) {
-      const unsigned s0 = pl.ballots[0], s1 = pl.ballots[1];
-      const unsigned below = tid < 32 ? (s0 & ((1u << tid) - 1u)) : s0;
-      const int gid = __popc(below) + (tid < 32 ? 0 : __popc(s1 & ((1u << (tid - 32)) - 1u)));
-      const int e = pl.flag[tid];
-      if (e >= 0) {
-        const int idx = adapter * E + e;
-        const uint16_t* A = p.a_table[idx];
-        const uint16_t* B = p.b_table[idx];
-        const uintptr_t ua = reinterpret_cast<uintptr_t>(A), ub = reinterpret_cast<uintptr_t>(B);
-        const bool usable = ua != 0 && ub != 0 && ((ua | ub) & 15u) == 0;
-        if (ua != 0 && ub != 0 && !usable) atomicOr(&g_lora_status, kDevMisaligned);
-        pl.gstart[gid] = tid;
-        pl.gA[gid] = usable ? A : nullptr;
-        pl.gB[gid] = B;
-        pl.gscale[gid] = usable ? p.scale_table[idx] : 0.f;
-      }
+      __syncthreads();
+      // Drop groups whose adapter matrices are NULL or misaligned (their rows stay unchanged).
       if (tid == 0) {
-        const int G = __popc(s0) + __popc(s1);
-        pl.G = G;
-        pl.gstart[G] = P;
+        int G1 = 0, nvk = 0;
+        const int G0 = pl.G;
+        for (int gi = 0; gi < G0; ++gi) {
+          const int a0 = pl.gstart[gi], a1 = pl.gstart[gi + 1];
+          if (pl.gA[gi] == nullptr) continue;
+          const uint16_t* Ap = pl.gA[gi];
+          const uint16_t* Bp = pl.gB[gi];
+          const float sc = pl.gscale[gi];
+          for (int i = a0; i < a1; ++i) pl.members[nvk + (i - a0)] = pl.members[i];
+          pl.gstart[G1] = nvk;
+          pl.gA[G1] = Ap;
+          pl.gB[G1] = Bp;
+          pl.gscale[G1] = sc;
+          nvk += a1 - a0;
+          ++G1;
+        }
+        pl.gstart[G1] = nvk;
+        pl.G = G1;
+        pl.NV = nvk;
       }
+      __syncthreads();
+      if (pl.G > 0) it0 += fold_engine<MAXT, false>(ea, g, pl, smem, cluster, 0, it0);
+      __syncthreads();   // the next pass rewrites the plan
     }
-    __syncthreads();
-    // Drop groups whose adapter matrices are NULL or misaligned (their rows stay unchanged).
-    if (tid == 0) {
-      int G = 0, nvk = 0;
-      const int G0 = pl.G;
-      for (int gi = 0; gi < G0; ++gi) {
-        const int a0 = pl.gstart[gi], a1 = pl.gstart[gi + 1];
-        if (pl.gA[gi] == nullptr) continue;
-        const uint16_t* A = pl.gA[gi];
-        const uint16_t* B = pl.gB[gi];
-        const float sc = pl.gscale[gi];
-        for (int i = a0; i < a1; ++i) pl.members[nvk + (i - a0)] = pl.members[i];
-        pl.gstart[G] = nvk;
-        pl.gA[G] = A;
-        pl.gB[G] = B;
-        pl.gscale[G] = sc;
-        nvk += a1 - a0;
-        ++G;
-      }
-      pl.gstart[G] = nvk;
-      pl.G = G;
-      pl.NV = nvk;
-    }
-    __syncthreads();
-    if (pl.G > 0) it0 += fold_engine<MAXT, false>(ea, g, pl, smem, cluster, crank, it0);
-    __syncthreads();   // the next pass rewrites the plan
+    // Another round: the ring serves as planning scratch again (every item of
+    // the last pass has been consumed).
   }
 }
 

@@ -108,16 +108,17 @@ def test_moe_xa_rows_cover_the_window():
     assert _moe(xa=None, xa_rows=-5, x=FAKE + 2) == -4         # xa_rows ignored without xa
 
 
-def test_moe_grid_that_overflows_a_launch_is_rejected():
-    """A window whose tiles x adapters grid would not fit one launch is refused
-    with an error (not folded partially or skipped)."""
+def test_moe_table_count_and_persistent_grid():
+    """The MoE tables hold at most LORA_MAX_LORAS (adapter, expert) entries; the
+    grid is persistent (one CTA per SM, fewer for small windows: at least 16 rows
+    each), so even the largest window launches a fixed grid."""
+    assert _moe(L=33, E=128) == -2            # 33 x 128 > 4096 table entries
+    assert "table entries" in L.lora_last_error()
     big = 2 ** 31 - 1
-    assert _moe(te=big, lo=0, hi=big, L=4096, xa=None) == -2
-    assert "grid size" in L.lora_last_error()
-    with pytest.raises(L.LoraError, match="grid size"):
-        L.lora_launch_geometry(1, big, 4096, 16, 768, 2048)
-    # the same window with 16 adapters still fits: 2^23 tiles of 256 rows x 16
-    assert L.lora_launch_geometry(1, big, 16, 16, 768, 2048)["clusters"] == (2 ** 23) * 16
+    assert L.lora_launch_geometry(1, big, 16, 16, 768, 2048)["clusters"] == 152
+    assert L.lora_launch_geometry(1, 40, 16, 16, 768, 2048)["clusters"] == 3
+    assert L.lora_launch_geometry(1, 0, 16, 16, 768, 2048)["clusters"] == 1
+    assert _moe(te=big, lo=0, hi=big, xa=None, x=FAKE + 2) == -4   # passes the size checks
 
 
 def _gather(**kw):
@@ -251,16 +252,18 @@ def test_gather_geometry_has_no_cluster_split():
     assert L.lora_launch_geometry(0, 512, 2048, 16, 768, 2048)["cluster"] == 4
 
 
-def test_moe_geometry_tiles():
-    # the largest scan tile (256, 128, 64 rows) that still gives >= 128 units
+def test_moe_geometry_persistent():
+    """The MoE grid: one CTA per SM (152 without a device), fewer for windows of
+    under 16 rows per CTA; passes of 64 rows; the arithmetic (k chunk, j chunk)
+    from the shapes alone, whatever the window."""
     g = L.lora_launch_geometry(1, 4096, 16, 16, 768, 2048)
-    assert g["rows_per_tile"] == 64 and g["cluster"] == 1
-    assert g["clusters"] == 16 * 16                     # 256-row tiles x adapters
-    assert L.lora_launch_geometry(1, 4096, 4, 16, 768, 2048)["clusters"] == 32 * 4
-    assert L.lora_launch_geometry(1, 4096, 1, 16, 768, 2048)["clusters"] == 64
-    assert L.lora_launch_geometry(1, 100, 1, 16, 768, 2048)["clusters"] == 2
-    assert L.lora_launch_geometry(1, 0, 1, 16, 768, 2048)["clusters"] == 1
-    assert L.lora_launch_geometry(1, 0, 16, 16, 768, 2048)["clusters"] == 16
+    assert g["rows_per_tile"] == 64 and g["cluster"] == 1 and g["clusters"] == 152
+    assert g["ring_stages"] >= 2 and g["smem_bytes"] <= 227 * 1024
+    assert L.lora_launch_geometry(1, 100, 1, 16, 768, 2048)["clusters"] == 7
+    for rows in (0, 100, 4096, 16384, 10 ** 6):
+        h = L.lora_launch_geometry(1, rows, 16, 16, 768, 2048)
+        assert (h["k_chunk"], h["j_chunk"], h["k_slice"], h["j_slice"]) == \
+            (g["k_chunk"], g["j_chunk"], g["k_slice"], g["j_slice"])
 
 
 def test_tensor_maps_only_from_the_minimum_rank():

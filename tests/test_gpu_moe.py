@@ -79,8 +79,9 @@ def test_moe_random(case):
 
 
 def _skewed(seed):
-    """One adapter takes 90% of the tokens: a 256-row tile then holds far more
-    than 64 rows of it, which the kernel folds in several passes."""
+    """One adapter takes 90% of the tokens: its (expert, adapter) groups are far
+    larger than the 16 rows of one fold group, and a CTA's share of them spans
+    several passes of 64 rows."""
     wl = W.make_moe("moe_skew", num_tokens=1024, top_k=4, num_experts=8, k_in=256, n_out=512,
                     max_loras=16, max_rank=16, rank=16, alpha=16.0, adapter_base_frac=0.0,
                     cap=4096, seed=seed)
@@ -90,20 +91,50 @@ def _skewed(seed):
     return wl
 
 
-def test_moe_multi_pass_units():
+def test_moe_large_groups_and_other_windows():
     wl = _skewed(321)
     assert wl.te == 4096
-    assert L.lora_launch_geometry(1, 4096, 16, 16, 256, 512)["clusters"] == 16 * 16  # 256-row tiles
     windows = [(0, 4096)]
     g_out, g_xas = gpu_moe(wl, windows)
     o_out, o_xas, o_d = oracle_moe(wl, windows)
     compare_moe(wl, windows, g_out, o_out, g_xas, o_xas, o_d, _routes_all(wl, windows))
-    # scan tiles of 256, 128 and 64 rows (windows of 4096, 1000 and 300) give the same bits
+    # windows of 1000 and 300 rows (other grids, other CTA shares) give the same bits
     for cap in (1000, 300):
         ws = [(lo, min(lo + cap, wl.te)) for lo in range(0, wl.te, cap)]
         w_out, w_xas = gpu_moe(wl, ws)
         assert np.array_equal(w_out, g_out)
         assert np.array_equal(np.concatenate(w_xas), g_xas[0])
+
+
+@pytest.mark.parametrize("name", ["moe_down_fold", "moe_gateup_fold"])
+def test_moe_workload_windows_of_any_size_give_the_same_bits(name):
+    """The benchmarked MoE workloads: windows of 4096 (as configured), 1000 and 300
+    sorted rows and one call over all rows fold every row to the same bits (the
+    grid and each CTA's share of the rows change with the window; a row's
+    arithmetic does not)."""
+    wl = W.by_name(name)
+    ref_out, ref_xa = gpu_moe(wl, [(0, wl.te)])
+    for cap in (4096, 1000, 300):
+        ws = [(lo, min(lo + cap, wl.te)) for lo in range(0, wl.te, cap)]
+        w_out, w_xas = gpu_moe(wl, ws)
+        assert np.array_equal(w_out, ref_out), cap
+        assert np.array_equal(np.concatenate(w_xas), ref_xa[0]), cap
+
+
+def test_moe_window_with_more_rows_than_one_planning_round():
+    """200000 sorted rows in one window: each of the 152 CTAs gets more rows than
+    one planning round holds (1024), and the window has more rows than the group
+    keys kept in shared memory (the rest are recomputed from the routing data)."""
+    wl = W.make_moe("moe_rounds", num_tokens=25000, top_k=8, num_experts=16, k_in=16, n_out=24,
+                    max_loras=4, max_rank=8, rank=8, alpha=16.0, adapter_base_frac=0.1,
+                    cap=200000, seed=333)
+    assert wl.te == 200000
+    windows = wl.windows()
+    g_out, g_xas = gpu_moe(wl, windows)
+    o_out, o_xas, o_d = oracle_moe(wl, windows)
+    st = compare_moe(wl, windows, g_out, o_out, g_xas, o_xas, o_d, _routes_all(wl, windows))
+    assert st["rows"] > 152 * 1024
+    assert L.lora_read_device_status(clear=True) == 0
 
 
 def test_moe_rows_outside_spans_bad_tokens_and_empty_window():
