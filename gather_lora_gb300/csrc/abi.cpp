@@ -178,7 +178,8 @@ bool make_geometry_at(bool moe, int rows, int max_loras, int planner_ints, int m
   // kConsumerWarps / ksplit warps each) when there are no peers or the exchange
   // is an all-gather; with a reduce-scatter the extra planes would lengthen it.
   g.gather = (g.cl > 1 && g.cl * g.rt * (max_rank + 4) * 4 <= kGatherBytes) ? 1 : 0;
-  g.ksplit = 1;
+  // (slot-parallel groups: two warps may share a slot, each with its own plane)
+  g.ksplit = g.group_parallel ? 2 : 1;
   if (!g.group_parallel && (g.cl == 1 || g.gather))
     while (g.ksplit < glora::kConsumerWarps && (glora::kConsumerWarps / (2 * g.ksplit)) >= tiles) g.ksplit *= 2;
   g.maxt = 1;
@@ -260,14 +261,23 @@ bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_
 // counts of their groups).
 bool moe_geometry(int window, int adapters, int num_experts, int max_rank, int k_in, int n_out, int sms,
                   glora::FoldGeometry& g) {
-  if (!make_geometry(true, window, adapters, 0, max_rank, k_in, n_out, g)) return false;
+  // The largest stage target whose ring still gets two stages beside the plan.
   const int budget = glora::kMoeCtasPerSm == 1 ? kBudgetOnePerSm : kBudgetTwoPerSm;
-  const int planes = g.ksplit + (g.gather ? g.cl : 0);
-  const int tail = planes * g.rt * g.pitch_part * 4 + g.rt * g.pitch_xa;
-  g.off_mplan = glora::kPlanBytes;
-  g.off_ring = round_up(g.off_mplan + static_cast<int>(sizeof(glora::MoePlan)), 1024);
-  const int ns = std::min(kMaxStages, (budget - g.off_ring - tail) / g.stage_bytes);
+  const int off_ring = round_up(glora::kPlanBytes + static_cast<int>(sizeof(glora::MoePlan)), 1024);
+  int ns = 0, tail = 0;
+  for (int target : {kMoeStageTarget, kStageTarget, kMinStage}) {
+    if (!make_geometry_at(true, window, adapters, 0, max_rank, k_in, n_out, g, GLORA_MAX_CLUSTER, false, target,
+                          kUnitRows))
+      continue;
+    const int planes = g.ksplit + (g.gather ? g.cl : 0);
+    tail = planes * g.rt * g.pitch_part * 4 + g.rt * g.pitch_xa;
+    ns = std::min(kMaxStages, (budget - off_ring - tail) / g.stage_bytes);
+    if (ns >= 2) break;
+  }
   if (ns < 2) return false;
+  const int planes = g.ksplit + (g.gather ? g.cl : 0);
+  g.off_mplan = glora::kPlanBytes;
+  g.off_ring = off_ring;
   g.ns = ns;
   g.off_part = g.off_ring + ns * g.stage_bytes;
   g.off_xa = g.off_part + planes * g.rt * g.pitch_part * 4;
@@ -275,7 +285,8 @@ bool moe_geometry(int window, int adapters, int num_experts, int max_rank, int k
   const long long bins = static_cast<long long>(num_experts) * adapters;
   // planner scratch: offsets, four unit arrays, the groups of a round
   const long long scratch = ((num_experts + 4) & ~3) * 4LL + (4LL * 64 + 4) * 4 +
-                            static_cast<long long>(std::max(glora::kMoeMaxDesc, adapters)) * 4;
+                            (static_cast<long long>(std::max(glora::kMoeMaxDesc, adapters)) + 2) * 4 +
+                            glora::kMoeMaxDesc * 20LL;
   const long long ring = static_cast<long long>(ns) * g.stage_bytes;
   if (bins > glora::kMoeMaxBins || scratch > ring) return false;
   g.clusters = static_cast<int>(std::max<long long>(1, std::min<long long>(static_cast<long long>(sms) * glora::kMoeCtasPerSm,

@@ -126,11 +126,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst_smem, const void* map, 
 __device__ __forceinline__ void prefetch_tensormap(const void* map) {
   asm volatile("prefetch.tensormap [%0];\n" ::"l"(map) : "memory");
 }
-// Fetch `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2
-// ahead of its use (no completion to wait for).
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
-}
 // Order this thread's generic-proxy shared-memory accesses before later
 // async-proxy (TMA) accesses of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -10,7 +10,10 @@ constexpr int kMaxRows = 64;        // rows (positions) per pass of a work unit
 constexpr int kMaxTilesPerWarp = 4; // 16x8 shrink tiles a warp may own: MT * NT <= 32
 constexpr int kPlanBytes = 4096;    // shared memory reserved for the work-unit plan
 constexpr int kMoeMaxDesc = 128;    // MoE: (expert, adapter) groups (runs) one CTA plans per round
-constexpr int kMoeMaxPos = 1024;    // MoE: rows one CTA scans (so at most folds) per round
+#ifndef GLORA_MOE_ROUND_ROWS
+#define GLORA_MOE_ROUND_ROWS 512
+#endif
+constexpr int kMoeMaxPos = GLORA_MOE_ROUND_ROWS;   // MoE: rows one CTA scans (so at most folds) per round
 constexpr int kMoeMaxBins = 4096;   // MoE: (expert, adapter) groups of a window (num_experts * adapters)
 constexpr int kConsumerWarps = 8;   // tensor-core / fold warps per CTA
 constexpr int kProducerWarps = 4;   // TMA-issuing warps per CTA (one warpgroup)
@@ -97,7 +100,7 @@ struct MoeArgs {
 // the CTA's plan of one round (its runs and their rows, run after run).
 struct MoeDesc {
   int e, a;                // expert, adapter
-  int i_lo, n;             // the run's rows: n rows of the group
+  int i_lo, n;             // the round's group of the run, and its rows
   int pos0;                // first position of the run in the CTA's row list
   float scale;
   const uint16_t* A;       // NULL: entry NULL or misaligned (the rows stay unchanged)

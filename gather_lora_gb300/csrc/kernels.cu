@@ -302,11 +302,14 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
   // of every chunk and keeps its partial sums in its own plane of part_s, and
   // the exchange adds the planes in phase order.
   const bool gpar = g.group_parallel != 0;
-  const bool idle = gpar && warp >= ns;          // slot-parallel with fewer slots than warps
-  // slot-parallel: group gi's one shrink item is ring item it0 + gi, in slot (it0 + gi) % ns
-  const int g_first = gpar ? ((warp - it0 % ns) + ns) % ns : 0, g_step = gpar ? ns : 1;
-  const int KS = gpar ? 1 : g.ksplit, TW = kConsumerWarps / KS;
-  const int kp = gpar ? 0 : warp / TW;
+  // Slot-parallel: group gi's one shrink item is ring item it0 + gi, in slot
+  // (it0 + gi) % ns, served by KSG warps (warps s, s + ns, ...) that take
+  // alternate k-steps into their own partial planes.
+  const int KSG = gpar ? max(1, min(g.ksplit, kConsumerWarps / ns)) : 1;
+  const bool idle = gpar && warp >= ns * KSG;   // slot-parallel with fewer slots than warps
+  const int g_first = gpar ? (((warp % ns) - it0 % ns) + ns) % ns : 0, g_step = gpar ? ns : 1;
+  const int KS = gpar ? KSG : g.ksplit, TW = kConsumerWarps / KS;
+  const int kp = gpar ? warp / ns : warp / TW;
   const int t_first = gpar ? 0 : warp % TW, t_step = gpar ? 1 : TW;
   const int MT = g.mr16 >> 4;
   const int plane = g.rt * g.pitch_part;         // floats per k-phase plane of part_s
@@ -396,7 +399,7 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
       }
       for (; si < nst; si += KS) step(st, si * 16, min(16, klen - si * 16), acc[0]);   // the rest on chain 0
       __syncwarp();
-      if (lane == 0) mbar_arrive_count(smem_u32(&pl.empty[s]), gpar ? kConsumerWarps : 1);
+      if (lane == 0) mbar_arrive_count(smem_u32(&pl.empty[s]), gpar ? kConsumerWarps / KSG : 1);
     }
 #pragma unroll
     for (int ch = 1; ch < kChains; ++ch)
@@ -925,7 +928,20 @@ __global__ void __launch_bounds__(kThreads, kMoeCtasPerSm) lora_moe_fold_kernel(
   int* u_lo = u_a0 + kMoeMaxMyUnits;           // its rows in the window: [u_lo, u_hi)
   int* u_row0 = u_lo + kMoeMaxMyUnits;         // prefix of the units' rows (+1 entry)
   int* bcnt = u_row0 + kMoeMaxMyUnits + 4;     // [units * ac] rows of each group in the round
+  const uint16_t** tabA = reinterpret_cast<const uint16_t**>(bcnt + ((max(kMoeMaxDesc, A) + 1) & ~1));   // their
+  const uint16_t** tabB = tabA + kMoeMaxDesc;                                                           // table
+  float* tabS = reinterpret_cast<float*>(tabB + kMoeMaxDesc);                                           // entries
 
+  // The ring's mbarriers read no input: they are set up while the previous
+  // grid on the stream may still be running.
+  if (tid == 0) {
+    for (int s = 0; s < g.ns; ++s) {
+      mbar_init(smem_u32(&pl.full[s]), kProducerWarps * 32);
+      mbar_init(smem_u32(&pl.empty[s]), kConsumerWarps);
+    }
+    pl.failed = 0;
+    mbar_fence_init();
+  }
   pdl_wait_then_release();
 
   // Expert of sorted row r (-1 outside the spans): the largest e with offs[e] <= r.
@@ -948,8 +964,8 @@ __global__ void __launch_bounds__(kThreads, kMoeCtasPerSm) lora_moe_fold_kernel(
   const int E_w = e_last - e_first + 1;
   const int n_chunks0 = min(A, max(1, (kMoeUnitsPerCta * G) / E_w));
   const int ac = (A + n_chunks0 - 1) / n_chunks0, n_chunks = (A + ac - 1) / ac;
-  const long long n_units = static_cast<long long>(E_w) * n_chunks;
-  const int my_units = n_units > b ? static_cast<int>((n_units - b + G - 1) / G) : 0;
+  const int n_units = E_w * n_chunks;   // <= num_experts * adapters <= kMoeMaxBins
+  const int my_units = n_units > b ? (n_units - b + G - 1) / G : 0;
 
   const EngineArgs ea{p.x, p.x_stride, p.out, p.out_stride, p.xa, p.max_rank, p.k_in, p.n_out};
   int it0 = 0;
@@ -969,14 +985,27 @@ __global__ void __launch_bounds__(kThreads, kMoeCtasPerSm) lora_moe_fold_kernel(
     const int v1 = min(my_units, v0 + min(kMoeMaxMyUnits, max(1, kMoeMaxDesc / ac)));
     const int nu = v1 - v0;
     if (tid < nu) {
-      const long long u = b + static_cast<long long>(v0 + tid) * G;
-      const int e = e_first + static_cast<int>(u / n_chunks);
+      const int u = b + (v0 + tid) * G;
+      const int e = e_first + u / n_chunks;
       u_e[tid] = e;
-      u_a0[tid] = static_cast<int>(u % n_chunks) * ac;
+      u_a0[tid] = (u % n_chunks) * ac;
       u_lo[tid] = max(offs[e], lo_w);
       u_row0[tid] = max(0, min(offs[e + 1], hi_w) - max(offs[e], lo_w));
     }
     for (int i = tid; i < nu * ac; i += kThreads) bcnt[i] = 0;
+    // the table entries of the round's groups, loaded beside the row scan
+    // (groups past the adapters are never routed)
+    if (nu * ac <= kMoeMaxDesc) {
+      for (int k = tid; k < nu * ac; k += kThreads) {
+        const int v = k / ac, a = (b + (v0 + v) * G) % n_chunks * ac + (k - v * ac);
+        const int e = e_first + (b + (v0 + v) * G) / n_chunks;
+        if (a < A) {
+          tabA[k] = p.a_table[a * E + e];
+          tabB[k] = p.b_table[a * E + e];
+          tabS[k] = p.scale_table[a * E + e];
+        }
+      }
+    }
     __syncthreads();
     if (tid == 0) {   // prefix of the units' rows
       int run = 0;
@@ -1044,7 +1073,7 @@ __global__ void __launch_bounds__(kThreads, kMoeCtasPerSm) lora_moe_fold_kernel(
           const int v = k / ac;
           dd.e = u_e[v];
           dd.a = u_a0[v] + (k - v * ac);
-          dd.i_lo = 0;
+          dd.i_lo = k;               // the group (its cached table entries)
           dd.n = n;
           dd.pos0 = carry_pos + incl - n;
           bcnt[k] = (d << 16) | 0;   // the run of group k (positions are pos0 + rank)
@@ -1070,17 +1099,18 @@ __global__ void __launch_bounds__(kThreads, kMoeCtasPerSm) lora_moe_fold_kernel(
     }
     const int nd = mp.nd, npos = mp.npos;
     // table entries of the runs
+    const bool cached = nu * ac <= kMoeMaxDesc;
     for (int k = tid; k < nd; k += kThreads) {
       MoeDesc& d = mp.desc[k];
       const int idx = d.a * E + d.e;
-      const uint16_t* Ap = p.a_table[idx];
-      const uint16_t* Bp = p.b_table[idx];
+      const uint16_t* Ap = cached ? tabA[d.i_lo] : p.a_table[idx];
+      const uint16_t* Bp = cached ? tabB[d.i_lo] : p.b_table[idx];
       const uintptr_t ua = reinterpret_cast<uintptr_t>(Ap), ub = reinterpret_cast<uintptr_t>(Bp);
       const bool usable = ua != 0 && ub != 0 && ((ua | ub) & 15u) == 0;
       if (ua != 0 && ub != 0 && !usable) atomicOr(&g_lora_status, kDevMisaligned);
       d.A = usable ? Ap : nullptr;
       d.B = Bp;
-      d.scale = usable ? p.scale_table[idx] : 0.f;
+      d.scale = usable ? (cached ? tabS[d.i_lo] : p.scale_table[idx]) : 0.f;
     }
     // next round
     if (row_end >= rows_all) {
@@ -1089,14 +1119,10 @@ __global__ void __launch_bounds__(kThreads, kMoeCtasPerSm) lora_moe_fold_kernel(
     } else {
       row_cur = row_end;
     }
+    // the planner's generic writes to the ring before the ring's TMA writes
+    fence_proxy_async_smem();
     __syncthreads();
-    if (!ring_ready) {
-      ring_init(pl, g.ns);   // (fences the planner's generic writes before the ring's TMA writes)
-      ring_ready = true;
-    } else {
-      fence_proxy_async_smem();
-      __syncthreads();
-    }
+    ring_ready = true;
 
     // ---- passes of up to kMaxRows positions ----
     for (int P0 = 0; P0 < npos; P0 += kMaxRows) {
