@@ -7,10 +7,12 @@ from the one before it: if a waiter can be two phases ahead, the wait passes
 falsely and a later arrival lands in the wrong phase. This model replays the
 kernels' exact schedule (every producer warp serves every item in order and
 arrives once per item; consumers either all take every item in order, or, for
-shrink items, each owns one slot and releases it with all eight arrivals)
-under random interleavings and checks that no parity wait
-passes early, no arrival lands in a wrong phase, and the schedule never
-deadlocks, including across the two cluster barriers between shrink and expand.
+shrink items, the KSG warps that own a slot (KSG = 1 or 2) take its items and
+each releases it with 8 / KSG arrivals) under random interleavings and checks
+that no parity wait passes early, no arrival lands in a wrong phase, and the
+schedule never deadlocks, including across the two cluster barriers between
+shrink and expand, and in the single-CTA form where the exchange barrier holds
+only the consumer warps while the producer keeps issuing.
 It also shows that a schedule in which producer warps split items by index
 (the broken variant) fails.
 """
@@ -49,9 +51,16 @@ class Barrier:
         return ok
 
 
-def run(ns, n_shrink, n_items, slot_parallel, seed, producer_split="all", passes=None):
+def run(ns, n_shrink, n_items, slot_parallel, seed, producer_split="all", passes=None, ksg=1, cl1=False,
+        full_release=False):
     """`passes`: [(n_shrink, n_items), ...] folded one after the other by one
-    CTA; ring item numbers continue across passes and a CTA barrier separates them."""
+    CTA; ring item numbers continue across passes and a CTA barrier separates them.
+    ksg: warps per slot in slot-parallel shrinks (at most CONSUMER_WARPS // ns).
+    cl1: single-CTA units: the producer issues every item without the exchange
+    barriers, which only the consumer warps take.
+    full_release: each owner warp releases a shrink slot with all eight arrivals
+    (the broken variant when two warps own a slot)."""
+    ksg = max(1, min(ksg, CONSUMER_WARPS // ns))
     rng = random.Random(seed)
     full = [Barrier(PRODUCER_WARPS) for _ in range(ns)]
     empty = [Barrier(CONSUMER_WARPS) for _ in range(ns)]
@@ -73,17 +82,21 @@ def run(ns, n_shrink, n_items, slot_parallel, seed, producer_split="all", passes
             else:   # items dealt to warps by index (broken)
                 a = [i for i in range(pre) if i % PRODUCER_WARPS == pw]
                 b = [i for i in range(pre, pn) if i % PRODUCER_WARPS == pw]
-            prog += [base + i for i in a] + ["SYNC", "SYNC"] + [base + i for i in b] + ["SYNC"]
+            if cl1:
+                prog += [base + i for i in range(pn)] + ["SYNC"]
+            else:
+                prog += [base + i for i in a] + ["SYNC", "SYNC"] + [base + i for i in b] + ["SYNC"]
         return prog
 
     def consumer(w):
         prog = []
         for base, ps, pn in bounds:
-            if slot_parallel:   # shrink items: slot owner only; expand items: every warp in order
-                sh = [base + i for i in range(ps) if (base + i) % ns == w] if w < ns else []
+            if slot_parallel:   # shrink items: the slot's owner warps; expand items: every warp in order
+                sh = [base + i for i in range(ps) if (base + i) % ns == w % ns] if w < ns * ksg else []
             else:
                 sh = [base + i for i in range(ps)]
-            prog += sh + ["SYNC", "SYNC"] + [base + i for i in range(ps, pn)] + ["SYNC"]
+            ex = ["CSYNC", "CSYNC"] if cl1 else ["SYNC", "SYNC"]
+            prog += sh + ex + [base + i for i in range(ps, pn)] + ["SYNC"]
         return prog
 
     agents = [("P", producer(p)) for p in range(PRODUCER_WARPS)] + \
@@ -104,11 +117,13 @@ def run(ns, n_shrink, n_items, slot_parallel, seed, producer_split="all", passes
             continue
         kind, prog = agents[choice]
         op = prog[pc[choice]]
-        if op == "SYNC":
-            sid = sum(1 for x in prog[:pc[choice] + 1] if x == "SYNC")
+        if op in ("SYNC", "CSYNC"):
+            # a barrier of every warp (SYNC) or of the consumer warps only (CSYNC)
+            sid = (op, sum(1 for x in prog[:pc[choice] + 1] if x == op))
             at_sync[choice] = sid
-            if all(at_sync[i] == sid for i in range(len(agents))):
-                for i in range(len(agents)):
+            group = [i for i in range(len(agents)) if op == "SYNC" or agents[i][0] == "C"]
+            if all(at_sync[i] == sid for i in group):
+                for i in group:
                     pc[i] += 1
                     at_sync[i] = None
             continue
@@ -123,7 +138,8 @@ def run(ns, n_shrink, n_items, slot_parallel, seed, producer_split="all", passes
             if not waited[choice]:
                 waited[choice] = full[s].try_wait(u)
                 continue
-            for _ in range(CONSUMER_WARPS if (slot_parallel and op in shrink_items) else 1):
+            n_arr = CONSUMER_WARPS if full_release else CONSUMER_WARPS // ksg
+            for _ in range(n_arr if (slot_parallel and op in shrink_items) else 1):
                 empty[s].arrive(u)
         waited[choice] = False
         pc[choice] += 1
@@ -146,6 +162,27 @@ def test_ring_schedule_across_passes_is_sound(slot_parallel, ns):
     for passes in ([(1, 4), (2, 9), (1, 1)], [(3, 8), (0, 5), (4, 4), (2, 7)], [(5, 6)] * 4):
         for seed in range(3):
             run(ns, 0, 0, slot_parallel, seed, passes=passes)
+
+
+@pytest.mark.parametrize("ns", [2, 3, 4, 5, 8])
+def test_single_cta_units_with_two_warps_per_slot_are_sound(ns):
+    """The MoE fold's schedule: slot-parallel shrinks with up to two warps per
+    slot, the exchange barrier of the consumer warps only, passes one after the
+    other."""
+    for passes in ([(4, 16)], [(5, 20), (1, 4), (3, 12)], [(0, 3), (6, 6)], [(2, 2)] * 3):
+        for seed in range(3):
+            run(ns, 0, 0, True, seed, passes=passes, ksg=2, cl1=True)
+            run(ns, 0, 0, False, seed, passes=passes, ksg=1, cl1=True)
+
+
+def test_two_owner_warps_releasing_a_slot_in_full_is_unsound():
+    failures = 0
+    for seed in range(10):
+        try:
+            run(4, 0, 0, True, seed, passes=[(8, 20)], ksg=2, cl1=True, full_release=True)
+        except AssertionError:
+            failures += 1
+    assert failures == 10
 
 
 def test_items_split_by_index_across_producers_is_unsound():
