@@ -15,8 +15,14 @@ constexpr int kMoeMaxDesc = 128;    // MoE: (expert, adapter) groups (runs) one 
 #endif
 constexpr int kMoeMaxPos = GLORA_MOE_ROUND_ROWS;   // MoE: rows one CTA scans (so at most folds) per round
 constexpr int kMoeMaxBins = 4096;   // MoE: (expert, adapter) groups of a window (num_experts * adapters)
-constexpr int kConsumerWarps = 8;   // tensor-core / fold warps per CTA
-constexpr int kProducerWarps = 4;   // TMA-issuing warps per CTA (one warpgroup)
+#ifndef GLORA_CONSUMER_WARPS
+#define GLORA_CONSUMER_WARPS 8
+#endif
+#ifndef GLORA_PRODUCER_WARPS
+#define GLORA_PRODUCER_WARPS 4
+#endif
+constexpr int kConsumerWarps = GLORA_CONSUMER_WARPS;   // tensor-core / fold warps per CTA
+constexpr int kProducerWarps = GLORA_PRODUCER_WARPS;   // TMA-issuing warps per CTA
 
 // Launch geometry and shared-memory layout of one fold launch. Every CTA of a
 // cluster of `cl` CTAs owns one k-slice of the shrink (ksl columns of A / x)

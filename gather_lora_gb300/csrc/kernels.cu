@@ -1146,6 +1146,7 @@ __global__ void __launch_bounds__(kThreads, kMoeCtasPerSm) lora_moe_fold_kernel(
         pl.flag[tid] = start ? k : -1;
       }
       __syncthreads();
+      bool usable = true;   // this thread's group (if it starts one) has its adapter matrices
       if (tid < P) {
         const unsigned s0 = pl.ballots[0], s1 = pl.ballots[1];
         const unsigned below = tid < 32 ? (s0 & ((1u << tid) - 1u)) : s0;
@@ -1157,6 +1158,7 @@ __global__ void __launch_bounds__(kThreads, kMoeCtasPerSm) lora_moe_fold_kernel(
           pl.gA[gid] = d.A;
           pl.gB[gid] = d.B;
           pl.gscale[gid] = d.scale;
+          usable = d.A != nullptr;
         }
         if (tid == 0) {
           const int G0 = __popc(s0) + __popc(s1);
@@ -1164,9 +1166,13 @@ __global__ void __launch_bounds__(kThreads, kMoeCtasPerSm) lora_moe_fold_kernel(
           pl.gstart[G0] = P;
         }
       }
-      __syncthreads();
-      // Drop groups whose adapter matrices are NULL or misaligned (their rows stay unchanged).
-      if (tid == 0) {
+      // Groups whose adapter matrices are NULL or misaligned are dropped (their
+      // rows stay unchanged); the common case, every group usable, needs no
+      // compaction. (The vote is also the barrier after the group table.)
+      const bool all_usable = __syncthreads_and(usable) != 0;
+      if (all_usable) {
+        if (tid == 0) pl.NV = P;
+      } else if (tid == 0) {
         int G1 = 0, nvk = 0;
         const int G0 = pl.G;
         for (int gi = 0; gi < G0; ++gi) {
