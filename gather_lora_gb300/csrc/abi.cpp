@@ -130,7 +130,8 @@ int balanced_chunk(int total, int cap) {
 // window), so a row's arithmetic — the k-slices, k-chunks and summation order —
 // is the same in every call with the same (k_in, n_out, max_rank).
 bool make_geometry_at(bool moe, int rows, int max_loras, int planner_ints, int max_rank, int k_in,
-                      int n_out, glora::FoldGeometry& g, int max_cl, bool a_tiled, int target, int unit_rows) {
+                      int n_out, glora::FoldGeometry& g, int max_cl, bool a_tiled, int target, int unit_rows,
+                      int cw = glora::kConsumerWarps) {
   g = glora::FoldGeometry{};
   // bgmv: a cluster splits each unit's k (shrink) and n_out (expand); MoE units
   // are many and small, so one CTA folds whole groups.
@@ -143,7 +144,7 @@ bool make_geometry_at(bool moe, int rows, int max_loras, int planner_ints, int m
   g.cl = moe ? 1 : pow2_floor(std::min(max_cl, std::max(1, std::max(k_in, n_out) / 512)));
   g.mr16 = round_up(max_rank, 16);
   const int mt = g.mr16 / 16;
-  const int tile_rows_cap = 8 * (glora::kMaxTilesPerWarp * glora::kConsumerWarps / mt);
+  const int tile_rows_cap = 8 * (glora::kMaxTilesPerWarp * cw / mt);
   if (moe) {
     g.rt = LORA_MOE_M_TILE;
     g.gmax = std::min(std::min(GLORA_MOE_GROUP_ROWS, glora::kMaxGroupRows), tile_rows_cap);
@@ -181,12 +182,12 @@ bool make_geometry_at(bool moe, int rows, int max_loras, int planner_ints, int m
   // (slot-parallel groups: two warps may share a slot, each with its own plane)
   g.ksplit = g.group_parallel ? 2 : 1;
   if (!g.group_parallel && (g.cl == 1 || g.gather))
-    while (g.ksplit < glora::kConsumerWarps && (glora::kConsumerWarps / (2 * g.ksplit)) >= tiles) g.ksplit *= 2;
+    while (g.ksplit < cw && cw % (2 * g.ksplit) == 0 && (cw / (2 * g.ksplit)) >= tiles) g.ksplit *= 2;
   g.maxt = 1;
   if (g.group_parallel) {
     while (g.maxt < tiles) g.maxt *= 2;
   } else {
-    while (g.maxt * (glora::kConsumerWarps / g.ksplit) < tiles) g.maxt *= 2;
+    while (g.maxt * (cw / g.ksplit) < tiles) g.maxt *= 2;
   }
   // The bgmv shrink runs on tcgen05 when A comes as TMA boxes of 128 rows and
   // a unit has at most 16 rows: M = 128 (A rows), N = 16 (the unit's x rows).
@@ -267,7 +268,7 @@ bool moe_geometry(int window, int adapters, int num_experts, int max_rank, int k
   int ns = 0, tail = 0;
   for (int target : {kMoeStageTarget, kStageTarget, kMinStage}) {
     if (!make_geometry_at(true, window, adapters, 0, max_rank, k_in, n_out, g, GLORA_MAX_CLUSTER, false, target,
-                          kUnitRows))
+                          kUnitRows, glora::kMoeConsumerWarps))
       continue;
     const int planes = g.ksplit + (g.gather ? g.cl : 0);
     tail = planes * g.rt * g.pitch_part * 4 + g.rt * g.pitch_xa;

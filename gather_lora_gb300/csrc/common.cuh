@@ -131,9 +131,10 @@ __device__ __forceinline__ void prefetch_tensormap(const void* map) {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
-// Barrier among the consumer warps only (named barrier 1).
+// Barrier among the CW consumer warps only (named barrier 1).
+template <int CW = kConsumerWarps>
 __device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;\n" ::"n"(kConsumerWarps * 32) : "memory");
+  asm volatile("bar.sync 1, %0;\n" ::"n"(CW * 32) : "memory");
 }
 
 // ---- shared-memory matrix fragments ----------------------------------------

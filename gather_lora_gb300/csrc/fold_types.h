@@ -21,8 +21,13 @@ constexpr int kMoeMaxBins = 4096;   // MoE: (expert, adapter) groups of a window
 #ifndef GLORA_PRODUCER_WARPS
 #define GLORA_PRODUCER_WARPS 4
 #endif
-constexpr int kConsumerWarps = GLORA_CONSUMER_WARPS;   // tensor-core / fold warps per CTA
+constexpr int kConsumerWarps = GLORA_CONSUMER_WARPS;   // tensor-core / fold warps per CTA (routed folds)
 constexpr int kProducerWarps = GLORA_PRODUCER_WARPS;   // TMA-issuing warps per CTA
+#ifndef GLORA_MOE_CONSUMER_WARPS
+#define GLORA_MOE_CONSUMER_WARPS 12
+#endif
+constexpr int kMoeConsumerWarps = GLORA_MOE_CONSUMER_WARPS;   // consumer warps of the MoE fold's CTA
+constexpr int kMaxWarps = 16;                                 // most warps of any fold CTA
 
 // Launch geometry and shared-memory layout of one fold launch. Every CTA of a
 // cluster of `cl` CTAs owns one k-slice of the shrink (ksl columns of A / x)

@@ -68,7 +68,7 @@ struct Plan {
   int G;                           // groups (0: nothing to do)
   int NV;                          // valid positions (sum of group sizes)
   int failed;                      // an mbarrier wait gave up: no further stores
-  int warp_sums[kWarps];
+  int warp_sums[kMaxWarps];
   int found_slot, found_tile;      // bgmv planning scratch
   int members[kMaxRows];           // positions, grouped, ascending within a group
   int gstart[kMaxRows + 1];        // group g = members[gstart[g] .. gstart[g+1])
@@ -112,12 +112,13 @@ __device__ __forceinline__ bool tiled_smem_ok(const FoldGeometry& g, const unsig
 
 // The ring's mbarriers, initialized once per CTA; passes of a work unit keep
 // counting ring items from where the previous pass stopped. Called by all threads.
+template <int CW = kConsumerWarps, int PW = kProducerWarps>
 __device__ __forceinline__ void ring_init(Plan& pl, int ns) {
   fence_proxy_async_smem();   // planning scratch in the ring: generic accesses before TMA writes
   if (threadIdx.x == 0) {
     for (int s = 0; s < ns; ++s) {
-      mbar_init(smem_u32(&pl.full[s]), kProducerWarps * 32);
-      mbar_init(smem_u32(&pl.empty[s]), kConsumerWarps);
+      mbar_init(smem_u32(&pl.full[s]), PW * 32);
+      mbar_init(smem_u32(&pl.empty[s]), CW);
     }
     pl.failed = 0;
     mbar_fence_init();
@@ -133,7 +134,7 @@ __device__ __forceinline__ void ring_init(Plan& pl, int ns) {
 // (launches with g.a_tiled); each instance has one A layout. TC: the shrink
 // runs on tcgen05 (launches with g.tc; one group per pass, TMEM allocated by
 // the caller at pl.tmem).
-template <int MAXT, bool TILED, bool TC = false>
+template <int MAXT, bool TILED, bool TC = false, int CW = kConsumerWarps, int PW = kProducerWarps>
 __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeometry& g, Plan& pl,
                                            unsigned char* smem, const cg::cluster_group& cluster,
                                            int crank, int it0) {
@@ -156,10 +157,10 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
   // otherwise only the consumer warps take part (the producer never touches
   // the partials or xa, so it keeps filling the ring meanwhile).
   auto unit_sync = [&]() {
-    if (g.cl > 1) cluster.sync(); else consumer_sync();
+    if (g.cl > 1) cluster.sync(); else consumer_sync<CW>();
   };
 
-  if (warp >= kConsumerWarps) {
+  if (warp >= CW) {
     // ===================== producer warpgroup =====================
     // All four producer warps serve every item, in item order (an mbarrier
     // parity wait only tells the current phase from the one before it). Rows
@@ -168,10 +169,10 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
     // chunks spread over all 128 producer threads. Every producer thread first
     // registers the TMA bytes it issues, then arrives on the item's full
     // barrier once its own cp.async chunks have landed.
-    const int pw = warp - kConsumerWarps;
-    const int pt = tid - kConsumerWarps * 32;          // 0 .. 127
-    constexpr int kP = kProducerWarps * 32;
-    const int q0 = pw + kProducerWarps * lane;         // this thread's first TMA copy
+    const int pw = warp - CW;
+    const int pt = tid - CW * 32;          // 0 .. 127
+    constexpr int kP = PW * 32;
+    const int q0 = pw + PW * lane;         // this thread's first TMA copy
     bool dead = false;   // this thread gave up on a stage: it issues no further copies
     auto produce = [&](int it) {
       const int ri = it0 + it, s = ri % ns;   // ring item
@@ -305,10 +306,10 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
   // Slot-parallel: group gi's one shrink item is ring item it0 + gi, in slot
   // (it0 + gi) % ns, served by KSG warps (warps s, s + ns, ...) that take
   // alternate k-steps into their own partial planes.
-  const int KSG = gpar ? max(1, min(g.ksplit, kConsumerWarps / ns)) : 1;
+  const int KSG = gpar ? max(1, min(g.ksplit, CW / ns)) : 1;
   const bool idle = gpar && warp >= ns * KSG;   // slot-parallel with fewer slots than warps
   const int g_first = gpar ? (((warp % ns) - it0 % ns) + ns) % ns : 0, g_step = gpar ? ns : 1;
-  const int KS = gpar ? KSG : g.ksplit, TW = kConsumerWarps / KS;
+  const int KS = gpar ? KSG : g.ksplit, TW = CW / KS;
   const int kp = gpar ? warp / ns : warp / TW;
   const int t_first = gpar ? 0 : warp % TW, t_step = gpar ? 1 : TW;
   const int MT = g.mr16 >> 4;
@@ -399,7 +400,7 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
       }
       for (; si < nst; si += KS) step(st, si * 16, min(16, klen - si * 16), acc[0]);   // the rest on chain 0
       __syncwarp();
-      if (lane == 0) mbar_arrive_count(smem_u32(&pl.empty[s]), gpar ? kConsumerWarps / KSG : 1);
+      if (lane == 0) mbar_arrive_count(smem_u32(&pl.empty[s]), gpar ? CW / KSG : 1);
     }
 #pragma unroll
     for (int ch = 1; ch < kChains; ++ch)
@@ -446,7 +447,7 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
                       smem_desc(xt + (s16 >> 2) * x_atom + off, 1024, Swz::k128), idesc, (kc | s16) != 0);
           }
           umma_commit(smem_u32(&pl.empty[s]));
-          mbar_arrive_count(smem_u32(&pl.empty[s]), kConsumerWarps - 1);   // the phase still waits for the commit
+          mbar_arrive_count(smem_u32(&pl.empty[s]), CW - 1);   // the phase still waits for the commit
         }
         umma_commit(smem_u32(&pl.tc_done));
       }
@@ -472,7 +473,7 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
     }
   }
   if (nk == 0) {  // empty k-slice: the partials are zero
-    for (int e = tid; e < KS * NV * p.max_rank; e += kConsumerWarps * 32) {
+    for (int e = tid; e < KS * NV * p.max_rank; e += CW * 32) {
       const int ph = e / (NV * p.max_rank), r = e - ph * NV * p.max_rank;
       const int mi = r / p.max_rank, c = r - mi * p.max_rank;
       part_s[ph * plane + pl.members[mi] * g.pitch_part + c] = 0.f;
@@ -488,8 +489,8 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
     // slot crank of every peer's gather buffer (one cluster barrier); then every
     // CTA adds the cl slots in rank order itself.
     float* gath = part_s + KS * plane;
-    consumer_sync();
-    for (int e = tid; e < NV * p.max_rank; e += kConsumerWarps * 32) {
+    consumer_sync<CW>();
+    for (int e = tid; e < NV * p.max_rank; e += CW * 32) {
       const int mi = e / p.max_rank, c = e - mi * p.max_rank;
       const int off = pl.members[mi] * g.pitch_part + c;
       float v = part_s[off];
@@ -497,7 +498,7 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
       for (int q = 0; q < g.cl; ++q) cluster.map_shared_rank(gath, q)[crank * plane + off] = v;
     }
     unit_sync();
-    for (int e = tid; e < NV * p.max_rank; e += kConsumerWarps * 32) {
+    for (int e = tid; e < NV * p.max_rank; e += CW * 32) {
       const int mi = e / p.max_rank, c = e - mi * p.max_rank, pos = pl.members[mi];
       const int off = pos * g.pitch_part + c;
       float sum = gath[off];
@@ -506,14 +507,14 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
       xa_s[pos * xa_pitch_el + c] = xb;
       if (store_xa && e % g.cl == crank) p.xa[(long long)pl.xarow[pos] * p.max_rank + c] = xb;
     }
-    consumer_sync();
+    consumer_sync<CW>();
   } else {
     // Reduce-scatter: CTA crank adds its share of the elements over the ranks'
     // partials (each rank first folds its own k-phase planes) and pushes the
     // BF16 result to every CTA of the cluster.
     if (KS > 1 && g.cl > 1) {
-      consumer_sync();
-      for (int e = tid; e < NV * p.max_rank; e += kConsumerWarps * 32) {
+      consumer_sync<CW>();
+      for (int e = tid; e < NV * p.max_rank; e += CW * 32) {
         const int mi = e / p.max_rank, c = e - mi * p.max_rank;
         const int off = pl.members[mi] * g.pitch_part + c;
         float v = part_s[off];
@@ -524,7 +525,7 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
     unit_sync();
     const int E = NV * p.max_rank, per = (E + g.cl - 1) / g.cl;
     const int e_lo = crank * per, e_hi = min(e_lo + per, E);
-    for (int e = e_lo + tid; e < e_hi; e += kConsumerWarps * 32) {
+    for (int e = e_lo + tid; e < e_hi; e += CW * 32) {
       const int mi = e / p.max_rank, c = e - mi * p.max_rank, pos = pl.members[mi];
       const int off = pos * g.pitch_part + c;
       float sum;
@@ -677,15 +678,15 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
         // Two blocks per step (cb and cb + 8): both blocks' loads and MMAs are
         // issued before either block's dependent fold.
         int cb = warp;
-        for (; cb + kConsumerWarps < NCB; cb += 2 * kConsumerWarps) {
+        for (; cb + CW < NCB; cb += 2 * CW) {
           float da[MR][2][4], db[MR][2][4];
           uint32_t oa[2 * MR][2], ob2[2 * MR][2];
           block_mma(cb, da);
-          block_mma(cb + kConsumerWarps, db);
+          block_mma(cb + CW, db);
           block_old(cb, oa);
-          block_old(cb + kConsumerWarps, ob2);
+          block_old(cb + CW, ob2);
           block_fold(cb, da, oa);
-          block_fold(cb + kConsumerWarps, db, ob2);
+          block_fold(cb + CW, db, ob2);
         }
         if (cb < NCB) {
           float da[MR][2][4];
@@ -901,13 +902,17 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
 // folded in passes of up to kMaxRows rows, split into groups of at most gmax
 // rows of one (expert, adapter) pair, each folded over the full k_in and n_out.
 // ============================================================================
-constexpr int kMoeUnitsPerCta = 2;
+#ifndef GLORA_MOE_UNITS_PER_CTA
+#define GLORA_MOE_UNITS_PER_CTA 3
+#endif
+constexpr int kMoeUnitsPerCta = GLORA_MOE_UNITS_PER_CTA;   // target units per CTA (sets the chunk size)
 constexpr int kMoeRoundRows = kMoeMaxPos;    // rows of the units' experts scanned per round
-constexpr int kMoeRowsPerThread = (kMoeRoundRows + kThreads - 1) / kThreads;
+constexpr int kMoeThreads = (kMoeConsumerWarps + kProducerWarps) * 32;   // the MoE kernel's CTA
+constexpr int kMoeRowsPerThread = (kMoeRoundRows + kMoeThreads - 1) / kMoeThreads;
 constexpr int kMoeMaxMyUnits = 64;           // units of one CTA planned per round
 
 template <int MAXT>
-__global__ void __launch_bounds__(kThreads, kMoeCtasPerSm) lora_moe_fold_kernel(const __grid_constant__ MoeArgs p) {
+__global__ void __launch_bounds__(kMoeThreads, kMoeCtasPerSm) lora_moe_fold_kernel(const __grid_constant__ MoeArgs p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const FoldGeometry& g = p.g;
   const cg::cluster_group cluster = cg::this_cluster();
@@ -937,7 +942,7 @@ __global__ void __launch_bounds__(kThreads, kMoeCtasPerSm) lora_moe_fold_kernel(
   if (tid == 0) {
     for (int s = 0; s < g.ns; ++s) {
       mbar_init(smem_u32(&pl.full[s]), kProducerWarps * 32);
-      mbar_init(smem_u32(&pl.empty[s]), kConsumerWarps);
+      mbar_init(smem_u32(&pl.empty[s]), kMoeConsumerWarps);
     }
     pl.failed = 0;
     mbar_fence_init();
@@ -955,7 +960,7 @@ __global__ void __launch_bounds__(kThreads, kMoeCtasPerSm) lora_moe_fold_kernel(
     return (offs[lo] <= r && r < offs[lo + 1]) ? lo : -1;
   };
 
-  for (int i = tid; i <= E; i += kThreads) offs[i] = p.expert_offsets[i];
+  for (int i = tid; i <= E; i += kMoeThreads) offs[i] = p.expert_offsets[i];
   __syncthreads();
   const int lo_w = max(p.row_offset, offs[0]), hi_w = min(p.row_end, offs[E]);
   if (hi_w <= lo_w) return;                      // every thread agrees
@@ -978,7 +983,7 @@ __global__ void __launch_bounds__(kThreads, kMoeCtasPerSm) lora_moe_fold_kernel(
   const int round_rows = ac > kMoeMaxDesc ? kMoeMaxDesc : kMoeRoundRows;
   while (v0 < my_units) {
     if (ring_ready) {   // the ring holds the last round's stages: reload the offsets
-      for (int i = tid; i <= E; i += kThreads) offs[i] = p.expert_offsets[i];
+      for (int i = tid; i <= E; i += kMoeThreads) offs[i] = p.expert_offsets[i];
       __syncthreads();
     }
     // at most kMoeMaxDesc groups (so runs) per round, or one unit
@@ -992,11 +997,11 @@ __global__ void __launch_bounds__(kThreads, kMoeCtasPerSm) lora_moe_fold_kernel(
       u_lo[tid] = max(offs[e], lo_w);
       u_row0[tid] = max(0, min(offs[e + 1], hi_w) - max(offs[e], lo_w));
     }
-    for (int i = tid; i < nu * ac; i += kThreads) bcnt[i] = 0;
+    for (int i = tid; i < nu * ac; i += kMoeThreads) bcnt[i] = 0;
     // the table entries of the round's groups, loaded beside the row scan
     // (groups past the adapters are never routed)
     if (nu * ac <= kMoeMaxDesc) {
-      for (int k = tid; k < nu * ac; k += kThreads) {
+      for (int k = tid; k < nu * ac; k += kMoeThreads) {
         const int v = k / ac, a = (b + (v0 + v) * G) % n_chunks * ac + (k - v * ac);
         const int e = e_first + (b + (v0 + v) * G) / n_chunks;
         if (a < A) {
@@ -1027,7 +1032,7 @@ __global__ void __launch_bounds__(kThreads, kMoeCtasPerSm) lora_moe_fold_kernel(
     int uv[kMoeRowsPerThread];
 #pragma unroll
     for (int j = 0; j < kMoeRowsPerThread; ++j) {
-      const int q = row_cur + tid + j * kThreads;
+      const int q = row_cur + tid + j * kMoeThreads;
       rr[j] = -1;
       tk[j] = 0;
       uv[j] = 0;
@@ -1100,7 +1105,7 @@ __global__ void __launch_bounds__(kThreads, kMoeCtasPerSm) lora_moe_fold_kernel(
     const int nd = mp.nd, npos = mp.npos;
     // table entries of the runs
     const bool cached = nu * ac <= kMoeMaxDesc;
-    for (int k = tid; k < nd; k += kThreads) {
+    for (int k = tid; k < nd; k += kMoeThreads) {
       MoeDesc& d = mp.desc[k];
       const int idx = d.a * E + d.e;
       const uint16_t* Ap = cached ? tabA[d.i_lo] : p.a_table[idx];
@@ -1194,7 +1199,7 @@ __global__ void __launch_bounds__(kThreads, kMoeCtasPerSm) lora_moe_fold_kernel(
         pl.NV = nvk;
       }
       __syncthreads();
-      if (pl.G > 0) it0 += fold_engine<MAXT, false>(ea, g, pl, smem, cluster, 0, it0);
+      if (pl.G > 0) it0 += fold_engine<MAXT, false, false, kMoeConsumerWarps, kProducerWarps>(ea, g, pl, smem, cluster, 0, it0);
       __syncthreads();   // the next pass rewrites the plan
     }
     // Another round: the ring serves as planning scratch again (every item of
@@ -1206,7 +1211,7 @@ __global__ void __launch_bounds__(kThreads, kMoeCtasPerSm) lora_moe_fold_kernel(
 // Launchers
 // ============================================================================
 template <typename Args>
-static int launch_fold(void (*kernel)(Args), const Args& a, void* stream) {
+static int launch_fold(void (*kernel)(Args), const Args& a, void* stream, int threads = kThreads) {
   const FoldGeometry& g = a.g;
   if (g.clusters <= 0) return 0;
   if (g.ns > kMaxStages) return static_cast<int>(cudaErrorInvalidValue);
@@ -1218,7 +1223,7 @@ static int launch_fold(void (*kernel)(Args), const Args& a, void* stream) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(g.clusters * g.cl), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(g.smem_bytes);
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attrs[2];
@@ -1260,9 +1265,9 @@ int launch_bgmv(const BgmvArgs& a, void* stream) {
 }
 int launch_moe(const MoeArgs& a, void* stream) {
   switch (a.g.maxt) {
-    case 1: return launch_fold(lora_moe_fold_kernel<1>, a, stream);
-    case 2: return launch_fold(lora_moe_fold_kernel<2>, a, stream);
-    case 4: return launch_fold(lora_moe_fold_kernel<4>, a, stream);
+    case 1: return launch_fold(lora_moe_fold_kernel<1>, a, stream, kMoeThreads);
+    case 2: return launch_fold(lora_moe_fold_kernel<2>, a, stream, kMoeThreads);
+    case 4: return launch_fold(lora_moe_fold_kernel<4>, a, stream, kMoeThreads);
     default: return static_cast<int>(cudaErrorInvalidValue);
   }
 }
