@@ -630,7 +630,10 @@ def oracle_rows_per_s(wl, budget_s: float, rows_per_call=None, threads: int = 1)
     unchanged). Returns (rows/s over all threads, rows timed, seconds)."""
     import threading
     total = oracle_total_rows(wl)
-    default = 256 if workload_kind(wl) == "moe" else max(1, total // threads)
+    # MoE: calls of 1/16 of the sorted rows (1024 of 16384), the chunk the
+    # reference arm hands each of 16 host threads; smaller calls let the Python
+    # side of each call (GIL-held) throttle the threads
+    default = max(1, -(-total // 16)) if workload_kind(wl) == "moe" else max(1, total // threads)
     rows_per_call = rows_per_call or default
     done = [0] * threads
     errors = []

@@ -286,8 +286,7 @@ bool moe_geometry(int window, int adapters, int num_experts, int max_rank, int k
   const long long bins = static_cast<long long>(num_experts) * adapters;
   // planner scratch: offsets, four unit arrays, the groups of a round
   const long long scratch = ((num_experts + 4) & ~3) * 4LL + (4LL * 64 + 4) * 4 +
-                            (static_cast<long long>(std::max(glora::kMoeMaxDesc, adapters)) + 2) * 4 +
-                            glora::kMoeMaxDesc * 20LL;
+                            ((static_cast<long long>(std::max(glora::kMoeMaxDesc, adapters)) + 4) & ~3LL) * 4;
   const long long ring = static_cast<long long>(ns) * g.stage_bytes;
   if (bins > glora::kMoeMaxBins || scratch > ring) return false;
   g.clusters = static_cast<int>(std::max<long long>(1, std::min<long long>(static_cast<long long>(sms) * glora::kMoeCtasPerSm,

@@ -111,14 +111,14 @@ struct MoeArgs {
 // the CTA's plan of one round (its runs and their rows, run after run).
 struct MoeDesc {
   int e, a;                // expert, adapter
-  int i_lo, n;             // the round's group of the run, and its rows
+  int n;                   // its rows
   int pos0;                // first position of the run in the CTA's row list
   float scale;
   const uint16_t* A;       // NULL: entry NULL or misaligned (the rows stay unchanged)
   const uint16_t* B;
 };
 struct MoePlan {
-  int nd, npos, more;
+  int nd, npos;
   MoeDesc desc[kMoeMaxDesc];
   int pos_row[kMoeMaxPos];     // sorted row of each position
   int pos_tok[kMoeMaxPos];     // its token (the x row of the gate/up form)

@@ -933,9 +933,10 @@ __global__ void __launch_bounds__(kMoeThreads, kMoeCtasPerSm) lora_moe_fold_kern
   int* u_lo = u_a0 + kMoeMaxMyUnits;           // its rows in the window: [u_lo, u_hi)
   int* u_row0 = u_lo + kMoeMaxMyUnits;         // prefix of the units' rows (+1 entry)
   int* bcnt = u_row0 + kMoeMaxMyUnits + 4;     // [units * ac] rows of each group in the round
-  const uint16_t** tabA = reinterpret_cast<const uint16_t**>(bcnt + ((max(kMoeMaxDesc, A) + 1) & ~1));   // their
-  const uint16_t** tabB = tabA + kMoeMaxDesc;                                                           // table
-  float* tabS = reinterpret_cast<float*>(tabB + kMoeMaxDesc);                                           // entries
+  // The planning inputs read first: the expert offsets.
+  auto load_inputs = [&]() {
+    for (int i = tid; i <= E; i += kMoeThreads) offs[i] = p.expert_offsets[i];
+  };
 
   // The ring's mbarriers read no input: they are set up while the previous
   // grid on the stream may still be running.
@@ -960,7 +961,7 @@ __global__ void __launch_bounds__(kMoeThreads, kMoeCtasPerSm) lora_moe_fold_kern
     return (offs[lo] <= r && r < offs[lo + 1]) ? lo : -1;
   };
 
-  for (int i = tid; i <= E; i += kMoeThreads) offs[i] = p.expert_offsets[i];
+  load_inputs();
   __syncthreads();
   const int lo_w = max(p.row_offset, offs[0]), hi_w = min(p.row_end, offs[E]);
   if (hi_w <= lo_w) return;                      // every thread agrees
@@ -982,8 +983,8 @@ __global__ void __launch_bounds__(kMoeThreads, kMoeCtasPerSm) lora_moe_fold_kern
   // alone has more groups than a round holds runs (each row at most one run).
   const int round_rows = ac > kMoeMaxDesc ? kMoeMaxDesc : kMoeRoundRows;
   while (v0 < my_units) {
-    if (ring_ready) {   // the ring holds the last round's stages: reload the offsets
-      for (int i = tid; i <= E; i += kMoeThreads) offs[i] = p.expert_offsets[i];
+    if (ring_ready) {   // the ring holds the last round's stages: reload the planning inputs
+      load_inputs();
       __syncthreads();
     }
     // at most kMoeMaxDesc groups (so runs) per round, or one unit
@@ -998,17 +999,20 @@ __global__ void __launch_bounds__(kMoeThreads, kMoeCtasPerSm) lora_moe_fold_kern
       u_row0[tid] = max(0, min(offs[e + 1], hi_w) - max(offs[e], lo_w));
     }
     for (int i = tid; i < nu * ac; i += kMoeThreads) bcnt[i] = 0;
-    // the table entries of the round's groups, loaded beside the row scan
-    // (groups past the adapters are never routed)
-    if (nu * ac <= kMoeMaxDesc) {
-      for (int k = tid; k < nu * ac; k += kMoeThreads) {
-        const int v = k / ac, a = (b + (v0 + v) * G) % n_chunks * ac + (k - v * ac);
-        const int e = e_first + (b + (v0 + v) * G) / n_chunks;
-        if (a < A) {
-          tabA[k] = p.a_table[a * E + e];
-          tabB[k] = p.b_table[a * E + e];
-          tabS[k] = p.scale_table[a * E + e];
-        }
+    // The table entries of the round's groups (at most kMoeMaxDesc, one per
+    // thread): loaded into registers here, consumed after the row scan, so the
+    // round trip overlaps it. Groups past the adapters are never routed.
+    const bool cached = nu * ac <= kMoeMaxDesc;
+    const uint16_t* tA = nullptr;
+    const uint16_t* tB = nullptr;
+    float tS = 0.f;
+    if (cached && tid < nu * ac) {
+      const int v = tid / ac, u = b + (v0 + v) * G;
+      const int a = (u % n_chunks) * ac + (tid - v * ac), e = e_first + u / n_chunks;
+      if (a < A) {
+        tA = p.a_table[a * E + e];
+        tB = p.b_table[a * E + e];
+        tS = p.scale_table[a * E + e];
       }
     }
     __syncthreads();
@@ -1078,10 +1082,9 @@ __global__ void __launch_bounds__(kMoeThreads, kMoeCtasPerSm) lora_moe_fold_kern
           const int v = k / ac;
           dd.e = u_e[v];
           dd.a = u_a0[v] + (k - v * ac);
-          dd.i_lo = k;               // the group (its cached table entries)
           dd.n = n;
           dd.pos0 = carry_pos + incl - n;
-          bcnt[k] = (d << 16) | 0;   // the run of group k (positions are pos0 + rank)
+          bcnt[k] = (d << 16) | 1;   // group k has rows, in run d (positions are pos0 + rank)
         }
         carry_pos += __shfl_sync(0xffffffffu, incl, 31);
         carry_run += __popc(has);
@@ -1104,18 +1107,22 @@ __global__ void __launch_bounds__(kMoeThreads, kMoeCtasPerSm) lora_moe_fold_kern
     }
     const int nd = mp.nd, npos = mp.npos;
     // table entries of the runs
-    const bool cached = nu * ac <= kMoeMaxDesc;
-    for (int k = tid; k < nd; k += kMoeThreads) {
-      MoeDesc& d = mp.desc[k];
-      const int idx = d.a * E + d.e;
-      const uint16_t* Ap = cached ? tabA[d.i_lo] : p.a_table[idx];
-      const uint16_t* Bp = cached ? tabB[d.i_lo] : p.b_table[idx];
+    auto set_entries = [&](MoeDesc& d, const uint16_t* Ap, const uint16_t* Bp, float sc) {
       const uintptr_t ua = reinterpret_cast<uintptr_t>(Ap), ub = reinterpret_cast<uintptr_t>(Bp);
       const bool usable = ua != 0 && ub != 0 && ((ua | ub) & 15u) == 0;
       if (ua != 0 && ub != 0 && !usable) atomicOr(&g_lora_status, kDevMisaligned);
       d.A = usable ? Ap : nullptr;
       d.B = Bp;
-      d.scale = usable ? (cached ? tabS[d.i_lo] : p.scale_table[idx]) : 0.f;
+      d.scale = usable ? sc : 0.f;
+    };
+    if (cached) {   // the thread of each group with rows fills in its run
+      if (tid < nu * ac && (bcnt[tid] & 1)) set_entries(mp.desc[bcnt[tid] >> 16], tA, tB, tS);
+    } else {
+      for (int k = tid; k < nd; k += kMoeThreads) {
+        MoeDesc& d = mp.desc[k];
+        const int idx = d.a * E + d.e;
+        set_entries(d, p.a_table[idx], p.b_table[idx], p.scale_table[idx]);
+      }
     }
     // next round
     if (row_end >= rows_all) {

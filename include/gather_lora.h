@@ -159,16 +159,17 @@ int lora_bgmv(const lora_bf16_t* x, int64_t x_row_stride,
  *                     launch; ignored when xa is NULL ("Module moe_lora_grouped",
  *                     `moe_lora_grouped_down`: the caller needs at least the window's rows)
  * The window must satisfy 0 <= row_offset <= row_end <= te (else LORA_ERR_WINDOW);
- * a window whose grid (below) would exceed one launch's 2^31 - 1 CTAs gives
- * LORA_ERR_SIZE and launches nothing. The launch grid is
- * ceil((row_end - row_offset) / T) tiles of T sorted rows (at least 1) times the
- * adapters (max_loras with a row_adapter, else 1), T in {64, 128, 256} the
- * largest that still gives 128 such units (64 otherwise), so the grid depends
- * only on the window size and the adapter count; each CTA folds the rows of
- * one adapter in one tile. Calls over windows [0, cap), [cap, 2cap), ... give
- * the same base_out as one call over [0, te). The fold never reads xa back, so
- * a caller whose xa holds all te rows, or who passes NULL, can make that one
- * call: it also spares the wait of each window for the previous one's last CTA.
+ * the tables may hold at most LORA_MAX_LORAS entries (max_loras * num_experts),
+ * else LORA_ERR_SIZE (so is a shape whose stages do not fit shared memory). The
+ * launch grid is persistent and static: one CTA per SM
+ * (fewer for windows under 16 rows per SM, at least 1), so it depends only on the
+ * window size and the device. Each CTA takes a fixed share of the window's units
+ * (one expert and a chunk of adapters) and folds the rows of their (expert,
+ * adapter) groups; which rows share a group never changes a row's bits. Calls
+ * over windows [0, cap), [cap, 2cap), ... give the same base_out as one call
+ * over [0, te). The fold never reads xa back, so a caller whose xa holds all te
+ * rows, or who passes NULL, can make that one call: it also spares the wait of
+ * each window for the previous one's last CTA.
  */
 int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, int32_t x_gather,
                           lora_bf16_t* base_out, int64_t out_row_stride,
