@@ -10,6 +10,12 @@ interleaved QKV row, dense FFN down_proj, the MoE gate/up form, both MoE folds
 as one call over all rows, the decode-path MoE gather fold, single-adapter
 prefill deltas) are measured the same way and reported under "workloads".
 
+Calls pass LORA_INPUTS_READY (routing, x and adapters of a step are written
+before its calls are issued, as in a model layer): each call plans and runs its
+shrink while the kernel before it finishes. Every figure is also taken with
+calls that wait for the previous kernel first (--wait-previous makes those the
+main figures).
+
 Timing: inputs are resident in HBM; consecutive steps rotate through enough
 independent copies of every input (adapter pools included) to exceed 2x the L2
 size, so no step finds its data in L2. The K steps are replayed from CUDA graphs
@@ -160,6 +166,7 @@ def gather_algorithmic_bytes(wl) -> dict:
 
 
 USE_TMAPS = True     # load A as 2-D TMA boxes through host-encoded tensor maps (--no-tmaps: rows)
+READY = 1            # calls pass LORA_INPUTS_READY (--wait-previous: 0)
 
 
 def a_load(wl) -> str:
@@ -278,6 +285,7 @@ class BgmvRunner:
         self.copies = [base] + [self._clone(base, wl) for _ in range(copies - 1)]
         self.maps = [a_maps_for(d.a_table, wl.max_rank, wl.k_in) for d in self.copies]
         self.launches_per_step = 1
+        self.flags = READY
 
     @staticmethod
     def _clone(d, wl):
@@ -301,7 +309,7 @@ class BgmvRunner:
         wl, d = self.wl, self.copies[c]
         L.lora_bgmv(d.x, wl.x_row_stride, d.out_ptr, wl.out_row_stride, d.seq_slot, wl.n,
                     d.a_table, d.b_table, d.scale, wl.max_loras, wl.max_rank, wl.k_in, wl.n_out,
-                    xa=d.xa, stream=stream, a_tmaps=self.maps[c])
+                    xa=d.xa, stream=stream, a_tmaps=self.maps[c], flags=self.flags)
 
 
 class MoeRunner:
@@ -311,6 +319,7 @@ class MoeRunner:
         self.windows = wl.windows()
         self.copies = [W.moe_to_device(wl, device, xa_rows=wl.cap) for _ in range(copies)]
         self.launches_per_step = len(self.windows)
+        self.flags = READY
 
     def bytes_per_copy(self):
         d = self.copies[0]
@@ -324,7 +333,7 @@ class MoeRunner:
                                     wl.num_experts, d.sorted_token_ids, wl.te, d.row_adapter,
                                     wl.num_tokens, lo, hi, d.a_table, d.b_table, d.scale,
                                     wl.max_loras, wl.max_rank, wl.k_in, wl.n_out, xa=d.xa,
-                                    stream=stream, x_gather=wl.x_gather)
+                                    stream=stream, x_gather=wl.x_gather, flags=self.flags)
 
 
 class GatherRunner:
@@ -334,6 +343,7 @@ class GatherRunner:
         self.copies = [W.gather_to_device(wl, device) for _ in range(copies)]
         self.maps = [a_maps_for(d.a_table, wl.max_rank, wl.k_in) for d in self.copies]
         self.launches_per_step = 1
+        self.flags = READY
 
     def bytes_per_copy(self):
         d = self.copies[0]
@@ -345,7 +355,7 @@ class GatherRunner:
         L.lora_moe_gather_bgmv(d.x, wl.k_in, d.out_buf, wl.n_out, d.indices, wl.n_rows, wl.top_k,
                                d.row_adapter, wl.num_tokens, wl.num_experts, d.a_table, d.b_table,
                                d.scale, wl.max_loras, wl.max_rank, wl.k_in, wl.n_out, xa=d.xa,
-                               stream=stream, a_tmaps=self.maps[c])
+                               stream=stream, a_tmaps=self.maps[c], flags=self.flags)
 
 
 class DeltaRunner:
@@ -354,6 +364,7 @@ class DeltaRunner:
         self.wl = wl
         self.copies = [W.delta_to_device(wl, device) for _ in range(copies)]
         self.launches_per_step = 1
+        self.flags = 0      # lora_delta takes no flags
 
     def bytes_per_copy(self):
         d = self.copies[0]
@@ -503,7 +514,7 @@ def e2e_run(wl, device, steps, warmup, copies):
         def call(c, d):
             L.lora_bgmv(d.x, wl.x_row_stride, d.out_ptr, wl.out_row_stride, d.seq_slot, wl.n,
                         d.a_table, d.b_table, d.scale, wl.max_loras, wl.max_rank, wl.k_in, wl.n_out,
-                        xa=d.xa, stream=stream, a_tmaps=maps[c])
+                        xa=d.xa, stream=stream, a_tmaps=maps[c], flags=READY)
         rows = wl.n
     elif kind == "moe":
         devs = [W.moe_to_device(wl, device, xa_rows=wl.cap) for _ in range(copies)]
@@ -517,7 +528,7 @@ def e2e_run(wl, device, steps, warmup, copies):
                                         wl.num_experts, d.sorted_token_ids, wl.te, d.row_adapter,
                                         wl.num_tokens, lo, hi, d.a_table, d.b_table, d.scale,
                                         wl.max_loras, wl.max_rank, wl.k_in, wl.n_out, xa=d.xa,
-                                        stream=stream, x_gather=wl.x_gather)
+                                        stream=stream, x_gather=wl.x_gather, flags=READY)
         rows = wl.te
     else:
         raise ValueError(f"no end-to-end run for {kind}")
@@ -624,45 +635,40 @@ def oracle_fold_rows(wl, start: int, count: int) -> None:
 def oracle_rows_per_s(wl, budget_s: float, rows_per_call=None, threads: int = 1):
     """Time the oracle on the host over a bounded sample of the workload's rows.
 
-    Each of `threads` host threads folds its own rotating rows, rows_per_call
-    at a time, until budget_s has passed (the oracle is a C call that releases
-    the interpreter lock, so the threads run in parallel; the oracle itself is
-    unchanged). Returns (rows/s over all threads, rows timed, seconds)."""
-    import threading
+    One thread folds rotating rows, rows_per_call at a time, until budget_s has
+    passed. With several threads the rows go in rounds, as the reference arm's
+    steps do: each round hands every thread its own rows_per_call rows (the
+    oracle is a C call that releases the interpreter lock, so they run in
+    parallel; the oracle itself is unchanged) and ends when all are done.
+    Returns (rows/s over all threads, rows timed, seconds)."""
+    from concurrent.futures import ThreadPoolExecutor
     total = oracle_total_rows(wl)
-    # MoE: calls of 1/16 of the sorted rows (1024 of 16384), the chunk the
-    # reference arm hands each of 16 host threads; smaller calls let the Python
-    # side of each call (GIL-held) throttle the threads
+    # MoE: 1/16 of the sorted rows per call (1024 of 16384), the chunk the
+    # reference arm gives each of 16 host threads
     default = max(1, -(-total // 16)) if workload_kind(wl) == "moe" else max(1, total // threads)
     rows_per_call = rows_per_call or default
-    done = [0] * threads
-    errors = []
+    done = 0
+    i0 = 0
     t0 = time.perf_counter()
-
-    def work(t):
-        try:
-            i0 = (t * rows_per_call) % total
+    if threads == 1:
+        while True:
+            oracle_fold_rows(wl, i0, rows_per_call)
+            done += rows_per_call
+            i0 = (i0 + rows_per_call) % total
+            if time.perf_counter() - t0 >= budget_s:
+                break
+    else:
+        with ThreadPoolExecutor(threads) as ex:
             while True:
-                oracle_fold_rows(wl, i0, rows_per_call)
-                done[t] += rows_per_call
+                starts = [(i0 + t * rows_per_call) % total for t in range(threads)]
+                # a failed call re-raises here: it must not shorten the count silently
+                list(ex.map(lambda st: oracle_fold_rows(wl, st, rows_per_call), starts))
+                done += threads * rows_per_call
                 i0 = (i0 + threads * rows_per_call) % total
                 if time.perf_counter() - t0 >= budget_s:
-                    return
-        except BaseException as e:   # re-raised below: a failed thread must not shorten the count silently
-            errors.append(e)
-
-    if threads == 1:
-        work(0)
-    else:
-        pool = [threading.Thread(target=work, args=(t,)) for t in range(threads)]
-        for th in pool:
-            th.start()
-        for th in pool:
-            th.join()
-    if errors:
-        raise errors[0]
+                    break
     el = time.perf_counter() - t0
-    return sum(done) / el, sum(done), el
+    return done / el, done, el
 
 
 def _rows_word(wl) -> str:
@@ -677,8 +683,8 @@ def cpu_baseline(wl, seconds: float) -> dict:
     vt, nt, st = oracle_rows_per_s(wl, seconds / 2, threads=threads)
     return {"value": vt, "unit": "rows/s", "cores": threads, "kind": "oracle",
             "cpu_model": cpu_model(),
-            "sample": f"{nt} {_rows_word(wl)} of the {wl.name} batch, {threads} host threads on "
-                      f"disjoint rows ({st:.1f} s)",
+            "sample": f"{nt} {_rows_word(wl)} of the {wl.name} batch in rounds of one call per host "
+                      f"thread ({threads} threads, disjoint rows; {st:.1f} s)",
             "single_thread": {"value": v1, "cores": 1,
                               "sample": f"{n1} {_rows_word(wl)}, 1 host thread ({s1:.1f} s)"}}
 
@@ -693,6 +699,7 @@ def workload_config(wl, alg) -> dict:
         cfg.update(num_experts=wl.num_experts, num_tokens=wl.num_tokens, te=wl.te,
                    windows=len(wl.windows()), window_rows=wl.cap, x_gather=bool(wl.x_gather))
     cfg["l2"] = "inputs rotate through device copies totalling more than 2x L2 between steps"
+    cfg["inputs_ready"] = bool(READY)
     return cfg
 
 
@@ -809,6 +816,25 @@ def run_ours(args):
     launches = args.steps * runner.launches_per_step
     geometry = geometry_of(L, wl)
 
+    def other_mode(r, steps_alt):
+        """The same steps with the other call mode (calls that wait for the
+        previous kernel first, or inputs-ready calls under --wait-previous)."""
+        if workload_kind(r.wl) == "delta":
+            return None
+        r.flags = 0 if READY else L.INPUTS_READY
+        m_alt, _ = time_steps(r, steps_alt, 5, device, dctx)
+        r.flags = READY
+        return m_alt / steps_alt
+
+    alt_steps = int(max(50, min(args.steps, 2000.0 / max(ms_max / args.steps, 1e-3))))
+    alt_ms = other_mode(runner, alt_steps)
+    other = None
+    if alt_ms is not None:
+        alt_gbs = bytes_per_launch / (alt_ms / runner.launches_per_step / 1e3) / 1e9
+        other = {"calls": "wait for the previous kernel" if READY else "LORA_INPUTS_READY",
+                 "ms_per_step": alt_ms, "steps": alt_steps, "rows_per_s": alg["rows"] / (alt_ms / 1e3),
+                 "achieved_gbs": alt_gbs, "frac_of_peak": alt_gbs / peak}
+
     # the other fold workloads (per-GPU numbers, same timing rules)
     side = {}
     for name in ([] if args.only else SIDE_WORKLOADS):
@@ -830,7 +856,12 @@ def run_ours(args):
             "ms_per_step": ms2, "launches_per_step": r2.launches_per_step, "steps": k2,
             "algorithmic_bytes": a2["bytes"], "achieved_gbs": gbs2, "frac_of_peak": gbs2 / peak,
             "frac_of_8tbs": gbs2 / 8000.0, "input_copies": len(r2.copies), "a_load": a_load(w2),
-            "traffic": recorded_traffic(name)}
+            "traffic": recorded_traffic(name), "inputs_ready": bool(r2.flags)}
+        ms_o = other_mode(r2, k2)
+        if ms_o is not None:
+            gbs_o = a2["bytes"] / (ms_o / 1e3) / 1e9
+            side[name]["other_calls"] = {"inputs_ready": not bool(r2.flags), "ms_per_step": ms_o,
+                                         "achieved_gbs": gbs_o, "frac_of_peak": gbs_o / peak}
         if dctx.rank == 0 and not args.no_cpu_baseline and workload_kind(w2) in ("bgmv", "moe") \
                 and not name.endswith("_one_launch"):
             vt, nt, st = oracle_rows_per_s(w2, 1.0, threads=host_threads())
@@ -864,7 +895,9 @@ def run_ours(args):
                        "copies_mib": round(C * runner.bytes_per_copy() / 2 ** 20),
                        "l2_mib": round(l2 / 2 ** 20),
                        "graph": "CUDA graph replay, programmatic dependent launch",
-                       "launches_per_step": runner.launches_per_step, "a_load": a_load(wl)},
+                       "launches_per_step": runner.launches_per_step, "a_load": a_load(wl),
+                       "calls": "LORA_INPUTS_READY" if READY else "wait for the previous kernel",
+                       "other_calls": other},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": recorded_traffic(head),
                          "peak_kind": peak_kind, "kernel": KERNEL_NAMES[head_kind],
@@ -892,11 +925,14 @@ def main(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-tmaps", action="store_true", help="load A row by row (no tensor maps)")
     p.add_argument("--only", default=None, help="time one named workload alone (profiling runs)")
+    p.add_argument("--wait-previous", action="store_true",
+                   help="calls wait for the previous kernel before reading anything (no LORA_INPUTS_READY)")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
-    global USE_TMAPS
+    global USE_TMAPS, READY
     USE_TMAPS = not args.no_tmaps
+    READY = 0 if args.wait_previous else 1
     return run_reference(args) if args.impl == "reference" else run_ours(args)
 
 

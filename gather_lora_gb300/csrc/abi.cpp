@@ -402,7 +402,8 @@ int lora_bgmv(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_t* base_out,
               const int32_t* seq_slot, int32_t n, const lora_bf16_t* const* a_table,
               const lora_bf16_t* const* b_table, const float* scale_table, int32_t max_loras,
               int32_t max_rank, int32_t k_in, int32_t n_out, lora_bf16_t* xa, const void* a_tmaps,
-              void* stream) {
+              uint32_t flags, void* stream) {
+  if (flags & ~LORA_INPUTS_READY) return fail(LORA_ERR_FLAGS, "unknown flags 0x%x", flags);
   if (n < 0 || n > LORA_MAX_ROWS) return fail(LORA_ERR_SIZE, "n %d outside [0, %d]", n, LORA_MAX_ROWS);
   if (max_loras < 1 || max_loras > LORA_MAX_LORAS)
     return fail(LORA_ERR_SIZE, "max_loras %d outside [1, %d]", max_loras, LORA_MAX_LORAS);
@@ -433,6 +434,7 @@ int lora_bgmv(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_t* base_out,
   a.k_in = k_in;
   a.n_out = n_out;
   a.xa = xa;
+  a.late = (flags & LORA_INPUTS_READY) ? 1 : 0;
   rc = glora::launch_bgmv(a, stream);
   return rc ? cuda_fail(rc, "lora_bgmv launch") : ok();
 }
@@ -443,7 +445,8 @@ int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, int32_t x_
                           int32_t num_tokens, int32_t row_offset, int32_t row_end,
                           const lora_bf16_t* const* a_table, const lora_bf16_t* const* b_table,
                           const float* scale_table, int32_t max_loras, int32_t max_rank, int32_t k_in,
-                          int32_t n_out, lora_bf16_t* xa, int32_t xa_rows, void* stream) {
+                          int32_t n_out, lora_bf16_t* xa, int32_t xa_rows, uint32_t flags, void* stream) {
+  if (flags & ~LORA_INPUTS_READY) return fail(LORA_ERR_FLAGS, "unknown flags 0x%x", flags);
   if (num_experts < 1 || num_experts > LORA_MAX_EXPERTS)
     return fail(LORA_ERR_SIZE, "num_experts %d outside [1, %d]", num_experts, LORA_MAX_EXPERTS);
   if (max_loras < 1 || max_loras > LORA_MAX_LORAS)
@@ -491,6 +494,7 @@ int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, int32_t x_
   a.k_in = k_in;
   a.n_out = n_out;
   a.xa = xa;
+  a.late = (flags & LORA_INPUTS_READY) ? 1 : 0;
   rc = glora::launch_moe(a, stream);
   return rc ? cuda_fail(rc, "lora_moe_grouped_fold launch") : ok();
 }
@@ -500,7 +504,8 @@ int lora_moe_gather_bgmv(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_t
                          const int32_t* row_adapter, int32_t num_tokens, int32_t num_experts,
                          const lora_bf16_t* const* a_table, const lora_bf16_t* const* b_table,
                          const float* scale_table, int32_t max_loras, int32_t max_rank, int32_t k_in,
-                         int32_t n_out, lora_bf16_t* xa, const void* a_tmaps, void* stream) {
+                         int32_t n_out, lora_bf16_t* xa, const void* a_tmaps, uint32_t flags, void* stream) {
+  if (flags & ~LORA_INPUTS_READY) return fail(LORA_ERR_FLAGS, "unknown flags 0x%x", flags);
   if (n_rows < 0 || n_rows > LORA_MAX_ROWS) return fail(LORA_ERR_SIZE, "n_rows %d outside [0, %d]", n_rows, LORA_MAX_ROWS);
   if (top_k < 1) return fail(LORA_ERR_SIZE, "top_k %d < 1", top_k);
   if (num_tokens < 0) return fail(LORA_ERR_SIZE, "num_tokens %d < 0", num_tokens);
@@ -545,6 +550,7 @@ int lora_moe_gather_bgmv(const lora_bf16_t* x, int64_t x_row_stride, lora_bf16_t
   a.k_in = k_in;
   a.n_out = n_out;
   a.xa = xa;
+  a.late = (flags & LORA_INPUTS_READY) ? 1 : 0;
   rc = glora::launch_bgmv(a, stream);
   return rc ? cuda_fail(rc, "lora_moe_gather_bgmv launch") : ok();
 }

@@ -82,6 +82,7 @@ struct BgmvArgs {
   int max_loras;
   int max_rank, k_in, n_out;
   uint16_t* xa;
+  int late;                  // 1: wait for the previous grid only before touching base_out or xa
   FoldGeometry g;
 };
 
@@ -98,6 +99,7 @@ struct MoeArgs {
   int x_gather;     // 1: x is token-major; sorted row r reads row sorted_token_ids[r]
   int row_offset, row_end;
   int adapters;     // adapters the routing distinguishes: max_loras with a row_adapter, else 1
+  int late;         // 1: wait for the previous grid only before touching base_out or xa
   const uint16_t* const* a_table;
   const uint16_t* const* b_table;
   const float* scale_table;

@@ -94,6 +94,7 @@ struct EngineArgs {
   long long out_stride;
   uint16_t* xa;
   int max_rank, k_in, n_out;
+  int late;   // wait for the previous grid on the stream only before base_out or xa is touched
 };
 
 __device__ __forceinline__ void record_timeout(Plan& pl) {
@@ -271,12 +272,15 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
     // Items whose stage is freed by shrink work can be issued before the
     // cluster exchange; the rest only after it (their stages are released by
     // expand work, which needs the exchanged xa).
-    const int pre = g.cl > 1 ? min(n_items, n_shrink + ns) : n_items;
+    // With a late wait (inputs ready), expand items, which read base_out, are
+    // issued only after the previous grid on the stream has completed.
+    const int pre = p.late ? n_shrink : g.cl > 1 ? min(n_items, n_shrink + ns) : n_items;
     for (int it = 0; it < pre; ++it) produce(it);
     if (g.cl > 1) {
       cluster.sync();
       if (!g.gather) cluster.sync();
     }
+    if (p.late) pdl_wait_then_release();
     for (int it = pre; it < n_items; ++it) produce(it);
     if (*reinterpret_cast<volatile int*>(&pl.failed)) {
       // A wait gave up somewhere: before the CTA can exit, let this thread's own
@@ -483,7 +487,9 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
   // ---- exchange: xa = bf16(sum of the partials: cluster ranks in order, and
   //      k-phase planes in order within a rank) ----
   const int xa_pitch_el = g.pitch_xa >> 1;
-  const bool store_xa = p.xa != nullptr && pl.failed == 0;
+  // xa is written here, or after the expand with a late wait (it may still be
+  // in use by the previous grid until then).
+  const bool store_xa = p.xa != nullptr && pl.failed == 0 && !p.late;
   if (g.gather) {
     // All-gather: each CTA adds its k-phase planes and stores the result into
     // slot crank of every peer's gather buffer (one cluster barrier); then every
@@ -554,6 +560,7 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
   // leaves it four adjacent columns, so each row leaves as one full 32-byte
   // sector of 8-byte stores. The TMA-filled stage is only read. Consumer warp
   // w takes blocks w, w + 8, ...
+  if (p.late) pdl_wait_then_release();   // base_out (and xa) only after the previous grid
   const uint32_t xa_base = smem_u32(xa_s);
   const int gq = lane >> 2, q = lane & 3;
   const bool odd = (q & 1) != 0;
@@ -675,7 +682,7 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
             }
           }
         };
-        // Two blocks per step (cb and cb + 8): both blocks' loads and MMAs are
+        // Two blocks per step (cb and cb + CW): both blocks' loads and MMAs are
         // issued before either block's dependent fold.
         int cb = warp;
         for (; cb + CW < NCB; cb += 2 * CW) {
@@ -713,6 +720,17 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
       by_rank(I1{});
     }
   }
+  // With a late wait xa leaves last: after the exchange every CTA of the
+  // cluster holds all of it in xa_s; CTA crank writes rows crank, crank + cl,
+  // ... in 4-byte pairs.
+  if (p.late && p.xa != nullptr && pl.failed == 0) {
+    const int half = p.max_rank >> 1, mine = NV > crank ? (NV - crank + g.cl - 1) / g.cl : 0;
+    for (int e = tid; e < mine * half; e += CW * 32) {
+      const int mi = crank + (e / half) * g.cl, c2 = e - (e / half) * half, pos = pl.members[mi];
+      const uint32_t v = *reinterpret_cast<const uint32_t*>(xa_s + pos * xa_pitch_el + 2 * c2);
+      *reinterpret_cast<uint32_t*>(p.xa + static_cast<long long>(pl.xarow[pos]) * p.max_rank + 2 * c2) = v;
+    }
+  }
   return n_items;
 }
 
@@ -739,8 +757,15 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   Plan& pl = *reinterpret_cast<Plan*>(smem);
 
-  pdl_wait_then_release();
-  if (!tiled_smem_ok(g, smem)) return;
+  // Without a late wait, nothing is read before the previous grid on the
+  // stream has completed. With one, the engine waits before it touches base_out
+  // or xa; a CTA that folds nothing leaves at once, except CTA 0, which waits,
+  // so that this grid never completes before the previous one.
+  if (!p.late) pdl_wait_then_release();
+  auto leave = [&]() {
+    if (p.late && blockIdx.x == 0) pdl_wait_then_release();
+  };
+  if (!tiled_smem_ok(g, smem)) return leave();
 
   const bool first_tile = g.direct && unit < p.max_loras;
   int slot = first_tile ? unit : -1, tile = 0;
@@ -798,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
     }
     __syncthreads();
     slot = pl.found_slot;
-    if (slot < 0) return;  // every CTA of the cluster takes this branch together
+    if (slot < 0) return leave();  // every CTA of the cluster takes this branch together
     tile = pl.found_tile;
     if (tid == 0) {
       if (TILED) prefetch_tensormap(a_map(slot));
@@ -840,7 +865,7 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
     }
     R = min(g.rt, base - want_lo);
   }
-  if (R <= 0) return;  // no rows for this unit (every thread computed the same count)
+  if (R <= 0) return leave();  // no rows for this unit (every thread computed the same count)
   if (tid == 0) {
     pl.gA[0] = tab_a;
     pl.gmap[0] = TILED ? a_map(slot) : nullptr;
@@ -860,7 +885,7 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
     pl.gstart[1] = R;
   }
   __syncthreads();
-  if (pl.G == 0) return;  // NULL or misaligned adapter: rows stay unchanged
+  if (pl.G == 0) return leave();  // NULL or misaligned adapter: rows stay unchanged
 
   if constexpr (TC) {   // the shrink's accumulator: 32 TMEM columns (16 used)
     if (warp == 0) {
@@ -872,7 +897,7 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
   }
   ring_init(pl, g.ns);
   if constexpr (TC) tc_fence_after();
-  const EngineArgs ea{p.x, p.x_stride, p.out, p.out_stride, p.xa, p.max_rank, p.k_in, p.n_out};
+  const EngineArgs ea{p.x, p.x_stride, p.out, p.out_stride, p.xa, p.max_rank, p.k_in, p.n_out, p.late};
   fold_engine<MAXT, TILED, TC>(ea, g, pl, smem, cluster, crank, 0);
   if constexpr (TC) {
     tc_fence_before();
@@ -948,7 +973,14 @@ __global__ void __launch_bounds__(kMoeThreads, kMoeCtasPerSm) lora_moe_fold_kern
     pl.failed = 0;
     mbar_fence_init();
   }
-  pdl_wait_then_release();
+  // Without a late wait nothing is read before the previous grid on the stream
+  // has completed; with one, the engine waits before it touches base_out or xa,
+  // and a CTA that folds nothing leaves at once, except CTA 0, which waits, so
+  // that this grid never completes before the previous one.
+  if (!p.late) pdl_wait_then_release();
+  auto leave = [&]() {
+    if (p.late && blockIdx.x == 0) pdl_wait_then_release();
+  };
 
   // Expert of sorted row r (-1 outside the spans): the largest e with offs[e] <= r.
   auto expert_of = [&](int r) -> int {
@@ -964,7 +996,7 @@ __global__ void __launch_bounds__(kMoeThreads, kMoeCtasPerSm) lora_moe_fold_kern
   load_inputs();
   __syncthreads();
   const int lo_w = max(p.row_offset, offs[0]), hi_w = min(p.row_end, offs[E]);
-  if (hi_w <= lo_w) return;                      // every thread agrees
+  if (hi_w <= lo_w) return leave();              // every thread agrees
   int e_first = expert_of(lo_w), e_last = expert_of(hi_w - 1);
   if (e_first < 0 || e_last < e_first) { e_first = 0; e_last = E - 1; }   // offsets out of order: all experts
   const int E_w = e_last - e_first + 1;
@@ -973,7 +1005,7 @@ __global__ void __launch_bounds__(kMoeThreads, kMoeCtasPerSm) lora_moe_fold_kern
   const int n_units = E_w * n_chunks;   // <= num_experts * adapters <= kMoeMaxBins
   const int my_units = n_units > b ? (n_units - b + G - 1) / G : 0;
 
-  const EngineArgs ea{p.x, p.x_stride, p.out, p.out_stride, p.xa, p.max_rank, p.k_in, p.n_out};
+  const EngineArgs ea{p.x, p.x_stride, p.out, p.out_stride, p.xa, p.max_rank, p.k_in, p.n_out, p.late};
   int it0 = 0;
   bool ring_ready = false;
   // Rounds over the CTA's units: units [v0, v1) of its list and, within their
@@ -1212,6 +1244,7 @@ __global__ void __launch_bounds__(kMoeThreads, kMoeCtasPerSm) lora_moe_fold_kern
     // Another round: the ring serves as planning scratch again (every item of
     // the last pass has been consumed).
   }
+  leave();
 }
 
 // ============================================================================

@@ -17,8 +17,9 @@ LIB_PATH = os.path.join(_HERE, "libgather_lora.so")
 LORA_OK = 0
 STATUS_NAMES = {-1: "LORA_ERR_NULL", -2: "LORA_ERR_SIZE", -3: "LORA_ERR_STRIDE",
                 -4: "LORA_ERR_ALIGN", -5: "LORA_ERR_WINDOW", -6: "LORA_ERR_CUDA",
-                -7: "LORA_ERR_UNSUPPORTED"}
+                -7: "LORA_ERR_UNSUPPORTED", -8: "LORA_ERR_FLAGS"}
 LORA_DEV_MISALIGNED = 0x1
+INPUTS_READY = 0x1         # LORA_INPUTS_READY (call flag)
 MOE_M_TILE = 64
 TMAP_MIN_RANK = 32         # LORA_TMAP_MIN_RANK: a_tmaps are used from this max_rank up
 DELTA_DENSE_MIN_ROWS = 256  # LORA_DELTA_DENSE_MIN_ROWS: lora_delta's tensor-core path from this m up
@@ -43,13 +44,14 @@ def load():
     lib = ctypes.CDLL(LIB_PATH)
     P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
     lib.lora_bgmv.restype = ctypes.c_int
-    lib.lora_bgmv.argtypes = [P, I64, P, I64, P, I32, P, P, P, I32, I32, I32, I32, P, P, P]
+    U32 = ctypes.c_uint32
+    lib.lora_bgmv.argtypes = [P, I64, P, I64, P, I32, P, P, P, I32, I32, I32, I32, P, P, U32, P]
     lib.lora_moe_grouped_fold.restype = ctypes.c_int
     lib.lora_moe_grouped_fold.argtypes = [P, I64, I32, P, I64, P, I32, P, I32, P, I32, I32, I32,
-                                          P, P, P, I32, I32, I32, I32, P, I32, P]
+                                          P, P, P, I32, I32, I32, I32, P, I32, U32, P]
     lib.lora_moe_gather_bgmv.restype = ctypes.c_int
     lib.lora_moe_gather_bgmv.argtypes = [P, I64, P, I64, P, I32, I32, P, I32, I32,
-                                         P, P, P, I32, I32, I32, I32, P, P, P]
+                                         P, P, P, I32, I32, I32, I32, P, P, U32, P]
     lib.lora_delta.restype = ctypes.c_int
     lib.lora_delta.argtypes = [P, I64, P, I64, I32, P, P, ctypes.c_float, I32, I32, I32, P, P]
     lib.lora_delta_geometry.restype = ctypes.c_int
@@ -106,12 +108,14 @@ def _check(rc: int) -> int:
 
 
 def lora_bgmv(x, x_row_stride, base_out, out_row_stride, seq_slot, n, a_table, b_table,
-              scale_table, max_loras, max_rank, k_in, n_out, xa=None, stream=None, a_tmaps=None):
-    """Routed bgmv fold (see lora_bgmv in include/gather_lora.h)."""
+              scale_table, max_loras, max_rank, k_in, n_out, xa=None, stream=None, a_tmaps=None,
+              flags=0):
+    """Routed bgmv fold (see lora_bgmv in include/gather_lora.h). flags: 0 or
+    INPUTS_READY."""
     return _check(load().lora_bgmv(_addr(x), x_row_stride, _addr(base_out), out_row_stride,
                                    _addr(seq_slot), n, _addr(a_table), _addr(b_table),
                                    _addr(scale_table), max_loras, max_rank, k_in, n_out,
-                                   _addr(xa), _addr(a_tmaps), _stream(stream)))
+                                   _addr(xa), _addr(a_tmaps), int(flags), _stream(stream)))
 
 
 def lora_delta(x, x_row_stride, base_out, out_row_stride, m, a, b, scale, max_rank, k_in, n_out,
@@ -134,11 +138,11 @@ def lora_delta_geometry(m, max_rank, k_in, n_out, sm_count=0) -> dict:
 def lora_moe_grouped_fold(x, x_row_stride, base_out, out_row_stride, expert_offsets, num_experts,
                           sorted_token_ids, te, row_adapter, num_tokens, row_offset, row_end,
                           a_table, b_table, scale_table, max_loras, max_rank, k_in, n_out,
-                          xa=None, stream=None, x_gather=False, xa_rows=None):
+                          xa=None, stream=None, x_gather=False, xa_rows=None, flags=0):
     """MoE grouped fold of one window (see lora_moe_grouped_fold in include/gather_lora.h).
     x_gather: x is token-major and sorted row r reads row sorted_token_ids[r] (gate/up).
     xa_rows: rows allocated for xa; taken from the tensor's size (numel // max_rank) when
-    xa is a tensor and xa_rows is not given."""
+    xa is a tensor and xa_rows is not given. flags: 0 or INPUTS_READY."""
     if xa is None:
         xa_rows = 0
     elif xa_rows is None:
@@ -149,19 +153,20 @@ def lora_moe_grouped_fold(x, x_row_stride, base_out, out_row_stride, expert_offs
         _addr(x), x_row_stride, 1 if x_gather else 0, _addr(base_out), out_row_stride, _addr(expert_offsets),
         num_experts, _addr(sorted_token_ids), te, _addr(row_adapter), num_tokens, row_offset,
         row_end, _addr(a_table), _addr(b_table), _addr(scale_table), max_loras, max_rank, k_in,
-        n_out, _addr(xa), int(xa_rows), _stream(stream)))
+        n_out, _addr(xa), int(xa_rows), int(flags), _stream(stream)))
 
 
 def lora_moe_gather_bgmv(x, x_row_stride, base_out, out_row_stride, indices, n_rows, top_k,
                          row_adapter, num_tokens, num_experts, a_table, b_table, scale_table,
-                         max_loras, max_rank, k_in, n_out, xa=None, stream=None, a_tmaps=None):
+                         max_loras, max_rank, k_in, n_out, xa=None, stream=None, a_tmaps=None,
+                         flags=0):
     """Decode-path MoE fold over flat (token, slot) rows (see lora_moe_gather_bgmv in
-    include/gather_lora.h)."""
+    include/gather_lora.h). flags: 0 or INPUTS_READY."""
     return _check(load().lora_moe_gather_bgmv(
         _addr(x), x_row_stride, _addr(base_out), out_row_stride, _addr(indices), n_rows, top_k,
         _addr(row_adapter), num_tokens, num_experts, _addr(a_table), _addr(b_table),
         _addr(scale_table), max_loras, max_rank, k_in, n_out, _addr(xa), _addr(a_tmaps),
-        _stream(stream)))
+        int(flags), _stream(stream)))
 
 
 def lora_encode_a_tmaps(a_ptrs, max_rank: int, k_in: int):

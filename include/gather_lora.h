@@ -60,8 +60,28 @@ enum lora_status {
     LORA_ERR_ALIGN = -4,       /* a pointer, stride or width breaks the alignment rule */
     LORA_ERR_WINDOW = -5,      /* MoE window outside [0, te] or row_end < row_offset */
     LORA_ERR_CUDA = -6,        /* the CUDA launch (or a device query) failed */
-    LORA_ERR_UNSUPPORTED = -7  /* the current device cannot run these kernels */
+    LORA_ERR_UNSUPPORTED = -7, /* the current device cannot run these kernels */
+    LORA_ERR_FLAGS = -8        /* an unknown bit is set in `flags` */
 };
+
+/*
+ * Call flags (the `flags` argument of lora_bgmv, lora_moe_grouped_fold and
+ * lora_moe_gather_bgmv; 0 = none).
+ *
+ * LORA_INPUTS_READY: the caller promises that every input of the call other
+ * than base_out and xa (x, the routing arrays, the tables and the adapter
+ * matrices they point to) is written by no kernel that may still be running
+ * when this call's kernel starts. The kernels of this library let the next
+ * launch on the stream start once they themselves have waited for the one
+ * before them, so for a stream of calls of this library the promise reads:
+ * the kernel launched just before this call does not write those inputs (as
+ * for successive windows of one MoE layer, or a fold right after the base
+ * GEMM that writes base_out). The kernel then plans, loads and runs its shrink
+ * while the previous kernel finishes, and waits for it only before it reads
+ * or writes base_out or writes xa. Without the flag it waits before reading
+ * anything. The results are the same bits either way.
+ */
+#define LORA_INPUTS_READY 0x1u
 
 /* Device status bits, set by kernels, read with lora_read_device_status(). */
 #define LORA_DEV_MISALIGNED 0x1u   /* an adapter table entry was not 16-byte aligned */
@@ -78,7 +98,7 @@ enum lora_status {
 #define LORA_TMAP_MIN_RANK 32      /* a_tmaps are used from this max_rank up */
 #define LORA_MAX_DELTA_ROWS (1 << 20)      /* m of lora_delta in [0, 2^20] */
 #define LORA_DELTA_DENSE_MIN_ROWS 256      /* lora_delta takes the tensor-core path from this m up */
-#define LORA_MOE_M_TILE 64         /* sorted rows per MoE tile (static grid unit) */
+#define LORA_MOE_M_TILE 64         /* sorted rows per MoE m-tile (window tile count; rows per fold pass) */
 
 /*
  * lora_bgmv — per-request routed LoRA delta over n rows.
@@ -116,6 +136,7 @@ enum lora_status {
  *                The results are the same bits either way. The caller keeps the
  *                maps in step with a_table (adapters are load-time fixed); an entry
  *                used by a routed row must describe that adapter.
+ *   flags        0 or LORA_INPUTS_READY (above); other bits give LORA_ERR_FLAGS
  *   n == 0 is a no-op (returns LORA_OK, nothing launched).
  */
 int lora_bgmv(const lora_bf16_t* x, int64_t x_row_stride,
@@ -124,7 +145,7 @@ int lora_bgmv(const lora_bf16_t* x, int64_t x_row_stride,
               const lora_bf16_t* const* a_table, const lora_bf16_t* const* b_table,
               const float* scale_table, int32_t max_loras,
               int32_t max_rank, int32_t k_in, int32_t n_out,
-              lora_bf16_t* xa, const void* a_tmaps, void* stream);
+              lora_bf16_t* xa, const void* a_tmaps, uint32_t flags, void* stream);
 
 /*
  * lora_moe_grouped_fold — the fold over expert-sorted MoE rows of one window.
@@ -158,6 +179,10 @@ int lora_bgmv(const lora_bf16_t* x, int64_t x_row_stride,
  *                     row_offset (or < 0) is rejected with LORA_ERR_SIZE before any
  *                     launch; ignored when xa is NULL ("Module moe_lora_grouped",
  *                     `moe_lora_grouped_down`: the caller needs at least the window's rows)
+ *   flags             0 or LORA_INPUTS_READY (above); other bits give LORA_ERR_FLAGS.
+ *                     Successive windows of one layer may all pass it: each window
+ *                     then plans and shrinks while the previous one finishes (xa
+ *                     is written only after that wait, so the windows may share it)
  * The window must satisfy 0 <= row_offset <= row_end <= te (else LORA_ERR_WINDOW);
  * the tables may hold at most LORA_MAX_LORAS entries (max_loras * num_experts),
  * else LORA_ERR_SIZE (so is a shape whose stages do not fit shared memory). The
@@ -180,7 +205,7 @@ int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, int32_t x_
                           const lora_bf16_t* const* a_table, const lora_bf16_t* const* b_table,
                           const float* scale_table, int32_t max_loras,
                           int32_t max_rank, int32_t k_in, int32_t n_out,
-                          lora_bf16_t* xa, int32_t xa_rows, void* stream);
+                          lora_bf16_t* xa, int32_t xa_rows, uint32_t flags, void* stream);
 
 /*
  * lora_moe_gather_bgmv — the decode-path MoE fold over flat, unsorted
@@ -203,6 +228,7 @@ int lora_moe_grouped_fold(const lora_bf16_t* x, int64_t x_row_stride, int32_t x_
  *                (max_loras * num_experts <= LORA_MAX_LORAS)
  *   xa           optional [n_rows, max_rank] BF16 shrink output at row r (routed rows)
  *   a_tmaps      optional [max_loras * num_experts] A tensor maps, as for lora_bgmv
+ *   flags        0 or LORA_INPUTS_READY, as for lora_bgmv
  * Rows of one table entry share a work unit; the launch grid depends only on
  * n_rows and the table count (capture-safe). Errors, alignment and ownership as
  * for lora_bgmv.
@@ -214,7 +240,7 @@ int lora_moe_gather_bgmv(const lora_bf16_t* x, int64_t x_row_stride,
                          const lora_bf16_t* const* a_table, const lora_bf16_t* const* b_table,
                          const float* scale_table, int32_t max_loras,
                          int32_t max_rank, int32_t k_in, int32_t n_out,
-                         lora_bf16_t* xa, const void* a_tmaps, void* stream);
+                         lora_bf16_t* xa, const void* a_tmaps, uint32_t flags, void* stream);
 
 /*
  * lora_delta — one adapter pair folded into every row: the pages' apply_lora_delta
@@ -309,7 +335,8 @@ int lora_launch_geometry(int moe, int32_t rows, int32_t max_loras, int32_t max_r
 
 /*
  * lora_grouped_down_wc — m-tile count of one window: max(1, ceil((row_end -
- * row_offset) / LORA_MOE_M_TILE)); the MoE fold's tile grid.
+ * row_offset) / LORA_MOE_M_TILE)), the method's tile grid of a window (the
+ * fold itself launches the persistent grid described at lora_moe_grouped_fold).
  * Defines: "Module moe_lora_grouped" rustdoc, `grouped_down_wc` entry.
  * Returns -1 if row_end < row_offset.
  */

@@ -52,10 +52,11 @@ def test_library_exports_every_declared_symbol():
 
 def _bgmv(**kw):
     a = dict(x=FAKE, xs=4096, out=FAKE, os=4096, seq=FAKE, n=4, at=FAKE, bt=FAKE, sc=FAKE, L=8,
-             R=16, k=4096, no=4096, xa=FAKE, maps=None)
+             R=16, k=4096, no=4096, xa=FAKE, maps=None, flags=0)
     a.update(kw)
     return L.load().lora_bgmv(a["x"], a["xs"], a["out"], a["os"], a["seq"], a["n"], a["at"],
-                              a["bt"], a["sc"], a["L"], a["R"], a["k"], a["no"], a["xa"], a["maps"], None)
+                              a["bt"], a["sc"], a["L"], a["R"], a["k"], a["no"], a["xa"], a["maps"],
+                              a["flags"], None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -65,6 +66,7 @@ def _bgmv(**kw):
     (dict(xs=4100), -4), (dict(x=None), -1), (dict(out=None), -1), (dict(seq=None), -1),
     (dict(at=None), -1), (dict(bt=None), -1), (dict(sc=None), -1), (dict(x=FAKE + 2), -4),
     (dict(out=FAKE + 8), -4), (dict(xa=FAKE + 4), -4), (dict(maps=FAKE + 32), -4),
+    (dict(flags=2), -8), (dict(flags=0x80000001), -8), (dict(flags=1, x=FAKE + 2), -4),
 ])
 def test_bgmv_rejects_bad_arguments_before_launch(kw, code):
     assert _bgmv(**kw) == code
@@ -79,12 +81,12 @@ def test_bgmv_zero_rows_is_a_no_op():
 def _moe(**kw):
     a = dict(x=FAKE, xs=768, xg=0, out=FAKE, os=2048, off=FAKE, E=128, sti=FAKE, te=16384, ra=FAKE,
              nt=2048, lo=0, hi=4096, at=FAKE, bt=FAKE, sc=FAKE, L=16, R=16, k=768, no=2048, xa=FAKE,
-             xa_rows=4096)
+             xa_rows=4096, flags=0)
     a.update(kw)
     return L.load().lora_moe_grouped_fold(a["x"], a["xs"], a["xg"], a["out"], a["os"], a["off"], a["E"],
                                           a["sti"], a["te"], a["ra"], a["nt"], a["lo"], a["hi"],
                                           a["at"], a["bt"], a["sc"], a["L"], a["R"], a["k"], a["no"],
-                                          a["xa"], a["xa_rows"], None)
+                                          a["xa"], a["xa_rows"], a["flags"], None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -94,6 +96,7 @@ def _moe(**kw):
     (dict(sti=None), -1), (dict(at=None), -1), (dict(x=FAKE + 2), -4),
     (dict(sti=None, ra=None, xg=1), -1),
     (dict(xa_rows=4095), -2), (dict(xa_rows=-1), -2), (dict(lo=100, hi=5000, xa_rows=4899), -2),
+    (dict(flags=4), -8), (dict(flags=1, x=FAKE + 2), -4),
 ])
 def test_moe_rejects_bad_arguments_before_launch(kw, code):
     assert _moe(**kw) == code
@@ -123,18 +126,19 @@ def test_moe_table_count_and_persistent_grid():
 
 def _gather(**kw):
     a = dict(x=FAKE, xs=768, out=FAKE, os=2048, idx=FAKE, n=512, k=8, ra=FAKE, nt=64, E=128,
-             at=FAKE, bt=FAKE, sc=FAKE, L=16, R=16, kin=768, no=2048, xa=FAKE, maps=None)
+             at=FAKE, bt=FAKE, sc=FAKE, L=16, R=16, kin=768, no=2048, xa=FAKE, maps=None, flags=0)
     a.update(kw)
     return L.load().lora_moe_gather_bgmv(a["x"], a["xs"], a["out"], a["os"], a["idx"], a["n"],
                                          a["k"], a["ra"], a["nt"], a["E"], a["at"], a["bt"],
                                          a["sc"], a["L"], a["R"], a["kin"], a["no"], a["xa"],
-                                         a["maps"], None)
+                                         a["maps"], a["flags"], None)
 
 
 @pytest.mark.parametrize("kw,code", [
     (dict(n=-1), -2), (dict(n=8193), -2), (dict(k=0), -2), (dict(nt=-1), -2), (dict(E=0), -2),
     (dict(E=1025), -2), (dict(L=0), -2), (dict(L=33), -2), (dict(R=4), -2), (dict(xs=700), -3),
     (dict(x=None), -1), (dict(idx=None), -1), (dict(at=None), -1), (dict(x=FAKE + 2), -4),
+    (dict(flags=8), -8),
 ])
 def test_gather_bgmv_rejects_bad_arguments_before_launch(kw, code):
     assert _gather(**kw) == code

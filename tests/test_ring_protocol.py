@@ -52,14 +52,16 @@ class Barrier:
 
 
 def run(ns, n_shrink, n_items, slot_parallel, seed, producer_split="all", passes=None, ksg=1, cl1=False,
-        full_release=False):
+        full_release=False, late=False):
     """`passes`: [(n_shrink, n_items), ...] folded one after the other by one
     CTA; ring item numbers continue across passes and a CTA barrier separates them.
     ksg: warps per slot in slot-parallel shrinks (at most CONSUMER_WARPS // ns).
     cl1: single-CTA units: the producer issues every item without the exchange
     barriers, which only the consumer warps take.
     full_release: each owner warp releases a shrink slot with all eight arrivals
-    (the broken variant when two warps own a slot)."""
+    (the broken variant when two warps own a slot).
+    late: the late-wait order: before the exchange barriers the producer issues
+    only the shrink items (the expand items read base_out, after the wait)."""
     ksg = max(1, min(ksg, CONSUMER_WARPS // ns))
     rng = random.Random(seed)
     full = [Barrier(PRODUCER_WARPS) for _ in range(ns)]
@@ -76,7 +78,7 @@ def run(ns, n_shrink, n_items, slot_parallel, seed, producer_split="all", passes
     def producer(pw):
         prog = []
         for base, ps, pn in bounds:
-            pre = min(pn, ps + ns)
+            pre = ps if late else min(pn, ps + ns)
             if producer_split == "all":
                 a, b = list(range(pre)), list(range(pre, pn))
             else:   # items dealt to warps by index (broken)
@@ -193,3 +195,16 @@ def test_items_split_by_index_across_producers_is_unsound():
         except AssertionError:
             failures += 1
     assert failures == 20
+
+
+@pytest.mark.parametrize("slot_parallel", [False, True])
+@pytest.mark.parametrize("ns", [2, 3, 4, 8])
+def test_late_wait_order_is_sound(slot_parallel, ns):
+    """Inputs-ready launches: the producer holds every expand item back until
+    after the exchange barriers (cluster units) or issues in item order (single
+    CTA units); both still complete for every item count and pass sequence."""
+    for passes in ([(1, 4)], [(5, 9), (0, 3)], [(16, 48)], [(3, 3), (2, 7)]):
+        for seed in range(3):
+            run(ns, 0, 0, slot_parallel, seed, passes=passes, late=True)
+            run(ns, 0, 0, slot_parallel, seed, passes=passes, late=True, cl1=True,
+                ksg=2 if slot_parallel else 1)
