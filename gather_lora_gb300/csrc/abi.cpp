@@ -92,6 +92,9 @@ int device_sm_count_or(int fallback) {
 #ifndef GLORA_MOE_TILE_SHRINK
 #define GLORA_MOE_TILE_SHRINK 0
 #endif
+#ifndef GLORA_MOE_TWO_PER_SM
+#define GLORA_MOE_TWO_PER_SM 1   // MoE folds with k_in > n_out use the two-CTAs-per-SM shape
+#endif
 #ifndef GLORA_MOE_GROUP_ROWS
 #define GLORA_MOE_GROUP_ROWS 16
 #endif
@@ -256,19 +259,24 @@ bool make_geometry(bool moe, int rows, int max_loras, int planner_ints, int max_
 // The MoE fold's launch: the arithmetic (k chunks, shrink mode, row tiles) from
 // the shapes alone, as for every fold, so a row's bits never depend on the
 // window; then the persistent layout: the CTA's plan (MoePlan) before the ring,
-// as many ring stages as fit kMoeCtasPerSm CTAs per SM, and a grid of one such
+// as many ring stages as fit the CTA shape's CTAs per SM, and a grid of one such
 // CTA set per SM (fewer for small windows, at least 16 rows per CTA). Each CTA
 // plans its units in the ring before its first fold (offsets, its units, the
 // counts of their groups).
-bool moe_geometry(int window, int adapters, int num_experts, int max_rank, int k_in, int n_out, int sms,
-                  glora::FoldGeometry& g) {
+//
+// CTA shape: two CTAs per SM of 8 + 2 warps when the shrink is the larger half
+// (k_in > n_out), else one CTA per SM of 12 + 4 warps. Measured on GB300 with
+// inputs-ready windows: the gate/up form (k_in 2048, n_out 768) 93.7 -> 79.6 us,
+// the down form (k_in 768, n_out 2048) 86.1 -> 89.7 us.
+bool moe_geometry_cfg(int cfg, int window, int adapters, int num_experts, int max_rank, int k_in, int n_out,
+                      int sms, glora::FoldGeometry& g) {
   // The largest stage target whose ring still gets two stages beside the plan.
-  const int budget = glora::kMoeCtasPerSm == 1 ? kBudgetOnePerSm : kBudgetTwoPerSm;
+  const int budget = glora::moe_ctas_per_sm(cfg) == 1 ? kBudgetOnePerSm : kBudgetTwoPerSm;
   const int off_ring = round_up(glora::kPlanBytes + static_cast<int>(sizeof(glora::MoePlan)), 1024);
   int ns = 0, tail = 0;
   for (int target : {kMoeStageTarget, kStageTarget, kMinStage}) {
     if (!make_geometry_at(true, window, adapters, 0, max_rank, k_in, n_out, g, GLORA_MAX_CLUSTER, false, target,
-                          kUnitRows, glora::kMoeConsumerWarps))
+                          kUnitRows, glora::moe_cw(cfg)))
       continue;
     const int planes = g.ksplit + (g.gather ? g.cl : 0);
     tail = planes * g.rt * g.pitch_part * 4 + g.rt * g.pitch_xa;
@@ -277,6 +285,7 @@ bool moe_geometry(int window, int adapters, int num_experts, int max_rank, int k
   }
   if (ns < 2) return false;
   const int planes = g.ksplit + (g.gather ? g.cl : 0);
+  g.moe_cfg = cfg;
   g.off_mplan = glora::kPlanBytes;
   g.off_ring = off_ring;
   g.ns = ns;
@@ -289,9 +298,17 @@ bool moe_geometry(int window, int adapters, int num_experts, int max_rank, int k
                             ((static_cast<long long>(std::max(glora::kMoeMaxDesc, adapters)) + 4) & ~3LL) * 4;
   const long long ring = static_cast<long long>(ns) * g.stage_bytes;
   if (bins > glora::kMoeMaxBins || scratch > ring) return false;
-  g.clusters = static_cast<int>(std::max<long long>(1, std::min<long long>(static_cast<long long>(sms) * glora::kMoeCtasPerSm,
-                                                                            ceil_div(window, 16))));
+  g.clusters = static_cast<int>(std::max<long long>(
+      1, std::min<long long>(static_cast<long long>(sms) * glora::moe_ctas_per_sm(cfg), ceil_div(window, 16))));
   return true;
+}
+
+bool moe_geometry(int window, int adapters, int num_experts, int max_rank, int k_in, int n_out, int sms,
+                  glora::FoldGeometry& g) {
+  if (k_in > n_out && GLORA_MOE_TWO_PER_SM &&
+      moe_geometry_cfg(1, window, adapters, num_experts, max_rank, k_in, n_out, sms, g))
+    return true;
+  return moe_geometry_cfg(0, window, adapters, num_experts, max_rank, k_in, n_out, sms, g);
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once (NULL without a driver).
@@ -670,7 +687,8 @@ int lora_launch_geometry(int moe, int32_t rows, int32_t max_loras, int32_t max_r
                                kind == 2 ? GLORA_GATHER_MAX_CL : GLORA_MAX_CLUSTER,
                                (moe & 16) ? &kAnyMaps : nullptr, kind == 2 ? kGatherUnitRows : kUnitRows))
     return fail(LORA_ERR_SIZE, "no launch geometry fits shared memory and the grid size");
-  const int64_t v[12] = {g.cl, g.rt, g.ksl, g.jsl, g.kch, g.jch, g.ns, g.clusters, g.smem_bytes, g.a_tiled, g.tc, g.direct};
+  const int64_t v[12] = {g.cl, g.rt, g.ksl, g.jsl, g.kch, g.jch, g.ns, g.clusters, g.smem_bytes, g.a_tiled, g.tc,
+                         grouped ? g.moe_cfg : g.direct};
   std::memcpy(out, v, sizeof v);
   return ok();
 }

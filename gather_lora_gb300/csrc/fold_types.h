@@ -23,11 +23,16 @@ constexpr int kMoeMaxBins = 4096;   // MoE: (expert, adapter) groups of a window
 #endif
 constexpr int kConsumerWarps = GLORA_CONSUMER_WARPS;   // tensor-core / fold warps per CTA (routed folds)
 constexpr int kProducerWarps = GLORA_PRODUCER_WARPS;   // TMA-issuing warps per CTA
-#ifndef GLORA_MOE_CONSUMER_WARPS
-#define GLORA_MOE_CONSUMER_WARPS 12
-#endif
-constexpr int kMoeConsumerWarps = GLORA_MOE_CONSUMER_WARPS;   // consumer warps of the MoE fold's CTA
 constexpr int kMaxWarps = 16;                                 // most warps of any fold CTA
+
+// The MoE fold's CTA shapes (FoldGeometry::moe_cfg): 0 = one CTA per SM with
+// 12 consumer and 4 producer warps; 1 = two CTAs per SM with 8 consumer and 2
+// producer warps (more CTAs in flight, half the ring each).
+template <int CFG> struct MoeShape;
+template <> struct MoeShape<0> { static constexpr int cw = 12, pw = 4, ctas = 1, threads = (cw + pw) * 32; };
+template <> struct MoeShape<1> { static constexpr int cw = 8, pw = 2, ctas = 2, threads = (cw + pw) * 32; };
+constexpr int moe_cw(int cfg) { return cfg ? MoeShape<1>::cw : MoeShape<0>::cw; }
+constexpr int moe_ctas_per_sm(int cfg) { return cfg ? MoeShape<1>::ctas : MoeShape<0>::ctas; }
 
 // Launch geometry and shared-memory layout of one fold launch. Every CTA of a
 // cluster of `cl` CTAs owns one k-slice of the shrink (ksl columns of A / x)
@@ -58,6 +63,7 @@ struct FoldGeometry {
   int stage_bytes;
   int off_ring, off_out, off_part, off_xa, smem_bytes;
   int off_mplan;    // MoE: the CTA's planned row runs and rows (MoePlan), before the ring
+  int moe_cfg;      // MoE: the CTA shape (MoeShape)
   int clusters;     // grid = clusters * cl CTAs
 };
 
@@ -126,11 +132,6 @@ struct MoePlan {
   int pos_tok[kMoeMaxPos];     // its token (the x row of the gate/up form)
   short pos_desc[kMoeMaxPos];  // its run
 };
-
-#ifndef GLORA_MOE_CTAS_PER_SM
-#define GLORA_MOE_CTAS_PER_SM 1
-#endif
-constexpr int kMoeCtasPerSm = GLORA_MOE_CTAS_PER_SM;   // resident MoE CTAs per SM (the persistent grid)
 
 // Launchers (kernels.cu). Return 0 or a cudaError_t value.
 int launch_bgmv(const BgmvArgs& a, void* stream);

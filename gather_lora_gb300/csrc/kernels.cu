@@ -932,12 +932,12 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
 #endif
 constexpr int kMoeUnitsPerCta = GLORA_MOE_UNITS_PER_CTA;   // target units per CTA (sets the chunk size)
 constexpr int kMoeRoundRows = kMoeMaxPos;    // rows of the units' experts scanned per round
-constexpr int kMoeThreads = (kMoeConsumerWarps + kProducerWarps) * 32;   // the MoE kernel's CTA
-constexpr int kMoeRowsPerThread = (kMoeRoundRows + kMoeThreads - 1) / kMoeThreads;
 constexpr int kMoeMaxMyUnits = 64;           // units of one CTA planned per round
 
-template <int MAXT>
-__global__ void __launch_bounds__(kMoeThreads, kMoeCtasPerSm) lora_moe_fold_kernel(const __grid_constant__ MoeArgs p) {
+template <int MAXT, int CFG>
+__global__ void __launch_bounds__(MoeShape<CFG>::threads, MoeShape<CFG>::ctas) lora_moe_fold_kernel(const __grid_constant__ MoeArgs p) {
+  constexpr int CW = MoeShape<CFG>::cw, PW = MoeShape<CFG>::pw, kMoeThreads = MoeShape<CFG>::threads;
+  constexpr int kMoeRowsPerThread = (kMoeRoundRows + kMoeThreads - 1) / kMoeThreads;
   extern __shared__ __align__(128) unsigned char smem[];
   const FoldGeometry& g = p.g;
   const cg::cluster_group cluster = cg::this_cluster();
@@ -967,8 +967,8 @@ __global__ void __launch_bounds__(kMoeThreads, kMoeCtasPerSm) lora_moe_fold_kern
   // grid on the stream may still be running.
   if (tid == 0) {
     for (int s = 0; s < g.ns; ++s) {
-      mbar_init(smem_u32(&pl.full[s]), kProducerWarps * 32);
-      mbar_init(smem_u32(&pl.empty[s]), kMoeConsumerWarps);
+      mbar_init(smem_u32(&pl.full[s]), PW * 32);
+      mbar_init(smem_u32(&pl.empty[s]), CW);
     }
     pl.failed = 0;
     mbar_fence_init();
@@ -1238,7 +1238,7 @@ __global__ void __launch_bounds__(kMoeThreads, kMoeCtasPerSm) lora_moe_fold_kern
         pl.NV = nvk;
       }
       __syncthreads();
-      if (pl.G > 0) it0 += fold_engine<MAXT, false, false, kMoeConsumerWarps, kProducerWarps>(ea, g, pl, smem, cluster, 0, it0);
+      if (pl.G > 0) it0 += fold_engine<MAXT, false, false, CW, PW>(ea, g, pl, smem, cluster, 0, it0);
       __syncthreads();   // the next pass rewrites the plan
     }
     // Another round: the ring serves as planning scratch again (every item of
@@ -1304,10 +1304,14 @@ int launch_bgmv(const BgmvArgs& a, void* stream) {
   }
 }
 int launch_moe(const MoeArgs& a, void* stream) {
-  switch (a.g.maxt) {
-    case 1: return launch_fold(lora_moe_fold_kernel<1>, a, stream, kMoeThreads);
-    case 2: return launch_fold(lora_moe_fold_kernel<2>, a, stream, kMoeThreads);
-    case 4: return launch_fold(lora_moe_fold_kernel<4>, a, stream, kMoeThreads);
+  const int key = a.g.maxt * 2 + (a.g.moe_cfg ? 1 : 0);
+  switch (key) {
+    case 2: return launch_fold(lora_moe_fold_kernel<1, 0>, a, stream, MoeShape<0>::threads);
+    case 3: return launch_fold(lora_moe_fold_kernel<1, 1>, a, stream, MoeShape<1>::threads);
+    case 4: return launch_fold(lora_moe_fold_kernel<2, 0>, a, stream, MoeShape<0>::threads);
+    case 5: return launch_fold(lora_moe_fold_kernel<2, 1>, a, stream, MoeShape<1>::threads);
+    case 8: return launch_fold(lora_moe_fold_kernel<4, 0>, a, stream, MoeShape<0>::threads);
+    case 9: return launch_fold(lora_moe_fold_kernel<4, 1>, a, stream, MoeShape<1>::threads);
     default: return static_cast<int>(cudaErrorInvalidValue);
   }
 }

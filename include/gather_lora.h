@@ -325,8 +325,10 @@ int lora_read_device_status(void* stream, uint32_t* status_out, int clear);
  * rows_per_tile, k_slice, j_slice, k_chunk, j_chunk, ring_stages, clusters,
  * smem_bytes, a_tiled (1 when A is loaded through the tensor maps), tc (1 when the shrink
  * runs on the tcgen05 tensor cores), direct (1: unit s is tile 0 of slot s; 0: units are
- * numbered slot by slot over the slots with rows)] to out[0..11]. The unit numbering
- * also depends on the current device's SM count (152 without a device).
+ * numbered slot by slot over the slots with rows; for the MoE grouped fold: its CTA
+ * shape, 0 = one CTA of 12 + 4 warps per SM, 1 = two CTAs of 8 + 2 warps per SM,
+ * taken when k_in > n_out)] to out[0..11]. The unit numbering and the MoE grid also
+ * depend on the current device's SM count (152 without a device).
  */
 int lora_launch_geometry(int moe, int32_t rows, int32_t max_loras, int32_t max_rank,
                          int32_t k_in, int32_t n_out, int64_t out[12]);

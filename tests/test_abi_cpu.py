@@ -124,6 +124,17 @@ def test_moe_table_count_and_persistent_grid():
     assert _moe(te=big, lo=0, hi=big, xa=None, x=FAKE + 2) == -4   # passes the size checks
 
 
+def test_moe_cta_shape_follows_the_larger_half():
+    """The MoE fold runs two CTAs of 8 + 2 warps per SM when its shrink is the larger
+    half (k_in > n_out: the gate/up form) and one CTA of 12 + 4 warps otherwise (the
+    down form); the grid is then up to two CTAs per SM."""
+    up = L.lora_launch_geometry(1, 1 << 20, 16, 16, 2048, 768)
+    down = L.lora_launch_geometry(1, 1 << 20, 16, 16, 768, 2048)
+    assert up["direct"] == 1 and up["clusters"] == 2 * 152 and up["smem_bytes"] <= 113 * 1024
+    assert down["direct"] == 0 and down["clusters"] == 152
+    assert L.lora_launch_geometry(1, 4096, 16, 16, 2048, 768)["clusters"] == 256
+
+
 def _gather(**kw):
     a = dict(x=FAKE, xs=768, out=FAKE, os=2048, idx=FAKE, n=512, k=8, ra=FAKE, nt=64, E=128,
              at=FAKE, bt=FAKE, sc=FAKE, L=16, R=16, kin=768, no=2048, xa=FAKE, maps=None, flags=0)
