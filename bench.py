@@ -380,8 +380,13 @@ class DeltaRunner:
 RUNNERS = {"bgmv": BgmvRunner, "moe": MoeRunner, "gather": GatherRunner, "delta": DeltaRunner}
 
 
-def copies_needed(bytes_per_copy, l2_bytes):
-    return max(1, min(64, math.ceil(2 * l2_bytes / max(bytes_per_copy, 1))))
+def copies_needed(bytes_per_copy, l2_bytes, touched_per_step=None):
+    """Input copies to rotate through so that a step never finds its data in L2:
+    the bytes the steps of one rotation touch (the algorithmic bytes of a step,
+    not the whole buffers: an adapter pool is mostly untouched by one batch)
+    exceed 2x L2."""
+    per = max(1, min(bytes_per_copy, touched_per_step or bytes_per_copy))
+    return max(1, min(64, math.ceil(2 * l2_bytes / per)))
 
 
 def time_steps(runner, steps, warmup, device, dist_ctx, sampler=None):
@@ -803,7 +808,7 @@ def run_ours(args):
     alg = algorithmic_bytes(wl)
     mk = RUNNERS[head_kind]
     probe = mk(wl, 1, device)
-    C = copies_needed(probe.bytes_per_copy(), l2)
+    C = copies_needed(probe.bytes_per_copy(), l2, alg["bytes"])
     runner = probe if C == 1 else mk(wl, C, device)
     del probe
     sampler = ClockSampler(smi_selector(torch, device)) if dctx.rank == 0 else None
@@ -842,7 +847,7 @@ def run_ours(args):
         a2 = algorithmic_bytes(w2)
         mk = RUNNERS[workload_kind(w2)]
         pr = mk(w2, 1, device)
-        c2 = copies_needed(pr.bytes_per_copy(), l2)
+        c2 = copies_needed(pr.bytes_per_copy(), l2, a2["bytes"])
         r2 = pr if c2 == 1 else mk(w2, c2, device)
         del pr
         # about 0.3 s of timed work, at least 20 steps
