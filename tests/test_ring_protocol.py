@@ -40,6 +40,10 @@ class Barrier:
         self.pending -= 1
         self._check()
 
+    def expect_tx(self, phase, tx):
+        assert phase == self.phase, f"bytes for phase {phase} expected in phase {self.phase}"
+        self.tx += tx
+
     def complete_tx(self, b):
         self.tx -= b
         self._check()
@@ -61,7 +65,9 @@ def run(ns, n_shrink, n_items, slot_parallel, seed, producer_split="all", passes
     full_release: each owner warp releases a shrink slot with all eight arrivals
     (the broken variant when two warps own a slot).
     late: the late-wait order: before the exchange barriers the producer issues
-    only the shrink items (the expand items read base_out, after the wait)."""
+    the shrink items and, with cluster peers, the first part (adapter rows, no
+    arrival) of the expand items whose slots the shrink frees; after them it
+    completes those items (out rows and its arrival), then the rest."""
     ksg = max(1, min(ksg, CONSUMER_WARPS // ns))
     rng = random.Random(seed)
     full = [Barrier(PRODUCER_WARPS) for _ in range(ns)]
@@ -79,15 +85,16 @@ def run(ns, n_shrink, n_items, slot_parallel, seed, producer_split="all", passes
         prog = []
         for base, ps, pn in bounds:
             pre = ps if late else min(pn, ps + ns)
+            early = min(pn, ps + ns) if (late and not cl1) else ps
             if producer_split == "all":
-                a, b = list(range(pre)), list(range(pre, pn))
+                a, b = list(range(pre)), list(range(max(pre, early), pn))
             else:   # items dealt to warps by index (broken)
                 a = [i for i in range(pre) if i % PRODUCER_WARPS == pw]
                 b = [i for i in range(pre, pn) if i % PRODUCER_WARPS == pw]
-            if cl1:
-                prog += [base + i for i in range(pn)] + ["SYNC"]
-            else:
-                prog += [base + i for i in a] + ["SYNC", "SYNC"] + [base + i for i in b] + ["SYNC"]
+            first = [("W", base + i) for i in range(ps, early)]     # part 1: slot wait, adapter rows
+            second = [("A", base + i) for i in range(ps, early)]    # part 2: out rows, arrival
+            syncs = [] if cl1 else ["SYNC", "SYNC"]
+            prog += [base + i for i in a] + first + syncs + second + [base + i for i in b] + ["SYNC"]
         return prog
 
     def consumer(w):
@@ -129,12 +136,18 @@ def run(ns, n_shrink, n_items, slot_parallel, seed, producer_split="all", passes
                     pc[i] += 1
                     at_sync[i] = None
             continue
+        part = None
+        if isinstance(op, tuple):
+            part, op = op
         s, u = op % ns, op // ns
         if kind == "P":
-            if not waited[choice]:
+            if part != "A" and not waited[choice]:
                 waited[choice] = u == 0 or empty[s].try_wait(u - 1)
                 continue
-            full[s].arrive(u, tx=per_copy)
+            if part == "W":            # adapter rows: bytes in flight, no arrival yet
+                full[s].expect_tx(u, per_copy)
+            else:
+                full[s].arrive(u, tx=per_copy)
             inflight.append(s)
         else:
             if not waited[choice]:
