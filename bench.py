@@ -504,12 +504,17 @@ def e2e_run(wl, device, steps, warmup, copies):
     the step's inputs from pinned host memory (bgmv: x, seq_slot, base_out; MoE:
     x, expert_offsets, sorted_token_ids, row_adapter, base_out), makes the fold's
     calls (MoE: one per window), and reads base_out back into pinned host memory,
-    all inside the timed region. Returns (rows/s, H2D bytes, D2H bytes) per step."""
+    all inside the timed region. Steps are pipelined the way a serving loop would
+    run them: the copies in, the calls and the copy out go on three streams, over
+    at least two device copies of the inputs, so step i's inputs travel while step
+    i - 1 folds and step i - 2's result comes back (events order each copy's uses).
+    Returns (rows/s, H2D bytes, D2H bytes) per step."""
     import torch
     from gather_lora_gb300 import lib as L
     from gather_lora_gb300 import workloads as W
     kind = workload_kind(wl)
-    stream = torch.cuda.Stream(device=device)
+    copies = max(2, copies)
+    s_in, s_run, s_out = (torch.cuda.Stream(device=device) for _ in range(3))
     if kind == "bgmv":
         devs = [W.bgmv_to_device(wl, device) for _ in range(copies)]
         maps = [a_maps_for(d.a_table, wl.max_rank, wl.k_in) for d in devs]
@@ -519,7 +524,7 @@ def e2e_run(wl, device, steps, warmup, copies):
         def call(c, d):
             L.lora_bgmv(d.x, wl.x_row_stride, d.out_ptr, wl.out_row_stride, d.seq_slot, wl.n,
                         d.a_table, d.b_table, d.scale, wl.max_loras, wl.max_rank, wl.k_in, wl.n_out,
-                        xa=d.xa, stream=stream, a_tmaps=maps[c], flags=READY)
+                        xa=d.xa, stream=s_run, a_tmaps=maps[c])
         rows = wl.n
     elif kind == "moe":
         devs = [W.moe_to_device(wl, device, xa_rows=wl.cap) for _ in range(copies)]
@@ -528,40 +533,66 @@ def e2e_run(wl, device, steps, warmup, copies):
                            (d.row_adapter, _pinned(wl.row_adapter)), (d.out_buf, _pinned(wl.out_buf))]
 
         def call(c, d):
-            for lo, hi in wl.windows():
+            # the first window follows this step's input copies (another stream): it
+            # waits for everything; the later windows follow only the window before
+            for j, (lo, hi) in enumerate(wl.windows()):
                 L.lora_moe_grouped_fold(d.x, wl.k_in, d.out_buf, wl.n_out, d.expert_offsets,
                                         wl.num_experts, d.sorted_token_ids, wl.te, d.row_adapter,
                                         wl.num_tokens, lo, hi, d.a_table, d.b_table, d.scale,
                                         wl.max_loras, wl.max_rank, wl.k_in, wl.n_out, xa=d.xa,
-                                        stream=stream, x_gather=wl.x_gather, flags=READY)
+                                        stream=s_run, x_gather=wl.x_gather,
+                                        flags=READY if j > 0 else 0)
         rows = wl.te
     else:
         raise ValueError(f"no end-to-end run for {kind}")
     host = [pairs(d) for d in devs]
-    hres = _pinned(wl.out_buf).clone().pin_memory()
+    hres = [_pinned(wl.out_buf).clone().pin_memory() for _ in range(copies)]
+    ev_in = [torch.cuda.Event() for _ in range(copies)]
+    ev_run = [torch.cuda.Event() for _ in range(copies)]
+    ev_out = [torch.cuda.Event() for _ in range(copies)]
 
     def one(i):
         c = i % copies
         d = devs[c]
-        for dst, src in host[c]:
-            dst.copy_(src, non_blocking=True)
+        if i >= copies:                      # copy c's last result has left the device
+            s_in.wait_event(ev_out[c])
+        with torch.cuda.stream(s_in):
+            for dst, src in host[c]:
+                dst.copy_(src, non_blocking=True)
+        ev_in[c].record(s_in)
+        s_run.wait_event(ev_in[c])
         call(c, d)
-        hres.copy_(d.out_buf, non_blocking=True)
+        ev_run[c].record(s_run)
+        s_out.wait_event(ev_run[c])
+        with torch.cuda.stream(s_out):
+            hres[c].copy_(d.out_buf, non_blocking=True)
+        ev_out[c].record(s_out)
 
-    with torch.cuda.stream(stream):
-        for i in range(warmup):
-            one(i)
+    for i in range(warmup):
+        one(i)
     torch.cuda.synchronize(device)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for i in range(steps):
-            one(i)
-        end.record(stream)
+    start.record(s_in)
+    for i in range(steps):
+        one(warmup + i)
+    for st in (s_in, s_run):
+        s_out.wait_stream(st)
+    end.record(s_out)
     torch.cuda.synchronize(device)
     ms = start.elapsed_time(end)
+    # every step folds the same host inputs: each copy's last result must equal
+    # one step run alone with nothing overlapping it
+    last = [hres[c].clone() for c in range(copies)]
+    with torch.cuda.stream(s_run):
+        for dst, src in host[0]:
+            dst.copy_(src, non_blocking=True)
+        call(0, devs[0])
+        hres[0].copy_(devs[0].out_buf, non_blocking=True)
+    torch.cuda.synchronize(device)
+    if not all(torch.equal(x, hres[0]) for x in last):
+        raise RuntimeError("end-to-end steps gave different results from a step run alone")
     h2d = sum(src.numel() * src.element_size() for _, src in host[0])
-    d2h = hres.numel() * hres.element_size()
+    d2h = hres[0].numel() * hres[0].element_size()
     return rows * steps / (ms / 1e3), h2d, d2h
 
 
