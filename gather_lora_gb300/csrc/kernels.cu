@@ -135,7 +135,7 @@ __device__ __forceinline__ void ring_init(Plan& pl, int ns) {
 // (launches with g.a_tiled); each instance has one A layout. TC: the shrink
 // runs on tcgen05 (launches with g.tc; one group per pass, TMEM allocated by
 // the caller at pl.tmem).
-template <int MAXT, bool TILED, bool TC = false, int CW = kConsumerWarps, int PW = kProducerWarps>
+template <int MAXT, bool TILED, bool TC = false, int CW = kConsumerWarps, int PW = kProducerWarps, int RK = 0>
 __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeometry& g, Plan& pl,
                                            unsigned char* smem, const cg::cluster_group& cluster,
                                            int crank, int it0) {
@@ -719,9 +719,14 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
     using I1 = std::integral_constant<int, 1>;
     using I2 = std::integral_constant<int, 2>;
     using I0 = std::integral_constant<int, 0>;
+    // The expand loop is compiled for the launch's rank class only (RK: 1 =
+    // max_rank 16 and 2 = max_rank 32, xa fragments held in registers; 0 = any
+    // max_rank, fragments loaded per step): one variant per kernel keeps its
+    // code small (measured on GB300: MoE down fold 86.4 -> 84.8 us, decode
+    // 8.6 -> 8.3 us with waiting calls).
     auto by_rank = [&](auto mr_c) {
-      if (p.max_rank == 16) items(mr_c, I1{});
-      else if (p.max_rank == 32) items(mr_c, I2{});
+      if constexpr (RK == 1) items(mr_c, I1{});
+      else if constexpr (RK == 2) items(mr_c, I2{});
       else items(mr_c, I0{});
     };
     if constexpr (kRT > 1) {
@@ -757,7 +762,7 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
 // table count. So does the single-adapter delta at small m (`single`): every
 // row is slot 0 of a one-entry table passed by value.
 // ============================================================================
-template <int MAXT, bool TILED, bool TC>
+template <int MAXT, bool TILED, bool TC, int RK>
 __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __grid_constant__ BgmvArgs p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const FoldGeometry& g = p.g;
@@ -908,7 +913,7 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
   ring_init(pl, g.ns);
   if constexpr (TC) tc_fence_after();
   const EngineArgs ea{p.x, p.x_stride, p.out, p.out_stride, p.xa, p.max_rank, p.k_in, p.n_out, p.late};
-  fold_engine<MAXT, TILED, TC>(ea, g, pl, smem, cluster, crank, 0);
+  fold_engine<MAXT, TILED, TC, kConsumerWarps, kProducerWarps, RK>(ea, g, pl, smem, cluster, crank, 0);
   if constexpr (TC) {
     tc_fence_before();
     __syncthreads();
@@ -944,7 +949,7 @@ constexpr int kMoeUnitsPerCta = GLORA_MOE_UNITS_PER_CTA;   // target units per C
 constexpr int kMoeRoundRows = kMoeMaxPos;    // rows of the units' experts scanned per round
 constexpr int kMoeMaxMyUnits = 64;           // units of one CTA planned per round
 
-template <int MAXT, int CFG>
+template <int MAXT, int CFG, int RK>
 __global__ void __launch_bounds__(MoeShape<CFG>::threads, MoeShape<CFG>::ctas) lora_moe_fold_kernel(const __grid_constant__ MoeArgs p) {
   constexpr int CW = MoeShape<CFG>::cw, PW = MoeShape<CFG>::pw, kMoeThreads = MoeShape<CFG>::threads;
   constexpr int kMoeRowsPerThread = (kMoeRoundRows + kMoeThreads - 1) / kMoeThreads;
@@ -1248,7 +1253,7 @@ __global__ void __launch_bounds__(MoeShape<CFG>::threads, MoeShape<CFG>::ctas) l
         pl.NV = nvk;
       }
       __syncthreads();
-      if (pl.G > 0) it0 += fold_engine<MAXT, false, false, CW, PW>(ea, g, pl, smem, cluster, 0, it0);
+      if (pl.G > 0) it0 += fold_engine<MAXT, false, false, CW, PW, RK>(ea, g, pl, smem, cluster, 0, it0);
       __syncthreads();   // the next pass rewrites the plan
     }
     // Another round: the ring serves as planning scratch again (every item of
@@ -1289,41 +1294,54 @@ static int launch_fold(void (*kernel)(Args), const Args& a, void* stream, int th
   return static_cast<int>(err);
 }
 
-int launch_bgmv(const BgmvArgs& a, void* stream) {
-  if (a.g.tc) {
-    switch (a.g.maxt) {
-      case 1: return launch_fold(lora_bgmv_fold_kernel<1, true, true>, a, stream);
-      case 2: return launch_fold(lora_bgmv_fold_kernel<2, true, true>, a, stream);
-      case 4: return launch_fold(lora_bgmv_fold_kernel<4, true, true>, a, stream);
-      default: return static_cast<int>(cudaErrorInvalidValue);
-    }
-  }
-  if (a.g.a_tiled) {
-    switch (a.g.maxt) {
-      case 1: return launch_fold(lora_bgmv_fold_kernel<1, true, false>, a, stream);
-      case 2: return launch_fold(lora_bgmv_fold_kernel<2, true, false>, a, stream);
-      case 4: return launch_fold(lora_bgmv_fold_kernel<4, true, false>, a, stream);
-      default: return static_cast<int>(cudaErrorInvalidValue);
-    }
-  }
+// Rank class of a launch (the expand loop's variant): 1 = max_rank 16, 2 = 32,
+// 0 = any other (the general variant, correct for every max_rank).
+static int rank_class(int max_rank) { return max_rank == 16 ? 1 : max_rank == 32 ? 2 : 0; }
+
+// maxt 4 needs more than one 16-row tile of rank (max_rank > 16): no rank-16 instance.
+template <bool TILED, bool TC, int RK>
+static int launch_bgmv_rk(const BgmvArgs& a, void* stream) {
   switch (a.g.maxt) {
-    case 1: return launch_fold(lora_bgmv_fold_kernel<1, false, false>, a, stream);
-    case 2: return launch_fold(lora_bgmv_fold_kernel<2, false, false>, a, stream);
-    case 4: return launch_fold(lora_bgmv_fold_kernel<4, false, false>, a, stream);
+    case 1: return launch_fold(lora_bgmv_fold_kernel<1, TILED, TC, RK>, a, stream);
+    case 2: return launch_fold(lora_bgmv_fold_kernel<2, TILED, TC, RK>, a, stream);
+    case 4:
+      if constexpr (RK != 1) return launch_fold(lora_bgmv_fold_kernel<4, TILED, TC, RK>, a, stream);
+      else return launch_fold(lora_bgmv_fold_kernel<4, TILED, TC, 0>, a, stream);
     default: return static_cast<int>(cudaErrorInvalidValue);
   }
 }
-int launch_moe(const MoeArgs& a, void* stream) {
-  const int key = a.g.maxt * 2 + (a.g.moe_cfg ? 1 : 0);
-  switch (key) {
-    case 2: return launch_fold(lora_moe_fold_kernel<1, 0>, a, stream, MoeShape<0>::threads);
-    case 3: return launch_fold(lora_moe_fold_kernel<1, 1>, a, stream, MoeShape<1>::threads);
-    case 4: return launch_fold(lora_moe_fold_kernel<2, 0>, a, stream, MoeShape<0>::threads);
-    case 5: return launch_fold(lora_moe_fold_kernel<2, 1>, a, stream, MoeShape<1>::threads);
-    case 8: return launch_fold(lora_moe_fold_kernel<4, 0>, a, stream, MoeShape<0>::threads);
-    case 9: return launch_fold(lora_moe_fold_kernel<4, 1>, a, stream, MoeShape<1>::threads);
+int launch_bgmv(const BgmvArgs& a, void* stream) {
+  const int rk = rank_class(a.max_rank);
+  // tcgen05 shrink: max_rank in (112, 128]; A tensor maps: max_rank >= 32
+  if (a.g.tc) return launch_bgmv_rk<true, true, 0>(a, stream);
+  if (a.g.a_tiled) return rk == 2 ? launch_bgmv_rk<true, false, 2>(a, stream) : launch_bgmv_rk<true, false, 0>(a, stream);
+  if (rk == 1) return launch_bgmv_rk<false, false, 1>(a, stream);
+  if (rk == 2) return launch_bgmv_rk<false, false, 2>(a, stream);
+  return launch_bgmv_rk<false, false, 0>(a, stream);
+}
+
+template <int CFG, int RK>
+static int launch_moe_rk(const MoeArgs& a, void* stream) {
+  constexpr int threads = MoeShape<CFG>::threads;
+  switch (a.g.maxt) {
+    case 1: return launch_fold(lora_moe_fold_kernel<1, CFG, RK>, a, stream, threads);
+    case 2: return launch_fold(lora_moe_fold_kernel<2, CFG, RK>, a, stream, threads);
+    case 4:
+      if constexpr (RK != 1) return launch_fold(lora_moe_fold_kernel<4, CFG, RK>, a, stream, threads);
+      else return launch_fold(lora_moe_fold_kernel<4, CFG, 0>, a, stream, threads);
     default: return static_cast<int>(cudaErrorInvalidValue);
   }
+}
+template <int CFG>
+static int launch_moe_cfg(const MoeArgs& a, void* stream) {
+  switch (rank_class(a.max_rank)) {
+    case 1: return launch_moe_rk<CFG, 1>(a, stream);
+    case 2: return launch_moe_rk<CFG, 2>(a, stream);
+    default: return launch_moe_rk<CFG, 0>(a, stream);
+  }
+}
+int launch_moe(const MoeArgs& a, void* stream) {
+  return a.g.moe_cfg ? launch_moe_cfg<1>(a, stream) : launch_moe_cfg<0>(a, stream);
 }
 
 // Self-test of the bounded wait every fold relies on: one thread waits on an
