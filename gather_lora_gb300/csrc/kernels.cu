@@ -48,6 +48,48 @@ namespace cg = cooperative_groups;
 // Device status word (LORA_DEV_* bits), read and cleared through read_device_status().
 __device__ unsigned int g_lora_status = 0;
 
+// Phase trace (diagnostic builds only, -DGLORA_TRACE=1; gather_lora_gb300/phase_trace.py):
+// one row of SM-clock stamps per CTA, written by one thread at each phase
+// boundary. Slots: 0 entry, 1 past the entry wait, 2 planned (engine entry),
+// 3 the producer's first item issued, 4 shrink done, 5 exchange done, 6 first
+// expand data, 7 expand done, 8 exit; 9/10 global timer (ns) at entry/exit;
+// 11 rows the CTA's last pass folded. A later pass of the same CTA overwrites
+// its engine stamps.
+#ifndef GLORA_TRACE
+#define GLORA_TRACE 0
+#endif
+#if GLORA_TRACE
+constexpr int kTraceCtas = 4096, kTraceSlots = 12;
+__device__ unsigned long long g_lora_trace[kTraceCtas][kTraceSlots];
+#define GLORA_STAMP(cond, slot)                                                                  \
+  do {                                                                                           \
+    if ((cond) && blockIdx.x < kTraceCtas) g_lora_trace[blockIdx.x][slot] = clock64();          \
+  } while (0)
+#define GLORA_GTIME(cond, slot)                                                                  \
+  do {                                                                                           \
+    if ((cond) && blockIdx.x < kTraceCtas) {                                                     \
+      unsigned long long t_;                                                                     \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                                     \
+      g_lora_trace[blockIdx.x][slot] = t_;                                                       \
+    }                                                                                            \
+  } while (0)
+#define GLORA_NOTE(cond, slot, v)                                                                \
+  do {                                                                                           \
+    if ((cond) && blockIdx.x < kTraceCtas) g_lora_trace[blockIdx.x][slot] = (v);                 \
+  } while (0)
+extern "C" int lora_trace_copy(void* dst, int bytes) {
+  return static_cast<int>(cudaMemcpyFromSymbol(dst, g_lora_trace, bytes));
+}
+extern "C" int lora_trace_clear(void) {
+  static unsigned long long zero[kTraceCtas][kTraceSlots];
+  return static_cast<int>(cudaMemcpyToSymbol(g_lora_trace, zero, sizeof zero));
+}
+#else
+#define GLORA_STAMP(cond, slot) do { } while (0)
+#define GLORA_GTIME(cond, slot) do { } while (0)
+#define GLORA_NOTE(cond, slot, v) do { } while (0)
+#endif
+
 namespace glora {
 
 constexpr unsigned kDevMisaligned = 0x1u;
@@ -283,7 +325,10 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
     // on GB300: qkv 21.3 -> 21.0 us; the single-CTA MoE units were slower).
     const int pre = p.late ? n_shrink : g.cl > 1 ? min(n_items, n_shrink + ns) : n_items;
     const int early = (p.late && g.cl > 1) ? min(n_items, n_shrink + ns) : n_shrink;   // items [n_shrink, early) in two parts
-    for (int it = 0; it < pre; ++it) produce(it);
+    for (int it = 0; it < pre; ++it) {
+      produce(it);
+      GLORA_STAMP(it == 0 && tid == CW * 32, 3);
+    }
     for (int it = n_shrink; it < early; ++it) produce(it, 1);
     if (g.cl > 1) {
       cluster.sync();
@@ -494,6 +539,8 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
     }
   }
 
+  GLORA_STAMP(tid == 0, 4);
+  GLORA_NOTE(tid == 0, 11, NV);
   // ---- exchange: xa = bf16(sum of the partials: cluster ranks in order, and
   //      k-phase planes in order within a rank) ----
   const int xa_pitch_el = g.pitch_xa >> 1;
@@ -571,6 +618,7 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
   // sector of 8-byte stores. The TMA-filled stage is only read. Consumer warp
   // w takes blocks w, w + 8, ...
   if (p.late) pdl_wait_then_release();   // base_out (and xa) only after the previous grid
+  GLORA_STAMP(tid == 0, 5);
   const uint32_t xa_base = smem_u32(xa_s);
   const int gq = lane >> 2, q = lane & 3;
   const bool odd = (q & 1) != 0;
@@ -611,6 +659,7 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
       for (int jc = 0; jc < nj; ++jc) {
         const int ri = it0 + n_shrink + gi * nj + jc, s = ri % ns;
         if (!mbar_wait(smem_u32(&pl.full[s]), (ri / ns) & 1) && lane == 0) record_timeout(pl);
+        GLORA_STAMP(tid == 0 && gi == 0 && jc == 0, 6);
         const uint32_t st = ring_u32 + s * g.stage_bytes;
         const int j0 = j_lo + jc * g.jch, jlen = min(g.jch, j_hi - j0), NCB = (jlen + 15) >> 4;
         const bool store = pl.failed == 0;
@@ -735,6 +784,7 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
       by_rank(I1{});
     }
   }
+  GLORA_STAMP(tid == 0, 7);
   // With a late wait xa leaves last: after the exchange every CTA of the
   // cluster holds all of it in xa_s; CTA crank writes rows crank, crank + cl,
   // ... in 4-byte pairs.
@@ -771,12 +821,15 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
   const int unit = static_cast<int>(blockIdx.x) / g.cl;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   Plan& pl = *reinterpret_cast<Plan*>(smem);
+  GLORA_STAMP(tid == 0, 0);
+  GLORA_GTIME(tid == 0, 9);
 
   // Without a late wait, nothing is read before the previous grid on the
   // stream has completed. With one, the engine waits before it touches base_out
   // or xa; a CTA that folds nothing leaves at once, except CTA 0, which waits,
   // so that this grid never completes before the previous one.
   if (!p.late) pdl_wait_then_release();
+  GLORA_STAMP(tid == 0, 1);
   auto leave = [&]() {
     if (p.late && blockIdx.x == 0) pdl_wait_then_release();
   };
@@ -913,6 +966,7 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
   ring_init(pl, g.ns);
   if constexpr (TC) tc_fence_after();
   const EngineArgs ea{p.x, p.x_stride, p.out, p.out_stride, p.xa, p.max_rank, p.k_in, p.n_out, p.late};
+  GLORA_STAMP(tid == 0, 2);
   fold_engine<MAXT, TILED, TC, kConsumerWarps, kProducerWarps, RK>(ea, g, pl, smem, cluster, crank, 0);
   if constexpr (TC) {
     tc_fence_before();
@@ -922,6 +976,8 @@ __global__ void __launch_bounds__(kThreads, 2) lora_bgmv_fold_kernel(const __gri
       tmem_dealloc(pl.tmem, 32);
     }
   }
+  GLORA_STAMP(tid == 0, 8);
+  GLORA_GTIME(tid == 0, 10);
 }
 
 // ============================================================================
@@ -988,11 +1044,14 @@ __global__ void __launch_bounds__(MoeShape<CFG>::threads, MoeShape<CFG>::ctas) l
     pl.failed = 0;
     mbar_fence_init();
   }
+  GLORA_STAMP(tid == 0, 0);
+  GLORA_GTIME(tid == 0, 9);
   // Without a late wait nothing is read before the previous grid on the stream
   // has completed; with one, the engine waits before it touches base_out or xa,
   // and a CTA that folds nothing leaves at once, except CTA 0, which waits, so
   // that this grid never completes before the previous one.
   if (!p.late) pdl_wait_then_release();
+  GLORA_STAMP(tid == 0, 1);
   auto leave = [&]() {
     if (p.late && blockIdx.x == 0) pdl_wait_then_release();
   };
@@ -1253,6 +1312,7 @@ __global__ void __launch_bounds__(MoeShape<CFG>::threads, MoeShape<CFG>::ctas) l
         pl.NV = nvk;
       }
       __syncthreads();
+      GLORA_STAMP(tid == 0, 2);
       if (pl.G > 0) it0 += fold_engine<MAXT, false, false, CW, PW, RK>(ea, g, pl, smem, cluster, 0, it0);
       __syncthreads();   // the next pass rewrites the plan
     }
@@ -1260,6 +1320,8 @@ __global__ void __launch_bounds__(MoeShape<CFG>::threads, MoeShape<CFG>::ctas) l
     // the last pass has been consumed).
   }
   leave();
+  GLORA_STAMP(tid == 0, 8);
+  GLORA_GTIME(tid == 0, 10);
 }
 
 // ============================================================================
