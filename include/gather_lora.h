@@ -79,7 +79,10 @@ enum lora_status {
  * GEMM that writes base_out). The kernel then plans, loads and runs its shrink
  * while the previous kernel finishes, and waits for it only before it reads
  * or writes base_out or writes xa. Without the flag it waits before reading
- * anything. The results are the same bits either way.
+ * anything. The results are the same bits either way. The overlap is CUDA's
+ * programmatic dependent launch, which relaxes only the order between two
+ * kernel launches: copies and event waits before the call on the stream are
+ * waited for as usual.
  */
 #define LORA_INPUTS_READY 0x1u
 
