@@ -725,8 +725,9 @@ def cpu_baseline(wl, seconds: float) -> dict:
                               "sample": f"{n1} {_rows_word(wl)}, 1 host thread ({s1:.1f} s)"}}
 
 
-def workload_config(wl, alg) -> dict:
-    """The `config` object of the JSON line: the workload and its shapes (both arms)."""
+def workload_config(wl, alg, world: int = 1) -> dict:
+    """The `config` object of the JSON line: the workload and its shapes, the same
+    in both arms (the reference arm is launched the same way, on the same N)."""
     kind = workload_kind(wl)
     cfg = {"workload": wl.name, "rows": alg["rows"], "routed_rows": alg["routed_rows"],
            "k_in": wl.k_in, "n_out": wl.n_out, "max_loras": getattr(wl, "max_loras", 1),
@@ -736,6 +737,7 @@ def workload_config(wl, alg) -> dict:
                    windows=len(wl.windows()), window_rows=wl.cap, x_gather=bool(wl.x_gather))
     cfg["l2"] = "inputs rotate through device copies totalling more than 2x L2 between steps"
     cfg["inputs_ready"] = bool(READY)
+    cfg["parallelism"] = f"replicas{world}"
     return cfg
 
 
@@ -795,7 +797,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(wl, alg),
+        "config": workload_config(wl, alg, dctx.world),
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": len(chunks), "kind": "oracle",
                          "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -919,8 +921,7 @@ def run_ours(args):
         cpu = cpu_baseline(wl, args.cpu_seconds)
 
     if dctx.rank == 0:
-        config = workload_config(wl, alg)
-        config["parallelism"] = f"replicas{dctx.world}"
+        config = workload_config(wl, alg, dctx.world)
         line = {
             "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": dctx.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
