@@ -352,10 +352,11 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
   // ========================= consumer warps =========================
   // Shrink items are either tile-parallel (one group per unit, bgmv): every
   // consumer warp takes part in every item, in order, splitting its tiles; or
-  // slot-parallel (many small MoE groups whose shrink is one k-chunk): consumer
-  // warp w alone serves ring slot w, computes all tiles of each shrink item in
-  // it and releases the slot with all eight arrivals, so the latency chains of
-  // several groups overlap while every slot keeps one in-order consumer.
+  // slot-parallel (many small MoE groups whose shrink is one k-chunk): the KSG
+  // consumer warps of ring slot s (warps s, s + ns, ...) alone serve it, each
+  // taking alternate k-steps of every shrink item in it into its own partial
+  // plane, and release the slot with CW / KSG arrivals each, so the latency
+  // chains of several groups overlap while every slot keeps in-order consumers.
   // Expand items are always tile-parallel.
   // Tile-parallel items with few tiles are also split over k: the consumer
   // warps form KS k-phases of TW warps; phase kp takes k-steps kp, kp + KS, ...
@@ -616,7 +617,7 @@ __device__ __forceinline__ int fold_engine(const EngineArgs& p, const FoldGeomet
   // with the staged old values in registers, and one exchange with lane q ^ 1
   // leaves it four adjacent columns, so each row leaves as one full 32-byte
   // sector of 8-byte stores. The TMA-filled stage is only read. Consumer warp
-  // w takes blocks w, w + 8, ...
+  // w takes blocks w, w + CW, ...
   if (p.late) pdl_wait_then_release();   // base_out (and xa) only after the previous grid
   GLORA_STAMP(tid == 0, 5);
   const uint32_t xa_base = smem_u32(xa_s);
