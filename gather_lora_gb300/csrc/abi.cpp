@@ -60,7 +60,7 @@ int device_sm_count_or(int fallback) {
 #define GLORA_BUDGET_TWO_PER_SM (112 * 1024)
 #endif
 #ifndef GLORA_STAGE_TARGET
-#define GLORA_STAGE_TARGET (40 * 1024)
+#define GLORA_STAGE_TARGET (42 * 1024)
 #endif
 #ifndef GLORA_MOE_STAGE_TARGET
 #define GLORA_MOE_STAGE_TARGET (56 * 1024)
