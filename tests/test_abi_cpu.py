@@ -124,6 +124,15 @@ def test_moe_table_count_and_persistent_grid():
     assert _moe(te=big, lo=0, hi=big, xa=None, x=FAKE + 2) == -4   # passes the size checks
 
 
+def test_strided_k_fold_geometry_takes_256_column_chunks():
+    """With A as tensor-map boxes at rank 64, a 256-column k chunk of the strided K
+    fold needs a 40.4 KB stage: the 42 KB target takes it (two stages) rather than
+    128-column chunks in three."""
+    g = L.lora_launch_geometry(16, 256, 128, 64, 4096, 1024)
+    assert g["a_tiled"] == 1 and g["cluster"] == 4 and g["k_slice"] == 1024
+    assert g["k_chunk"] == 256 and g["ring_stages"] == 2 and g["smem_bytes"] <= 113 * 1024
+
+
 def test_moe_cta_shape_follows_the_larger_half():
     """The MoE fold runs two CTAs of 8 + 2 warps per SM when its shrink is the larger
     half (k_in > n_out: the gate/up form) and one CTA of 12 + 4 warps otherwise (the
