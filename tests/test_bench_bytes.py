@@ -90,3 +90,18 @@ def test_counter_digest_follows_code_not_comments():
     assert bench.code_only(src) != bench.code_only(src.replace("a + 1", "a + 2"))
     assert "//" not in bench.code_only(src) and "/*" not in bench.code_only(src)
     assert len(bench.kernel_source_digest()) == 16
+
+
+def test_input_rotation_counts_the_bytes_a_step_touches():
+    """The rotation covers more than 2x L2 with the bytes the steps touch, not with the
+    whole buffers: an adapter pool mostly untouched by one batch must not count."""
+    import bench
+    l2 = 126 * 2 ** 20
+    # one step touching 34 MB of a 190 MB copy (the decode gather fold's shape)
+    assert bench.copies_needed(190 * 10 ** 6, l2, 34 * 10 ** 6) == 8
+    # whole buffers smaller than the touched estimate: the buffers bound it
+    assert bench.copies_needed(9 * 10 ** 6, l2, 10 ** 9) == 30
+    # a step that streams more than 2x L2 needs no second copy
+    assert bench.copies_needed(300 * 10 ** 6, l2, 315 * 10 ** 6) == 1
+    # at most 64 copies
+    assert bench.copies_needed(10 ** 3, l2, 10 ** 3) == 64
