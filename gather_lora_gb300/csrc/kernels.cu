@@ -1134,7 +1134,7 @@ __global__ void __launch_bounds__(MoeShape<CFG>::threads, MoeShape<CFG>::ctas) l
     }
     __syncthreads();
     const int rows_all = u_row0[nu];
-    // this round: rows [row_cur, row_end) of the units' concatenated rows
+    // this planning round: rows [row_cur, row_end) of the units' concatenated rows
     const int row_end = min(rows_all, row_cur + round_rows);
     // Each thread takes up to kMoeRowsPerThread rows of the round: their unit,
     // token and adapter (all token loads, then all adapter loads); a routed row
