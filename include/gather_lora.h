@@ -1,16 +1,22 @@
 /*
  * gather_lora.h — C ABI of the routed multi-LoRA fold for NVIDIA GB300 (sm_103a).
  *
- * Two operations, each one kernel launch on the caller's stream:
+ * Four folds, each one kernel launch on the caller's stream (lora_delta on
+ * its row-by-row path: one per LORA_MAX_ROWS rows):
  *
  *   lora_bgmv             per-request routed LoRA delta over n rows
  *   lora_moe_grouped_fold the same fold over expert-sorted MoE rows of one window
+ *   lora_moe_gather_bgmv  the decode-path MoE fold over flat (token, slot) rows
+ *   lora_delta            one adapter pair folded into every row (prefill)
  *
- * and three pure host helpers (no GPU needed) for the MoE windows and tables.
+ * plus lora_encode_a_tmaps (TMA tensor maps of the A matrices, encoded once on
+ * the host), diagnostics (status word, geometry queries, a bounded-wait self
+ * test) and five pure host helpers (no GPU needed) for the MoE windows, grids
+ * and tables.
  *
  * Conventions for every entry point
  *   - BF16 values are raw 16-bit patterns (lora_bf16_t); f32 is IEEE float.
- *   - Every pointer argument of the two folds is DEVICE memory owned by the
+ *   - Every pointer argument of the folds is DEVICE memory owned by the
  *     caller; the library allocates, frees and synchronizes nothing, and
  *     returns as soon as the launch is queued.
  *   - Strides are in ELEMENTS, not bytes.
@@ -24,7 +30,7 @@
  *     spans all mean "this row gets no delta". A table entry that is not
  *     16-byte aligned is skipped too and sets LORA_DEV_MISALIGNED in the
  *     device status word (lora_read_device_status).
- *   - Both folds are capture-safe: the launch shape depends only on the host
+ *   - Every fold is capture-safe: the launch shape depends only on the host
  *     integers passed in, so a CUDA graph captured once replays correctly
  *     when only device buffer CONTENTS (seq_slot, row_adapter, offsets, x,
  *     base_out) change.
@@ -189,8 +195,9 @@ int lora_bgmv(const lora_bf16_t* x, int64_t x_row_stride,
  * The window must satisfy 0 <= row_offset <= row_end <= te (else LORA_ERR_WINDOW);
  * the tables may hold at most LORA_MAX_LORAS entries (max_loras * num_experts),
  * else LORA_ERR_SIZE (so is a shape whose stages do not fit shared memory). The
- * launch grid is persistent and static: one CTA per SM
- * (fewer for windows under 16 rows per SM, at least 1), so it depends only on the
+ * launch grid is persistent and static: one CTA per SM, or two smaller ones when
+ * the shrink is the larger half of the work (k_in > n_out), fewer for windows
+ * under 16 rows per CTA (at least 1), so it depends only on the shapes, the
  * window size and the device. Each CTA takes a fixed share of the window's units
  * (one expert and a chunk of adapters) and folds the rows of their (expert,
  * adapter) groups; which rows share a group never changes a row's bits. Calls
