@@ -1,10 +1,9 @@
 """A CPU model of the routed fold kernel's planner (`lora_bgmv_fold_kernel`).
 
-The launcher sizes a static grid from host integers alone ("Function
-apply_lora_bgmv": the grid depends only on the batch size and the slot count,
-so a call can be captured once and replayed with new routing): rows / rt +
-min(rows, max_loras) clusters, each owning one unit, a tile of at most rt rows
-of one slot. Units are numbered either directly (unit s < max_loras is tile 0
+The launcher sizes a static grid from host integers alone, so that a call
+captured once replays with new routing ("Function apply_lora_bgmv", GRAPH-SAFE
+paragraph): rows / rt + min(rows, max_loras) clusters, each owning one unit, a
+tile of at most rt rows of one slot. Units are numbered either directly (unit s < max_loras is tile 0
 of slot s, the units after them the further tiles of the slots in slot order)
 or slot by slot (the tiles of the slots with rows, in slot order). A unit takes
 the rows of its slot in ascending order, ranks [tile * rt, tile * rt + rt).
@@ -22,6 +21,8 @@ with the oracle on routings of these kinds.
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import pytest
 
@@ -30,6 +31,15 @@ from gather_lora_gb300 import workloads as W
 
 MAX_ROWS = 8192      # LORA_MAX_ROWS
 MAX_LORAS = 4096     # LORA_MAX_LORAS
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    """The launcher's geometry comes from the library's host code (no GPU needed)."""
+    if not os.path.exists(L.LIB_PATH):
+        from gather_lora_gb300 import build
+        build.build()
+    L.load()
 
 
 def plan(slots, max_loras, rt, direct, clusters, mutant=None):

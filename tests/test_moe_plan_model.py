@@ -42,6 +42,15 @@ from gather_lora_gb300 import workloads as W
 CSRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "gather_lora_gb300", "csrc")
 
 
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    """The launcher's geometry comes from the library's host code (no GPU needed)."""
+    if not os.path.exists(L.LIB_PATH):
+        from gather_lora_gb300 import build
+        build.build()
+    L.load()
+
+
 def _source(name):
     with open(os.path.join(CSRC, name)) as f:
         return f.read()
