@@ -257,6 +257,24 @@ def test_geometry_depends_on_shapes_only():
         assert g1["k_slice"] * g1["cluster"] >= k and g1["j_slice"] * g1["cluster"] >= no
 
 
+def test_every_supported_shape_has_a_launch_geometry():
+    """Every max_rank of the supported range (multiples of 8 up to 256), k_in and
+    n_out from 8 to 2^20, for each fold kind (bgmv with and without A maps, the
+    decode gather fold, the MoE fold): a geometry exists, fits the 227 KB of
+    shared memory a CTA may take, has at least two ring stages, and its cluster
+    slices cover k_in and n_out."""
+    dims = (8, 64, 136, 768, 2048, 4096, 12288, 65536, 1 << 20)
+    for R in range(8, 256 + 1, 8):      # LORA_MAX_RANK
+        for k in dims:
+            for no in dims:
+                for kind in (0, 16, 2, 18, 1):
+                    g = L.lora_launch_geometry(kind, 512, 16 if kind == 1 else 64, R, k, no)
+                    assert g["smem_bytes"] <= 227 * 1024 and g["ring_stages"] >= 2, (kind, R, k, no)
+                    assert g["cluster"] in (1, 2, 4, 8)
+                    assert g["k_slice"] * g["cluster"] >= k and g["j_slice"] * g["cluster"] >= no
+                    assert g["k_chunk"] % 8 == 0 and g["j_chunk"] % 8 == 0
+
+
 def test_bgmv_grid_bounds_every_routing():
     """clusters = n/rt + min(n, max_loras) covers sum_s ceil(count_s / rt) for any routing."""
     rng = np.random.default_rng(1)
