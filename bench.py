@@ -509,7 +509,8 @@ def e2e_run(wl, device, steps, warmup, copies):
     run them: the copies in, the calls and the copy out go on three streams, over
     at least two device copies of the inputs, so step i's inputs travel while step
     i - 1 folds and step i - 2's result comes back (events order each copy's uses).
-    Returns (rows/s, H2D bytes, D2H bytes) per step."""
+    Returns rows/s, the H2D and D2H bytes per step, and the time and rows/s of one
+    step's copies alone (in and out at once, no fold): the bound of the pipeline."""
     import torch
     from gather_lora_gb300 import lib as L
     from gather_lora_gb300 import workloads as W
@@ -602,7 +603,28 @@ def e2e_run(wl, device, steps, warmup, copies):
         raise RuntimeError("end-to-end steps gave different results from a step run alone")
     h2d = sum(src.numel() * src.element_size() for _, src in host[0])
     d2h = hres[0].numel() * hres[0].element_size()
-    return rows * steps / (ms / 1e3), h2d, d2h
+    # The bound the pipeline can reach: one step's copies alone, its inputs in and
+    # a result out at once on the same streams, with no fold (steps serialized).
+    big0 = max(host[0], key=lambda ds: ds[1].numel() * ds[1].element_size())
+    cur = torch.cuda.current_stream(device)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 20
+    for r in range(reps + 3):
+        if r == 3:
+            t0.record(cur)
+        for st in (s_in, s_big, s_out):
+            st.wait_stream(cur)
+        for pair in host[0]:
+            with torch.cuda.stream(s_big if pair is big0 else s_in):
+                pair[0].copy_(pair[1], non_blocking=True)
+        with torch.cuda.stream(s_out):
+            hres[1].copy_(devs[1].out_buf, non_blocking=True)
+        for st in (s_in, s_big, s_out):
+            cur.wait_stream(st)
+    t1.record(cur)
+    torch.cuda.synchronize(device)
+    copy_ms = t0.elapsed_time(t1) / reps
+    return rows * steps / (ms / 1e3), h2d, d2h, copy_ms, rows / (copy_ms / 1e3)
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -921,9 +943,13 @@ def run_ours(args):
     e2e = None
     if head_kind in ("bgmv", "moe"):
         e2e_steps = max(50, min(args.steps, 2000 if head_kind == "bgmv" else 400))
-        e2e_val, h2d, d2h = e2e_run(wl, device, e2e_steps, 10, C)
+        e2e_val, h2d, d2h, copy_ms, copy_rows = e2e_run(wl, device, e2e_steps, 10, C)
         e2e = {"value": dctx.sum(e2e_val), "unit": "rows/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+               "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "copy_bound": {"value": dctx.sum(copy_rows), "unit": "rows/s", "ms_per_step": copy_ms,
+                              "what": "one step's host copies alone, inputs in and base_out out at once, "
+                                      "no fold"},
+               "frac_of_copy_bound": e2e_val / copy_rows}
 
     cpu = None
     if dctx.rank == 0 and not args.no_cpu_baseline and head_kind in ("bgmv", "moe"):
