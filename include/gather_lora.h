@@ -176,7 +176,9 @@ int lora_bgmv(const lora_bf16_t* x, int64_t x_row_stride,
  *       x[xr*x_row_stride ..] (xr = x_gather ? t : r) and
  *       base_out[r*out_row_stride ..] with A_t, B_t, scale_table[t].
  *
- *   expert_offsets    [num_experts + 1] int32 prefix sum (non-decreasing)
+ *   expert_offsets    [num_experts + 1] int32 prefix sum (non-decreasing; offsets out
+ *                     of order are bad data that fold no row twice, for windows under
+ *                     2^25 rows: the planner sums its units' spans in 32 bits)
  *   sorted_token_ids  [te] int32 sorted row -> token; may be NULL when row_adapter is
  *                     NULL and x_gather == 0
  *   row_adapter       [num_tokens] int32 (< 0 = no delta), or NULL: every row uses adapter 0
