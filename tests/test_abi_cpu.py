@@ -273,6 +273,10 @@ def test_every_supported_shape_has_a_launch_geometry():
                     assert g["cluster"] in (1, 2, 4, 8)
                     assert g["k_slice"] * g["cluster"] >= k and g["j_slice"] * g["cluster"] >= no
                     assert g["k_chunk"] % 8 == 0 and g["j_chunk"] % 8 == 0
+                # the largest batch and slot count (the planner's scratch is the largest)
+                for kind in (0, 16, 2):
+                    g = L.lora_launch_geometry(kind, 8192, 4096, R, k, 2048)
+                    assert g["smem_bytes"] <= 227 * 1024 and g["ring_stages"] >= 2, (kind, R, k)
 
 
 def test_bgmv_grid_bounds_every_routing():
